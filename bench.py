@@ -1,0 +1,427 @@
+"""Benchmark: fused RNN training step (forward_training + backward_data +
+backward_weights) on the Deep Speech 2 LSTM layer shape, 1 GPU per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ds2_lstm]
+                    [--impl ours|reference]
+
+One JSON line on rank 0.  A step is one pass of the whole hot path over one
+batch (N=20 sequences of T=300) with inputs resident in HBM; L2 is flushed
+(256 MiB write, untimed) before every timed step; each step is bracketed by
+CUDA events on the launching stream.  Under torchrun every rank runs an
+independent replica (the operator has no data-path exchange on one GPU);
+value = sequences of all ranks / max-over-ranks step time.
+
+``--impl reference`` times the float64 CPU oracle (the only other
+implementation) on a bounded sample of the same workload on the host cores.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from layer_rnn_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "LSTM/GRU fwd+bwd sequences/s and effective TFLOP/s at DS2 shape, 1×GB300"
+PHASE_NAMES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")
+PHASE_KERNELS = {"input_gemm": "gemm_kernel (input projection)",
+                 "rec_fwd": "rec_fwd_kernel", "rec_bwd": "rec_bwd_kernel",
+                 "dx_gemm": "gemm_kernel (dX)", "dw_gemm": "gemm_kernel + colsum_kernel (dW, db)"}
+
+
+def gates(mode):
+    return wl.GATES[mode]
+
+
+def phase_flops(cfg):
+    """Algorithmic flops per phase for one training step (whole stack)."""
+    G, H, T, N, D = gates(cfg["mode"]), cfg["H"], cfg["T"], cfg["N"], wl.num_directions(cfg)
+    out = dict.fromkeys(PHASE_NAMES, 0.0)
+    for l in range(cfg["L"]):
+        I_l = cfg["I"] if l == 0 else D * H
+        per = 2.0 * T * N * G * H
+        out["input_gemm"] += D * per * I_l
+        out["rec_fwd"] += D * per * H
+        out["rec_bwd"] += D * per * H
+        out["dx_gemm"] += D * per * I_l
+        out["dw_gemm"] += D * per * (I_l + H)
+    return out
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_simt_peak_tflops(num_sms, sm_mhz):
+    # 128 fp32 FMA lanes per SM per clock, 2 flop per FMA
+    return num_sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas; barrier and max over ranks only)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def max_over_ranks(value, dist, device="cpu"):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle, timed (baseline / reference arm)
+# ----------------------------------------------------------------------------
+def time_oracle(cfg, budget_s=20.0, max_reps=3):
+    """Oracle fwd+bwd on a prefix of the sequences (shorter T), scaled to full
+    sequences.  Returns (sequences_per_s, sample description, seconds spent)."""
+    import oracle
+    T_full = cfg["T"]
+    # probe on a short prefix, then grow within the budget
+    T_s = max(1, min(T_full, 10))
+    spent = 0.0
+    best = None
+    reps = 0
+    while True:
+        c = wl.with_sizes(cfg, T=T_s)
+        inp = wl.make_inputs(c)
+        t0 = time.perf_counter()
+        oracle.run_flat(c["mode"], c["L"], c["bidir"], c["I"], c["H"], inp["x"], inp["h0"],
+                        inp["c0"], inp["w"], inp["dy"], inp["dhy"], inp["dcy"])
+        dt = time.perf_counter() - t0
+        spent += dt
+        reps += 1
+        per_full_seq = dt * (T_full / T_s) / c["N"]
+        best = per_full_seq if best is None else min(best, per_full_seq)
+        if T_s < T_full and spent + dt * min(T_full / T_s, 4) * 1.5 < budget_s:
+            T_s = min(T_full, T_s * 4)
+            continue
+        if reps < max_reps and spent + dt < budget_s:
+            continue
+        break
+    sample = ("float64 oracle fwd+bwd on the first %d of %d time steps of the %s workload "
+              "(N=%d sequences), best of %d runs, scaled by %d/%d to whole sequences"
+              % (T_s, T_full, cfg["name"], cfg["N"], reps, T_full, T_s))
+    return 1.0 / best, sample, spent
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, cfg):
+    import torch
+    from layer_rnn_gb300 import binding as B
+    from tests import harness
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init("nccl")
+    T, N, I, H, L = cfg["T"], cfg["N"], cfg["I"], cfg["H"], cfg["L"]
+    D = wl.num_directions(cfg)
+    dt = cfg["dtype"]
+    lstm = cfg["mode"] == "lstm"
+    inp = wl.make_inputs(cfg, seed=cfg["seed"] + rank)
+    r = B.Rnn(cfg["mode"], L, cfg["bidir"], I, H, dt, 0)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        x = harness.to_dev(inp["x"], dt, dev)
+        h0 = harness.to_dev(inp["h0"], dt, dev)
+        c0 = harness.to_dev(inp["c0"], "f32", dev) if lstm else None
+        W = harness.to_dev(inp["w"], dt, dev)
+        dy = harness.to_dev(inp["dy"], dt, dev)
+        dhy = harness.to_dev(inp["dhy"], dt, dev)
+        dcy = harness.to_dev(inp["dcy"], "f32", dev) if lstm else None
+        y = harness.empty((T, N, D * H), dt, dev)
+        hy = harness.empty((L * D, N, H), dt, dev)
+        cy = harness.empty((L * D, N, H), "f32", dev) if lstm else None
+        dx = harness.empty((T, N, I), dt, dev)
+        dh0 = harness.empty((L * D, N, H), dt, dev)
+        dc0 = harness.empty((L * D, N, H), "f32", dev) if lstm else None
+        dW = harness.empty((inp["w"].size,), dt, dev)
+        ws = r.alloc_workspace(T, N, dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream.synchronize()
+
+    def step():
+        r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
+        r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+        r.backward_weights(x, h0, y, ws, dW, stream)
+
+    def timed(n, fn):
+        evs = []
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        stream.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # warm-up
+    for _ in range(args.warmup):
+        step()
+    st = r.check_status(stream)
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+
+    # device-resident timed region
+    sampler = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)
+    wall0 = time.perf_counter()
+    ms = timed(args.steps, step)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(dist)
+    clocks = sampler.stop()
+    st = r.check_status(stream)
+    if st != 0:
+        raise RuntimeError("device status %d in timed region" % st)
+    ms_step = statistics.mean(ms)
+    ms_step_max = max_over_ranks(ms_step, dist, dev)
+
+    # per-phase CUDA events on the launching stream (a second pass of K steps)
+    B.rnn_enable_phase_timing(r.h, 1)
+    ms2 = timed(args.steps, step)
+    phases = B.rnn_get_phase_times(r.h)
+    B.rnn_enable_phase_timing(r.h, 0)
+    launches_per_step = sum(n for _, n in phases.values()) / args.steps
+
+    # end to end: pinned host inputs in, results out, every step
+    pin = {}
+    for k, t in dict(x=x, h0=h0, c0=c0, W=W, dy=dy, dhy=dhy, dcy=dcy).items():
+        if t is not None:
+            pin[k] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            pin[k].copy_(t)
+    outs = dict(y=y, hy=hy, cy=cy, dx=dx, dh0=dh0, dc0=dc0, dW=dW)
+    pout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            for k, t in outs.items() if t is not None}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in pout.values())
+    dev_in = dict(x=x, h0=h0, c0=c0, W=W, dy=dy, dhy=dhy, dcy=dcy)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k, t in pin.items():
+                dev_in[k].copy_(t, non_blocking=True)
+        step()
+        with torch.cuda.stream(stream):
+            for k, t in pout.items():
+                t.copy_(outs[k], non_blocking=True)
+
+    barrier(dist)
+    ms_e2e = timed(args.steps, e2e_step)
+    ms_e2e_max = max_over_ranks(statistics.mean(ms_e2e), dist, dev)
+    r.close()
+
+    peaks, peak_src = load_peaks()
+    fl = phase_flops(cfg)
+    total_flop = sum(fl.values())
+    # dominant phase by time share
+    dom = max(PHASE_NAMES, key=lambda p: phases[p][0])
+    n_launch = max(1, phases[dom][1])
+    avg_ms = phases[dom][0] / max(1, args.steps)
+    sm_clk = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if dt == "bf16" and dom.endswith("gemm"):
+        bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
+        peak_note = "%s bf16 dense (cuBLAS burst)" % peak_src
+    else:
+        bound, unit = "alu", "TFLOP/s"
+        peak = fp32_simt_peak_tflops(num_sms, sm_clk)
+        peak_note = ("fp32 FMA issue peak: %d SMs x 128 lanes x 2 flop x %.0f MHz (derived)"
+                     % (num_sms, sm_clk))
+    achieved = fl[dom] / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
+    value = N * ws_n / (ms_step_max * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "sequences/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if dt == "f32" else "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, U(-1/sqrt(H), 1/sqrt(H)) weights)",
+        "config": {"workload": cfg["name"], "mode": cfg["mode"], "layers": L,
+                   "bidirectional": cfg["bidir"], "T": T, "N": N, "I": I, "H": H,
+                   "global_batch": N * ws_n, "seq_len": T,
+                   "parallelism": "replicas x%d" % ws_n if ws_n > 1 else "single GPU",
+                   "l2": "flushed before every timed step (256 MiB write, untimed)"},
+        "effective_tflops": round(total_flop * ws_n / (ms_step_max * 1e-3) / 1e12, 3),
+        "phase_ms_per_step": {p: round(phases[p][0] / args.steps, 4) for p in PHASE_NAMES},
+        "phase_kernels_per_step": {p: phases[p][1] / args.steps for p in PHASE_NAMES},
+        "roofline": {"kernel": PHASE_KERNELS[dom], "phase": dom, "bound": bound,
+                     "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
+                     "frac": round(achieved / peak, 4) if peak else None,
+                     "traffic": None, "peak_source": peak_note,
+                     "algorithmic_flop_per_step": fl[dom],
+                     "avg_phase_ms": round(avg_ms, 4)},
+        "e2e": {"value": round(N * ws_n / (ms_e2e_max * 1e-3), 2), "unit": "sequences/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e_max, 4)},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "wall_s_timed_region": round(wall, 3),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, spent = time_oracle(cfg, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "sequences/s",
+                                "cores": os.cpu_count(), "kind": "oracle", "sample": sample,
+                                "seconds": round(spent, 2)}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, cfg):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    # the oracle, as it stands, on bounded samples; W warm-up + K timed samples
+    budget = max(2.0, args.cpu_budget / max(1, K + W))
+    vals = []
+    sample = None
+    for i in range(W + K):
+        v, sample, _ = time_oracle(cfg, budget_s=budget, max_reps=1)
+        if i >= W:
+            vals.append(v)
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": round(v, 4), "unit": "sequences/s", "n_gpus": ws_n,
+            "steps": K, "warmup": W, "ms_per_step": round(cfg["N"] / v * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg["name"], "T": cfg["T"], "N": cfg["N"], "I": cfg["I"],
+                       "H": cfg["H"], "mode": cfg["mode"], "layers": cfg["L"],
+                       "bidirectional": cfg["bidir"]},
+            "cpu_baseline": {"value": round(v, 4), "unit": "sequences/s",
+                             "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "sequences/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ds2_lstm", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    cfg = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * layer_rnn.h -- C ABI of liblayer_rnn.so, a fused multi-layer RNN operator
+ * (tanh RNN, LSTM, GRU; stacked, optionally bidirectional) for one GB300 GPU.
+ *
+ * The operator follows the shape the pages give a fused RNN:
+ *   - one operator for a whole multi-layer (optionally bidirectional) RNN
+ *     ("Fused RNN operator for CPU", MXNet design page: Problem Statement and
+ *     Operator Registration; the "CudnnLSTM(num_layers, num_units,
+ *     input_size)" call quoted in Keras issue #3692);
+ *   - a training forward that fills a workspace which the backward pass then
+ *     reads ("rnn training example?", oneDNN issue #218: the six workspace
+ *     steps -- create forward_training, query the workspace size, allocate it,
+ *     pass it as an output of forward and as an input of backward);
+ *   - PyTorch's tensor names and shapes (same issue: w_ih, w_hh, b_ih, b_hh
+ *     and their gradients as separate tensors; hx / cx / hy / cy of shape
+ *     (num_layers * num_directions, batch, hidden); input in TNC order).
+ *
+ * Recurrences (a = pre-activation, * = elementwise):
+ *   tanh RNN: h' = tanh(W_ih x + b_ih + W_hh h + b_hh)
+ *   LSTM    : gate blocks i, f, g, o;  c' = f*c + i*g;  h' = o*tanh(c')
+ *   GRU     : gate blocks r, z, n (the PyTorch / cuDNN flavour of the oneDNN
+ *             issue, "PyTorch equations"): n = tanh(W_in x + b_in +
+ *             r*(W_hn h + b_hn)),  h' = (1-z)*n + z*h.
+ * Direction 1 of a bidirectional layer walks t = T-1 .. 0 and writes its
+ * output at the original time index; a layer's output is [fwd || bwd] along
+ * features and feeds the next layer.
+ *
+ * Conventions for every call below
+ *   - All tensors and the workspace are caller-owned DEVICE memory, dense,
+ *     row-major, 16-byte aligned (the workspace 256-byte aligned); otherwise
+ *     RNN_ERR_MISALIGNED.  Pointers of different arguments must not overlap,
+ *     except that the weight buffer W may be shared by several calls.
+ *   - x [T, N, I]; y, dy [T, N, D*H]; h0, hy, dh0, dhy, c0, cy, dc0, dcy
+ *     [L*D, N, H] with index layer*D + direction.
+ *   - Element types: RNN_F32 -> every tensor float32.  RNN_BF16 -> x, y, dy,
+ *     dx, W, dW, h0, hy, dhy, dh0 are bfloat16; c0, cy, dcy, dc0 (cell
+ *     state) are float32.  Accumulation and the cell state are float32
+ *     internally in both.
+ *   - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and return after enqueueing.  Argument errors
+ *     are returned before anything is enqueued.  A device-side failure (a
+ *     step barrier that ran past its time limit) is recorded in a status word
+ *     that rnn_check_status() returns; with RNN_FLAG_SYNC_CHECK every compute
+ *     call synchronises and returns it itself.
+ *   - One handle serves one stream at a time (it owns the step-barrier
+ *     counters its kernels use).  No call allocates device memory except
+ *     rnn_forward_inference (first call per (T, N) growth, see there) and the
+ *     first compute call of a handle (its 4 KB of barrier counters).
+ */
+#ifndef LAYER_RNN_H
+#define LAYER_RNN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct rnn_handle* rnn_t;
+
+typedef enum { RNN_TANH = 0, RNN_LSTM = 1, RNN_GRU = 2 } rnn_mode_t;
+typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
+
+typedef enum {
+  RNN_OK = 0,
+  RNN_ERR_INVALID_ARG = 1,        /* bad mode/dtype/size, NULL required pointer  */
+  RNN_ERR_UNSUPPORTED = 2,        /* valid but beyond what the kernels support   */
+  RNN_ERR_WORKSPACE_TOO_SMALL = 3,
+  RNN_ERR_MISALIGNED = 4,
+  RNN_ERR_CUDA = 5,               /* a CUDA runtime call failed                  */
+  RNN_ERR_TIMEOUT = 6,            /* a step barrier gave up waiting (device)     */
+  RNN_ERR_NO_RESIDENCY = 7        /* the persistent grid cannot be co-resident   */
+} rnn_status_t;
+
+/* flags for rnn_create */
+#define RNN_FLAG_SYNC_CHECK 0x1u  /* each compute call synchronises `stream` and
+                                     returns the device status word            */
+#define RNN_FLAG_SIMT_GEMM  0x2u  /* dense phases on the CUDA-core GEMM instead
+                                     of the tensor-core GEMM                    */
+
+/* regions for rnn_workspace_layout */
+typedef enum {
+  RNN_WS_GATES = 0,   /* per (l,d): [T, N, G'*H] f32 saved activations; G' = 4 for
+                         LSTM (i,f,g,o) and GRU (r,z,n, W_hn h + b_hn), 1 for tanh
+                         RNN (h); time-indexed                                      */
+  RNN_WS_CSEQ = 1,    /* per (l,d): [T+1, N, H] f32 cell states (LSTM only); slot
+                         0 (dir 0) or T (dir 1) holds c0, slot t+1 / t holds c_t    */
+  RNN_WS_HSEQ = 2,    /* per (l,d): [T+1, N, H] hidden states, same slots as CSEQ,
+                         element type of h                                          */
+  RNN_WS_YLAYER = 3,  /* per l < L-1: [T, N, D*H] layer output (next layer's input) */
+  RNN_WS_DGX = 4,     /* per (l,d): [T, N, G*H] gate-gradients w.r.t. W_ih x + b_ih
+                         (f32, or bf16 for RNN_BF16)                                */
+  RNN_WS_DGH = 5,     /* per (l,d): [T, N, G*H] gate-gradients w.r.t. W_hh h + b_hh
+                         (GRU only; equals DGX for LSTM / tanh RNN)                 */
+  RNN_WS_GX = 6,      /* [D, T, N, G*H] f32 input projection scratch                */
+  RNN_WS_DY = 7,      /* [2, T, N, D*H] f32 gradient ping-pong between layers       */
+  RNN_WS_NUM_REGIONS = 8
+} rnn_ws_region_t;
+
+/* phases for rnn_get_phase_times */
+typedef enum {
+  RNN_PHASE_INPUT_GEMM = 0,   /* G_x = X W_ih^T + b over all T (per layer)           */
+  RNN_PHASE_REC_FWD = 1,      /* persistent recurrent forward (per layer)            */
+  RNN_PHASE_REC_BWD = 2,      /* persistent recurrent backward (per layer)           */
+  RNN_PHASE_DX_GEMM = 3,      /* dX = dG_x W_ih (per layer)                          */
+  RNN_PHASE_DW_GEMM = 4,      /* dW_ih, dW_hh and db (per layer and direction)       */
+  RNN_PHASE_NUM = 5
+} rnn_phase_t;
+
+/* Create a handle.  mode: rnn_mode_t; num_layers >= 1; bidirectional 0/1;
+ * input_size, hidden_size >= 1; dtype: rnn_dtype_t; flags: RNN_FLAG_*.
+ * Host only (no CUDA call).  *out is owned by the caller until rnn_destroy. */
+rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
+                        int64_t input_size, int64_t hidden_size, int dtype,
+                        uint32_t flags);
+
+/* Release the handle and the device memory it owns.  NULL is accepted.
+ * Waits for nothing: the caller must have finished using it on the device. */
+rnn_status_t rnn_destroy(rnn_t h);
+
+/* Number of elements (of the handle's element type) of the canonical weight
+ * buffer W / dW.  Host only. */
+rnn_status_t rnn_weight_count(rnn_t h, int64_t* n_elems);
+
+/* Canonical weight buffer layout.  For each (layer, dir) in order
+ * layer*D + dir: W_ih [G*H, I_l] (which=0), W_hh [G*H, H] (1), b_ih [G*H] (2),
+ * b_hh [G*H] (3), row-major and back to back; I_l = input_size for layer 0 and
+ * D*H above.  Gate blocks along the G*H rows: LSTM i,f,g,o; GRU r,z,n; tanh
+ * RNN one block -- the PyTorch order.  Returns the element offset and the
+ * shape (cols = 1 for biases).  Host only. */
+rnn_status_t rnn_weight_layout(rnn_t h, int layer, int dir, int which,
+                               int64_t* offset, int64_t* rows, int64_t* cols);
+
+/* Bytes of the training workspace for sequence length T and batch N
+ * (forward_training writes it; backward_data and backward_weights read it,
+ * backward_data also writes the gate-gradient regions).  Host only. */
+rnn_status_t rnn_workspace_size(rnn_t h, int64_t T, int64_t N, int64_t* bytes);
+
+/* Byte offset and size of one workspace region (rnn_ws_region_t) for
+ * (layer, dir); per-layer regions ignore dir, global ones ignore both.
+ * A region that does not exist for the mode reports bytes = 0.  Host only. */
+rnn_status_t rnn_workspace_layout(rnn_t h, int64_t T, int64_t N, int region,
+                                  int layer, int dir, int64_t* offset, int64_t* bytes);
+
+/* Training forward: y = the top layer's output, hy / cy = final states, and
+ * the workspace filled for the backward calls.  h0 / c0 NULL = zeros;
+ * hy / cy NULL = not written; c0 / cy ignored unless LSTM. */
+rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N,
+                                  const void* x, const void* h0, const void* c0,
+                                  const void* W, void* y, void* hy, void* cy,
+                                  void* workspace, int64_t ws_bytes);
+
+/* Inference forward: as rnn_forward_training without a workspace.  The
+ * handle keeps device scratch for the input projection and the intermediate
+ * layer outputs, allocated (cudaMalloc) when a call needs more than it has;
+ * make one call per shape before capturing a CUDA graph. */
+rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N,
+                                   const void* x, const void* h0, const void* c0,
+                                   const void* W, void* y, void* hy, void* cy);
+
+/* Backward through time for the data: dx (and dh0, dc0) of the loss
+ * sum(y*dy) + sum(hy*dhy) + sum(cy*dcy).  Needs the workspace of the
+ * matching rnn_forward_training (same T, N, W), writes its DGX / DGH / DY
+ * regions.  dhy / dcy NULL = zeros; dh0 / dc0 NULL = not written. */
+rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N,
+                               const void* W, const void* dy, const void* dhy,
+                               const void* dcy, void* dx, void* dh0, void* dc0,
+                               void* workspace, int64_t ws_bytes);
+
+/* Weight gradients dW (canonical layout, overwritten -- not accumulated):
+ * dW_ih = sum_t dG_x[t]^T x_t, dW_hh = sum_t dG_h[t]^T h_{t-1}, db_ih =
+ * sum dG_x, db_hh = sum dG_h.  Must follow rnn_backward_data on the same
+ * workspace.  x is the forward input.  h0 and y may be NULL: the workspace
+ * already holds the hidden-state sequences. */
+rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N,
+                                  const void* x, const void* h0, const void* y,
+                                  const void* workspace, int64_t ws_bytes, void* dW);
+
+/* Synchronise `stream`, then return and clear the device status word
+ * (RNN_OK or RNN_ERR_TIMEOUT). */
+rnn_status_t rnn_check_status(rnn_t h, void* stream);
+
+/* Test hook for failure detection.  timeout_ns > 0 sets the step-barrier
+ * time limit (default 2 s).  fault_block >= 0 makes that block of the next
+ * persistent launches skip its barrier arrival at step fault_step, so every
+ * waiting block runs into the time limit, records RNN_ERR_TIMEOUT and
+ * returns (no trap, no unbounded wait).  fault_block = -1 disables. */
+rnn_status_t rnn_set_debug(rnn_t h, int fault_block, int fault_step, int64_t timeout_ns);
+
+/* Per-phase timing with CUDA events recorded on the launching stream.
+ * enable = 1 starts recording (and zeroes the totals), 0 stops. */
+rnn_status_t rnn_enable_phase_timing(rnn_t h, int enable);
+
+/* Synchronise the events recorded so far and return, per rnn_phase_t, the
+ * summed milliseconds between the events bracketing the phase and the number
+ * of kernels the library launched inside it (arrays of RNN_PHASE_NUM). */
+rnn_status_t rnn_get_phase_times(rnn_t h, double* ms, int64_t* launches);
+
+/* Static description of the status code. */
+const char* rnn_status_string(rnn_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYER_RNN_H */

@@ -1,0 +1,230 @@
+"""ctypes binding of liblayer_rnn.so (include/layer_rnn.h).
+
+Functions keep the C names and arguments; pointers are passed as integers
+(device addresses, e.g. ``tensor.data_ptr()``) and streams as integers
+(``torch.cuda.current_stream().cuda_stream``).  Non-zero status codes raise
+``RnnError``.  ``Rnn`` is a small convenience wrapper around one handle that
+takes torch tensors; it only marshals arguments -- every step of the operator
+runs in the library's kernels.  Nothing here computes on the CPU, and loading
+fails loudly when the library has not been built.
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblayer_rnn.so")
+
+RNN_TANH, RNN_LSTM, RNN_GRU = 0, 1, 2
+RNN_F32, RNN_BF16 = 0, 1
+RNN_FLAG_SYNC_CHECK, RNN_FLAG_SIMT_GEMM = 0x1, 0x2
+(RNN_WS_GATES, RNN_WS_CSEQ, RNN_WS_HSEQ, RNN_WS_YLAYER, RNN_WS_DGX, RNN_WS_DGH,
+ RNN_WS_GX, RNN_WS_DY) = range(8)
+PHASES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")
+STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
+          3: "RNN_ERR_WORKSPACE_TOO_SMALL", 4: "RNN_ERR_MISALIGNED", 5: "RNN_ERR_CUDA",
+          6: "RNN_ERR_TIMEOUT", 7: "RNN_ERR_NO_RESIDENCY"}
+MODES = {"rnn_tanh": RNN_TANH, "lstm": RNN_LSTM, "gru": RNN_GRU}
+DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
+
+# exported symbol -> (restype, argtypes)
+_i64, _i32, _u32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_void_p
+_pi64 = ctypes.POINTER(ctypes.c_int64)
+SIGNATURES = {
+    "rnn_create": (_i32, [ctypes.POINTER(_vp), _i32, _i32, _i32, _i64, _i64, _i32, _u32]),
+    "rnn_destroy": (_i32, [_vp]),
+    "rnn_weight_count": (_i32, [_vp, _pi64]),
+    "rnn_weight_layout": (_i32, [_vp, _i32, _i32, _i32, _pi64, _pi64, _pi64]),
+    "rnn_workspace_size": (_i32, [_vp, _i64, _i64, _pi64]),
+    "rnn_workspace_layout": (_i32, [_vp, _i64, _i64, _i32, _i32, _i32, _pi64, _pi64]),
+    "rnn_forward_training": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _i64]),
+    "rnn_forward_inference": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "rnn_backward_data": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                 _i64]),
+    "rnn_backward_weights": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "rnn_check_status": (_i32, [_vp, _vp]),
+    "rnn_set_debug": (_i32, [_vp, _i32, _i32, _i64]),
+    "rnn_enable_phase_timing": (_i32, [_vp, _i32]),
+    "rnn_get_phase_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _pi64]),
+    "rnn_status_string": (ctypes.c_char_p, [_i32]),
+}
+
+
+class RnnError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s returned %s" % (fn, STATUS.get(code, code)))
+
+
+_lib = None
+
+
+def lib():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("liblayer_rnn.so is not built; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _call(name, *args):
+    code = getattr(lib(), name)(*args)
+    if code != 0:
+        raise RnnError(name, code)
+
+
+def _p(t):
+    """Device pointer of a tensor (or None)."""
+    return None if t is None else t.data_ptr()
+
+
+def rnn_create(mode, num_layers, bidirectional, input_size, hidden_size, dtype, flags=0):
+    h = _vp()
+    _call("rnn_create", ctypes.byref(h), mode, num_layers, int(bidirectional), input_size,
+          hidden_size, dtype, flags)
+    return h
+
+
+def rnn_destroy(h):
+    _call("rnn_destroy", h)
+
+
+def rnn_weight_count(h):
+    n = ctypes.c_int64()
+    _call("rnn_weight_count", h, ctypes.byref(n))
+    return n.value
+
+
+def rnn_weight_layout(h, layer, direction, which):
+    o, r, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _call("rnn_weight_layout", h, layer, direction, which, ctypes.byref(o), ctypes.byref(r),
+          ctypes.byref(c))
+    return o.value, r.value, c.value
+
+
+def rnn_workspace_size(h, T, N):
+    b = ctypes.c_int64()
+    _call("rnn_workspace_size", h, T, N, ctypes.byref(b))
+    return b.value
+
+
+def rnn_workspace_layout(h, T, N, region, layer=0, direction=0):
+    o, b = ctypes.c_int64(), ctypes.c_int64()
+    _call("rnn_workspace_layout", h, T, N, region, layer, direction, ctypes.byref(o),
+          ctypes.byref(b))
+    return o.value, b.value
+
+
+def rnn_forward_training(h, stream, T, N, x, h0, c0, W, y, hy, cy, ws, ws_bytes):
+    _call("rnn_forward_training", h, stream, T, N, x, h0, c0, W, y, hy, cy, ws, ws_bytes)
+
+
+def rnn_forward_inference(h, stream, T, N, x, h0, c0, W, y, hy, cy):
+    _call("rnn_forward_inference", h, stream, T, N, x, h0, c0, W, y, hy, cy)
+
+
+def rnn_backward_data(h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes):
+    _call("rnn_backward_data", h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes)
+
+
+def rnn_backward_weights(h, stream, T, N, x, h0, y, ws, ws_bytes, dW):
+    _call("rnn_backward_weights", h, stream, T, N, x, h0, y, ws, ws_bytes, dW)
+
+
+def rnn_check_status(h, stream):
+    return getattr(lib(), "rnn_check_status")(h, stream)
+
+
+def rnn_set_debug(h, fault_block, fault_step, timeout_ns):
+    _call("rnn_set_debug", h, fault_block, fault_step, timeout_ns)
+
+
+def rnn_enable_phase_timing(h, enable):
+    _call("rnn_enable_phase_timing", h, int(enable))
+
+
+def rnn_get_phase_times(h):
+    ms = (ctypes.c_double * len(PHASES))()
+    n = (ctypes.c_int64 * len(PHASES))()
+    _call("rnn_get_phase_times", h, ms, n)
+    return {p: (ms[i], n[i]) for i, p in enumerate(PHASES)}
+
+
+def rnn_status_string(code):
+    return lib().rnn_status_string(code).decode()
+
+
+class Rnn:
+    """One handle plus torch-tensor marshalling (device memory and streams only)."""
+
+    def __init__(self, mode, num_layers, bidirectional, input_size, hidden_size, dtype="f32",
+                 flags=0):
+        import torch  # memory and streams only
+        self.torch = torch
+        self.mode = mode
+        self.L = num_layers
+        self.D = 2 if bidirectional else 1
+        self.I = input_size
+        self.H = hidden_size
+        self.dtype = dtype
+        self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.h = rnn_create(MODES[mode], num_layers, bidirectional, input_size, hidden_size,
+                            DTYPES[dtype], flags)
+
+    def close(self):
+        if self.h is not None:
+            rnn_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return s.cuda_stream
+
+    def weight_count(self):
+        return rnn_weight_count(self.h)
+
+    def workspace_bytes(self, T, N):
+        return rnn_workspace_size(self.h, T, N)
+
+    def alloc_workspace(self, T, N, device="cuda"):
+        return self.torch.empty(self.workspace_bytes(T, N), dtype=self.torch.uint8, device=device)
+
+    def forward_training(self, x, h0, c0, W, y, hy, cy, ws, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_forward_training(self.h, self._stream(stream), T, N, _p(x), _p(h0), _p(c0), _p(W),
+                             _p(y), _p(hy), _p(cy), _p(ws), ws.numel())
+
+    def forward_inference(self, x, h0, c0, W, y, hy, cy, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_forward_inference(self.h, self._stream(stream), T, N, _p(x), _p(h0), _p(c0), _p(W),
+                              _p(y), _p(hy), _p(cy))
+
+    def backward_data(self, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream=None):
+        T, N = dy.shape[0], dy.shape[1]
+        rnn_backward_data(self.h, self._stream(stream), T, N, _p(W), _p(dy), _p(dhy), _p(dcy),
+                          _p(dx), _p(dh0), _p(dc0), _p(ws), ws.numel())
+
+    def backward_weights(self, x, h0, y, ws, dW, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_backward_weights(self.h, self._stream(stream), T, N, _p(x), _p(h0), _p(y), _p(ws),
+                             ws.numel(), _p(dW))
+
+    def check_status(self, stream=None):
+        return rnn_check_status(self.h, self._stream(stream))

@@ -1,0 +1,655 @@
+// C ABI of liblayer_rnn.so: handle, argument checks, weight and workspace
+// layouts, and the order of the phases of each call.  See include/layer_rnn.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/layer_rnn.h"
+#include "internal.h"
+
+using namespace lr;
+
+struct PhaseMark {
+  int phase;
+  int64_t kernels;
+  cudaEvent_t start, stop;
+};
+
+struct rnn_handle {
+  int mode = 0, L = 1, D = 1, dtype = 0, G = 1, Gs = 1;
+  int64_t I = 0, H = 0;
+  uint32_t flags = 0;
+  // device state, set up by the first compute call
+  int device = -1;
+  int num_sms = 0;
+  size_t smem_optin = 0;
+  unsigned* d_sync = nullptr;  // [512] step flags, then the status word
+  int* d_status = nullptr;
+  void* scratch = nullptr;     // inference scratch
+  size_t scratch_bytes = 0;
+  // debug / failure-detection hook
+  long long timeout_ns = 2000000000LL;
+  int fault_block = -1, fault_step = -1;
+  // phase timing
+  bool timing = false;
+  std::vector<PhaseMark> marks;
+  double ms[RNN_PHASE_NUM] = {0};
+  int64_t launches[RNN_PHASE_NUM] = {0};
+};
+
+namespace {
+
+constexpr size_t kSyncBytes = 4096;
+
+int64_t esize(const rnn_handle* h) { return h->dtype == RNN_BF16 ? 2 : 4; }
+int64_t layer_in(const rnn_handle* h, int l) { return l == 0 ? h->I : h->D * h->H; }
+
+// ----------------------------------------------------------------------------
+// canonical weight layout
+// ----------------------------------------------------------------------------
+int64_t weight_block(const rnn_handle* h, int l) {
+  const int64_t GH = h->G * h->H;
+  return GH * layer_in(h, l) + GH * h->H + 2 * GH;
+}
+
+int64_t weight_count(const rnn_handle* h) {
+  int64_t n = 0;
+  for (int l = 0; l < h->L; ++l) n += h->D * weight_block(h, l);
+  return n;
+}
+
+// element offset of tensor `which` of (l, d)
+int64_t weight_offset(const rnn_handle* h, int l, int d, int which) {
+  int64_t off = 0;
+  for (int k = 0; k < l; ++k) off += h->D * weight_block(h, k);
+  off += d * weight_block(h, l);
+  const int64_t GH = h->G * h->H;
+  const int64_t sizes[4] = {GH * layer_in(h, l), GH * h->H, GH, GH};
+  for (int w = 0; w < which; ++w) off += sizes[w];
+  return off;
+}
+
+// ----------------------------------------------------------------------------
+// workspace layout
+// ----------------------------------------------------------------------------
+struct Region {
+  int64_t off = 0, bytes = 0;
+};
+
+struct WsLayout {
+  std::vector<Region> r;  // indexed [region][l][d]
+  int L = 0, D = 0;
+  int64_t total = 0;
+  Region& at(int region, int l, int d) { return r[((size_t)region * L + l) * D + d]; }
+};
+
+int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
+
+WsLayout ws_layout(const rnn_handle* h, int64_t T, int64_t N) {
+  WsLayout w;
+  w.L = h->L;
+  w.D = h->D;
+  w.r.assign((size_t)RNN_WS_NUM_REGIONS * h->L * h->D, Region());
+  const int64_t e = esize(h), H = h->H, G = h->G, D = h->D;
+  int64_t off = 0;
+  auto put = [&](int region, int l, int d, int64_t bytes) {
+    Region& R = w.at(region, l, d);
+    R.off = bytes > 0 ? off : 0;
+    R.bytes = bytes;
+    off += align256(bytes);
+  };
+  for (int l = 0; l < h->L; ++l)
+    for (int d = 0; d < h->D; ++d) {
+      put(RNN_WS_GATES, l, d, T * N * h->Gs * H * 4);
+      put(RNN_WS_CSEQ, l, d, h->mode == RNN_LSTM ? (T + 1) * N * H * 4 : 0);
+      put(RNN_WS_HSEQ, l, d, (T + 1) * N * H * e);
+      put(RNN_WS_DGX, l, d, T * N * G * H * e);
+      put(RNN_WS_DGH, l, d, h->mode == RNN_GRU ? T * N * G * H * e : 0);
+    }
+  for (int l = 0; l < h->L; ++l) put(RNN_WS_YLAYER, l, 0, l < h->L - 1 ? T * N * D * H * e : 0);
+  put(RNN_WS_GX, 0, 0, D * T * N * G * H * 4);
+  put(RNN_WS_DY, 0, 0, h->L > 1 ? 2 * T * N * D * H * 4 : 0);
+  w.total = off;
+  return w;
+}
+
+// ----------------------------------------------------------------------------
+// checks and device set-up
+// ----------------------------------------------------------------------------
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+rnn_status_t check_sizes(const rnn_handle* h, int64_t T, int64_t N) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  if (T < 1 || N < 1) return RNN_ERR_INVALID_ARG;
+  if (T > (1 << 24) || N > (1 << 20)) return RNN_ERR_UNSUPPORTED;
+  // 32-bit index products inside the kernels
+  if (T * N * std::max<int64_t>(h->G * h->H * 4, std::max(h->I, h->D * h->H)) > (int64_t(1) << 31))
+    return RNN_ERR_UNSUPPORTED;
+  return RNN_OK;
+}
+
+rnn_status_t device_setup(rnn_handle* h) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
+  if (h->device == dev && h->d_sync) return RNN_OK;
+  if (h->device >= 0 && h->device != dev) return RNN_ERR_INVALID_ARG;  // one device per handle
+  int sms = 0, optin = 0, coop = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+    return RNN_ERR_CUDA;
+  if (!coop) return RNN_ERR_UNSUPPORTED;
+  void* p = nullptr;
+  if (cudaMalloc(&p, kSyncBytes) != cudaSuccess) return RNN_ERR_CUDA;
+  if (cudaMemset(p, 0, kSyncBytes) != cudaSuccess) {
+    cudaFree(p);
+    return RNN_ERR_CUDA;
+  }
+  h->d_sync = static_cast<unsigned*>(p);
+  h->d_status = reinterpret_cast<int*>(static_cast<char*>(p) + kSyncBytes - 64);
+  h->device = dev;
+  h->num_sms = sms;
+  h->smem_optin = (size_t)optin;
+  return RNN_OK;
+}
+
+rnn_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RNN_OK;
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return RNN_ERR_NO_RESIDENCY;
+  }
+  return RNN_ERR_CUDA;
+}
+
+rnn_status_t read_status(rnn_handle* h, cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RNN_ERR_CUDA;
+  if (!h->d_status) return RNN_OK;
+  int v = 0;
+  if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RNN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(h->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return RNN_ERR_CUDA;
+  }
+  return (rnn_status_t)v;
+}
+
+rnn_status_t finish(rnn_handle* h, cudaStream_t st, rnn_status_t s) {
+  if (s != RNN_OK) return s;
+  if (h->flags & RNN_FLAG_SYNC_CHECK) return read_status(h, st);
+  return RNN_OK;
+}
+
+// phase timing helpers
+struct PhaseScope {
+  rnn_handle* h;
+  cudaStream_t st;
+  PhaseMark m;
+  bool on;
+  PhaseScope(rnn_handle* hh, cudaStream_t s, int phase) : h(hh), st(s), on(hh->timing) {
+    if (!on) return;
+    m.phase = phase;
+    m.kernels = g_kernel_launches.load();
+    cudaEventCreate(&m.start);
+    cudaEventCreate(&m.stop);
+    cudaEventRecord(m.start, st);
+  }
+  ~PhaseScope() {
+    if (!on) return;
+    cudaEventRecord(m.stop, st);
+    m.kernels = g_kernel_launches.load() - m.kernels;
+    h->marks.push_back(m);
+  }
+};
+
+rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
+  if (!rec_make_plan(backward, h->mode, h->dtype == RNN_BF16, h->D, (int)h->H, (int)N, h->num_sms,
+                     h->smem_optin, pl))
+    return RNN_ERR_UNSUPPORTED;
+  if (pl->P * h->D > h->num_sms) return RNN_ERR_NO_RESIDENCY;
+  return RNN_OK;
+}
+
+void fill_rec_common(rnn_handle* h, int64_t T, int64_t N, RecParams* rp) {
+  rp->mode = h->mode;
+  rp->T = (int)T;
+  rp->N = (int)N;
+  rp->H = (int)h->H;
+  rp->G = h->G;
+  rp->Gs = h->Gs;
+  rp->D = h->D;
+  rp->bf16 = h->dtype == RNN_BF16;
+  rp->flags = h->d_sync;
+  rp->status = h->d_status;
+  rp->timeout_ns = h->timeout_ns;
+  rp->fault_block = h->fault_block;
+  rp->fault_step = h->fault_step;
+}
+
+template <typename P>
+const P* cp(const void* base, int64_t byte_off) {
+  return reinterpret_cast<const P*>(static_cast<const char*>(base) + byte_off);
+}
+template <typename P>
+P* mp(void* base, int64_t byte_off) {
+  return reinterpret_cast<P*>(static_cast<char*>(base) + byte_off);
+}
+
+// G_x[d] = in W_ih[l,d]^T + b_ih + b_hh (GRU: b_hn stays in the recurrence)
+rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, int64_t N,
+                              const void* in, const void* W, float* gx) {
+  const int64_t e = esize(h), GH = h->G * h->H, I_l = layer_in(h, l);
+  for (int d = 0; d < h->D; ++d) {
+    GemmArgs g;
+    g.M = T * N; g.N = GH; g.K = I_l;
+    g.A = in; g.sam = I_l; g.sak = 1;
+    g.B = cp<char>(W, weight_offset(h, l, d, 0) * e); g.sbk = 1; g.sbn = I_l;
+    g.C = gx + (int64_t)d * T * N * GH; g.ldc = GH;
+    g.bias1 = cp<char>(W, weight_offset(h, l, d, 2) * e);
+    g.bias2 = cp<char>(W, weight_offset(h, l, d, 3) * e);
+    g.bias2_limit = h->mode == RNN_GRU ? 2 * h->H : GH;
+    g.in_bf16 = g.bias_bf16 = h->dtype == RNN_BF16;
+    g.out_bf16 = 0;
+    if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+  }
+  return RNN_OK;
+}
+
+rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, const void* x,
+                          const void* h0, const void* c0, const void* W, void* y, void* hy,
+                          void* cy, char* ws, bool training) {
+  const int64_t e = esize(h), H = h->H, NH = N * H;
+  WsLayout lay = ws_layout(h, T, N);
+  float* gx;
+  void* ybuf[2] = {nullptr, nullptr};
+  if (training) {
+    gx = mp<float>(ws, lay.at(RNN_WS_GX, 0, 0).off);
+  } else {
+    gx = static_cast<float*>(h->scratch);
+    const int64_t gx_bytes = align256(h->D * T * N * h->G * H * 4);
+    const int64_t yb = align256(T * N * h->D * H * e);
+    ybuf[0] = mp<char>(h->scratch, gx_bytes);
+    ybuf[1] = mp<char>(h->scratch, gx_bytes + yb);
+  }
+  RecPlan plan;
+  rnn_status_t s = plan_rec(h, false, N, &plan);
+  if (s != RNN_OK) return s;
+  const void* in = x;
+  for (int l = 0; l < h->L; ++l) {
+    void* out;
+    if (l == h->L - 1) out = y;
+    else if (training) out = mp<char>(ws, lay.at(RNN_WS_YLAYER, l, 0).off);
+    else out = ybuf[l & 1];
+    {
+      PhaseScope ps(h, st, RNN_PHASE_INPUT_GEMM);
+      s = input_projection(h, st, l, T, N, in, W, gx);
+      if (s != RNN_OK) return s;
+    }
+    RecParams rp;
+    fill_rec_common(h, T, N, &rp);
+    rp.plan = plan;
+    rp.ldy = h->D * H;
+    for (int d = 0; d < h->D; ++d) {
+      RecDirArgs& a = rp.dir[d];
+      const int k = l * h->D + d;
+      a.gx = gx + (int64_t)d * T * N * h->G * H;
+      a.whh = cp<char>(W, weight_offset(h, l, d, 1) * e);
+      a.bhh = cp<char>(W, weight_offset(h, l, d, 3) * e);
+      a.h0 = h0 ? cp<char>(h0, k * NH * e) : nullptr;
+      a.c0 = (c0 && h->mode == RNN_LSTM) ? cp<float>(c0, k * NH * 4) : nullptr;
+      a.y = out;
+      a.hy = hy ? mp<char>(hy, k * NH * e) : nullptr;
+      a.cy = (cy && h->mode == RNN_LSTM) ? mp<float>(cy, k * NH * 4) : nullptr;
+      if (training) {
+        a.hseq = mp<char>(ws, lay.at(RNN_WS_HSEQ, l, d).off);
+        a.gates = mp<float>(ws, lay.at(RNN_WS_GATES, l, d).off);
+        a.cseq = h->mode == RNN_LSTM ? mp<float>(ws, lay.at(RNN_WS_CSEQ, l, d).off) : nullptr;
+      }
+    }
+    {
+      PhaseScope ps(h, st, RNN_PHASE_REC_FWD);
+      s = cuda_status(rec_forward(rp, st));
+      if (s != RNN_OK) return s;
+    }
+    in = out;
+  }
+  return RNN_OK;
+}
+
+
+}  // namespace
+
+// ============================================================================
+// exported
+// ============================================================================
+extern "C" {
+
+rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
+                        int64_t input_size, int64_t hidden_size, int dtype, uint32_t flags) {
+  if (!out) return RNN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (mode < RNN_TANH || mode > RNN_GRU) return RNN_ERR_INVALID_ARG;
+  if (num_layers < 1 || (bidirectional != 0 && bidirectional != 1)) return RNN_ERR_INVALID_ARG;
+  if (input_size < 1 || hidden_size < 1) return RNN_ERR_INVALID_ARG;
+  if (dtype != RNN_F32 && dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
+  if ((flags & ~(RNN_FLAG_SYNC_CHECK | RNN_FLAG_SIMT_GEMM)) != 0) return RNN_ERR_INVALID_ARG;
+  if (hidden_size > 65536 || input_size > (int64_t(1) << 24) || num_layers > 1024)
+    return RNN_ERR_UNSUPPORTED;
+  rnn_handle* h = new (std::nothrow) rnn_handle();
+  if (!h) return RNN_ERR_INVALID_ARG;
+  h->mode = mode;
+  h->L = num_layers;
+  h->D = bidirectional ? 2 : 1;
+  h->I = input_size;
+  h->H = hidden_size;
+  h->dtype = dtype;
+  h->flags = flags;
+  h->G = mode == RNN_LSTM ? 4 : mode == RNN_GRU ? 3 : 1;
+  h->Gs = mode == RNN_TANH ? 1 : 4;
+  *out = h;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_destroy(rnn_t h) {
+  if (!h) return RNN_OK;
+  for (auto& m : h->marks) {
+    cudaEventDestroy(m.start);
+    cudaEventDestroy(m.stop);
+  }
+  if (h->d_sync) cudaFree(h->d_sync);
+  if (h->scratch) cudaFree(h->scratch);
+  delete h;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_weight_count(rnn_t h, int64_t* n) {
+  if (!h || !n) return RNN_ERR_INVALID_ARG;
+  *n = weight_count(h);
+  return RNN_OK;
+}
+
+rnn_status_t rnn_weight_layout(rnn_t h, int layer, int dir, int which, int64_t* offset,
+                               int64_t* rows, int64_t* cols) {
+  if (!h || !offset || !rows || !cols) return RNN_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L || dir < 0 || dir >= h->D || which < 0 || which > 3)
+    return RNN_ERR_INVALID_ARG;
+  *offset = weight_offset(h, layer, dir, which);
+  *rows = h->G * h->H;
+  *cols = which == 0 ? layer_in(h, layer) : which == 1 ? h->H : 1;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_workspace_size(rnn_t h, int64_t T, int64_t N, int64_t* bytes) {
+  if (!bytes) return RNN_ERR_INVALID_ARG;
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  *bytes = ws_layout(h, T, N).total;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_workspace_layout(rnn_t h, int64_t T, int64_t N, int region, int layer, int dir,
+                                  int64_t* offset, int64_t* bytes) {
+  if (!offset || !bytes) return RNN_ERR_INVALID_ARG;
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (region < 0 || region >= RNN_WS_NUM_REGIONS) return RNN_ERR_INVALID_ARG;
+  const bool per_layer = region == RNN_WS_YLAYER;
+  const bool global = region == RNN_WS_GX || region == RNN_WS_DY;
+  if (global) layer = 0;
+  if (global || per_layer) dir = 0;
+  if (layer < 0 || layer >= h->L || dir < 0 || dir >= h->D) return RNN_ERR_INVALID_ARG;
+  WsLayout w = ws_layout(h, T, N);
+  *offset = w.at(region, layer, dir).off;
+  *bytes = w.at(region, layer, dir).bytes;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
+                                  const void* h0, const void* c0, const void* W, void* y,
+                                  void* hy, void* cy, void* workspace, int64_t ws_bytes) {
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (!x || !W || !y || !workspace) return RNN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 16) || !aligned(h0, 16) ||
+      !aligned(c0, 16) || !aligned(hy, 16) || !aligned(cy, 16) || !aligned(workspace, 256))
+    return RNN_ERR_MISALIGNED;
+  if (ws_bytes < ws_layout(h, T, N).total) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  s = device_setup(h);
+  if (s != RNN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true);
+  return finish(h, st, s);
+}
+
+rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
+                                   const void* h0, const void* c0, const void* W, void* y,
+                                   void* hy, void* cy) {
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (!x || !W || !y) return RNN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 16) || !aligned(h0, 16) ||
+      !aligned(c0, 16) || !aligned(hy, 16) || !aligned(cy, 16))
+    return RNN_ERR_MISALIGNED;
+  s = device_setup(h);
+  if (s != RNN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = (size_t)(align256(h->D * T * N * h->G * h->H * 4) +
+                               2 * align256(T * N * h->D * h->H * esize(h)));
+  if (need > h->scratch_bytes) {
+    // the old scratch may still be in use by earlier work on the stream
+    if (h->scratch) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return RNN_ERR_CUDA;
+      cudaFree(h->scratch);
+      h->scratch = nullptr;
+      h->scratch_bytes = 0;
+    }
+    if (cudaMalloc(&h->scratch, need) != cudaSuccess) {
+      h->scratch = nullptr;
+      return RNN_ERR_CUDA;
+    }
+    h->scratch_bytes = need;
+  }
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false);
+  return finish(h, st, s);
+}
+
+rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, const void* W,
+                               const void* dy, const void* dhy, const void* dcy, void* dx,
+                               void* dh0, void* dc0, void* workspace, int64_t ws_bytes) {
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (!W || !dy || !dx || !workspace) return RNN_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(dy, 16) || !aligned(dx, 16) || !aligned(dhy, 16) ||
+      !aligned(dcy, 16) || !aligned(dh0, 16) || !aligned(dc0, 16) || !aligned(workspace, 256))
+    return RNN_ERR_MISALIGNED;
+  WsLayout lay = ws_layout(h, T, N);
+  if (ws_bytes < lay.total) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  s = device_setup(h);
+  if (s != RNN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int64_t e = esize(h), H = h->H, NH = N * H, GH = h->G * H;
+  const bool bf = h->dtype == RNN_BF16;
+  RecPlan plan;
+  s = plan_rec(h, true, N, &plan);
+  if (s != RNN_OK) return finish(h, st, s);
+  const void* dcur = dy;
+  int dcur_bf16 = bf;
+  for (int l = h->L - 1; l >= 0; --l) {
+    RecParams rp;
+    fill_rec_common(h, T, N, &rp);
+    rp.plan = plan;
+    rp.ldy = h->D * H;
+    rp.lddy = h->D * H;
+    for (int d = 0; d < h->D; ++d) {
+      RecDirArgs& a = rp.dir[d];
+      const int k = l * h->D + d;
+      a.whh = cp<char>(W, weight_offset(h, l, d, 1) * e);
+      a.gates = mp<float>(ws, lay.at(RNN_WS_GATES, l, d).off);
+      a.cseq = h->mode == RNN_LSTM ? mp<float>(ws, lay.at(RNN_WS_CSEQ, l, d).off) : nullptr;
+      a.hseq = mp<char>(ws, lay.at(RNN_WS_HSEQ, l, d).off);
+      a.dy = dcur;
+      a.dy_bf16 = dcur_bf16;
+      a.dhy = dhy ? cp<char>(dhy, k * NH * e) : nullptr;
+      a.dcy = (dcy && h->mode == RNN_LSTM) ? cp<float>(dcy, k * NH * 4) : nullptr;
+      a.dgx = mp<char>(ws, lay.at(RNN_WS_DGX, l, d).off);
+      a.dgh = h->mode == RNN_GRU ? mp<char>(ws, lay.at(RNN_WS_DGH, l, d).off) : a.dgx;
+      a.dh0 = dh0 ? mp<char>(dh0, k * NH * e) : nullptr;
+      a.dc0 = (dc0 && h->mode == RNN_LSTM) ? mp<float>(dc0, k * NH * 4) : nullptr;
+    }
+    {
+      PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
+      s = cuda_status(rec_backward(rp, st));
+      if (s != RNN_OK) return finish(h, st, s);
+    }
+    // dX = sum_d dG_x[d] W_ih[l,d]; for l > 0 it is dy of the layer below
+    const int64_t I_l = layer_in(h, l);
+    void* target;
+    int target_bf16;
+    if (l == 0) {
+      target = dx;
+      target_bf16 = bf;
+    } else {
+      target = mp<char>(ws, lay.at(RNN_WS_DY, 0, 0).off + (int64_t)((l - 1) & 1) * T * N * h->D * H * 4);
+      target_bf16 = 0;
+    }
+    GemmArgs g;
+    g.M = T * N; g.N = I_l; g.K = GH;
+    g.A = rp.dir[0].dgx; g.sam = GH; g.sak = 1;
+    g.B = cp<char>(W, weight_offset(h, l, 0, 0) * e); g.sbk = I_l; g.sbn = 1;
+    if (h->D == 2) {
+      g.K2 = GH;
+      g.A2 = rp.dir[1].dgx; g.sam2 = GH; g.sak2 = 1;
+      g.B2 = cp<char>(W, weight_offset(h, l, 1, 0) * e); g.sbk2 = I_l; g.sbn2 = 1;
+    }
+    g.C = target; g.ldc = I_l;
+    g.in_bf16 = bf;
+    g.out_bf16 = target_bf16;
+    {
+      PhaseScope ps(h, st, RNN_PHASE_DX_GEMM);
+      if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+    }
+    dcur = target;
+    dcur_bf16 = target_bf16;
+  }
+  return finish(h, st, RNN_OK);
+}
+
+rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
+                                  const void* h0, const void* y, const void* workspace,
+                                  int64_t ws_bytes, void* dW) {
+  (void)h0;
+  (void)y;
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (!x || !workspace || !dW) return RNN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(dW, 16) || !aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
+  WsLayout lay = ws_layout(h, T, N);
+  if (ws_bytes < lay.total) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  s = device_setup(h);
+  if (s != RNN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* ws = static_cast<const char*>(workspace);
+  const int64_t e = esize(h), H = h->H, GH = h->G * H;
+  const bool bf = h->dtype == RNN_BF16;
+  PhaseScope ps(h, st, RNN_PHASE_DW_GEMM);
+  for (int l = 0; l < h->L; ++l) {
+    const int64_t I_l = layer_in(h, l);
+    const void* in = l == 0 ? x : static_cast<const void*>(ws + lay.at(RNN_WS_YLAYER, l - 1, 0).off);
+    for (int d = 0; d < h->D; ++d) {
+      const void* dgx = ws + lay.at(RNN_WS_DGX, l, d).off;
+      const void* dgh = h->mode == RNN_GRU ? ws + lay.at(RNN_WS_DGH, l, d).off : dgx;
+      const char* hseq = ws + lay.at(RNN_WS_HSEQ, l, d).off;
+      const void* hprev = hseq + (d == 1 ? N * H * e : 0);
+      GemmArgs g;
+      g.M = GH; g.N = I_l; g.K = T * N;
+      g.A = dgx; g.sam = 1; g.sak = GH;
+      g.B = in; g.sbk = I_l; g.sbn = 1;
+      g.C = mp<char>(dW, weight_offset(h, l, d, 0) * e); g.ldc = I_l;
+      g.in_bf16 = bf; g.out_bf16 = bf;
+      if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+      GemmArgs g2;
+      g2.M = GH; g2.N = H; g2.K = T * N;
+      g2.A = dgh; g2.sam = 1; g2.sak = GH;
+      g2.B = hprev; g2.sbk = H; g2.sbn = 1;
+      g2.C = mp<char>(dW, weight_offset(h, l, d, 1) * e); g2.ldc = H;
+      g2.in_bf16 = bf; g2.out_bf16 = bf;
+      if (gemm_simt(g2, st) != cudaSuccess) return RNN_ERR_CUDA;
+      if (colsum(mp<char>(dW, weight_offset(h, l, d, 2) * e), bf, dgx, bf, T * N, GH, GH, st) !=
+              cudaSuccess ||
+          colsum(mp<char>(dW, weight_offset(h, l, d, 3) * e), bf, dgh, bf, T * N, GH, GH, st) !=
+              cudaSuccess)
+        return RNN_ERR_CUDA;
+    }
+  }
+  return finish(h, st, RNN_OK);
+}
+
+rnn_status_t rnn_check_status(rnn_t h, void* stream) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  return read_status(h, static_cast<cudaStream_t>(stream));
+}
+
+rnn_status_t rnn_set_debug(rnn_t h, int fault_block, int fault_step, int64_t timeout_ns) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  if (timeout_ns > 0) h->timeout_ns = timeout_ns;
+  h->fault_block = fault_block;
+  h->fault_step = fault_step;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_enable_phase_timing(rnn_t h, int enable) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  for (auto& m : h->marks) {
+    cudaEventDestroy(m.start);
+    cudaEventDestroy(m.stop);
+  }
+  h->marks.clear();
+  for (int i = 0; i < RNN_PHASE_NUM; ++i) {
+    h->ms[i] = 0;
+    h->launches[i] = 0;
+  }
+  h->timing = enable != 0;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_get_phase_times(rnn_t h, double* ms, int64_t* launches) {
+  if (!h || !ms || !launches) return RNN_ERR_INVALID_ARG;
+  for (auto& m : h->marks) {
+    if (cudaEventSynchronize(m.stop) != cudaSuccess) return RNN_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, m.start, m.stop) != cudaSuccess) return RNN_ERR_CUDA;
+    h->ms[m.phase] += t;
+    h->launches[m.phase] += m.kernels;
+    cudaEventDestroy(m.start);
+    cudaEventDestroy(m.stop);
+  }
+  h->marks.clear();
+  for (int i = 0; i < RNN_PHASE_NUM; ++i) {
+    ms[i] = h->ms[i];
+    launches[i] = h->launches[i];
+  }
+  return RNN_OK;
+}
+
+const char* rnn_status_string(rnn_status_t s) {
+  switch (s) {
+    case RNN_OK: return "ok";
+    case RNN_ERR_INVALID_ARG: return "invalid argument";
+    case RNN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RNN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case RNN_ERR_MISALIGNED: return "misaligned pointer";
+    case RNN_ERR_CUDA: return "CUDA runtime error";
+    case RNN_ERR_TIMEOUT: return "step barrier timed out";
+    case RNN_ERR_NO_RESIDENCY: return "persistent grid cannot be co-resident";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Host-side declarations shared by the translation units of liblayer_rnn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace lr {
+
+// kernels launched by this library (all handles, all threads); the phase
+// timing of a handle reports its share per phase
+extern std::atomic<int64_t> g_kernel_launches;
+
+// ---------------------------------------------------------------------------
+// dense phases: C[M, N] (+)= A[M, K] B[K, N] (+ A2 B2) + bias
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  int64_t M = 0, N = 0, K = 0;
+  const void* A = nullptr; int64_t sam = 0, sak = 0;   // A(m, k) = A[m*sam + k*sak]
+  const void* B = nullptr; int64_t sbk = 0, sbn = 0;   // B(k, n) = B[k*sbk + n*sbn]
+  // optional second product over K2 accumulated into the same result
+  int64_t K2 = 0;
+  const void* A2 = nullptr; int64_t sam2 = 0, sak2 = 0;
+  const void* B2 = nullptr; int64_t sbk2 = 0, sbn2 = 0;
+  void* C = nullptr; int64_t ldc = 0;                  // C(m, n) = C[m*ldc + n]
+  const void* bias1 = nullptr;                         // + bias1[n]
+  const void* bias2 = nullptr; int64_t bias2_limit = 0;  // + bias2[n] for n < limit
+  int in_bf16 = 0;    // A, B (and A2, B2) element type
+  int out_bf16 = 0;   // C element type
+  int bias_bf16 = 0;  // bias element type
+  int accumulate = 0; // C += result instead of C = result
+};
+
+cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
+
+// column sums: dst[c] = sum_r src[r*ld + c], r < rows (fp32 accumulate, fixed order)
+cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16,
+                   int64_t rows, int64_t cols, int64_t ld, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// persistent recurrent kernels
+// ---------------------------------------------------------------------------
+struct RecDirArgs {
+  // forward
+  const float* gx = nullptr;     // [T][N][G*H] input projection + folded biases
+  const void* whh = nullptr;     // canonical W_hh [G*H][H]
+  const void* bhh = nullptr;     // canonical b_hh [G*H] (GRU: its n block is used)
+  const void* h0 = nullptr;      // [N][H] or null (zeros)
+  const float* c0 = nullptr;     // [N][H] or null (zeros)
+  void* y = nullptr;             // layer output, row (t*N+n)*ldy, column d*H + j
+  void* hseq = nullptr;          // [T+1][N][H] or null
+  float* gates = nullptr;        // [T][N][Gs*H] or null
+  float* cseq = nullptr;         // [T+1][N][H] or null
+  void* hy = nullptr;            // [N][H] or null
+  float* cy = nullptr;           // [N][H] or null
+  // backward
+  const void* dy = nullptr;      // row (t*N+n)*lddy, column d*H + j
+  int dy_bf16 = 0;
+  const void* dhy = nullptr;     // [N][H] or null
+  const float* dcy = nullptr;    // [N][H] or null
+  void* dgx = nullptr;           // [T][N][G*H] (compute type)
+  void* dgh = nullptr;           // [T][N][G*H] (compute type), == dgx unless GRU
+  void* dh0 = nullptr;           // [N][H] or null
+  float* dc0 = nullptr;          // [N][H] or null
+};
+
+struct RecPlan {
+  int shape = 0;        // register-tile shape id (see recurrent.cu)
+  int P = 0;            // blocks per direction
+  int U = 0;            // hidden units per block (last block may have fewer)
+  int Mloc = 0, Mp = 0; // rows of the resident operand, padded to the tile
+  int K = 0, lda = 0;   // contraction length, smem row stride (elements)
+  int nb = 0, nbp = 0;  // batch chunk and its padded size
+  int KC = 0, ldb = 0;  // K chunk of the staged operand, its smem row stride
+  int tiles_m = 0, tiles_n = 0, WK = 0;
+  size_t smem = 0;
+};
+
+struct RecParams {
+  int mode = 0, T = 0, N = 0, H = 0, G = 0, Gs = 0, D = 1;
+  int bf16 = 0;
+  int64_t ldy = 0, lddy = 0;
+  RecPlan plan;
+  unsigned* flags = nullptr;   // [D][P] step flags, zeroed before the launch
+  int* status = nullptr;
+  long long timeout_ns = 0;
+  int fault_block = -1, fault_step = -1;
+  RecDirArgs dir[2];
+};
+
+// Choose the tiling for the forward (backward = false) or backward kernel.
+// Returns false when no supported tiling fits in shared memory.
+bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
+                   size_t smem_limit, RecPlan* out);
+
+// Launch (cooperative, so the whole grid is co-resident).  Zeroes the flags
+// on the stream first.
+cudaError_t rec_forward(const RecParams& p, cudaStream_t st);
+cudaError_t rec_backward(const RecParams& p, cudaStream_t st);
+
+}  // namespace lr

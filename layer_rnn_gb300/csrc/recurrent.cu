@@ -1,0 +1,540 @@
+// Persistent recurrent kernels: the serial time loop of one layer (both
+// directions of a bidirectional layer in the same launch, on disjoint blocks).
+//
+// Design (the persistent-RNN idea of the TVM "Persist RNN Implementation"
+// thread: recurrent weights stay on chip across time steps, one launch per
+// sequence):
+//   * every block owns U consecutive hidden units j0 .. j0+U-1 of one
+//     direction and keeps, for the whole launch, the slice of W_hh it needs in
+//     shared memory:
+//       forward : the G*U gate rows of those units (rows ordered g*U + u), so
+//                 all gates of a unit land in the same block and the gate
+//                 nonlinearities, the cell update and the workspace stores are
+//                 fused behind the contraction ("fused point-wise operations"
+//                 of the cuDNN optimisation table quoted in Keras issue #3692);
+//       backward: the U columns of W_hh (stored transposed), so that
+//                 dh_{t-1}[j] = sum_r dG_h[r] W_hh[r][j] is local to the block;
+//   * per step each block stages the previous step's broadcast vector (h_{t-1}
+//     in forward, dG_h of the previous step in backward; written by all blocks)
+//     from L2 into shared memory, contracts it with its resident slice on the
+//     CUDA cores (fp32 FMA, register-tiled), applies the fused pointwise math
+//     for its units and stores its slice of the next broadcast vector;
+//   * blocks of a direction meet at a bounded step barrier (flags in global
+//     memory), see common.cuh.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lr {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+// register-tile shapes: RM x RN outputs per lane, lanes LM (rows) x LN (batch)
+// x LK (split of K inside the warp, LK = 32 / (LM*LN))
+struct Shape { int RM, RN, LM, LN; };
+constexpr Shape kShapes[4] = {{3, 5, 8, 4}, {4, 4, 8, 4}, {3, 5, 2, 4}, {4, 4, 2, 4}};
+constexpr int kNumShapes = 4;
+
+__device__ __forceinline__ float lane_f32(const uint4& v, int e) {
+  const unsigned w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+  return __uint_as_float(w);
+}
+__device__ __forceinline__ float lane_bf16(const uint4& v, int e) {
+  const int q = e >> 1;
+  const unsigned w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// acc[i][j] += sum over this lane's 16-byte K vectors of A[lm + LM*i][k] * B[ln + LN*j][k]
+template <typename T, int RM, int RN, int LM, int LN>
+__device__ __forceinline__ void warp_tile_fma(float (&acc)[RM][RN], const T* As, int lda,
+                                              const T* Bs, int ldb, int v_begin, int v_end,
+                                              int lane) {
+  constexpr int LK = 32 / (LM * LN);
+  constexpr int VK = 16 / (int)sizeof(T);
+  const int lm = lane % LM, ln = (lane / LM) % LN, kl = lane / (LM * LN);
+  const T* a0 = As + lm * lda;
+  const T* b0 = Bs + ln * ldb;
+  for (int v = v_begin + kl; v < v_end; v += LK) {
+    uint4 av[RM], bv[RN];
+#pragma unroll
+    for (int i = 0; i < RM; ++i) av[i] = *reinterpret_cast<const uint4*>(a0 + (LM * i) * lda + v * VK);
+#pragma unroll
+    for (int j = 0; j < RN; ++j) bv[j] = *reinterpret_cast<const uint4*>(b0 + (LN * j) * ldb + v * VK);
+#pragma unroll
+    for (int e = 0; e < VK; ++e) {
+      float af[RM], bf[RN];
+#pragma unroll
+      for (int i = 0; i < RM; ++i) af[i] = sizeof(T) == 4 ? lane_f32(av[i], e) : lane_bf16(av[i], e);
+#pragma unroll
+      for (int j = 0; j < RN; ++j) bf[j] = sizeof(T) == 4 ? lane_f32(bv[j], e) : lane_bf16(bv[j], e);
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
+    }
+  }
+}
+
+// copy rows x cols elements (row stride lds) from global into shared (row stride
+// ldd); src == nullptr writes zeros.  Uses 16-byte cp.async when `vec` says every
+// row start is 16-byte aligned on both sides.
+template <typename T>
+__device__ __forceinline__ void stage_rows(T* dst, int ldd, const T* src, int64_t lds,
+                                           int rows, int cols, bool vec) {
+  const int tid = threadIdx.x;
+  if (src == nullptr) {
+    for (int idx = tid; idx < rows * cols; idx += kThreads) {
+      const int r = idx / cols, c = idx - r * cols;
+      dst[r * ldd + c] = from_f<T>(0.f);
+    }
+    return;
+  }
+  constexpr int VE = 16 / (int)sizeof(T);
+  int done = 0;
+  if (vec) {
+    const int cv = cols / VE;
+    for (int idx = tid; idx < rows * cv; idx += kThreads) {
+      const int r = idx / cv, c = idx - r * cv;
+      cp_async16(dst + r * ldd + c * VE, src + r * lds + c * VE);
+    }
+    cp_async_commit();
+    done = cv * VE;
+  }
+  const int rest = cols - done;
+  if (rest > 0) {
+    for (int idx = tid; idx < rows * rest; idx += kThreads) {
+      const int r = idx / rest, c = done + (idx - r * rest);
+      dst[r * ldd + c] = from_f<T>(ldcg_f(src + r * lds + c));
+    }
+  }
+  if (vec) cp_async_wait_all();
+}
+
+// Reduce the per-warp register tiles (intra-warp over the LK lanes, then over
+// the WK warps of each tile in a fixed order) into outs[m * nbp + n].
+template <int RM, int RN, int LM, int LN>
+__device__ __forceinline__ void reduce_tiles(float (&acc)[RM][RN], float* red, float* outs,
+                                             const RecPlan& pl, bool active, int warp, int lane) {
+  constexpr int TE = RM * RN * LM * LN;
+#pragma unroll
+  for (int off = LM * LN; off < 32; off <<= 1)
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+      for (int j = 0; j < RN; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], off);
+  const int lm = lane % LM, ln = (lane / LM) % LN, kl = lane / (LM * LN);
+  if (active && kl == 0) {
+    float* r = red + warp * TE;
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+      for (int j = 0; j < RN; ++j) r[(i * RN + j) * (LM * LN) + ln * LM + lm] = acc[i][j];
+  }
+  __syncthreads();
+  const int ntile = pl.tiles_m * pl.tiles_n;
+  for (int idx = threadIdx.x; idx < ntile * TE; idx += kThreads) {
+    const int tl = idx / TE, e = idx - tl * TE;
+    float sum = 0.f;
+    for (int w = 0; w < pl.WK; ++w) sum += red[(tl * pl.WK + w) * TE + e];
+    const int ij = e / (LM * LN), lp = e - ij * (LM * LN);
+    const int i = ij / RN, j = ij - i * RN;
+    const int m = (tl / pl.tiles_n) * (LM * RM) + (lp % LM) + LM * i;
+    const int n = (tl % pl.tiles_n) * (LN * RN) + (lp / LM) + LN * j;
+    outs[m * pl.nbp + n] = sum;
+  }
+  __syncthreads();
+}
+
+struct Smem {
+  void* A; void* B; float* red; float* outs; float* st0; float* st1;
+};
+
+template <typename T, int RM, int RN, int LM, int LN>
+__device__ __forceinline__ Smem carve(unsigned char* smem, const RecPlan& pl, int N) {
+  Smem s;
+  T* A = reinterpret_cast<T*>(smem);
+  T* B = A + (size_t)pl.Mp * pl.lda;
+  s.A = A;
+  s.B = B;
+  s.red = reinterpret_cast<float*>(B + (size_t)pl.nbp * pl.ldb);
+  s.outs = s.red + kWarps * RM * RN * LM * LN;
+  s.st0 = s.outs + (size_t)pl.Mp * pl.nbp;
+  s.st1 = s.st0 + (size_t)pl.U * N;
+  return s;
+}
+
+// One batch chunk of the per-step contraction: outs[m][n] = sum_k A[m][k] B[n][k]
+// with B[n][k] = src[(n0 + n) * lds + k] (src == nullptr: zeros).
+template <typename T, int RM, int RN, int LM, int LN>
+__device__ __forceinline__ void step_contract(const Smem& sm, const RecPlan& pl, const T* src,
+                                              int64_t lds, int nbc, bool vec) {
+  constexpr int VK = 16 / (int)sizeof(T);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ntile = pl.tiles_m * pl.tiles_n;
+  const int tile = warp / pl.WK, wk = warp - tile * pl.WK;
+  const bool active = tile < ntile;
+  const int tm = active ? tile / pl.tiles_n : 0, tn = active ? tile % pl.tiles_n : 0;
+  const T* As = reinterpret_cast<const T*>(sm.A);
+  T* Bs = reinterpret_cast<T*>(sm.B);
+  float acc[RM][RN];
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < pl.K; k0 += pl.KC) {
+    const int kc = min(pl.KC, pl.K - k0);
+    stage_rows<T>(Bs, pl.ldb, src ? src + k0 : nullptr, lds, nbc, kc, vec);
+    __syncthreads();
+    if (active) {
+      const int nv = (kc + VK - 1) / VK;
+      const int vb = (wk * nv) / pl.WK, ve = ((wk + 1) * nv) / pl.WK;
+      warp_tile_fma<T, RM, RN, LM, LN>(acc, As + (size_t)(tm * LM * RM) * pl.lda + k0, pl.lda,
+                                       Bs + (size_t)(tn * LN * RN) * pl.ldb, pl.ldb, vb, ve, lane);
+    }
+    __syncthreads();
+  }
+  reduce_tiles<RM, RN, LM, LN>(acc, sm.red, sm.outs, pl, active, warp, lane);
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+template <typename T, int RM, int RN, int LM, int LN>
+__global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_constant__ RecParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const RecPlan& pl = p.plan;
+  const int d = blockIdx.x / pl.P;
+  const int blk = blockIdx.x - d * pl.P;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, nT = p.T, G = p.G, U = pl.U;
+  const int j0 = blk * U;
+  const int Uc = min(U, H - j0);
+  const int tid = threadIdx.x;
+  const Smem sm = carve<T, RM, RN, LM, LN>(smem, pl, N);
+  T* As = reinterpret_cast<T*>(sm.A);
+  float* hown = sm.st0;   // [U][N] fp32 hidden state of the own units
+  float* cst = sm.st1;    // [U][N] fp32 cell state (LSTM)
+
+  if (ld_volatile_int(p.status) != kDevOk) return;
+
+  // resident slice: row g*U + u <- W_hh[g*H + j0 + u][:]; zero padding
+  const T* W = reinterpret_cast<const T*>(a.whh);
+  for (int64_t idx = tid; idx < (int64_t)pl.Mp * pl.lda; idx += kThreads) {
+    const int r = (int)(idx / pl.lda), k = (int)(idx - (int64_t)r * pl.lda);
+    const int g = r / U, u = r - g * U;
+    As[idx] = (g < G && u < Uc && k < H) ? W[(int64_t)(g * H + j0 + u) * H + k] : from_f<T>(0.f);
+  }
+  T* Bs = reinterpret_cast<T*>(sm.B);
+  for (int idx = tid; idx < pl.nbp * pl.ldb; idx += kThreads) Bs[idx] = from_f<T>(0.f);
+  const int slot0 = d ? nT : 0;
+  for (int idx = tid; idx < U * N; idx += kThreads) {
+    const int u = idx / N, n = idx - u * N;
+    float hv = 0.f, cv = 0.f;
+    if (u < Uc) {
+      const int64_t o = (int64_t)n * H + j0 + u;
+      if (a.h0) hv = to_f(reinterpret_cast<const T*>(a.h0)[o]);
+      if (a.c0) cv = a.c0[o];
+      if (a.hseq) reinterpret_cast<T*>(a.hseq)[(int64_t)slot0 * N * H + o] = from_f<T>(hv);
+      if (a.cseq) a.cseq[(int64_t)slot0 * N * H + o] = cv;
+    }
+    hown[idx] = hv;
+    cst[idx] = cv;
+  }
+  __syncthreads();
+
+  const bool vec = ((H * (int)sizeof(T)) % 16 == 0) && ((p.ldy * (int64_t)sizeof(T)) % 16 == 0);
+  const T* bhh = reinterpret_cast<const T*>(a.bhh);
+  T* y = reinterpret_cast<T*>(a.y);
+  T* hseq = reinterpret_cast<T*>(a.hseq);
+  const int64_t GH = (int64_t)G * H;
+
+  for (int s = 0; s < nT; ++s) {
+    const int t = d ? nT - 1 - s : s;
+    const int tp = d ? t + 1 : t - 1;
+    const T* src;
+    int64_t lds;
+    if (s == 0) {
+      src = reinterpret_cast<const T*>(a.h0);
+      lds = H;
+    } else {
+      src = y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
+      lds = p.ldy;
+    }
+    const int slot = d ? t : t + 1;
+    for (int n0 = 0; n0 < N; n0 += pl.nb) {
+      const int nbc = min(pl.nb, N - n0);
+      step_contract<T, RM, RN, LM, LN>(sm, pl, src ? src + (int64_t)n0 * lds : nullptr, lds, nbc,
+                                       vec);
+      const float* outs = sm.outs;
+      for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+        const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+        const int64_t row = (int64_t)t * N + n;
+        const float* gxr = a.gx + row * GH + j;
+        float h;
+        if (p.mode == 1) {  // LSTM, gate blocks i, f, g, o
+          const float ig = sigmoidf_(__ldg(gxr) + outs[(0 * U + u) * pl.nbp + nn]);
+          const float fg = sigmoidf_(__ldg(gxr + H) + outs[(1 * U + u) * pl.nbp + nn]);
+          const float gg = tanhf(__ldg(gxr + 2 * H) + outs[(2 * U + u) * pl.nbp + nn]);
+          const float og = sigmoidf_(__ldg(gxr + 3 * H) + outs[(3 * U + u) * pl.nbp + nn]);
+          const float c = fg * cst[u * N + n] + ig * gg;
+          h = og * tanhf(c);
+          cst[u * N + n] = c;
+          if (a.gates) {
+            float* gp = a.gates + row * 4 * H + j;
+            gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
+          }
+          if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
+        } else if (p.mode == 2) {  // GRU, gate blocks r, z, n
+          const float ghn = outs[(2 * U + u) * pl.nbp + nn] + to_f(bhh[2 * H + j]);
+          const float r = sigmoidf_(__ldg(gxr) + outs[(0 * U + u) * pl.nbp + nn]);
+          const float z = sigmoidf_(__ldg(gxr + H) + outs[(1 * U + u) * pl.nbp + nn]);
+          const float nv = tanhf(__ldg(gxr + 2 * H) + r * ghn);
+          h = (1.f - z) * nv + z * hown[u * N + n];
+          if (a.gates) {
+            float* gp = a.gates + row * 4 * H + j;
+            gp[0] = r; gp[H] = z; gp[2 * H] = nv; gp[3 * H] = ghn;
+          }
+        } else {  // tanh RNN
+          h = tanhf(__ldg(gxr) + outs[u * pl.nbp + nn]);
+          if (a.gates) a.gates[row * H + j] = h;
+        }
+        hown[u * N + n] = h;
+        y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
+        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
+      }
+      __syncthreads();
+    }
+    if (s + 1 < nT) {
+      const bool skip = (blockIdx.x == p.fault_block) && (s == p.fault_step);
+      if (!step_barrier(p.flags + d * pl.P, pl.P, blk, (unsigned)(s + 1), p.status, p.timeout_ns,
+                        skip))
+        return;
+    }
+  }
+  for (int idx = tid; idx < Uc * N; idx += kThreads) {
+    const int u = idx % Uc, n = idx / Uc;
+    const int64_t o = (int64_t)n * H + j0 + u;
+    if (a.hy) reinterpret_cast<T*>(a.hy)[o] = from_f<T>(hown[u * N + n]);
+    if (a.cy) a.cy[o] = cst[u * N + n];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+template <typename T, int RM, int RN, int LM, int LN>
+__global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_constant__ RecParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const RecPlan& pl = p.plan;
+  const int d = blockIdx.x / pl.P;
+  const int blk = blockIdx.x - d * pl.P;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, nT = p.T, G = p.G, U = pl.U;
+  const int j0 = blk * U;
+  const int Uc = min(U, H - j0);
+  const int tid = threadIdx.x;
+  const Smem sm = carve<T, RM, RN, LM, LN>(smem, pl, N);
+  T* As = reinterpret_cast<T*>(sm.A);
+  float* dcs = sm.st0;    // [U][N] dc carried to the previous step (LSTM)
+  float* carry = sm.st1;  // [U][N] dh * z carried to the previous step (GRU)
+
+  if (ld_volatile_int(p.status) != kDevOk) return;
+
+  const int64_t GH = (int64_t)G * H;
+  // resident slice, transposed: A[u][r] = W_hh[r][j0 + u]; consecutive threads
+  // read consecutive units of one row
+  const T* W = reinterpret_cast<const T*>(a.whh);
+  for (int64_t idx = tid; idx < (int64_t)pl.Mp * pl.lda; idx += kThreads) {
+    const int r = (int)(idx / pl.Mp), u = (int)(idx - (int64_t)r * pl.Mp);
+    As[(int64_t)u * pl.lda + r] = (u < Uc && r < GH) ? W[(int64_t)r * H + j0 + u] : from_f<T>(0.f);
+  }
+  T* Bs = reinterpret_cast<T*>(sm.B);
+  for (int idx = tid; idx < pl.nbp * pl.ldb; idx += kThreads) Bs[idx] = from_f<T>(0.f);
+  for (int idx = tid; idx < U * N; idx += kThreads) {
+    const int u = idx / N, n = idx - u * N;
+    float dc = 0.f;
+    if (u < Uc && a.dcy) dc = a.dcy[(int64_t)n * H + j0 + u];
+    dcs[idx] = dc;
+    carry[idx] = 0.f;
+  }
+  __syncthreads();
+
+  const bool vec = ((GH * (int64_t)sizeof(T)) % 16 == 0);
+  T* dgx = reinterpret_cast<T*>(a.dgx);
+  T* dgh = reinterpret_cast<T*>(a.dgh);
+  const T* hseq = reinterpret_cast<const T*>(a.hseq);
+
+  for (int s = 0; s <= nT; ++s) {
+    const int t = d ? s : nT - 1 - s;        // time processed at this step (s < T)
+    const int tp = d ? s - 1 : nT - s;       // time processed at the previous step (s > 0)
+    if (s > 0) {
+      const bool skip = (blockIdx.x == p.fault_block) && (s - 1 == p.fault_step);
+      if (!step_barrier(p.flags + d * pl.P, pl.P, blk, (unsigned)s, p.status, p.timeout_ns, skip))
+        return;
+    }
+    for (int n0 = 0; n0 < N; n0 += pl.nb) {
+      const int nbc = min(pl.nb, N - n0);
+      if (s > 0)
+        step_contract<T, RM, RN, LM, LN>(sm, pl, dgh + ((int64_t)tp * N + n0) * GH, GH, nbc, vec);
+      const float* outs = sm.outs;
+      for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+        const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+        // gradient arriving at h_t from the later steps (or from hy)
+        float dhf;
+        if (s == 0)
+          dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
+        else
+          dhf = outs[u * pl.nbp + nn] + carry[u * N + n];
+        if (s == nT) {
+          if (a.dh0) reinterpret_cast<T*>(a.dh0)[(int64_t)n * H + j] = from_f<T>(dhf);
+          if (a.dc0) a.dc0[(int64_t)n * H + j] = dcs[u * N + n];
+          continue;
+        }
+        const int64_t row = (int64_t)t * N + n;
+        const float dh = load_any(a.dy, row * p.lddy + (int64_t)d * H + j, a.dy_bf16) + dhf;
+        T* gxo = dgx + row * GH + j;
+        if (p.mode == 1) {  // LSTM
+          const float* gp = a.gates + row * 4 * H + j;
+          const float ig = gp[0], fg = gp[H], gg = gp[2 * H], og = gp[3 * H];
+          const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+          const float c = a.cseq[((int64_t)sc * N + n) * H + j];
+          const float cp = a.cseq[((int64_t)sp * N + n) * H + j];
+          const float tc = tanhf(c);
+          const float dout = dh * tc;
+          const float dc = dcs[u * N + n] + dh * og * (1.f - tc * tc);
+          gxo[0] = from_f<T>(dc * gg * ig * (1.f - ig));
+          gxo[H] = from_f<T>(dc * cp * fg * (1.f - fg));
+          gxo[2 * H] = from_f<T>(dc * ig * (1.f - gg * gg));
+          gxo[3 * H] = from_f<T>(dout * og * (1.f - og));
+          dcs[u * N + n] = dc * fg;
+        } else if (p.mode == 2) {  // GRU
+          const float* gp = a.gates + row * 4 * H + j;
+          const float r = gp[0], z = gp[H], nv = gp[2 * H], ghn = gp[3 * H];
+          const int sp = d ? t + 1 : t;
+          const float hp = to_f(hseq[((int64_t)sp * N + n) * H + j]);
+          const float dan = dh * (1.f - z) * (1.f - nv * nv);
+          const float daz = dh * (hp - nv) * z * (1.f - z);
+          const float dar = dan * ghn * r * (1.f - r);
+          gxo[0] = from_f<T>(dar);
+          gxo[H] = from_f<T>(daz);
+          gxo[2 * H] = from_f<T>(dan);
+          T* gho = dgh + row * GH + j;
+          gho[0] = from_f<T>(dar);
+          gho[H] = from_f<T>(daz);
+          gho[2 * H] = from_f<T>(dan * r);
+          carry[u * N + n] = dh * z;
+        } else {  // tanh RNN
+          const float hv = a.gates[row * H + j];
+          gxo[0] = from_f<T>(dh * (1.f - hv * hv));
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <typename T, int S>
+void* fwd_fn() {
+  return (void*)rec_fwd_kernel<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
+}
+template <typename T, int S>
+void* bwd_fn() {
+  return (void*)rec_bwd_kernel<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
+}
+
+void* pick_kernel(bool backward, int is_bf16, int shape) {
+  static void* const table[2][2][kNumShapes] = {
+      {{fwd_fn<float, 0>(), fwd_fn<float, 1>(), fwd_fn<float, 2>(), fwd_fn<float, 3>()},
+       {fwd_fn<bf16, 0>(), fwd_fn<bf16, 1>(), fwd_fn<bf16, 2>(), fwd_fn<bf16, 3>()}},
+      {{bwd_fn<float, 0>(), bwd_fn<float, 1>(), bwd_fn<float, 2>(), bwd_fn<float, 3>()},
+       {bwd_fn<bf16, 0>(), bwd_fn<bf16, 1>(), bwd_fn<bf16, 2>(), bwd_fn<bf16, 3>()}}};
+  return table[backward ? 1 : 0][is_bf16 ? 1 : 0][shape];
+}
+
+cudaError_t launch(bool backward, const RecParams& p, cudaStream_t st) {
+  const RecPlan& pl = p.plan;
+  void* fn = pick_kernel(backward, p.bf16, pl.shape);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P, st);
+  if (e != cudaSuccess) return e;
+  RecParams copy = p;
+  void* args[] = {&copy};
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaLaunchCooperativeKernel(fn, dim3(p.D * pl.P), dim3(kThreads), args, pl.smem, st);
+}
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
+                   size_t smem_limit, RecPlan* out) {
+  const int G = mode == 1 ? 4 : mode == 2 ? 3 : 1;
+  const int e = bf16 ? 2 : 4;
+  const int VK = 16 / e;
+  int P = num_sms / D;
+  if (P < 1) P = 1;
+  if (P > kThreads) P = kThreads;
+  if (P > H) P = H;
+  const int U = (H + P - 1) / P;
+  P = (H + U - 1) / U;
+  const int Mloc = backward ? U : G * U;
+  const int K = backward ? G * H : H;
+  bool found = false;
+  double best_cost = 0;
+  RecPlan best;
+  for (int sh = 0; sh < kNumShapes; ++sh) {
+    const Shape S = kShapes[sh];
+    const int LK = 32 / (S.LM * S.LN);
+    const int tmr = S.LM * S.RM, tnc = S.LN * S.RN;
+    const int tiles_m = (Mloc + tmr - 1) / tmr;
+    if (tiles_m > kWarps) continue;
+    const int max_tn = kWarps / tiles_m;
+    const int nchunks = (N + max_tn * tnc - 1) / (max_tn * tnc);
+    const int nb = (N + nchunks - 1) / nchunks;
+    const int tiles_n = (nb + tnc - 1) / tnc;
+    const int WK = kWarps / (tiles_m * tiles_n);
+    RecPlan pl;
+    pl.shape = sh; pl.P = P; pl.U = U; pl.Mloc = Mloc; pl.Mp = tiles_m * tmr;
+    pl.K = K; pl.nb = nb; pl.nbp = tiles_n * tnc;
+    pl.tiles_m = tiles_m; pl.tiles_n = tiles_n; pl.WK = WK;
+    const int pad = (16 * LK) / e;          // bank offset between consecutive rows
+    const int row_align = 128 / e;
+    pl.lda = (int)(round_up(round_up(K, VK), row_align) + pad);
+    const size_t fixed = (size_t)pl.Mp * pl.lda * e + (size_t)kWarps * S.RM * S.RN * 32 * 4 +
+                         (size_t)pl.Mp * pl.nbp * 4 + (size_t)2 * U * N * 4 + 256;
+    if (fixed >= smem_limit) continue;
+    const size_t room = smem_limit - fixed;
+    // largest K chunk (multiple of row_align, or all of K) whose staging fits
+    int KC = (int)round_up(K, VK);
+    auto bytes_for = [&](int kc) { return (size_t)pl.nbp * (round_up(kc, row_align) + pad) * e; };
+    if (bytes_for(KC) > room) {
+      KC = (int)(room / ((size_t)pl.nbp * e)) - pad;
+      KC = KC / row_align * row_align;
+      while (KC > 0 && bytes_for(KC) > room) KC -= row_align;
+    }
+    if (KC < row_align && KC < K) continue;
+    pl.KC = KC;
+    pl.ldb = (int)(round_up(KC, row_align) + pad);
+    pl.smem = fixed + bytes_for(KC);
+    const double cost = (double)nchunks * S.RM * S.RN * ((double)K / (WK * LK)) *
+                        (1.0 + 0.02 * ((K + KC - 1) / KC));
+    if (!found || cost < best_cost) {
+      found = true;
+      best_cost = cost;
+      best = pl;
+    }
+  }
+  if (found) *out = best;
+  return found;
+}
+
+cudaError_t rec_forward(const RecParams& p, cudaStream_t st) { return launch(false, p, st); }
+cudaError_t rec_backward(const RecParams& p, cudaStream_t st) { return launch(true, p, st); }
+
+}  // namespace lr

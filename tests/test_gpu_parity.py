@@ -1,0 +1,123 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Small cases span several GEMM tiles and recurrent blocks with ragged tails
+(hidden / input sizes that are not multiples of any tile, batch chunking, T=1,
+N=1); the full-size cases are the five workloads of the operator's benchmark
+set, run in the same launch configuration the bench uses.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+
+from layer_rnn_gb300 import workloads as wl
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    harness.ensure_built()
+
+
+SMALL = [
+    # mode, L, bidir, T, N, I, H, dtype
+    ("lstm", 1, False, 7, 5, 19, 37, "f32"),
+    ("gru", 2, True, 6, 3, 11, 29, "f32"),
+    ("rnn_tanh", 2, True, 9, 4, 13, 21, "f32"),
+    ("lstm", 3, True, 5, 6, 9, 40, "f32"),
+    ("lstm", 1, False, 20, 33, 160, 300, "f32"),
+    ("gru", 1, False, 4, 130, 64, 96, "f32"),
+    ("rnn_tanh", 1, False, 3, 1, 5, 3, "f32"),
+    ("lstm", 2, True, 1, 2, 3, 5, "f32"),
+    ("gru", 1, False, 1, 1, 1, 1, "f32"),
+    ("lstm", 2, False, 8, 9, 24, 48, "bf16"),
+    ("gru", 1, True, 6, 3, 16, 24, "bf16"),
+    ("rnn_tanh", 2, True, 5, 7, 40, 56, "bf16"),
+    ("lstm", 1, False, 6, 130, 70, 150, "bf16"),
+]
+
+
+def _case_id(c):
+    return "%s-L%d-%s-T%d-N%d-I%d-H%d-%s" % (c[0], c[1], "bi" if c[2] else "uni", *c[3:])
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[_case_id(c) for c in SMALL])
+def test_small_parity(case):
+    mode, L, bidir, T, N, I, H, dt = case
+    cfg = wl.make_config(mode, L, bidir, T, N, I, H, dt, 0.5, seed=zlib.crc32(_case_id(case).encode()) % 10000)
+    inp = wl.make_inputs(cfg)
+    gpu = harness.run_gpu(cfg, inp)
+    ref = harness.run_oracle(cfg, inp)
+    harness.assert_parity(cfg, gpu, ref)
+    # inference forward is the same computation without the workspace
+    assert np.array_equal(gpu["y_inf"], gpu["y"])
+    assert np.array_equal(gpu["hy_inf"], gpu["hy"])
+
+
+@pytest.mark.parametrize("name", ["tiny_lstm", "ds2_lstm", "ds2_gru", "bi5_rnn_tanh", "bi5_lstm",
+                                  "bi5_gru"])
+def test_workload_parity(name):
+    cfg = wl.WORKLOADS[name]
+    inp = wl.make_inputs(cfg)
+    gpu = harness.run_gpu(cfg, inp)
+    ref = harness.run_oracle(cfg, inp)
+    res = harness.assert_parity(cfg, gpu, ref)
+    print(name, {k: "%.2e" % v[0] for k, v in res.items() if not k.startswith("d") or k in
+                 ("dx", "dh0", "dc0")})
+    assert np.array_equal(gpu["y_inf"], gpu["y"])
+
+
+def test_workload_parity_lstm4_bf16():
+    cfg = wl.WORKLOADS["lstm4_bf16"]
+    inp = wl.make_inputs(cfg)
+    gpu = harness.run_gpu(cfg, inp)
+    ref = harness.run_oracle(cfg, inp)
+    res = harness.assert_parity(cfg, gpu, ref)
+    print("lstm4_bf16", {k: "%.2e" % v[0] for k, v in res.items()})
+    assert np.array_equal(gpu["y_inf"], gpu["y"])
+
+
+def test_deterministic_across_calls():
+    cfg = wl.make_config("gru", 2, True, 12, 20, 64, 80, "f32", 0.3, seed=9)
+    inp = wl.make_inputs(cfg)
+    a = harness.run_gpu(cfg, inp, inference=False)
+    b = harness.run_gpu(cfg, inp, inference=False)
+    for k in a:
+        if a[k] is not None:
+            assert np.array_equal(a[k], b[k]), k
+
+
+def test_barrier_timeout_is_reported_and_context_survives():
+    import torch
+    from layer_rnn_gb300 import binding as B
+    cfg = wl.WORKLOADS["tiny_lstm"]
+    inp = wl.make_inputs(cfg)
+    T, N, I, H = cfg["T"], cfg["N"], cfg["I"], cfg["H"]
+    r = B.Rnn("lstm", 1, False, I, H, "f32", 0)
+    try:
+        x = harness.to_dev(inp["x"], "f32")
+        W = harness.to_dev(inp["w"], "f32")
+        y = harness.empty((T, N, H), "f32")
+        ws = r.alloc_workspace(T, N)
+        # block 0 never announces step 2: every other block waits 50 ms, gives up
+        B.rnn_set_debug(r.h, 0, 2, 50_000_000)
+        r.forward_training(x, None, None, W, y, None, None, ws)
+        assert r.check_status() == 6  # RNN_ERR_TIMEOUT
+        assert r.check_status() == 0  # cleared by the read
+        # the context is usable and the next call is correct
+        B.rnn_set_debug(r.h, -1, -1, 2_000_000_000)
+        r.forward_training(x, None, None, W, y, None, None, ws)
+        assert r.check_status() == 0
+        import oracle
+        params = oracle.unflatten_weights(inp["w"], "lstm", 1, False, I, H)
+        ref, _, _, _ = oracle.forward("lstm", inp["x"], None, None, params, 1, False)
+        assert harness.rel_err(harness.from_dev(y), ref) < harness.TOL_F32_FWD
+        torch.cuda.synchronize()
+    finally:
+        r.close()
