@@ -45,7 +45,8 @@
  *   - One handle serves one stream at a time (it owns the step-barrier
  *     counters its kernels use).  No call allocates device memory except
  *     rnn_forward_inference (first call per (T, N) growth, see there) and the
- *     first compute call of a handle (its 4 KB of barrier counters).
+ *     first compute call of a handle (its 4 KB of barrier counters);
+ *     rnn_forward_inference_static never allocates.
  */
 #ifndef LAYER_RNN_H
 #define LAYER_RNN_H
@@ -157,6 +158,28 @@ rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N,
 rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N,
                                    const void* x, const void* h0, const void* c0,
                                    const void* W, void* y, void* hy, void* cy);
+
+/* Inference forward that allocates nothing.  The pages have no counterpart of
+ * this call: it exists for callers that cannot allocate device memory (a
+ * memory pool that owns the device, an allocator that must not be re-entered,
+ * a fixed memory budget), since rnn_forward_inference allocates its scratch on
+ * first use.  Arguments, results and errors are those of
+ * rnn_forward_inference.  All scratch -- step flags and status word, the input
+ * projection, two intermediate layer outputs -- lives in one static device
+ * array of 32 MiB per device, held by every GPU that loads the library until
+ * the process exits.  A call needs 4096 + A(D*T*N*G*H*4) bytes, plus
+ * 2*A(T*N*D*H*elem) when num_layers > 1 (A = round up to 256, elem = 4 for
+ * RNN_F32, 2 for RNN_BF16); larger problems return
+ * RNN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  Every call on a device shares
+ * the array and leaves its contents behind: calls that overlap on the GPU
+ * (other streams, other handles) race and must be serialised by the caller.
+ * Each call clears the array's status word first, so a barrier timeout is
+ * reported only by the call itself when the handle has RNN_FLAG_SYNC_CHECK. */
+rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          const void* x, const void* h0, const void* c0,
+                                          const void* W, void* y, void* hy, void* cy);
 
 /* Backward through time for the data: dx (and dh0, dc0) of the loss
  * sum(y*dy) + sum(hy*dhy) + sum(cy*dcy).  Needs the workspace of the

@@ -40,6 +40,8 @@ SIGNATURES = {
     "rnn_forward_training": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _i64]),
     "rnn_forward_inference": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "rnn_forward_inference_static": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
+                                            _vp]),
     "rnn_backward_data": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _i64]),
     "rnn_backward_weights": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
@@ -130,6 +132,10 @@ def rnn_forward_training(h, stream, T, N, x, h0, c0, W, y, hy, cy, ws, ws_bytes)
 
 def rnn_forward_inference(h, stream, T, N, x, h0, c0, W, y, hy, cy):
     _call("rnn_forward_inference", h, stream, T, N, x, h0, c0, W, y, hy, cy)
+
+
+def rnn_forward_inference_static(h, stream, T, N, x, h0, c0, W, y, hy, cy):
+    _call("rnn_forward_inference_static", h, stream, T, N, x, h0, c0, W, y, hy, cy)
 
 
 def rnn_backward_data(h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes):

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -653,3 +654,98 @@ const char* rnn_status_string(rnn_status_t s) {
 }
 
 }  // extern "C"
+
+// ============================================================================
+// Inference forward without any device allocation
+//
+// For callers that cannot allocate device memory themselves or let a library
+// do it: code running while a memory pool owns the whole device, allocators
+// that must not be re-entered, or processes with a fixed memory budget set at
+// start-up.  rnn_forward_inference keeps its scratch in handle-owned memory
+// that it allocates on first use (and the handle allocates 4 KB of barrier
+// flags on its first compute call); this entry point instead places all of its
+// scratch -- the step flags and status word, the input projection and the two
+// intermediate layer outputs -- in one file-scope device array, so the call
+// performs no cudaMalloc or cudaFree at all.
+// ============================================================================
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB per device
+
+// Every GPU that loads this library holds this array until the process exits.
+// All calls of rnn_forward_inference_static on a device share it.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {nullptr};
+
+// Device address of the array for the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device with that device current and cached.
+rnn_status_t static_scratch_address(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return RNN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return RNN_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return RNN_OK;
+}
+
+}  // namespace
+
+extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int64_t T, int64_t N,
+                                                     const void* x, const void* h0,
+                                                     const void* c0, const void* W, void* y,
+                                                     void* hy, void* cy) {
+  rnn_status_t s = check_sizes(h, T, N);
+  if (s != RNN_OK) return s;
+  if (!x || !W || !y) return RNN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 16) || !aligned(h0, 16) ||
+      !aligned(c0, 16) || !aligned(hy, 16) || !aligned(cy, 16))
+    return RNN_ERR_MISALIGNED;
+  // scratch: [flags + status | input projection | two intermediate outputs]
+  const int64_t gx_bytes = align256(h->D * T * N * h->G * h->H * 4);
+  const int64_t yb = align256(T * N * h->D * h->H * esize(h));
+  const int64_t need = (int64_t)kSyncBytes + gx_bytes + (h->L > 1 ? 2 * yb : 0);
+  if (need > (int64_t)kStaticScratchBytes) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
+  void* base = nullptr;
+  s = static_scratch_address(dev, &base);
+  if (s != RNN_OK) return s;
+  int sms = 0, optin = 0, coop = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+    return RNN_ERR_CUDA;
+  if (!coop) return RNN_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the status word keeps the previous call's value: clear it (flags are
+  // cleared before every persistent launch)
+  if (cudaMemsetAsync(base, 0, kSyncBytes, st) != cudaSuccess) return RNN_ERR_CUDA;
+  // a view of the handle whose device state points into the static array
+  rnn_handle v;
+  v.mode = h->mode; v.L = h->L; v.D = h->D; v.dtype = h->dtype; v.G = h->G; v.Gs = h->Gs;
+  v.I = h->I; v.H = h->H; v.flags = h->flags;
+  v.device = dev;
+  v.num_sms = sms;
+  v.smem_optin = (size_t)optin;
+  v.d_sync = static_cast<unsigned*>(base);
+  v.d_status = reinterpret_cast<int*>(static_cast<char*>(base) + kSyncBytes - 64);
+  v.scratch = static_cast<char*>(base) + kSyncBytes;
+  v.scratch_bytes = kStaticScratchBytes - kSyncBytes;
+  v.timeout_ns = h->timeout_ns;
+  v.fault_block = h->fault_block;
+  v.fault_step = h->fault_step;
+  v.timing = false;
+  s = forward_impl(&v, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false);
+  s = finish(&v, st, s);
+  v.d_sync = nullptr;  // not owned: keep the view's destructor path inert
+  v.scratch = nullptr;
+  return s;
+}
