@@ -45,7 +45,7 @@
  *   - One handle serves one stream at a time (it owns the step-barrier
  *     counters its kernels use).  No call allocates device memory except
  *     rnn_forward_inference (first call per (T, N) growth, see there) and the
- *     first compute call of a handle (its 4 KB of barrier counters);
+ *     first compute call of a handle (its 64 KB of step flags);
  *     rnn_forward_inference_static never allocates.
  */
 #ifndef LAYER_RNN_H
@@ -167,7 +167,7 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N,
  * rnn_forward_inference.  All scratch -- step flags and status word, the input
  * projection, two intermediate layer outputs -- lives in one static device
  * array of 32 MiB per device, held by every GPU that loads the library until
- * the process exits.  A call needs 4096 + A(D*T*N*G*H*4) bytes, plus
+ * the process exits.  A call needs 65536 + A(D*T*N*G*H*4) bytes, plus
  * 2*A(T*N*D*H*elem) when num_layers > 1 (A = round up to 256, elem = 4 for
  * RNN_F32, 2 for RNN_BF16); larger problems return
  * RNN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The first call on

@@ -34,8 +34,8 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src, extra, build_dir=BUILD):
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc()] + ARCH + FLAGS + extra + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -43,25 +43,27 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(verbose=False, extra=()):
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose=False, extra=(), out=LIB, build_dir=BUILD):
+    """Compile every csrc/*.cu and link `out`.  `extra` adds nvcc flags (e.g.
+    -DLAYER_RNN_TRACE for the step-trace build, written to its own `out`)."""
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sources()
     extra = list(extra)
     if verbose:
         extra += ["-Xptxas", "-v"]
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
     objs = [o for o, _ in results]
     if verbose:
         for (o, err), s in zip(results, srcs):
             sys.stderr.write("== %s\n%s" % (os.path.basename(s), err))
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -28,7 +28,9 @@ struct rnn_handle {
   int device = -1;
   int num_sms = 0;
   size_t smem_optin = 0;
-  unsigned* d_sync = nullptr;  // [512] step flags, then the status word
+  int max_clusters[9] = {0};   // co-resident clusters of 1..8 blocks (cluster kernels)
+  size_t cluster_smem = 0;     // largest dynamic shared memory at which clusters fit
+  unsigned* d_sync = nullptr;  // step flags (one per 128-byte line), status word at the end
   int* d_status = nullptr;
   void* scratch = nullptr;     // inference scratch
   size_t scratch_bytes = 0;
@@ -44,7 +46,7 @@ struct rnn_handle {
 
 namespace {
 
-constexpr size_t kSyncBytes = 4096;
+constexpr size_t kSyncBytes = 65536;  // step flags (128 B apart) and, at the end, the status word
 
 int64_t esize(const rnn_handle* h) { return h->dtype == RNN_BF16 ? 2 : 4; }
 int64_t layer_in(const rnn_handle* h, int l) { return l == 0 ? h->I : h->D * h->H; }
@@ -133,6 +135,23 @@ rnn_status_t check_sizes(const rnn_handle* h, int64_t T, int64_t N) {
   return RNN_OK;
 }
 
+// Clusters need a little shared memory of each SM for themselves: find the
+// largest per-block size at which a cluster of 2 still fits, and the number of
+// co-resident clusters of 2, 4 and 8 blocks at that size.  No allocation.
+void query_clusters(int optin, size_t* cluster_smem, int* max_clusters) {
+  *cluster_smem = 0;
+  for (int c = 0; c < 9; ++c) max_clusters[c] = 0;
+  for (size_t sm : {(size_t)optin, (size_t)optin - 1024, (size_t)optin - 4096,
+                    (size_t)optin - 16384, (size_t)200 * 1024}) {
+    if (rec_cluster_capacity(2, sm) > 0) {
+      *cluster_smem = sm;
+      break;
+    }
+  }
+  if (*cluster_smem)
+    for (int c : {2, 4, 8}) max_clusters[c] = rec_cluster_capacity(c, *cluster_smem);
+}
+
 rnn_status_t device_setup(rnn_handle* h) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
@@ -155,6 +174,7 @@ rnn_status_t device_setup(rnn_handle* h) {
   h->device = dev;
   h->num_sms = sms;
   h->smem_optin = (size_t)optin;
+  query_clusters(optin, &h->cluster_smem, h->max_clusters);
   return RNN_OK;
 }
 
@@ -210,10 +230,14 @@ struct PhaseScope {
 };
 
 rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
-  if (!rec_make_plan(backward, h->mode, h->dtype == RNN_BF16, h->D, (int)h->H, (int)N, h->num_sms,
-                     h->smem_optin, pl))
+  const bool bf = h->dtype == RNN_BF16;
+  if (!rec_cluster_plan(backward, h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms,
+                        h->cluster_smem, h->max_clusters, pl) &&
+      !rec_make_plan(backward, h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
+                     pl))
     return RNN_ERR_UNSUPPORTED;
   if (pl->P * h->D > h->num_sms) return RNN_ERR_NO_RESIDENCY;
+  if ((size_t)pl->P * h->D * 128 > kSyncBytes - 64) return RNN_ERR_UNSUPPORTED;
   return RNN_OK;
 }
 
@@ -231,6 +255,10 @@ void fill_rec_common(rnn_handle* h, int64_t T, int64_t N, RecParams* rp) {
   rp->timeout_ns = h->timeout_ns;
   rp->fault_block = h->fault_block;
   rp->fault_step = h->fault_step;
+#ifdef LAYER_RNN_TRACE
+  if (const char* v = getenv("LAYER_RNN_FLAG_STRIDE")) rp->flag_stride = atoi(v);
+  if (const char* v = getenv("LAYER_RNN_SPIN_NS")) rp->spin_ns = atoi(v);
+#endif
 }
 
 template <typename P>
@@ -315,7 +343,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_FWD);
-      s = cuda_status(rec_forward(rp, st));
+      s = cuda_status(rp.plan.cluster ? rec_cluster_launch(false, rp, st) : rec_forward(rp, st));
       if (s != RNN_OK) return s;
     }
     in = out;
@@ -506,7 +534,7 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
-      s = cuda_status(rec_backward(rp, st));
+      s = cuda_status(rp.plan.cluster ? rec_cluster_launch(true, rp, st) : rec_backward(rp, st));
       if (s != RNN_OK) return finish(h, st, s);
     }
     // dX = sum_d dG_x[d] W_ih[l,d]; for l > 0 it is dy of the layer below
@@ -735,6 +763,7 @@ extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int6
   v.device = dev;
   v.num_sms = sms;
   v.smem_optin = (size_t)optin;
+  query_clusters(optin, &v.cluster_smem, v.max_clusters);
   v.d_sync = static_cast<unsigned*>(base);
   v.d_status = reinterpret_cast<int*>(static_cast<char*>(base) + kSyncBytes - 64);
   v.scratch = static_cast<char*>(base) + kSyncBytes;

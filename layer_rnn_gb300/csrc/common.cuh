@@ -32,6 +32,17 @@ __device__ __forceinline__ float load_any(const void* p, int64_t i, int is_bf16)
                  : ldcg_f(reinterpret_cast<const float*>(p) + i);
 }
 
+// element e of a 16-byte vector of fp32 (e < 4) or bf16 (e < 8) values
+__device__ __forceinline__ float lane_f32(const uint4& v, int e) {
+  const unsigned w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+  return __uint_as_float(w);
+}
+__device__ __forceinline__ float lane_bf16(const uint4& v, int e) {
+  const int q = e >> 1;
+  const unsigned w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -61,39 +72,74 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// Step barrier among the `nblocks` blocks of one direction.  Each block
-// publishes `value` in its own flag (release); threads 0..nblocks-1 of every
-// block wait, each on one flag (acquire), until it reaches `value`.  Every wait
-// is bounded: past `timeout_ns`, or once another block has recorded a failure
-// in *status, the block records kDevTimeout and the call returns false, so
-// the kernel can leave without touching the data of the unfinished step.
-// Needs nblocks <= blockDim.x.  All threads of the block must call it.
-__device__ __forceinline__ bool step_barrier(unsigned* flags, int nblocks, int me,
-                                             unsigned value, int* status,
-                                             long long timeout_ns, bool skip_arrive) {
-  __syncthreads();
-  if (threadIdx.x == 0 && !skip_arrive) {
-    __threadfence();
-    st_release_gpu(flags + me, value);
-  }
-  int fail = 0;
-  if ((int)threadIdx.x < nblocks) {
-    const unsigned* f = flags + threadIdx.x;
-    if (ld_acquire_gpu(f) < value) {
-      const unsigned long long t0 = globaltimer_ns();
-      unsigned it = 0;
-      while (ld_acquire_gpu(f) < value) {
-        if ((++it & 31u) == 0) {
-          if (ld_volatile_int(status) != kDevOk) { fail = 1; break; }
-          if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
-            atomicCAS(status, kDevOk, kDevTimeout);
-            fail = 1;
-            break;
-          }
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 16-byte load that bypasses L1 (data written by other blocks of this launch)
+__device__ __forceinline__ uint4 ldcg16(const void* p) {
+  return __ldcg(reinterpret_cast<const uint4*>(p));
+}
+
+// Wait until *f >= value: spin on relaxed loads, finish with one acquire load.
+// Bounded: gives up once `timeout_ns` has passed or another block has recorded
+// a failure in *status (then records kDevTimeout itself and returns false).
+__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned value, int* status,
+                                          long long timeout_ns, int spin_ns) {
+  if (ld_relaxed_gpu(f) < value) {
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned it = 0;
+    while (ld_relaxed_gpu(f) < value) {
+      if (spin_ns > 0) __nanosleep(spin_ns);
+      if ((++it & 31u) == 0) {
+        if (ld_volatile_int(status) != kDevOk) return false;
+        if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+          atomicCAS(status, kDevOk, kDevTimeout);
+          return false;
         }
       }
     }
   }
+  (void)ld_acquire_gpu(f);
+  return true;
+}
+
+// Publish `value` in this block's flag after every thread's stores of the step
+// (call after __syncthreads, from one thread).
+__device__ __forceinline__ void publish_flag(unsigned* f, unsigned value) {
+  __threadfence();
+  st_release_gpu(f, value);
+}
+
+// The lanes of a warp wait, together, for the flags of blocks lo..hi
+// (inclusive; block b's flag at flags[b * stride]) to reach `value`.
+// Returns false (in every lane) if any wait gave up.
+__device__ __forceinline__ bool warp_wait_flags(const unsigned* flags, int stride, int lo, int hi,
+                                                unsigned value, int* status,
+                                                long long timeout_ns, int spin_ns) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  for (int i = lo + lane; i <= hi && ok; i += 32)
+    ok = wait_flag(flags + (size_t)i * stride, value, status, timeout_ns, spin_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Step barrier among the `nblocks` blocks of one direction.  Each block
+// publishes `value` in its own flag (flags[b * stride]); threads
+// 0..nblocks-1 of every block wait, each on one flag.  Every wait is bounded
+// (see wait_flag), so the kernel can leave without touching the data of an
+// unfinished step.  Needs nblocks <= blockDim.x.  All threads must call it.
+__device__ __forceinline__ bool step_barrier(unsigned* flags, int stride, int nblocks, int me,
+                                             unsigned value, int* status, long long timeout_ns,
+                                             int spin_ns, bool skip_arrive) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !skip_arrive) publish_flag(flags + (size_t)me * stride, value);
+  int fail = 0;
+  if ((int)threadIdx.x < nblocks)
+    fail = wait_flag(flags + (size_t)threadIdx.x * stride, value, status, timeout_ns, spin_ns) ? 0
+                                                                                             : 1;
   return __syncthreads_or(fail) == 0;
 }
 

@@ -66,14 +66,25 @@ struct RecDirArgs {
 };
 
 struct RecPlan {
+  int direct = 0;       // 1: per-warp dataflow path (one batch chunk)
   int shape = 0;        // register-tile shape id (see recurrent.cu)
   int P = 0;            // blocks per direction
   int U = 0;            // hidden units per block (last block may have fewer)
   int Mloc = 0, Mp = 0; // rows of the resident operand, padded to the tile
   int K = 0, lda = 0;   // contraction length, smem row stride (elements)
   int nb = 0, nbp = 0;  // batch chunk and its padded size
-  int KC = 0, ldb = 0;  // K chunk of the staged operand, its smem row stride
+  int KC = 0, ldb = 0;  // K chunk of the staged operand and its smem row stride
+                        // (direct path: in 16-byte vectors, per warp)
   int tiles_m = 0, tiles_n = 0, WK = 0;
+  int nst = 1;          // direct path: staging stages per warp (1 or 2)
+  // cluster path (cluster > 0): blocks of a cluster split K; block (r, q) of a
+  // direction is cluster r, rank q
+  int cluster = 0;      // blocks per cluster (K split); 0 = path not used
+  int Pr = 0;           // clusters (row groups) per direction
+  int Ur = 0, Uq = 0;   // units per row group; units per block in the pointwise
+  int Kk = 0;           // K elements per cluster rank (multiple of 16 bytes)
+  int Wm = 0, Wk = 0;   // warps along rows x along K inside a block
+  int ldbs = 0;         // shared-memory row stride of the staged K slice (elements)
   size_t smem = 0;
 };
 
@@ -82,7 +93,10 @@ struct RecParams {
   int bf16 = 0;
   int64_t ldy = 0, lddy = 0;
   RecPlan plan;
-  unsigned* flags = nullptr;   // [D][P] step flags, zeroed before the launch
+  unsigned* flags = nullptr;   // step flags of block b of direction d at
+                               // flags[(d * P + b) * flag_stride], zeroed before the launch
+  int flag_stride = 32;        // one flag per 128-byte line
+  int spin_ns = 0;             // back-off between polls of a flag (0 = none)
   int* status = nullptr;
   long long timeout_ns = 0;
   int fault_block = -1, fault_step = -1;
@@ -93,6 +107,14 @@ struct RecParams {
 // Returns false when no supported tiling fits in shared memory.
 bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
                    size_t smem_limit, RecPlan* out);
+
+// Cluster path: plan (false if the problem does not qualify) and launch.
+// max_clusters[c] = co-resident clusters of c blocks (c = 1, 2, 4, 8; 0 = unknown).
+bool rec_cluster_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
+                      size_t smem_limit, const int* max_clusters, RecPlan* out);
+cudaError_t rec_cluster_launch(bool backward, const RecParams& p, cudaStream_t st);
+// co-resident clusters of `cluster` blocks of the cluster kernels with `smem` bytes
+int rec_cluster_capacity(int cluster, size_t smem);
 
 // Launch (cooperative, so the whole grid is co-resident).  Zeroes the flags
 // on the stream first.

@@ -21,6 +21,8 @@
 //     for its units and stores its slice of the next broadcast vector;
 //   * blocks of a direction meet at a bounded step barrier (flags in global
 //     memory), see common.cuh.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,15 +39,6 @@ struct Shape { int RM, RN, LM, LN; };
 constexpr Shape kShapes[4] = {{3, 5, 8, 4}, {4, 4, 8, 4}, {3, 5, 2, 4}, {4, 4, 2, 4}};
 constexpr int kNumShapes = 4;
 
-__device__ __forceinline__ float lane_f32(const uint4& v, int e) {
-  const unsigned w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-  return __uint_as_float(w);
-}
-__device__ __forceinline__ float lane_bf16(const uint4& v, int e) {
-  const int q = e >> 1;
-  const unsigned w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-}
 
 // acc[i][j] += sum over this lane's 16-byte K vectors of A[lm + LM*i][k] * B[ln + LN*j][k]
 template <typename T, int RM, int RN, int LM, int LN>
@@ -309,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
     }
     if (s + 1 < nT) {
       const bool skip = (blockIdx.x == p.fault_block) && (s == p.fault_step);
-      if (!step_barrier(p.flags + d * pl.P, pl.P, blk, (unsigned)(s + 1), p.status, p.timeout_ns,
-                        skip))
+      if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
+                        (unsigned)(s + 1), p.status, p.timeout_ns, p.spin_ns, skip))
         return;
     }
   }
@@ -372,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
     const int tp = d ? s - 1 : nT - s;       // time processed at the previous step (s > 0)
     if (s > 0) {
       const bool skip = (blockIdx.x == p.fault_block) && (s - 1 == p.fault_step);
-      if (!step_barrier(p.flags + d * pl.P, pl.P, blk, (unsigned)s, p.status, p.timeout_ns, skip))
+      if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
+                        (unsigned)s, p.status, p.timeout_ns, p.spin_ns, skip))
         return;
     }
     for (int n0 = 0; n0 < N; n0 += pl.nb) {
@@ -436,6 +430,462 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------------------------------------
+// direct path (one batch chunk, N <= LN*RN, and at most one pointwise item --
+// one (unit, sequence) pair -- per thread).  No block-wide staging: every warp
+// owns a contiguous slice of K, waits only for the blocks that produce that
+// slice of the previous step's broadcast vector, reads it straight from L2
+// with 16-byte loads and contracts it with the resident rows of all tiles.
+// Per-item state (h, c, dc, carry) stays in registers, and the pointwise
+// inputs of the next step (G_x, or dy and the saved activations) are loaded
+// into registers one step ahead, hiding their latency behind the contraction.
+// ---------------------------------------------------------------------------
+constexpr int kMaxTilesM = 3;
+
+// Optional step trace (build with -DLAYER_RNN_TRACE): thread 0 of a few blocks
+// stamps %globaltimer at the phase boundaries of every step, and
+// rnn_debug_trace_copy() copies the stamps out.  Off in normal builds.
+#ifdef LAYER_RNN_TRACE
+constexpr int kTraceBlocks = 4, kTraceSteps = 1024, kTraceMarks = 8;
+__device__ unsigned long long g_trace[4][1024][8];
+__device__ __forceinline__ void trace_mark(int s, int k, int nblk) {
+  const int b = blockIdx.x == 0 ? 0 : blockIdx.x == nblk / 3 ? 1 : blockIdx.x == (2 * nblk) / 3 ? 2
+              : blockIdx.x == nblk - 1 ? 3 : -1;
+  if (b >= 0 && threadIdx.x == 0 && s < kTraceSteps) g_trace[b][s][k] = globaltimer_ns();
+}
+#define TRACE(s, k) trace_mark((s), (k), pl.P)
+#else
+#define TRACE(s, k) ((void)0)
+#endif
+
+// Per-warp contraction over this warp's K vectors [vb, ve):
+//   acc[tm][i][j] += sum_k A[tm*LM*RM + lm + LM*i][k] * B[ln + LN*j][k]
+// A is resident in shared memory; B rows (row stride ldb elements, nrows of
+// them) are streamed from L2 into the warp's own double-buffered staging area
+// with 16-byte cp.async, `chv` vectors per chunk, so that a whole chunk is in
+// flight at once and the next chunk loads while this one is computed.
+template <typename T, int RM, int RN, int LM, int LN>
+__device__ __forceinline__ void warp_direct_contract(float (&acc)[kMaxTilesM][RM][RN], int tiles_m,
+                                                     const T* As, int lda, const T* B, int64_t ldb,
+                                                     int nrows, int vb, int ve, int lane,
+                                                     uint4* wbuf, int chv, int wstride, int nst,
+                                                     int trace_s, int trace_nblk) {
+  (void)trace_s;
+  (void)trace_nblk;
+  constexpr int LK = 32 / (LM * LN);
+  constexpr int VK = 16 / (int)sizeof(T);
+  constexpr int NR = LN * RN;
+  const int lm = lane % LM, ln = (lane / LM) % LN, kl = lane / (LM * LN);
+  const int nchunks = (ve - vb + chv - 1) / chv;
+  auto issue = [&](int c) {
+    const int v0 = vb + c * chv, nv = min(chv, ve - v0);
+    uint4* dst = wbuf + (c % nst) * NR * wstride;
+    for (int idx = lane; idx < nrows * nv; idx += 32) {
+      const int r = idx / nv, q = idx - r * nv;
+      cp_async16(dst + r * wstride + q, B + r * ldb + (int64_t)(v0 + q) * VK);
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  for (int c = 0; c < nchunks; ++c) {
+    if (c + 1 < nchunks && nst > 1) {
+      issue(c + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncwarp();
+#ifdef LAYER_RNN_TRACE
+    if (c == 0) trace_mark(trace_s, 6, trace_nblk);
+#endif
+    const int v0 = vb + c * chv, nv = min(chv, ve - v0);
+    const uint4* bs = wbuf + (c % nst) * NR * wstride;
+    const T* arow = As + lm * lda + v0 * VK;
+    for (int q = kl; q < nv; q += LK) {
+      uint4 bv[RN];
+#pragma unroll
+      for (int j = 0; j < RN; ++j) {
+        const int r = ln + LN * j;
+        bv[j] = r < nrows ? bs[r * wstride + q] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int tm = 0; tm < kMaxTilesM; ++tm) {
+        if (tm < tiles_m) {
+          uint4 av[RM];
+#pragma unroll
+          for (int i = 0; i < RM; ++i)
+            av[i] = *reinterpret_cast<const uint4*>(arow + (tm * LM * RM + LM * i) * lda + q * VK);
+#pragma unroll
+          for (int e = 0; e < VK; ++e) {
+            float af[RM], bf[RN];
+#pragma unroll
+            for (int i = 0; i < RM; ++i) af[i] = sizeof(T) == 4 ? lane_f32(av[i], e) : lane_bf16(av[i], e);
+#pragma unroll
+            for (int j = 0; j < RN; ++j) bf[j] = sizeof(T) == 4 ? lane_f32(bv[j], e) : lane_bf16(bv[j], e);
+#pragma unroll
+            for (int i = 0; i < RM; ++i)
+#pragma unroll
+              for (int j = 0; j < RN; ++j) acc[tm][i][j] = fmaf(af[i], bf[j], acc[tm][i][j]);
+          }
+        }
+      }
+    }
+    __syncwarp();  // the stage is refilled by a later chunk
+    if (nst == 1 && c + 1 < nchunks) issue(c + 1);
+  }
+}
+
+// intra-warp reduction over the LK lanes, warp partials to red[warp][tm][TE],
+// block sync, fixed-order sum over the warps into outs[m * nbp + n], block sync.
+// Returns false (uniformly) when some warp recorded a failed wait in *fail.
+template <int RM, int RN, int LM, int LN>
+__device__ __forceinline__ bool direct_reduce(float (&acc)[kMaxTilesM][RM][RN], int tiles_m,
+                                              uint4* wall, int wslot, float* outs, int nbp,
+                                              int lane, int warp, volatile int* fail) {
+  constexpr int TE = RM * RN * LM * LN;
+#pragma unroll
+  for (int tm = 0; tm < kMaxTilesM; ++tm)
+#pragma unroll
+    for (int off = LM * LN; off < 32; off <<= 1)
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) acc[tm][i][j] += __shfl_xor_sync(0xffffffffu, acc[tm][i][j], off);
+  const int lm = lane % LM, ln = (lane / LM) % LN, kl = lane / (LM * LN);
+  if (kl == 0) {
+#pragma unroll
+    for (int tm = 0; tm < kMaxTilesM; ++tm) {
+      if (tm < tiles_m) {
+        float* r = reinterpret_cast<float*>(wall + (size_t)warp * wslot) + tm * TE;
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+          for (int j = 0; j < RN; ++j) r[(i * RN + j) * (LM * LN) + ln * LM + lm] = acc[tm][i][j];
+      }
+    }
+  }
+  __syncthreads();
+  if (*fail) return false;
+  for (int idx = threadIdx.x; idx < tiles_m * TE; idx += kThreads) {
+    const int tm = idx / TE, e = idx - tm * TE;
+    float sum = 0.f;
+#pragma unroll 4
+    for (int w = 0; w < kWarps; ++w)
+      sum += reinterpret_cast<const float*>(wall + (size_t)w * wslot)[tm * TE + e];
+    const int ij = e / (LM * LN), lp = e - ij * (LM * LN);
+    const int i = ij / RN, j = ij - i * RN;
+    const int m = tm * (LM * RM) + (lp % LM) + LM * i;
+    const int n = (lp / LM) + LN * j;
+    outs[m * nbp + n] = sum;
+  }
+  __syncthreads();
+  return true;
+}
+
+template <typename T, int RM, int RN, int LM, int LN>
+__global__ void __launch_bounds__(kThreads, 1)
+    rec_fwd_direct(const __grid_constant__ RecParams p) {
+  constexpr int VK = 16 / (int)sizeof(T);
+  constexpr int TE = RM * RN * LM * LN;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_fail;
+  const RecPlan& pl = p.plan;
+  const int d = blockIdx.x / pl.P;
+  const int blk = blockIdx.x - d * pl.P;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, nT = p.T, G = p.G, U = pl.U;
+  const int j0 = blk * U;
+  const int Uc = min(U, H - j0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  T* As = reinterpret_cast<T*>(smem);
+  float* outs = reinterpret_cast<float*>(As + (size_t)pl.Mp * pl.lda);
+  // per-warp slots: staging stages during the contraction, then the warp's
+  // partial tiles for the cross-warp reduction
+  uint4* wall = reinterpret_cast<uint4*>(outs + pl.Mp * pl.nbp);
+  const int wslot = max(pl.nst * (LN * RN) * pl.ldb, (pl.tiles_m * TE * 4 + 15) / 16);
+  uint4* wbuf = wall + (size_t)warp * wslot;
+
+  if (ld_volatile_int(p.status) != kDevOk) return;
+  if (tid == 0) s_fail = 0;
+  const T* W = reinterpret_cast<const T*>(a.whh);
+  for (int64_t idx = tid; idx < (int64_t)pl.Mp * pl.lda; idx += kThreads) {
+    const int r = (int)(idx / pl.lda), k = (int)(idx - (int64_t)r * pl.lda);
+    const int g = r / U, u = r - g * U;
+    As[idx] = (g < G && u < Uc && k < H) ? W[(int64_t)(g * H + j0 + u) * H + k] : from_f<T>(0.f);
+  }
+
+  // the (unit, sequence) item of this thread
+  const bool item = tid < Uc * N;
+  const int u = item ? tid % Uc : 0, n = item ? tid / Uc : 0, j = j0 + u;
+  const int64_t GH = (int64_t)G * H;
+  float h_own = 0.f, c_own = 0.f, bhn = 0.f;
+  float gxv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (item) {
+    const int64_t o = (int64_t)n * H + j;
+    if (a.h0) h_own = to_f(reinterpret_cast<const T*>(a.h0)[o]);
+    if (a.c0) c_own = a.c0[o];
+    const int slot0 = d ? nT : 0;
+    if (a.hseq) reinterpret_cast<T*>(a.hseq)[(int64_t)slot0 * N * H + o] = from_f<T>(h_own);
+    if (a.cseq) a.cseq[(int64_t)slot0 * N * H + o] = c_own;
+    if (p.mode == 2) bhn = to_f(reinterpret_cast<const T*>(a.bhh)[2 * H + j]);
+    const float* gp = a.gx + ((int64_t)(d ? nT - 1 : 0) * N + n) * GH + j;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < G) gxv[g] = __ldg(gp + g * H);
+  }
+  // this warp's slice of K (16-byte vectors) and the blocks that produce it
+  const int nvec = H / VK;
+  const int vb = warp * nvec / kWarps, ve = (warp + 1) * nvec / kWarps;
+  const int plo = (vb * VK) / U, phi = ve > vb ? (ve * VK - 1) / U : -1;
+  unsigned* flags = p.flags + (size_t)d * pl.P * p.flag_stride;
+  T* y = reinterpret_cast<T*>(a.y);
+  T* hseq = reinterpret_cast<T*>(a.hseq);
+  __syncthreads();
+
+  for (int s = 0; s < nT; ++s) {
+    TRACE(s, 0);
+    const int t = d ? nT - 1 - s : s;
+    const int tp = d ? t + 1 : t - 1;
+    float acc[kMaxTilesM][RM][RN];
+#pragma unroll
+    for (int tm = 0; tm < kMaxTilesM; ++tm)
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int jj = 0; jj < RN; ++jj) acc[tm][i][jj] = 0.f;
+    const T* B = nullptr;
+    int64_t ldb = 0;
+    if (s == 0) {
+      B = reinterpret_cast<const T*>(a.h0);
+      ldb = H;
+    } else {
+      B = y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
+      ldb = p.ldy;
+    }
+    if (B != nullptr && ve > vb) {
+      bool ok = true;
+      if (s > 0)
+        ok = warp_wait_flags(flags, p.flag_stride, plo, phi, (unsigned)s, p.status, p.timeout_ns,
+                             p.spin_ns);
+      TRACE(s, 1);
+      if (ok)
+        warp_direct_contract<T, RM, RN, LM, LN>(acc, pl.tiles_m, As, pl.lda, B, ldb, N, vb, ve,
+                                                lane, wbuf, pl.KC, pl.ldb, pl.nst, s, pl.P);
+      else if (lane == 0)
+        s_fail = 1;
+      TRACE(s, 2);
+    }
+    if (!direct_reduce<RM, RN, LM, LN>(acc, pl.tiles_m, wall, wslot, outs, pl.nbp, lane, warp,
+                                       &s_fail))
+      return;
+    TRACE(s, 3);
+    if (item) {
+      const int64_t row = (int64_t)t * N + n;
+      const int slot = d ? t : t + 1;
+      float h;
+      if (p.mode == 1) {  // LSTM, gate blocks i, f, g, o
+        const float ig = sigmoidf_(gxv[0] + outs[(0 * U + u) * pl.nbp + n]);
+        const float fg = sigmoidf_(gxv[1] + outs[(1 * U + u) * pl.nbp + n]);
+        const float gg = tanhf(gxv[2] + outs[(2 * U + u) * pl.nbp + n]);
+        const float og = sigmoidf_(gxv[3] + outs[(3 * U + u) * pl.nbp + n]);
+        c_own = fg * c_own + ig * gg;
+        h = og * tanhf(c_own);
+        if (a.gates) {
+          float* gp = a.gates + row * 4 * H + j;
+          gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
+        }
+        if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c_own;
+      } else if (p.mode == 2) {  // GRU, gate blocks r, z, n
+        const float ghn = outs[(2 * U + u) * pl.nbp + n] + bhn;
+        const float r = sigmoidf_(gxv[0] + outs[(0 * U + u) * pl.nbp + n]);
+        const float z = sigmoidf_(gxv[1] + outs[(1 * U + u) * pl.nbp + n]);
+        const float nv = tanhf(gxv[2] + r * ghn);
+        h = (1.f - z) * nv + z * h_own;
+        if (a.gates) {
+          float* gp = a.gates + row * 4 * H + j;
+          gp[0] = r; gp[H] = z; gp[2 * H] = nv; gp[3 * H] = ghn;
+        }
+      } else {  // tanh RNN
+        h = tanhf(gxv[0] + outs[u * pl.nbp + n]);
+        if (a.gates) a.gates[row * H + j] = h;
+      }
+      h_own = h;
+      y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
+      if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
+      if (s + 1 < nT) {  // next step's input projection, one step ahead
+        const int tn = d ? t - 1 : t + 1;
+        const float* gp = a.gx + ((int64_t)tn * N + n) * GH + j;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (g < G) gxv[g] = __ldg(gp + g * H);
+      }
+    }
+    if (s + 1 < nT) {
+      __syncthreads();
+      TRACE(s, 4);
+      if (tid == 0 && !(blockIdx.x == p.fault_block && s == p.fault_step))
+        publish_flag(flags + (size_t)blk * p.flag_stride, (unsigned)(s + 1));
+      TRACE(s, 5);
+    }
+  }
+  if (item) {
+    const int64_t o = (int64_t)n * H + j;
+    if (a.hy) reinterpret_cast<T*>(a.hy)[o] = from_f<T>(h_own);
+    if (a.cy) a.cy[o] = c_own;
+  }
+}
+
+template <typename T, int RM, int RN, int LM, int LN>
+__global__ void __launch_bounds__(kThreads, 1)
+    rec_bwd_direct(const __grid_constant__ RecParams p) {
+  constexpr int VK = 16 / (int)sizeof(T);
+  constexpr int TE = RM * RN * LM * LN;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_fail;
+  const RecPlan& pl = p.plan;
+  const int d = blockIdx.x / pl.P;
+  const int blk = blockIdx.x - d * pl.P;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, nT = p.T, G = p.G, U = pl.U;
+  const int j0 = blk * U;
+  const int Uc = min(U, H - j0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t GH = (int64_t)G * H;
+  T* As = reinterpret_cast<T*>(smem);
+  float* outs = reinterpret_cast<float*>(As + (size_t)pl.Mp * pl.lda);
+  // per-warp slots: staging stages during the contraction, then the warp's
+  // partial tiles for the cross-warp reduction
+  uint4* wall = reinterpret_cast<uint4*>(outs + pl.Mp * pl.nbp);
+  const int wslot = max(pl.nst * (LN * RN) * pl.ldb, (pl.tiles_m * TE * 4 + 15) / 16);
+  uint4* wbuf = wall + (size_t)warp * wslot;
+
+  if (ld_volatile_int(p.status) != kDevOk) return;
+  if (tid == 0) s_fail = 0;
+  // resident slice, transposed: A[u][r] = W_hh[r][j0 + u]
+  const T* W = reinterpret_cast<const T*>(a.whh);
+  for (int64_t idx = tid; idx < (int64_t)pl.Mp * pl.lda; idx += kThreads) {
+    const int r = (int)(idx / pl.Mp), u = (int)(idx - (int64_t)r * pl.Mp);
+    As[(int64_t)u * pl.lda + r] = (u < Uc && r < GH) ? W[(int64_t)r * H + j0 + u] : from_f<T>(0.f);
+  }
+
+  const bool item = tid < Uc * N;
+  const int u = item ? tid % Uc : 0, n = item ? tid / Uc : 0, j = j0 + u;
+  float dc_own = 0.f, carry = 0.f;
+  // inputs of the coming step's pointwise math, loaded one step ahead
+  float dyv = 0.f, g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, cc = 0.f, cpv = 0.f, hp = 0.f;
+  const T* hseq = reinterpret_cast<const T*>(a.hseq);
+  auto load_inputs = [&](int t) {
+    const int64_t row = (int64_t)t * N + n;
+    dyv = load_any(a.dy, row * p.lddy + (int64_t)d * H + j, a.dy_bf16);
+    if (p.mode == 0) {
+      g0 = __ldg(a.gates + row * H + j);
+    } else {
+      const float* gp = a.gates + row * 4 * H + j;
+      g0 = __ldg(gp); g1 = __ldg(gp + H); g2 = __ldg(gp + 2 * H); g3 = __ldg(gp + 3 * H);
+      const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+      if (p.mode == 1) {
+        cc = __ldg(a.cseq + ((int64_t)sc * N + n) * H + j);
+        cpv = __ldg(a.cseq + ((int64_t)sp * N + n) * H + j);
+      } else {
+        hp = to_f(hseq[((int64_t)sp * N + n) * H + j]);
+      }
+    }
+  };
+  if (item) {
+    if (a.dcy) dc_own = a.dcy[(int64_t)n * H + j];
+    load_inputs(d ? 0 : nT - 1);
+  }
+  // this warp's slice of K = G*H and the blocks that produce it
+  const int nvec = (int)(GH / VK);
+  const int vb = warp * nvec / kWarps, ve = (warp + 1) * nvec / kWarps;
+  unsigned* flags = p.flags + (size_t)d * pl.P * p.flag_stride;
+  T* dgx = reinterpret_cast<T*>(a.dgx);
+  T* dgh = reinterpret_cast<T*>(a.dgh);
+  __syncthreads();
+
+  for (int s = 0; s <= nT; ++s) {
+    TRACE(s, 0);
+    const int t = d ? s : nT - 1 - s;    // time processed at this step (s < nT)
+    const int tp = d ? s - 1 : nT - s;   // time processed at the previous step (s > 0)
+    if (s > 0) {
+      float acc[kMaxTilesM][RM][RN];
+#pragma unroll
+      for (int tm = 0; tm < kMaxTilesM; ++tm)
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+          for (int jj = 0; jj < RN; ++jj) acc[tm][i][jj] = 0.f;
+      if (ve > vb) {
+        bool ok = true;
+        for (int g = 0; g < G && ok; ++g) {
+          const int lo = max(vb * VK, g * H), hi = min(ve * VK, (g + 1) * H);
+          if (lo < hi)
+            ok = warp_wait_flags(flags, p.flag_stride, (lo - g * H) / U, (hi - 1 - g * H) / U,
+                                 (unsigned)s, p.status, p.timeout_ns, p.spin_ns);
+        }
+        TRACE(s, 1);
+        if (ok)
+          warp_direct_contract<T, RM, RN, LM, LN>(acc, pl.tiles_m, As, pl.lda,
+                                                  dgh + (int64_t)tp * N * GH, GH, N, vb, ve, lane,
+                                                  wbuf, pl.KC, pl.ldb, pl.nst, s, pl.P);
+        else if (lane == 0)
+          s_fail = 1;
+      }
+      TRACE(s, 2);
+      if (!direct_reduce<RM, RN, LM, LN>(acc, pl.tiles_m, wall, wslot, outs, pl.nbp, lane, warp,
+                                         &s_fail))
+        return;
+      TRACE(s, 3);
+    }
+    if (item) {
+      float dhf;
+      if (s == 0)
+        dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
+      else
+        dhf = outs[u * pl.nbp + n] + carry;
+      if (s == nT) {
+        if (a.dh0) reinterpret_cast<T*>(a.dh0)[(int64_t)n * H + j] = from_f<T>(dhf);
+        if (a.dc0) a.dc0[(int64_t)n * H + j] = dc_own;
+      } else {
+        const int64_t row = (int64_t)t * N + n;
+        const float dh = dyv + dhf;
+        T* gxo = dgx + row * GH + j;
+        if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o; cc = c_t; cpv = c_{t-1}
+          const float tc = tanhf(cc);
+          const float dc = dc_own + dh * g3 * (1.f - tc * tc);
+          gxo[0] = from_f<T>(dc * g2 * g0 * (1.f - g0));
+          gxo[H] = from_f<T>(dc * cpv * g1 * (1.f - g1));
+          gxo[2 * H] = from_f<T>(dc * g0 * (1.f - g2 * g2));
+          gxo[3 * H] = from_f<T>(dh * tc * g3 * (1.f - g3));
+          dc_own = dc * g1;
+        } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn; hp = h_{t-1}
+          const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
+          const float daz = dh * (hp - g2) * g1 * (1.f - g1);
+          const float dar = dan * g3 * g0 * (1.f - g0);
+          gxo[0] = from_f<T>(dar);
+          gxo[H] = from_f<T>(daz);
+          gxo[2 * H] = from_f<T>(dan);
+          T* gho = dgh + row * GH + j;
+          gho[0] = from_f<T>(dar);
+          gho[H] = from_f<T>(daz);
+          gho[2 * H] = from_f<T>(dan * g0);
+          carry = dh * g1;
+        } else {  // tanh RNN: g0 = h_t
+          gxo[0] = from_f<T>(dh * (1.f - g0 * g0));
+        }
+        if (s + 1 < nT) load_inputs(d ? t + 1 : t - 1);
+      }
+    }
+    if (s < nT) {
+      __syncthreads();
+      TRACE(s, 4);
+      if (tid == 0 && !(blockIdx.x == p.fault_block && s == p.fault_step))
+        publish_flag(flags + (size_t)blk * p.flag_stride, (unsigned)(s + 1));
+      TRACE(s, 5);
+    }
+  }
+}
+
 template <typename T, int S>
 void* fwd_fn() {
   return (void*)rec_fwd_kernel<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
@@ -444,23 +894,39 @@ template <typename T, int S>
 void* bwd_fn() {
   return (void*)rec_bwd_kernel<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
 }
+template <typename T, int S>
+void* fwd_direct_fn() {
+  return (void*)rec_fwd_direct<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
+}
+template <typename T, int S>
+void* bwd_direct_fn() {
+  return (void*)rec_bwd_direct<T, kShapes[S].RM, kShapes[S].RN, kShapes[S].LM, kShapes[S].LN>;
+}
 
-void* pick_kernel(bool backward, int is_bf16, int shape) {
-  static void* const table[2][2][kNumShapes] = {
-      {{fwd_fn<float, 0>(), fwd_fn<float, 1>(), fwd_fn<float, 2>(), fwd_fn<float, 3>()},
-       {fwd_fn<bf16, 0>(), fwd_fn<bf16, 1>(), fwd_fn<bf16, 2>(), fwd_fn<bf16, 3>()}},
-      {{bwd_fn<float, 0>(), bwd_fn<float, 1>(), bwd_fn<float, 2>(), bwd_fn<float, 3>()},
-       {bwd_fn<bf16, 0>(), bwd_fn<bf16, 1>(), bwd_fn<bf16, 2>(), bwd_fn<bf16, 3>()}}};
-  return table[backward ? 1 : 0][is_bf16 ? 1 : 0][shape];
+void* pick_kernel(bool backward, bool direct, int is_bf16, int shape) {
+  static void* const table[2][2][2][kNumShapes] = {
+      {{{fwd_fn<float, 0>(), fwd_fn<float, 1>(), fwd_fn<float, 2>(), fwd_fn<float, 3>()},
+        {fwd_fn<bf16, 0>(), fwd_fn<bf16, 1>(), fwd_fn<bf16, 2>(), fwd_fn<bf16, 3>()}},
+       {{bwd_fn<float, 0>(), bwd_fn<float, 1>(), bwd_fn<float, 2>(), bwd_fn<float, 3>()},
+        {bwd_fn<bf16, 0>(), bwd_fn<bf16, 1>(), bwd_fn<bf16, 2>(), bwd_fn<bf16, 3>()}}},
+      {{{fwd_direct_fn<float, 0>(), fwd_direct_fn<float, 1>(), fwd_direct_fn<float, 2>(),
+         fwd_direct_fn<float, 3>()},
+        {fwd_direct_fn<bf16, 0>(), fwd_direct_fn<bf16, 1>(), fwd_direct_fn<bf16, 2>(),
+         fwd_direct_fn<bf16, 3>()}},
+       {{bwd_direct_fn<float, 0>(), bwd_direct_fn<float, 1>(), bwd_direct_fn<float, 2>(),
+         bwd_direct_fn<float, 3>()},
+        {bwd_direct_fn<bf16, 0>(), bwd_direct_fn<bf16, 1>(), bwd_direct_fn<bf16, 2>(),
+         bwd_direct_fn<bf16, 3>()}}}};
+  return table[direct ? 1 : 0][backward ? 1 : 0][is_bf16 ? 1 : 0][shape];
 }
 
 cudaError_t launch(bool backward, const RecParams& p, cudaStream_t st) {
   const RecPlan& pl = p.plan;
-  void* fn = pick_kernel(backward, p.bf16, pl.shape);
+  void* fn = pick_kernel(backward, pl.direct != 0, p.bf16, pl.shape);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P, st);
+  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
   if (e != cudaSuccess) return e;
   RecParams copy = p;
   void* args[] = {&copy};
@@ -470,7 +936,84 @@ cudaError_t launch(bool backward, const RecParams& p, cudaStream_t st) {
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
+// direct-path plan, or false when the problem does not qualify
+bool make_direct_plan(bool backward, int G, int e, int D, int H, int N, int P, int U,
+                      size_t smem_limit, RecPlan* out) {
+  const int VK = 16 / e;
+  const int Mloc = backward ? U : G * U;
+  const int K = backward ? G * H : H;
+  if (K % VK != 0 || (H * e) % 16 != 0) return false;
+  if ((int64_t)U * N > kThreads) return false;
+  bool found = false;
+  double best_cost = 0;
+  RecPlan best;
+  for (int sh = 0; sh < kNumShapes; ++sh) {
+    const Shape S = kShapes[sh];
+    const int LK = 32 / (S.LM * S.LN);
+    const int tmr = S.LM * S.RM, tnc = S.LN * S.RN;
+    if (N > tnc) continue;
+    const int tiles_m = (Mloc + tmr - 1) / tmr;
+    if (tiles_m > kMaxTilesM) continue;
+    const int nvec = K / VK;
+    if (nvec < kWarps * LK / 2) continue;  // too little K to spread over the warps
+    RecPlan pl;
+    pl.direct = 1;
+    pl.shape = sh; pl.P = P; pl.U = U; pl.Mloc = Mloc; pl.Mp = tiles_m * tmr;
+    pl.K = K; pl.nb = N; pl.nbp = tnc;
+    pl.tiles_m = tiles_m; pl.tiles_n = 1; pl.WK = kWarps;
+    const int pad = (16 * LK) / e;
+    pl.lda = (int)(round_up(K, 128 / e) + pad);
+    const size_t fixed = (size_t)pl.Mp * pl.lda * e + (size_t)pl.Mp * pl.nbp * 4 + 256;
+    if (fixed >= smem_limit) continue;
+    // per-warp slots of nst stages x tnc rows x stride vectors of 16 B; the row
+    // stride puts the rows a warp reads together on distinct bank groups, and a
+    // slot also holds the warp's partial tiles after the contraction
+    const int slice = (nvec + kWarps - 1) / kWarps;
+    // row strides that keep the rows one warp-wide load touches on distinct
+    // bank groups: 4 rows x 16 B (LK = 1) need stride % 4 != 0; 4 rows x 64 B
+    // (LK = 4) need stride % 8 == 4
+    auto stride_of = [&](int c) {
+      int st = std::max(c, 1);
+      while (LK == 1 ? (st % 4 == 0) : (st % 8 != 4)) ++st;
+      return st;
+    };
+    const int part_vecs = (tiles_m * S.RM * S.RN * S.LM * S.LN * 4 + 15) / 16;
+    auto slot_vecs = [&](int c, int st) {
+      return std::max(st * tnc * stride_of(c), part_vecs);
+    };
+    auto bytes_of = [&](int c, int st) { return fixed + (size_t)kWarps * slot_vecs(c, st) * 16; };
+    int chv = slice, nst = 1;
+    if (bytes_of(chv, 1) > smem_limit) {
+      nst = 2;
+      while (chv > 1 && bytes_of(chv, 2) > smem_limit) --chv;
+    }
+    if (bytes_of(chv, nst) > smem_limit) continue;
+    if (chv < LK && chv < slice) continue;
+    pl.KC = chv;
+    pl.nst = nst;
+    pl.ldb = stride_of(chv);
+    pl.smem = bytes_of(chv, nst);
+    const int nchunk = (slice + chv - 1) / chv;
+    const double cost = (double)tiles_m * S.RM * S.RN * ((double)K / (kWarps * LK)) *
+                        ((double)N / tnc > 0.5 ? 1.0 : 1.25) * (1.0 + 0.15 * nchunk);
+    if (!found || cost < best_cost) {
+      found = true;
+      best_cost = cost;
+      best = pl;
+    }
+  }
+  if (found) *out = best;
+  return found;
+}
+
 }  // namespace
+
+#ifdef LAYER_RNN_TRACE
+extern "C" int rnn_debug_trace_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
+}
+#endif
 
 bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
                    size_t smem_limit, RecPlan* out) {
@@ -483,6 +1026,7 @@ bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int n
   if (P > H) P = H;
   const int U = (H + P - 1) / P;
   P = (H + U - 1) / U;
+  if (make_direct_plan(backward, G, e, D, H, N, P, U, smem_limit, out)) return true;
   const int Mloc = backward ? U : G * U;
   const int K = backward ? G * H : H;
   bool found = false;
