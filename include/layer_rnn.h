@@ -70,7 +70,9 @@ typedef enum {
   RNN_ERR_MISALIGNED = 4,
   RNN_ERR_CUDA = 5,               /* a CUDA runtime call failed                  */
   RNN_ERR_TIMEOUT = 6,            /* a step barrier gave up waiting (device)     */
-  RNN_ERR_NO_RESIDENCY = 7        /* the persistent grid cannot be co-resident   */
+  RNN_ERR_NO_RESIDENCY = 7,       /* the persistent grid cannot be co-resident   */
+  RNN_ERR_DEVICE_CHECK = 8        /* a kernel's own index check failed; the
+                                     access was skipped (device)                */
 } rnn_status_t;
 
 /* flags for rnn_create */
@@ -95,7 +97,9 @@ typedef enum {
                          (GRU only; equals DGX for LSTM / tanh RNN)                 */
   RNN_WS_GX = 6,      /* [D, T, N, G*H] f32 input projection scratch                */
   RNN_WS_DY = 7,      /* [2, T, N, D*H] f32 gradient ping-pong between layers       */
-  RNN_WS_NUM_REGIONS = 8
+  RNN_WS_GEMM = 8,    /* tensor-core GEMM operand copies (K-major, fp32 hi/lo split)
+                         and split-K partial sums; scratch between calls            */
+  RNN_WS_NUM_REGIONS = 9
 } rnn_ws_region_t;
 
 /* phases for rnn_get_phase_times */
@@ -134,7 +138,8 @@ rnn_status_t rnn_weight_layout(rnn_t h, int layer, int dir, int which,
 
 /* Bytes of the training workspace for sequence length T and batch N
  * (forward_training writes it; backward_data and backward_weights read it,
- * backward_data also writes the gate-gradient regions).  Host only. */
+ * backward_data also writes the gate-gradient regions; RNN_WS_GEMM is scratch
+ * of every call).  Host only. */
 rnn_status_t rnn_workspace_size(rnn_t h, int64_t T, int64_t N, int64_t* bytes);
 
 /* Byte offset and size of one workspace region (rnn_ws_region_t) for
@@ -194,13 +199,14 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N,
  * dW_ih = sum_t dG_x[t]^T x_t, dW_hh = sum_t dG_h[t]^T h_{t-1}, db_ih =
  * sum dG_x, db_hh = sum dG_h.  Must follow rnn_backward_data on the same
  * workspace.  x is the forward input.  h0 and y may be NULL: the workspace
- * already holds the hidden-state sequences. */
+ * already holds the hidden-state sequences.  The call reads the workspace and
+ * overwrites only its RNN_WS_GEMM region (scratch of every call). */
 rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N,
                                   const void* x, const void* h0, const void* y,
                                   const void* workspace, int64_t ws_bytes, void* dW);
 
 /* Synchronise `stream`, then return and clear the device status word
- * (RNN_OK or RNN_ERR_TIMEOUT). */
+ * (RNN_OK, RNN_ERR_TIMEOUT or RNN_ERR_DEVICE_CHECK). */
 rnn_status_t rnn_check_status(rnn_t h, void* stream);
 
 /* Test hook for failure detection.  timeout_ns > 0 sets the step-barrier

@@ -19,11 +19,11 @@ RNN_TANH, RNN_LSTM, RNN_GRU = 0, 1, 2
 RNN_F32, RNN_BF16 = 0, 1
 RNN_FLAG_SYNC_CHECK, RNN_FLAG_SIMT_GEMM = 0x1, 0x2
 (RNN_WS_GATES, RNN_WS_CSEQ, RNN_WS_HSEQ, RNN_WS_YLAYER, RNN_WS_DGX, RNN_WS_DGH,
- RNN_WS_GX, RNN_WS_DY) = range(8)
+ RNN_WS_GX, RNN_WS_DY, RNN_WS_GEMM) = range(9)
 PHASES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_WORKSPACE_TOO_SMALL", 4: "RNN_ERR_MISALIGNED", 5: "RNN_ERR_CUDA",
-          6: "RNN_ERR_TIMEOUT", 7: "RNN_ERR_NO_RESIDENCY"}
+          6: "RNN_ERR_TIMEOUT", 7: "RNN_ERR_NO_RESIDENCY", 8: "RNN_ERR_DEVICE_CHECK"}
 MODES = {"rnn_tanh": RNN_TANH, "lstm": RNN_LSTM, "gru": RNN_GRU}
 DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 

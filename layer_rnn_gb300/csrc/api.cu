@@ -92,6 +92,116 @@ struct WsLayout {
 
 int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 
+// ----------------------------------------------------------------------------
+// tensor-core GEMM operands: every operand is presented K-major; fp32 operands
+// are split into hi / lo parts; copies live in a scratch region
+// ----------------------------------------------------------------------------
+constexpr int kMaxKsplit = 8;
+
+int64_t kpad(int64_t K, bool tf32) { return tf32 ? (K + 3) / 4 * 4 : (K + 7) / 8 * 8; }
+
+// bytes of one operand copy: rows x K (hi and lo for fp32)
+int64_t opnd_bytes(int64_t rows, int64_t K, bool tf32) {
+  return align256(rows * kpad(K, tf32) * (tf32 ? 4 : 2)) * (tf32 ? 2 : 1);
+}
+
+// scratch the GEMM phases of one call need (maximum over the phases)
+int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool training) {
+  const bool tf = h->dtype != RNN_BF16;
+  const int64_t GH = h->G * h->H, TN = T * N, D = h->D;
+  int64_t need = 0;
+  for (int l = 0; l < h->L; ++l) {
+    const int64_t I_l = l == 0 ? h->I : D * h->H;
+    // input projection: X [TN][I_l] and W_ih [GH][I_l], both K-major already
+    if (tf) need = std::max(need, opnd_bytes(TN, I_l, tf) + opnd_bytes(GH, I_l, tf));
+    if (!training) continue;
+    // dX: dG [TN][GH] per direction, W_ih transposed [I_l][GH] per direction
+    need = std::max(need, D * ((tf ? opnd_bytes(TN, GH, tf) : 0) + opnd_bytes(I_l, GH, tf)) +
+                              align256((int64_t)kMaxKsplit * TN * I_l * 4));
+    // dW_ih, dW_hh: dG^T [GH][TN] (two for GRU), X^T [I_l][TN], h_prev^T [H][TN]
+    const int64_t dgt = opnd_bytes(GH, TN, tf) * (h->mode == RNN_GRU ? 2 : 1);
+    need = std::max(need, dgt + opnd_bytes(std::max(I_l, h->H), TN, tf) +
+                              align256((int64_t)kMaxKsplit * GH * std::max(I_l, h->H) * 4));
+  }
+  return need + 4096;
+}
+
+struct Scratch {
+  char* base = nullptr;
+  int64_t cap = 0, off = 0;
+  void* take(int64_t bytes) {
+    const int64_t o = align256(off);
+    if (!base || o + bytes > cap) return nullptr;
+    off = o + bytes;
+    return base + o;
+  }
+};
+
+// One GEMM operand given by strides (element (r, k) at p[r * sr + k * sk]) as a
+// K-major TcGemm operand; copies into `sc` when needed.  false: cannot.
+bool prep_operand(const void* p, int64_t rows, int64_t K, int64_t sr, int64_t sk, bool tf,
+                  Scratch* sc, const void** hi, const void** lo, int64_t* ld, cudaStream_t st) {
+  const int64_t kp = kpad(K, tf);
+  if (tf) {
+    float* h = static_cast<float*>(sc->take(align256(rows * kp * 4)));
+    float* l = static_cast<float*>(sc->take(align256(rows * kp * 4)));
+    if (!h || !l) return false;
+    const bool kmaj = sk == 1;
+    cudaError_t e = kmaj ? split_operand(static_cast<const float*>(p), rows, K, sr, h, l, kp, false, st)
+                         : split_operand(static_cast<const float*>(p), K, rows, sk, h, l, kp, true, st);
+    if (e != cudaSuccess) return false;
+    *hi = h;
+    *lo = l;
+    *ld = kp;
+    return true;
+  }
+  if (sk == 1 && (reinterpret_cast<uintptr_t>(p) % 16 == 0) && (sr * 2) % 16 == 0) {
+    *hi = p;
+    *lo = nullptr;
+    *ld = sr;
+    return true;
+  }
+  if (sr != 1) return false;
+  void* t = sc->take(align256(rows * kp * 2));
+  if (!t) return false;
+  if (transpose_bf16(p, K, rows, sk, t, kp, st) != cudaSuccess) return false;
+  *hi = t;
+  *lo = nullptr;
+  *ld = kp;
+  return true;
+}
+
+// A dense phase: tensor-core GEMM when the operands can be presented to it
+// (alignment, scratch room), otherwise the CUDA-core GEMM.
+rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaStream_t st) {
+  if (!(h->flags & RNN_FLAG_SIMT_GEMM)) {
+    const bool tf = !g.in_bf16;
+    TcGemm t;
+    t.M = g.M; t.N = g.N; t.K = g.K; t.tf32 = tf ? 1 : 0;
+    bool ok = prep_operand(g.A, g.M, g.K, g.sam, g.sak, tf, &sc, &t.A_hi, &t.A_lo, &t.lda, st) &&
+              prep_operand(g.B, g.N, g.K, g.sbn, g.sbk, tf, &sc, &t.B_hi, &t.B_lo, &t.ldb, st);
+    if (ok && g.K2 > 0) {
+      t.K2 = g.K2;
+      ok = prep_operand(g.A2, g.M, g.K2, g.sam2, g.sak2, tf, &sc, &t.A2_hi, &t.A2_lo, &t.lda2, st) &&
+           prep_operand(g.B2, g.N, g.K2, g.sbn2, g.sbk2, tf, &sc, &t.B2_hi, &t.B2_lo, &t.ldb2, st);
+    }
+    if (ok) {
+      t.C = g.C; t.ldc = g.ldc; t.out_bf16 = g.out_bf16; t.accumulate = g.accumulate;
+      t.bias1 = g.bias1; t.bias2 = g.bias2; t.bias2_limit = g.bias2_limit;
+      t.bias_bf16 = g.bias_bf16;
+      t.status = h->d_status;
+      t.timeout_ns = h->timeout_ns;
+      const int ks = gemm_tc_splitk(g.M, g.N, g.K + g.K2, tf, h->num_sms);
+      if (ks > 1) {
+        t.part = static_cast<float*>(sc.take(ks * g.M * g.N * 4));
+        if (t.part) t.ksplit = ks;
+      }
+      if (gemm_tc_supported(t)) return gemm_tc(t, st) == cudaSuccess ? RNN_OK : RNN_ERR_CUDA;
+    }
+  }
+  return gemm_simt(g, st) == cudaSuccess ? RNN_OK : RNN_ERR_CUDA;
+}
+
 WsLayout ws_layout(const rnn_handle* h, int64_t T, int64_t N) {
   WsLayout w;
   w.L = h->L;
@@ -116,6 +226,7 @@ WsLayout ws_layout(const rnn_handle* h, int64_t T, int64_t N) {
   for (int l = 0; l < h->L; ++l) put(RNN_WS_YLAYER, l, 0, l < h->L - 1 ? T * N * D * H * e : 0);
   put(RNN_WS_GX, 0, 0, D * T * N * G * H * 4);
   put(RNN_WS_DY, 0, 0, h->L > 1 ? 2 * T * N * D * H * 4 : 0);
+  put(RNN_WS_GEMM, 0, 0, gemm_scratch_bytes(h, T, N, true));
   w.total = off;
   return w;
 }
@@ -272,7 +383,7 @@ P* mp(void* base, int64_t byte_off) {
 
 // G_x[d] = in W_ih[l,d]^T + b_ih + b_hh (GRU: b_hn stays in the recurrence)
 rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, int64_t N,
-                              const void* in, const void* W, float* gx) {
+                              const void* in, const void* W, float* gx, Scratch sc) {
   const int64_t e = esize(h), GH = h->G * h->H, I_l = layer_in(h, l);
   for (int d = 0; d < h->D; ++d) {
     GemmArgs g;
@@ -285,14 +396,15 @@ rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, 
     g.bias2_limit = h->mode == RNN_GRU ? 2 * h->H : GH;
     g.in_bf16 = g.bias_bf16 = h->dtype == RNN_BF16;
     g.out_bf16 = 0;
-    if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+    rnn_status_t s = run_gemm(h, g, sc, st);
+    if (s != RNN_OK) return s;
   }
   return RNN_OK;
 }
 
 rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, const void* x,
                           const void* h0, const void* c0, const void* W, void* y, void* hy,
-                          void* cy, char* ws, bool training) {
+                          void* cy, char* ws, bool training, Scratch sc) {
   const int64_t e = esize(h), H = h->H, NH = N * H;
   WsLayout lay = ws_layout(h, T, N);
   float* gx;
@@ -317,7 +429,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     else out = ybuf[l & 1];
     {
       PhaseScope ps(h, st, RNN_PHASE_INPUT_GEMM);
-      s = input_projection(h, st, l, T, N, in, W, gx);
+      s = input_projection(h, st, l, T, N, in, W, gx, sc);
       if (s != RNN_OK) return s;
     }
     RecParams rp;
@@ -429,7 +541,7 @@ rnn_status_t rnn_workspace_layout(rnn_t h, int64_t T, int64_t N, int region, int
   if (s != RNN_OK) return s;
   if (region < 0 || region >= RNN_WS_NUM_REGIONS) return RNN_ERR_INVALID_ARG;
   const bool per_layer = region == RNN_WS_YLAYER;
-  const bool global = region == RNN_WS_GX || region == RNN_WS_DY;
+  const bool global = region == RNN_WS_GX || region == RNN_WS_DY || region == RNN_WS_GEMM;
   if (global) layer = 0;
   if (global || per_layer) dir = 0;
   if (layer < 0 || layer >= h->L || dir < 0 || dir >= h->D) return RNN_ERR_INVALID_ARG;
@@ -452,7 +564,13 @@ rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, c
   s = device_setup(h);
   if (s != RNN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true);
+  Scratch sc;
+  {
+    const Region& R = ws_layout(h, T, N).at(RNN_WS_GEMM, 0, 0);
+    sc.base = static_cast<char*>(workspace) + R.off;
+    sc.cap = R.bytes;
+  }
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true, sc);
   return finish(h, st, s);
 }
 
@@ -468,8 +586,9 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, 
   s = device_setup(h);
   if (s != RNN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t need = (size_t)(align256(h->D * T * N * h->G * h->H * 4) +
-                               2 * align256(T * N * h->D * h->H * esize(h)));
+  const int64_t base_bytes = align256(h->D * T * N * h->G * h->H * 4) +
+                             2 * align256(T * N * h->D * h->H * esize(h));
+  const size_t need = (size_t)(base_bytes + gemm_scratch_bytes(h, T, N, false));
   if (need > h->scratch_bytes) {
     // the old scratch may still be in use by earlier work on the stream
     if (h->scratch) {
@@ -484,7 +603,10 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, 
     }
     h->scratch_bytes = need;
   }
-  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false);
+  Scratch sc;
+  sc.base = static_cast<char*>(h->scratch) + base_bytes;
+  sc.cap = (int64_t)h->scratch_bytes - base_bytes;
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false, sc);
   return finish(h, st, s);
 }
 
@@ -508,6 +630,9 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
   RecPlan plan;
   s = plan_rec(h, true, N, &plan);
   if (s != RNN_OK) return finish(h, st, s);
+  Scratch sc;
+  sc.base = ws + lay.at(RNN_WS_GEMM, 0, 0).off;
+  sc.cap = lay.at(RNN_WS_GEMM, 0, 0).bytes;
   const void* dcur = dy;
   int dcur_bf16 = bf;
   for (int l = h->L - 1; l >= 0; --l) {
@@ -562,7 +687,8 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     g.out_bf16 = target_bf16;
     {
       PhaseScope ps(h, st, RNN_PHASE_DX_GEMM);
-      if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+      s = run_gemm(h, g, sc, st);
+      if (s != RNN_OK) return s;
     }
     dcur = target;
     dcur_bf16 = target_bf16;
@@ -587,6 +713,10 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
   const char* ws = static_cast<const char*>(workspace);
   const int64_t e = esize(h), H = h->H, GH = h->G * H;
   const bool bf = h->dtype == RNN_BF16;
+  // the GEMM scratch region is the one part of the workspace this call writes
+  Scratch sc;
+  sc.base = const_cast<char*>(ws) + lay.at(RNN_WS_GEMM, 0, 0).off;
+  sc.cap = lay.at(RNN_WS_GEMM, 0, 0).bytes;
   PhaseScope ps(h, st, RNN_PHASE_DW_GEMM);
   for (int l = 0; l < h->L; ++l) {
     const int64_t I_l = layer_in(h, l);
@@ -602,14 +732,16 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       g.B = in; g.sbk = I_l; g.sbn = 1;
       g.C = mp<char>(dW, weight_offset(h, l, d, 0) * e); g.ldc = I_l;
       g.in_bf16 = bf; g.out_bf16 = bf;
-      if (gemm_simt(g, st) != cudaSuccess) return RNN_ERR_CUDA;
+      s = run_gemm(h, g, sc, st);
+      if (s != RNN_OK) return s;
       GemmArgs g2;
       g2.M = GH; g2.N = H; g2.K = T * N;
       g2.A = dgh; g2.sam = 1; g2.sak = GH;
       g2.B = hprev; g2.sbk = H; g2.sbn = 1;
       g2.C = mp<char>(dW, weight_offset(h, l, d, 1) * e); g2.ldc = H;
       g2.in_bf16 = bf; g2.out_bf16 = bf;
-      if (gemm_simt(g2, st) != cudaSuccess) return RNN_ERR_CUDA;
+      s = run_gemm(h, g2, sc, st);
+      if (s != RNN_OK) return s;
       if (colsum(mp<char>(dW, weight_offset(h, l, d, 2) * e), bf, dgx, bf, T * N, GH, GH, st) !=
               cudaSuccess ||
           colsum(mp<char>(dW, weight_offset(h, l, d, 3) * e), bf, dgh, bf, T * N, GH, GH, st) !=
@@ -677,6 +809,7 @@ const char* rnn_status_string(rnn_status_t s) {
     case RNN_ERR_CUDA: return "CUDA runtime error";
     case RNN_ERR_TIMEOUT: return "step barrier timed out";
     case RNN_ERR_NO_RESIDENCY: return "persistent grid cannot be co-resident";
+    case RNN_ERR_DEVICE_CHECK: return "a kernel's index check failed (access skipped)";
   }
   return "unknown status";
 }
@@ -772,7 +905,12 @@ extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int6
   v.fault_block = h->fault_block;
   v.fault_step = h->fault_step;
   v.timing = false;
-  s = forward_impl(&v, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false);
+  // what the array has left after the projection and layer outputs serves the
+  // tensor-core GEMM's operand copies; without room the GEMM runs on CUDA cores
+  Scratch sc;
+  sc.base = static_cast<char*>(base) + need;
+  sc.cap = (int64_t)kStaticScratchBytes - need;
+  s = forward_impl(&v, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false, sc);
   s = finish(&v, st, s);
   v.d_sync = nullptr;  // not owned: keep the view's destructor path inert
   v.scratch = nullptr;

@@ -12,6 +12,7 @@ typedef __nv_bfloat16 bf16;
 // device status word values (same numbers as rnn_status_t)
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 6;
+constexpr int kDevCheck = 8;   // a kernel's own index check failed (access skipped)
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
@@ -106,10 +107,10 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned value, int
   return true;
 }
 
-// Publish `value` in this block's flag after every thread's stores of the step
-// (call after __syncthreads, from one thread).
+// Publish `value` in this block's flag after every thread's stores of the step:
+// call after __syncthreads, from one thread.  The release store is cumulative
+// over the writes the barrier ordered before it, so no separate fence.
 __device__ __forceinline__ void publish_flag(unsigned* f, unsigned value) {
-  __threadfence();
   st_release_gpu(f, value);
 }
 

@@ -1,0 +1,553 @@
+// Tensor-core GEMM for the dense phases on sm_103a: tcgen05.mma with the
+// accumulator in tensor memory, operands staged by TMA (cp.async.bulk.tensor,
+// 128-byte swizzle) through a multi-stage shared-memory ring.
+//
+//   C[m][n] (+)= sum_k A[m][k] * B[n][k]   (+ a second product over K2)
+//
+// A and B are K-major (row-major with K contiguous).  bf16 operands run one
+// kind::f16 pass.  fp32 operands run three kind::tf32 passes on pre-split
+// operands, A_hi*B_hi + A_hi*B_lo + A_lo*B_hi, where x_hi is x with its low 13
+// mantissa bits cleared (exactly representable in tf32) and x_lo = x - x_hi
+// (the split of the error-compensated tf32 GEMM of Ootomo & Yokota, 2022),
+// which keeps the product error near fp32 level.
+//
+// One CTA computes one 128 x BN output tile (or one K range of it when the
+// problem is split along K; the partial tiles are then summed in a fixed order
+// by splitk_reduce_kernel).  Thread 0 issues the TMA loads, thread 32 the MMAs,
+// and all four warps read the accumulator out of tensor memory for the
+// epilogue.  Every mbarrier wait is bounded by %globaltimer.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lr {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int kTcThreads = 128;
+constexpr int kSmemBudget = 200 * 1024;
+
+struct TcKParams {
+  int M, N;
+  int nk1, nk2;         // 128-byte K blocks of product 1 and 2
+  int ksplit;
+  int stages;
+  void* C;
+  int64_t ldc;
+  int out_bf16;
+  int accumulate;
+  const void* bias1;
+  const void* bias2;
+  int64_t bias2_limit;
+  int bias_bf16;
+  float* part;          // split-K partials [ksplit][M][N] (fp32), or null
+  int* status;
+  long long timeout_ns;
+};
+
+struct TcMaps {
+  CUtensorMap a1h, a1l, b1h, b1l, a2h, a2l, b2h, b2l;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait for the phase of `parity` to complete
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
+                                          long long timeout_ns, volatile int* abort_flag) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  unsigned it = 0;
+  while (!mbar_try(bar, parity)) {
+    if ((++it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+        atomicCAS(status, kDevOk, kDevTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// shared-memory matrix descriptor: K-major tile of rows x 128 bytes, 128-byte
+// swizzle, 8-row groups 1024 bytes apart (tile base 1024-byte aligned)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN, bool TF32>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcKParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  constexpr int kA = BM * 128;                     // bytes of one A tile
+  constexpr int kB = BN * 128;                     // bytes of one B tile
+  constexpr int kStage = (kA + kB) * (TF32 ? 2 : 1);
+  constexpr uint32_t kIdesc = (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) |
+                              ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]), done = smem_u32(&bars[16]);
+
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nkt = p.nk1 + p.nk2;
+  const int z = blockIdx.z;
+  const int kb0 = (int)((int64_t)z * nkt / p.ksplit), kb1 = (int)((int64_t)(z + 1) * nkt / p.ksplit);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_slot)),
+                 "r"(BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_slot;
+
+  if (threadIdx.x == 0) {
+    // TMA producer
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int it = kb - kb0, s = it % S;
+      const uint32_t ph = (uint32_t)((it / S) & 1);
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, p.status, p.timeout_ns, &abort_flag)) break;
+      const uint32_t st = base + (uint32_t)(s * kStage);
+      const uint32_t fb = full0 + 8 * s;
+      mbar_expect_tx(fb, (uint32_t)kStage);
+      const bool second = kb >= p.nk1;
+      const int kx = (second ? kb - p.nk1 : kb) * (TF32 ? 32 : 64);
+      const CUtensorMap* ah = second ? &maps.a2h : &maps.a1h;
+      const CUtensorMap* bh = second ? &maps.b2h : &maps.b1h;
+      tma_load_2d(st, ah, kx, m0, fb);
+      tma_load_2d(st + kA, bh, kx, n0, fb);
+      if (TF32) {
+        const CUtensorMap* al = second ? &maps.a2l : &maps.a1l;
+        const CUtensorMap* bl = second ? &maps.b2l : &maps.b1l;
+        tma_load_2d(st + kA + kB, al, kx, m0, fb);
+        tma_load_2d(st + 2 * kA + kB, bl, kx, n0, fb);
+      }
+    }
+  } else if (threadIdx.x == 32) {
+    // MMA issuer
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int it = kb - kb0, s = it % S;
+      const uint32_t ph = (uint32_t)((it / S) & 1);
+      if (!mbar_wait(full0 + 8 * s, ph, p.status, p.timeout_ns, &abort_flag)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t st = base + (uint32_t)(s * kStage);
+      const uint64_t ah = sw128_desc(st), bh = sw128_desc(st + kA);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
+        const uint64_t adv = (uint64_t)(kk * 2);
+        const uint32_t acc0 = (it > 0 || kk > 0) ? 1u : 0u;
+        if (TF32) {
+          const uint64_t al = sw128_desc(st + kA + kB), bl = sw128_desc(st + 2 * kA + kB);
+          mma_tf32(tmem, ah + adv, bh + adv, kIdesc, acc0);
+          mma_tf32(tmem, ah + adv, bl + adv, kIdesc, 1u);
+          mma_tf32(tmem, al + adv, bh + adv, kIdesc, 1u);
+        } else {
+          mma_f16(tmem, ah + adv, bh + adv, kIdesc, acc0);
+        }
+      }
+      mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // epilogue: warp w owns TMEM lanes / tile rows 32w .. 32w+31
+  const bool have_k = kb1 > kb0;
+  bool ok = true;
+  if (have_k) ok = mbar_wait(done, 0, p.status, p.timeout_ns, &abort_flag);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (ok && !abort_flag) {
+    // the pipeline stages are free now: each warp stages its 32 rows x BN
+    // accumulators in shared memory (row pitch BN + 1 floats, conflict-free),
+    // then writes them row by row, 32 consecutive columns per instruction
+    float* tile = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw))) +
+                  (size_t)warp * 32 * (BN + 1);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      if (have_k) {
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) tile[lane * (BN + 1) + c0 + i] = v[i];
+    }
+    __syncwarp();
+    const int rbase = m0 + warp * 32;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      const int n = n0 + c0 + lane;
+      if (n >= p.N) continue;
+      float bias = 0.f;
+      if (!p.part) {
+        if (p.bias1) bias += load_any(p.bias1, n, p.bias_bf16);
+        if (p.bias2 && n < p.bias2_limit) bias += load_any(p.bias2, n, p.bias_bf16);
+      }
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) {
+        const int row = rbase + r;
+        if (row >= p.M) break;
+        float x = tile[r * (BN + 1) + c0 + lane];
+        if (p.part) {
+          p.part[((int64_t)z * p.M + row) * p.N + n] = x;
+          continue;
+        }
+        x += bias;
+        if (p.out_bf16) {
+          bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+          if (p.accumulate) x += __bfloat162float(*c);
+          *c = __float2bfloat16_rn(x);
+        } else {
+          float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + n;
+          if (p.accumulate) x += *c;
+          *c = x;
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 2)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+                 : "memory");
+}
+
+// C = sum_z part[z] (+ bias) (+ C); fixed order over z
+__global__ void splitk_reduce_kernel(const float* part, int ks, int64_t M, int64_t N, void* C,
+                                     int64_t ldc, int out_bf16, int accumulate, const void* bias1,
+                                     const void* bias2, int64_t bias2_limit, int bias_bf16) {
+  const int64_t total = M * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / N, n = i - m * N;
+    float x = 0.f;
+    for (int zz = 0; zz < ks; ++zz) x += part[(int64_t)zz * total + i];
+    if (bias1) x += load_any(bias1, n, bias_bf16);
+    if (bias2 && n < bias2_limit) x += load_any(bias2, n, bias_bf16);
+    if (out_bf16) {
+      bf16* c = reinterpret_cast<bf16*>(C) + m * ldc + n;
+      if (accumulate) x += __bfloat162float(*c);
+      *c = __float2bfloat16_rn(x);
+    } else {
+      float* c = reinterpret_cast<float*>(C) + m * ldc + n;
+      if (accumulate) x += *c;
+      *c = x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// operand preparation: fp32 -> (hi, lo) split, optionally transposed; bf16
+// transpose.  32 x 32 tiles through shared memory.
+// ---------------------------------------------------------------------------
+__global__ void split_kernel(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                             float* hi, float* lo, int64_t ldd, int transpose) {
+  __shared__ float tile[32][33];
+  const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int k = ty; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + tx;
+    tile[k][tx] = (r < rows && c < cols) ? src[r * lds + c] : 0.f;
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    float v;
+    int64_t orow, ocol;
+    if (transpose) {
+      v = tile[tx][k];
+      orow = c0 + k;
+      ocol = r0 + tx;
+      if (orow >= cols || ocol >= rows) continue;
+    } else {
+      v = tile[k][tx];
+      orow = r0 + k;
+      ocol = c0 + tx;
+      if (orow >= rows || ocol >= cols) continue;
+    }
+    const float h = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+    hi[orow * ldd + ocol] = h;
+    if (lo) lo[orow * ldd + ocol] = v - h;
+  }
+}
+
+__global__ void transpose_bf16_kernel(const bf16* src, int64_t rows, int64_t cols, int64_t lds,
+                                      bf16* dst, int64_t ldd) {
+  __shared__ bf16 tile[32][34];
+  const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int k = ty; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + tx;
+    tile[k][tx] = (r < rows && c < cols) ? src[r * lds + c] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int64_t orow = c0 + k, ocol = r0 + tx;
+    if (orow < cols && ocol < rows) dst[orow * ldd + ocol] = tile[tx][k];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// K-major operand [rows][K] with row stride ld (elements); box = kpe x box_rows
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld, bool bf,
+              int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !ptr) return false;
+  const int e = bf ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * e)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+             const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool operand_ok(const void* p, int64_t ld, int e) {
+  return p && (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * e) % 16 == 0);
+}
+
+template <int BN, bool TF32>
+cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaStream_t st) {
+  constexpr int kStage = (BM * 128 + BN * 128) * (TF32 ? 2 : 1);
+  const size_t smem = (size_t)kp.stages * kStage + 1024;
+  auto fn = gemm_tc_kernel<BN, TF32>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  fn<<<grid, kTcThreads, smem, st>>>(maps, kp);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms) {
+  const int BN = N > 64 ? 128 : 64;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t nkt = (K_total * (tf32 ? 4 : 2) + 127) / 128;
+  if (tiles >= (int64_t)num_sms * 3 / 2 || nkt < 8) return 1;
+  int ks = (int)((2 * (int64_t)num_sms + tiles - 1) / tiles);
+  ks = (int)std::min<int64_t>(ks, nkt / 4);
+  return std::max(1, std::min(ks, 8));
+}
+
+bool gemm_tc_supported(const TcGemm& g) {
+  const int e = g.tf32 ? 4 : 2;
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+  if (!operand_ok(g.A_hi, g.lda, e) || !operand_ok(g.B_hi, g.ldb, e)) return false;
+  if (g.tf32 && (!operand_ok(g.A_lo, g.lda, e) || !operand_ok(g.B_lo, g.ldb, e))) return false;
+  if (g.K2 > 0) {
+    if (!operand_ok(g.A2_hi, g.lda2, e) || !operand_ok(g.B2_hi, g.ldb2, e)) return false;
+    if (g.tf32 && (!operand_ok(g.A2_lo, g.lda2, e) || !operand_ok(g.B2_lo, g.ldb2, e)))
+      return false;
+  }
+  return encode_fn() != nullptr;
+}
+
+cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
+  const bool tf32 = g.tf32 != 0;
+  const int BN = g.N > 64 ? 128 : 64;
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, !tf32, BM) &&
+            make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, !tf32, BN);
+  if (tf32)
+    ok = ok && make_map(&maps.a1l, g.A_lo, g.M, g.K, g.lda, false, BM) &&
+         make_map(&maps.b1l, g.B_lo, g.N, g.K, g.ldb, false, BN);
+  if (g.K2 > 0) {
+    ok = ok && make_map(&maps.a2h, g.A2_hi, g.M, g.K2, g.lda2, !tf32, BM) &&
+         make_map(&maps.b2h, g.B2_hi, g.N, g.K2, g.ldb2, !tf32, BN);
+    if (tf32)
+      ok = ok && make_map(&maps.a2l, g.A2_lo, g.M, g.K2, g.lda2, false, BM) &&
+           make_map(&maps.b2l, g.B2_lo, g.N, g.K2, g.ldb2, false, BN);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const int kpe = tf32 ? 32 : 64;
+  TcKParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.M = (int)g.M;
+  kp.N = (int)g.N;
+  kp.nk1 = (int)((g.K + kpe - 1) / kpe);
+  kp.nk2 = g.K2 > 0 ? (int)((g.K2 + kpe - 1) / kpe) : 0;
+  kp.ksplit = std::max(1, g.ksplit);
+  const int stage = (BM * 128 + BN * 128) * (tf32 ? 2 : 1);
+  kp.stages = std::max(2, std::min(8, kSmemBudget / stage));
+  kp.status = g.status;
+  kp.timeout_ns = g.timeout_ns;
+  if (kp.ksplit > 1) {
+    kp.part = g.part;
+    if (!kp.part) return cudaErrorInvalidValue;
+  } else {
+    kp.C = g.C;
+    kp.ldc = g.ldc;
+    kp.out_bf16 = g.out_bf16;
+    kp.accumulate = g.accumulate;
+    kp.bias1 = g.bias1;
+    kp.bias2 = g.bias2;
+    kp.bias2_limit = g.bias2_limit;
+    kp.bias_bf16 = g.bias_bf16;
+  }
+  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)kp.ksplit);
+  cudaError_t e;
+  if (tf32)
+    e = BN == 128 ? launch_tc<128, true>(maps, kp, grid, st) : launch_tc<64, true>(maps, kp, grid, st);
+  else
+    e = BN == 128 ? launch_tc<128, false>(maps, kp, grid, st)
+                  : launch_tc<64, false>(maps, kp, grid, st);
+  if (e != cudaSuccess || kp.ksplit == 1) return e;
+  const int64_t total = g.M * g.N;
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+  splitk_reduce_kernel<<<blocks, 256, 0, st>>>(g.part, kp.ksplit, g.M, g.N, g.C, g.ldc, g.out_bf16,
+                                               g.accumulate, g.bias1, g.bias2, g.bias2_limit,
+                                               g.bias_bf16);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t lds, float* hi,
+                          float* lo, int64_t ldd, bool transpose, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+  split_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd, transpose ? 1 : 0);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
+                           int64_t ldd, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const bf16*>(src), rows, cols, lds,
+                                              reinterpret_cast<bf16*>(dst), ldd);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+}  // namespace lr

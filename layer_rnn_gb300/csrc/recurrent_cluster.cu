@@ -8,9 +8,11 @@
 // for the whole sequence, so per step it only stages its K slice of the
 // previous step's broadcast vector (h_{t-1} forward, dG_h backward) instead of
 // the whole vector.  The cluster's partial sums meet through distributed shared
-// memory: after a cluster barrier, each block sums, in a fixed order, the
-// partials of the units whose pointwise math it owns (deterministic), applies
-// the fused gate math, stores, and publishes its step flag.
+// memory: every block stores each row's partial straight into the shared
+// memory of the block that owns that unit's pointwise step; after a cluster
+// barrier each block sums the partials it received in rank order
+// (deterministic), applies the fused gate math, stores, and publishes its step
+// flag.
 //
 // Every wait is bounded.  The cluster barrier itself has no time limit, so a
 // block that gives up on a step flag keeps executing every cluster barrier of
@@ -47,23 +49,32 @@ struct Shape { int RM, RN, LM, LN; };
 constexpr Shape kCShapes[4] = {{3, 5, 8, 4}, {3, 5, 4, 4}, {3, 5, 2, 4}, {3, 5, 1, 4}};
 constexpr int kNumCShapes = 4;
 
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// load a float from the same shared-memory offset in block `rank` of this cluster
-__device__ __forceinline__ float ld_peer_f32(const float* local_ptr, unsigned rank) {
+// store a float to the same shared-memory offset in block `rank` of this cluster
+__device__ __forceinline__ void st_peer_f32(float* local_ptr, unsigned rank, float v) {
   const unsigned laddr = static_cast<unsigned>(__cvta_generic_to_shared(local_ptr));
   unsigned raddr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
 }
 
 struct CSmem {
-  void* A; void* B; float* red; float* part; float* outs;
+  void* A; void* B; float* red; float* part; float* recv; float* outs;
 };
 
 template <typename T>
@@ -75,8 +86,10 @@ __device__ __forceinline__ CSmem carve_c(unsigned char* smem, const RecPlan& pl,
   c.B = B;
   c.red = reinterpret_cast<float*>(B + (size_t)kNB * pl.ldbs);
   c.part = c.red + (pl.Wk > 1 ? (size_t)pl.Wk * pl.Mp * kNB : 0);
-  c.outs = c.part + (size_t)2 * pl.Mp * kNB;
-  (void)orows;
+  // partials pushed by every rank of the cluster, by step parity:
+  // recv[parity][sender][orows][kNB]
+  c.recv = c.part + (size_t)pl.Mp * kNB;
+  c.outs = c.recv + (size_t)2 * pl.cluster * orows * kNB;
   return c;
 }
 
@@ -93,6 +106,7 @@ __device__ __forceinline__ void stage_slice(T* Bs, int ldbs, const T* src, int64
                                             int Kc) {
   constexpr int VE = 16 / (int)sizeof(T);
   const int nv = Kc / VE;
+  if (N > kNB || Kc > ldbs) return;  // never, by construction (checked by the plan)
   for (int idx = threadIdx.x; idx < N * nv; idx += kThreads) {
     const int n = idx / nv, c = idx - n * nv;
     cp_async16(Bs + n * ldbs + c * VE, src + n * ldsrc + c * VE);
@@ -224,7 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   T* Bs = reinterpret_cast<T*>(sm.B);
   const int64_t GH = (int64_t)G * H;
 
-  if (tid == 0) s_fail = ld_volatile_int(p.status) != kDevOk;
+  if (tid == 0) {
+    s_fail = ld_volatile_int(p.status) != kDevOk;
+    // the launch must have formed the planned clusters, with this block at rank
+    // q: otherwise no peer shared memory is touched at all
+    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q) {
+      atomicCAS(p.status, kDevOk, kDevCheck);
+      s_fail = 1;
+    }
+  }
   // resident slice: row g*Ur + u, column kk <- W_hh[g*H + u0 + u][k0 + kk]
   const T* W = reinterpret_cast<const T*>(a.whh);
   for (int64_t idx = tid; idx < (int64_t)pl.Mp * pl.lda; idx += kThreads) {
@@ -265,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int s = 0; s < nT; ++s) {
     const int t = d ? nT - 1 - s : s;
     const int tp = d ? t + 1 : t - 1;
-    float* part = sm.part + (size_t)(s & 1) * pl.Mp * kNB;
+    float* part = sm.part;
     CTRACE(s, 0);
     if (!failed && s > 0 && Kc > 0 && warp == 0) {
       if (!warp_wait_flags(flags, p.flag_stride, flo, fhi, (unsigned)s, p.status, p.timeout_ns,
@@ -284,17 +306,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     CTRACE(s, 6);
     block_contract<T, RM, RN, LM, LN>(sm, pl, Kc, have, part);
+    __syncthreads();
     CTRACE(s, 2);
+    // push each row's partial to the rank that owns the unit's pointwise step
+    float* recv = sm.recv + (size_t)(s & 1) * Pk * G * Uq * kNB;
+    if (!failed) {
+      for (int idx = tid; idx < G * Urc * N; idx += kThreads) {
+        const int g = idx / (Urc * N), rem = idx - g * (Urc * N);
+        const int u = rem / N, nn = rem - u * N;
+        const int owner = u / Uq, uo = u - owner * Uq;
+        if (owner >= Pk || nn >= kNB || g * Ur + u >= pl.Mp) {  // never, by construction
+          atomicCAS(p.status, kDevOk, kDevCheck);
+          continue;
+        }
+        st_peer_f32(recv + ((size_t)q * G * Uq + g * Uq + uo) * kNB + nn, (unsigned)owner,
+                    part[(g * Ur + u) * kNB + nn]);
+      }
+    }
     cluster_sync_all();
-    // this block's units: sum the cluster's partials in rank order
     float* outs = sm.outs;
     if (!failed) {
       for (int idx = tid; idx < G * Uqc * N; idx += kThreads) {
         const int g = idx / (Uqc * N), rem = idx - g * (Uqc * N);
         const int u = rem / N, nn = rem - u * N;
-        const float* src_p = part + (g * Ur + uq0 + u) * kNB + nn;
         float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank) v += ld_peer_f32(src_p, (unsigned)rank);
+        for (int rank = 0; rank < Pk; ++rank)
+          v += recv[((size_t)rank * G * Uq + g * Uq + u) * kNB + nn];
         outs[(g * Uq + u) * kNB + nn] = v;
       }
     }
@@ -347,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
     CTRACE(s, 5);
   }
-  cluster_sync_all();  // peers may still be reading this block's partials
+  cluster_sync_all();  // no block leaves while a peer may still store into it
   if (!failed && item) {
     const int64_t o = (int64_t)n * H + j;
     if (a.hy) reinterpret_cast<T*>(a.hy)[o] = from_f<T>(h_own);
@@ -379,7 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   T* As = reinterpret_cast<T*>(sm.A);
   T* Bs = reinterpret_cast<T*>(sm.B);
 
-  if (tid == 0) s_fail = ld_volatile_int(p.status) != kDevOk;
+  if (tid == 0) {
+    s_fail = ld_volatile_int(p.status) != kDevOk;
+    // the launch must have formed the planned clusters, with this block at rank
+    // q: otherwise no peer shared memory is touched at all
+    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q) {
+      atomicCAS(p.status, kDevOk, kDevCheck);
+      s_fail = 1;
+    }
+  }
   // resident slice, transposed: A[u][kk] = W_hh[k0 + kk][u0 + u]; consecutive
   // threads read consecutive units of one row
   const T* W = reinterpret_cast<const T*>(a.whh);
@@ -425,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int s = 0; s <= nT; ++s) {
     const int t = d ? s : nT - 1 - s;    // time processed at this step (s < nT)
     const int tp = d ? s - 1 : nT - s;   // time processed at the previous step (s > 0)
-    float* part = sm.part + (size_t)(s & 1) * pl.Mp * kNB;
+    float* part = sm.part;
     CTRACE(s, 0);
     if (!failed && s > 0 && Kc > 0 && warp == 0) {
       bool ok = true;
@@ -446,15 +491,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     CTRACE(s, 6);
     block_contract<T, RM, RN, LM, LN>(sm, pl, Kc, have, part);
+    __syncthreads();
     CTRACE(s, 2);
+    float* recv = sm.recv + (size_t)(s & 1) * Pk * Uq * kNB;
+    if (!failed) {
+      for (int idx = tid; idx < Urc * N; idx += kThreads) {
+        const int u = idx / N, nn = idx - u * N;
+        const int owner = u / Uq, uo = u - owner * Uq;
+        if (owner >= Pk || nn >= kNB || u >= pl.Mp) {  // never, by construction
+          atomicCAS(p.status, kDevOk, kDevCheck);
+          continue;
+        }
+        st_peer_f32(recv + ((size_t)q * Uq + uo) * kNB + nn, (unsigned)owner, part[u * kNB + nn]);
+      }
+    }
     cluster_sync_all();
     float* outs = sm.outs;
     if (!failed) {
       for (int idx = tid; idx < Uqc * N; idx += kThreads) {
         const int u = idx / N, nn = idx - u * N;
-        const float* src_p = part + (uq0 + u) * kNB + nn;
         float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank) v += ld_peer_f32(src_p, (unsigned)rank);
+        for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * Uq + u) * kNB + nn];
         outs[u * kNB + nn] = v;
       }
     }
@@ -597,8 +654,8 @@ bool rec_cluster_plan(bool backward, int mode, int bf16, int D, int H, int N, in
         pl.ldbs = (int)(rup(Kk, 128 / e) + pad);
         const int orows = backward ? Uq : G * Uq;
         pl.smem = (size_t)pl.Mp * pl.lda * e + (size_t)kNB * pl.ldbs * e +
-                  (Wk > 1 ? (size_t)Wk * pl.Mp * kNB * 4 : 0) + (size_t)2 * pl.Mp * kNB * 4 +
-                  (size_t)orows * kNB * 4 + 256;
+                  (Wk > 1 ? (size_t)Wk * pl.Mp * kNB * 4 : 0) + (size_t)pl.Mp * kNB * 4 +
+                  (size_t)2 * Pk * orows * kNB * 4 + (size_t)orows * kNB * 4 + 256;
         if (pl.smem > smem_limit) continue;
         if (D * pl.P > num_sms) continue;
         // rough cycle estimate per step: the contraction is bound by FMA issue
@@ -610,7 +667,7 @@ bool rec_cluster_plan(bool backward, int mode, int bf16, int D, int H, int N, in
                                     (double)kWarps * vec_per_warp * wf) * 1.2;
         const double stage = (double)N * Kk * e / 64.0;
         const double lred = Wk > 1 ? (double)pl.Mp * kNB * Wk / kThreads * 8 + 60 : 0;
-        const double cred = (double)Pk * orows * N / kThreads * 30 + 200;
+        const double cred = (double)Mb * N / kThreads * 10 + (double)Pk * orows * N / kThreads * 4 + 150;
         const double cost = fma + stage + lred + cred;
         if (!found || cost < best_cost) {
           found = true;
@@ -639,24 +696,18 @@ cudaError_t rec_cluster_launch(bool backward, const RecParams& p, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  // Not a cooperative launch: the plan keeps the grid within the measured
+  // co-resident cluster capacity (one block per SM), and every step wait is
+  // bounded, so a cluster that is not resident shows up as RNN_ERR_TIMEOUT.
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = pl.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e != cudaSuccess) {
-    // cooperative + cluster not accepted: the plan already fits the grid in the
-    // co-resident cluster capacity; every step wait is bounded either way
-    cudaGetLastError();
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-  }
   return e;
 }
 

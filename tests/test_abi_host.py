@@ -99,9 +99,9 @@ def test_workspace_regions_disjoint_and_aligned(B, mode, L, bidir, dtype):
         total = B.rnn_workspace_size(h, T, N)
         D = 2 if bidir else 1
         spans = []
-        for region in range(8):
+        for region in range(9):
             per_layer = region == B.RNN_WS_YLAYER
-            glob = region in (B.RNN_WS_GX, B.RNN_WS_DY)
+            glob = region in (B.RNN_WS_GX, B.RNN_WS_DY, B.RNN_WS_GEMM)
             for l in range(1 if glob else L):
                 for d in range(1 if (glob or per_layer) else D):
                     off, nb = B.rnn_workspace_layout(h, T, N, region, l, d)
@@ -122,7 +122,7 @@ def test_workspace_regions_disjoint_and_aligned(B, mode, L, bidir, dtype):
         with pytest.raises(B.RnnError):
             B.rnn_workspace_size(h, 0, N)
         with pytest.raises(B.RnnError):
-            B.rnn_workspace_layout(h, T, N, 8, 0, 0)
+            B.rnn_workspace_layout(h, T, N, 9, 0, 0)
     finally:
         B.rnn_destroy(h)
 

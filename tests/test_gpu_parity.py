@@ -83,6 +83,20 @@ def test_workload_parity_lstm4_bf16():
     assert np.array_equal(gpu["y_inf"], gpu["y"])
 
 
+@pytest.mark.parametrize("case", [("lstm", 2, True, 6, 5, 24, 40, "f32"),
+                                  ("gru", 1, False, 7, 9, 64, 48, "bf16")],
+                         ids=["lstm-f32", "gru-bf16"])
+def test_cuda_core_gemm_flag_parity(case):
+    # the CUDA-core GEMM path, selected by flag, against the oracle as well
+    from layer_rnn_gb300 import binding as B
+    mode, L, bidir, T, N, I, H, dt = case
+    cfg = wl.make_config(mode, L, bidir, T, N, I, H, dt, 0.4, seed=77)
+    inp = wl.make_inputs(cfg)
+    gpu = harness.run_gpu(cfg, inp, flags=B.RNN_FLAG_SIMT_GEMM)
+    ref = harness.run_oracle(cfg, inp)
+    harness.assert_parity(cfg, gpu, ref)
+
+
 def test_deterministic_across_calls():
     cfg = wl.make_config("gru", 2, True, 12, 20, 64, 80, "f32", 0.3, seed=9)
     inp = wl.make_inputs(cfg)
