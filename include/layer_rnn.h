@@ -80,6 +80,8 @@ typedef enum {
                                      returns the device status word            */
 #define RNN_FLAG_SIMT_GEMM  0x2u  /* dense phases on the CUDA-core GEMM instead
                                      of the tensor-core GEMM                    */
+#define RNN_FLAG_SIMT_RECURRENT 0x4u  /* recurrent forward on the CUDA-core
+                                         kernels instead of the tensor-core one  */
 
 /* regions for rnn_workspace_layout */
 typedef enum {

@@ -342,6 +342,10 @@ struct PhaseScope {
 
 rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
   const bool bf = h->dtype == RNN_BF16;
+  if (!backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
+      rec_tc_plan(h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
+                  h->max_clusters, pl))
+    return RNN_OK;
   if (!rec_cluster_plan(backward, h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms,
                         h->cluster_smem, h->max_clusters, pl) &&
       !rec_make_plan(backward, h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
@@ -455,7 +459,9 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_FWD);
-      s = cuda_status(rp.plan.cluster ? rec_cluster_launch(false, rp, st) : rec_forward(rp, st));
+      s = cuda_status(rp.plan.tc        ? rec_tc_launch(rp, st)
+                      : rp.plan.cluster ? rec_cluster_launch(false, rp, st)
+                                        : rec_forward(rp, st));
       if (s != RNN_OK) return s;
     }
     in = out;
@@ -479,7 +485,8 @@ rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
   if (num_layers < 1 || (bidirectional != 0 && bidirectional != 1)) return RNN_ERR_INVALID_ARG;
   if (input_size < 1 || hidden_size < 1) return RNN_ERR_INVALID_ARG;
   if (dtype != RNN_F32 && dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
-  if ((flags & ~(RNN_FLAG_SYNC_CHECK | RNN_FLAG_SIMT_GEMM)) != 0) return RNN_ERR_INVALID_ARG;
+  if ((flags & ~(RNN_FLAG_SYNC_CHECK | RNN_FLAG_SIMT_GEMM | RNN_FLAG_SIMT_RECURRENT)) != 0)
+    return RNN_ERR_INVALID_ARG;
   if (hidden_size > 65536 || input_size > (int64_t(1) << 24) || num_layers > 1024)
     return RNN_ERR_UNSUPPORTED;
   rnn_handle* h = new (std::nothrow) rnn_handle();

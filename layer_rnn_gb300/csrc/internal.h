@@ -94,6 +94,7 @@ struct RecDirArgs {
 
 struct RecPlan {
   int direct = 0;       // 1: per-warp dataflow path (one batch chunk)
+  int tc = 0;           // 1: tensor-core forward path (recurrent_tc.cu)
   int shape = 0;        // register-tile shape id (see recurrent.cu)
   int P = 0;            // blocks per direction
   int U = 0;            // hidden units per block (last block may have fewer)
@@ -140,6 +141,10 @@ bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int n
 bool rec_cluster_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
                       size_t smem_limit, const int* max_clusters, RecPlan* out);
 cudaError_t rec_cluster_launch(bool backward, const RecParams& p, cudaStream_t st);
+// Tensor-core forward path: plan (false if the problem does not qualify) and launch.
+bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
+                 const int* max_clusters, RecPlan* out);
+cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st);
 // co-resident clusters of `cluster` blocks of the cluster kernels with `smem` bytes
 int rec_cluster_capacity(int cluster, size_t smem);
 
