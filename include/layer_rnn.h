@@ -82,6 +82,8 @@ typedef enum {
                                      of the tensor-core GEMM                    */
 #define RNN_FLAG_SIMT_RECURRENT 0x4u  /* recurrent forward on the CUDA-core
                                          kernels instead of the tensor-core one  */
+#define RNN_FLAG_NO_WAVEFRONT 0x8u    /* unidirectional stacks run layer after
+                                         layer instead of as one layer wavefront */
 
 /* regions for rnn_workspace_layout */
 typedef enum {

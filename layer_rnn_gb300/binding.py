@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "liblayer_rnn.so")
 RNN_TANH, RNN_LSTM, RNN_GRU = 0, 1, 2
 RNN_F32, RNN_BF16 = 0, 1
 RNN_FLAG_SYNC_CHECK, RNN_FLAG_SIMT_GEMM, RNN_FLAG_SIMT_RECURRENT = 0x1, 0x2, 0x4
+RNN_FLAG_NO_WAVEFRONT = 0x8
 (RNN_WS_GATES, RNN_WS_CSEQ, RNN_WS_HSEQ, RNN_WS_YLAYER, RNN_WS_DGX, RNN_WS_DGH,
  RNN_WS_GX, RNN_WS_DY, RNN_WS_GEMM) = range(9)
 PHASES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")

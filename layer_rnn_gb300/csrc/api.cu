@@ -105,6 +105,23 @@ int64_t opnd_bytes(int64_t rows, int64_t K, bool tf32) {
   return align256(rows * kpad(K, tf32) * (tf32 ? 4 : 2)) * (tf32 ? 2 : 1);
 }
 
+// whether a call may take the layer-wavefront path (host-side conditions; the
+// device-dependent plan can still decline)
+bool wf_candidate(const rnn_handle* h, int64_t N) {
+  return h->dtype == RNN_BF16 && h->D == 1 && h->L >= 2 && h->L <= kWfMaxLayers && N <= 128 &&
+         h->H % 8 == 0 && h->I % 8 == 0 &&
+         !(h->flags & (RNN_FLAG_NO_WAVEFRONT | RNN_FLAG_SIMT_RECURRENT));
+}
+
+// scratch of the wavefront path: packed weights and biases, plus (inference)
+// the per-layer hidden-state sequences the layers read from one another
+int64_t wf_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool training) {
+  if (!wf_candidate(h, N)) return 0;
+  int64_t b = wf_pack_bytes_bound(h->mode, h->L, h->I, h->H);
+  if (!training) b += h->L * align256((T + 1) * N * h->H * 2);
+  return b + 4096;
+}
+
 // scratch the GEMM phases of one call need (maximum over the phases)
 int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool training) {
   const bool tf = h->dtype != RNN_BF16;
@@ -123,7 +140,7 @@ int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool train
     need = std::max(need, dgt + opnd_bytes(std::max(I_l, h->H), TN, tf) +
                               align256((int64_t)kMaxKsplit * GH * std::max(I_l, h->H) * 4));
   }
-  return need + 4096;
+  return std::max(need, wf_scratch_bytes(h, T, N, training)) + 4096;
 }
 
 struct Scratch {
@@ -406,6 +423,80 @@ rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, 
   return RNN_OK;
 }
 
+// Layer wavefront (unidirectional bf16 stacks): all layers in one persistent
+// launch.  *used = false (and nothing enqueued) when the problem or the scratch
+// does not qualify; the layers then run one after another.
+rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N,
+                               const void* x, const void* h0, const void* c0, const void* W,
+                               void* y, void* hy, void* cy, char* ws, bool training, Scratch sc,
+                               bool* used) {
+  *used = false;
+  if (!wf_candidate(h, N)) return RNN_OK;
+  WfPlan pl;
+  if (!wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &pl))
+    return RNN_OK;
+  if ((size_t)h->L * pl.Pr * 128 > kSyncBytes - 64) return RNN_OK;
+  const int64_t H = h->H, NH = N * H, e = 2;
+  WfParams p;
+  p.mode = h->mode;
+  p.T = (int)T;
+  p.N = (int)N;
+  p.H = (int)H;
+  p.I = (int)h->I;
+  p.L = h->L;
+  p.Gs = h->Gs;
+  p.plan = pl;
+  p.x = x;
+  p.flags = h->d_sync;
+  p.status = h->d_status;
+  p.timeout_ns = h->timeout_ns;
+  p.fault_block = h->fault_block;
+  p.fault_step = h->fault_step;
+  WsLayout lay;
+  if (training) lay = ws_layout(h, T, N);
+  const int64_t rows = (int64_t)pl.Pr * pl.R * pl.Ur;
+  for (int l = 0; l < h->L; ++l) {
+    WfLayer& a = p.layer[l];
+    const int64_t I_l = layer_in(h, l);
+    a.kp = wf_kp(I_l, H);
+    a.nchx = (int)((I_l + 63) / 64);
+    a.nch = (int)(a.kp / 64);
+    a.wp = sc.take(align256(rows * a.kp * 2));
+    a.bias = static_cast<float*>(sc.take(align256(rows * 4)));
+    if (!a.wp || !a.bias) return RNN_OK;
+    if (training) {
+      a.hseq = mp<char>(ws, lay.at(RNN_WS_HSEQ, l, 0).off);
+      a.gates = mp<float>(ws, lay.at(RNN_WS_GATES, l, 0).off);
+      a.cseq = h->mode == RNN_LSTM ? mp<float>(ws, lay.at(RNN_WS_CSEQ, l, 0).off) : nullptr;
+      a.y = l == h->L - 1 ? y : mp<char>(ws, lay.at(RNN_WS_YLAYER, l, 0).off);
+    } else {
+      a.hseq = sc.take(align256((T + 1) * NH * e));
+      if (!a.hseq) return RNN_OK;
+      a.y = l == h->L - 1 ? y : nullptr;
+    }
+    a.h0 = h0 ? cp<char>(h0, l * NH * e) : nullptr;
+    a.c0 = (c0 && h->mode == RNN_LSTM) ? cp<float>(c0, l * NH * 4) : nullptr;
+    a.hy = hy ? mp<char>(hy, l * NH * e) : nullptr;
+    a.cy = (cy && h->mode == RNN_LSTM) ? mp<float>(cy, l * NH * 4) : nullptr;
+  }
+  *used = true;
+  {
+    PhaseScope ps(h, st, RNN_PHASE_INPUT_GEMM);
+    for (int l = 0; l < h->L; ++l) {
+      WfLayer& a = p.layer[l];
+      const cudaError_t ce =
+          wf_pack(pl, h->mode, layer_in(h, l), H, cp<char>(W, weight_offset(h, l, 0, 0) * e),
+                  cp<char>(W, weight_offset(h, l, 0, 1) * e),
+                  cp<char>(W, weight_offset(h, l, 0, 2) * e),
+                  cp<char>(W, weight_offset(h, l, 0, 3) * e), const_cast<void*>(a.wp),
+                  const_cast<float*>(a.bias), st);
+      if (ce != cudaSuccess) return RNN_ERR_CUDA;
+    }
+  }
+  PhaseScope ps(h, st, RNN_PHASE_REC_FWD);
+  return cuda_status(wf_launch(p, st));
+}
+
 rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, const void* x,
                           const void* h0, const void* c0, const void* W, void* y, void* hy,
                           void* cy, char* ws, bool training, Scratch sc) {
@@ -422,8 +513,12 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     ybuf[0] = mp<char>(h->scratch, gx_bytes);
     ybuf[1] = mp<char>(h->scratch, gx_bytes + yb);
   }
+  bool wf_used = false;
+  rnn_status_t s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc,
+                                     &wf_used);
+  if (wf_used || s != RNN_OK) return s;
   RecPlan plan;
-  rnn_status_t s = plan_rec(h, false, N, &plan);
+  s = plan_rec(h, false, N, &plan);
   if (s != RNN_OK) return s;
   const void* in = x;
   for (int l = 0; l < h->L; ++l) {
@@ -485,7 +580,8 @@ rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
   if (num_layers < 1 || (bidirectional != 0 && bidirectional != 1)) return RNN_ERR_INVALID_ARG;
   if (input_size < 1 || hidden_size < 1) return RNN_ERR_INVALID_ARG;
   if (dtype != RNN_F32 && dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
-  if ((flags & ~(RNN_FLAG_SYNC_CHECK | RNN_FLAG_SIMT_GEMM | RNN_FLAG_SIMT_RECURRENT)) != 0)
+  if ((flags & ~(RNN_FLAG_SYNC_CHECK | RNN_FLAG_SIMT_GEMM | RNN_FLAG_SIMT_RECURRENT |
+                 RNN_FLAG_NO_WAVEFRONT)) != 0)
     return RNN_ERR_INVALID_ARG;
   if (hidden_size > 65536 || input_size > (int64_t(1) << 24) || num_layers > 1024)
     return RNN_ERR_UNSUPPORTED;

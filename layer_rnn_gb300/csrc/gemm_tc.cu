@@ -448,6 +448,24 @@ cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaSt
 
 }  // namespace
 
+bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !ptr || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3], sb[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    bx[i] = (cuuint32_t)box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) sb[i] = (cuuint64_t)strides_bytes[i];
+  return enc(static_cast<CUtensorMap*>(map),
+             bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             (cuuint32_t)rank, const_cast<void*>(ptr), d, sb, bx, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms) {
   const int BN = N > 64 ? 128 : 64;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
