@@ -245,6 +245,7 @@ def run_ours(args, cfg):
     lstm = cfg["mode"] == "lstm"
     inp = wl.make_inputs(cfg, seed=cfg["seed"] + rank)
     r = B.Rnn(cfg["mode"], L, cfg["bidir"], I, H, dt, 0)
+    paths = B.rnn_get_paths(r.h, N)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         x = harness.to_dev(inp["x"], dt, dev)
@@ -345,6 +346,11 @@ def run_ours(args, cfg):
 
     peaks, peak_src = load_peaks()
     fl = phase_flops(cfg)
+    if paths[0] == "wavefront":
+        # the wavefront computes each step's input projection inside the
+        # recurrent kernel; the input phase only packs the weights
+        fl["rec_fwd"] += fl["input_gemm"]
+        fl["input_gemm"] = 0.0
     total_flop = sum(fl.values())
     sm_clk = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -352,7 +358,9 @@ def run_ours(args, cfg):
 
     def phase_roof(ph):
         """(bound, peak TFLOP/s, note) of one phase, timed inside the step."""
-        if ph.endswith("gemm"):
+        on_tensor = ph.endswith("gemm") or (ph == "rec_fwd" and paths[0] in ("tensor", "wavefront")) \
+            or (ph == "rec_bwd" and paths[1] == "tensor")
+        if on_tensor:
             if dt == "bf16":
                 return "tensor", bf16_sus, "%s bf16 dense, sustained (cuBLAS loop)" % peak_src
             return ("tensor", bf16_sus * 1.1 / 2.25 / 3.0,
@@ -370,7 +378,14 @@ def run_ours(args, cfg):
         per_phase[ph] = {"ms": round(ms_ph, 4), "kernels": phases[ph][1] / args.steps,
                          "algorithmic_tflop": round(fl[ph] / 1e12, 6), "bound": b_,
                          "achieved": round(ach, 3), "peak": round(pk_, 3),
-                         "frac": round(ach / pk_, 4) if pk_ else None}
+                         "frac": round(ach / pk_, 4) if pk_ and fl[ph] else None}
+        if ph in ("rec_fwd", "rec_bwd"):
+            # serial steps of the phase: L * T layer steps, or T + L - 1
+            # wavefront steps when all layers run in one launch
+            wave = ph == "rec_fwd" and paths[0] == "wavefront"
+            nsteps = (T + L - 1) if wave else L * T
+            per_phase[ph]["path"] = paths[0] if ph == "rec_fwd" else paths[1]
+            per_phase[ph]["us_per_step"] = round(ms_ph * 1e3 / nsteps, 3)
     # dominant phase by time share
     dom = max(PHASE_NAMES, key=lambda p: phases[p][0])
     avg_ms = phases[dom][0] / max(1, args.steps)
@@ -398,6 +413,7 @@ def run_ours(args, cfg):
                    "l2": "flushed before every timed step (256 MiB write, untimed)"},
         "effective_tflops": round(total_flop * ws_n / (ms_step_max * 1e-3) / 1e12, 3),
         "phases": per_phase,
+        "recurrent_paths": {"fwd": paths[0], "bwd": paths[1]},
         "roofline": {"kernel": PHASE_KERNELS[dom], "phase": dom, "bound": bound,
                      "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
                      "frac": round(achieved / peak, 4) if peak else None,

@@ -80,8 +80,9 @@ typedef enum {
                                      returns the device status word            */
 #define RNN_FLAG_SIMT_GEMM  0x2u  /* dense phases on the CUDA-core GEMM instead
                                      of the tensor-core GEMM                    */
-#define RNN_FLAG_SIMT_RECURRENT 0x4u  /* recurrent forward on the CUDA-core
-                                         kernels instead of the tensor-core one  */
+#define RNN_FLAG_SIMT_RECURRENT 0x4u  /* recurrent forward and backward on the
+                                         CUDA-core kernels instead of the
+                                         tensor-core ones                        */
 #define RNN_FLAG_NO_WAVEFRONT 0x8u    /* unidirectional stacks run layer after
                                          layer instead of as one layer wavefront */
 
@@ -228,6 +229,19 @@ rnn_status_t rnn_enable_phase_timing(rnn_t h, int enable);
  * summed milliseconds between the events bracketing the phase and the number
  * of kernels the library launched inside it (arrays of RNN_PHASE_NUM). */
 rnn_status_t rnn_get_phase_times(rnn_t h, double* ms, int64_t* launches);
+
+/* Kernels the recurrent phases of a call with batch N run on this device
+ * (the choice depends on the sizes, the flags and the device).  Sets up the
+ * handle's device state like a compute call; enqueues nothing.
+ *   *fwd: RNN_PATH_* of the recurrent forward; *bwd: of the backward. */
+typedef enum {
+  RNN_PATH_STAGED = 0,     /* CUDA-core, per-block slice in shared memory      */
+  RNN_PATH_DIRECT = 1,     /* CUDA-core, per-warp dataflow                     */
+  RNN_PATH_CLUSTER = 2,    /* CUDA-core, cluster K split over DSMEM            */
+  RNN_PATH_TENSOR = 3,     /* tcgen05, slice in tensor memory, cluster K split */
+  RNN_PATH_WAVEFRONT = 4   /* tcgen05 layer wavefront, all layers in one launch */
+} rnn_path_t;
+rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
 
 /* Static description of the status code. */
 const char* rnn_status_string(rnn_status_t s);

@@ -50,6 +50,8 @@ SIGNATURES = {
     "rnn_set_debug": (_i32, [_vp, _i32, _i32, _i64]),
     "rnn_enable_phase_timing": (_i32, [_vp, _i32]),
     "rnn_get_phase_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _pi64]),
+    "rnn_get_paths": (_i32, [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int),
+                             ctypes.POINTER(ctypes.c_int)]),
     "rnn_status_string": (ctypes.c_char_p, [_i32]),
 }
 
@@ -164,6 +166,16 @@ def rnn_get_phase_times(h):
     n = (ctypes.c_int64 * len(PHASES))()
     _call("rnn_get_phase_times", h, ms, n)
     return {p: (ms[i], n[i]) for i, p in enumerate(PHASES)}
+
+
+PATHS = {0: "staged", 1: "direct", 2: "cluster", 3: "tensor", 4: "wavefront"}
+
+
+def rnn_get_paths(h, N):
+    """(forward, backward) recurrent kernel paths of a call with batch N."""
+    f, b = ctypes.c_int(), ctypes.c_int()
+    _call("rnn_get_paths", h, N, ctypes.byref(f), ctypes.byref(b))
+    return PATHS[f.value], PATHS[b.value]
 
 
 def rnn_status_string(code):

@@ -29,6 +29,7 @@ struct rnn_handle {
   int num_sms = 0;
   size_t smem_optin = 0;
   int max_clusters[9] = {0};   // co-resident clusters of 1..8 blocks (cluster kernels)
+  int bwd_caps[17] = {0};      // co-resident clusters of up to 16 blocks (tensor-core backward)
   size_t cluster_smem = 0;     // largest dynamic shared memory at which clusters fit
   unsigned* d_sync = nullptr;  // step flags (one per 128-byte line), status word at the end
   int* d_status = nullptr;
@@ -303,6 +304,7 @@ rnn_status_t device_setup(rnn_handle* h) {
   h->num_sms = sms;
   h->smem_optin = (size_t)optin;
   query_clusters(optin, &h->cluster_smem, h->max_clusters);
+  for (int c : {4, 8, 12, 14, 16}) h->bwd_caps[c] = rec_tc_bwd_capacity(c, 120 * 1024);
   return RNN_OK;
 }
 
@@ -362,6 +364,11 @@ rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
   if (!backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
       rec_tc_plan(h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
                   h->max_clusters, pl))
+    return RNN_OK;
+  if (backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
+      rec_tc_bwd_plan(h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
+                      h->bwd_caps, pl) &&
+      (size_t)pl->P * h->D * 128 <= kSyncBytes - 64)
     return RNN_OK;
   if (!rec_cluster_plan(backward, h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms,
                         h->cluster_smem, h->max_clusters, pl) &&
@@ -762,7 +769,9 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
-      s = cuda_status(rp.plan.cluster ? rec_cluster_launch(true, rp, st) : rec_backward(rp, st));
+      s = cuda_status(rp.plan.tc        ? rec_tc_bwd_launch(rp, st)
+                      : rp.plan.cluster ? rec_cluster_launch(true, rp, st)
+                                        : rec_backward(rp, st));
       if (s != RNN_OK) return finish(h, st, s);
     }
     // dX = sum_d dG_x[d] W_ih[l,d]; for l > 0 it is dy of the layer below
@@ -899,6 +908,32 @@ rnn_status_t rnn_get_phase_times(rnn_t h, double* ms, int64_t* launches) {
     ms[i] = h->ms[i];
     launches[i] = h->launches[i];
   }
+  return RNN_OK;
+}
+
+rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
+  if (!h || !fwd || !bwd || N < 1) return RNN_ERR_INVALID_ARG;
+  rnn_status_t s = device_setup(h);
+  if (s != RNN_OK) return s;
+  auto kind = [](const RecPlan& pl) {
+    return pl.tc ? RNN_PATH_TENSOR : pl.cluster ? RNN_PATH_CLUSTER
+                                   : pl.direct  ? RNN_PATH_DIRECT
+                                                : RNN_PATH_STAGED;
+  };
+  WfPlan wp;
+  RecPlan pl;
+  if (wf_candidate(h, N) &&
+      wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &wp) &&
+      (size_t)h->L * wp.Pr * 128 <= kSyncBytes - 64) {
+    *fwd = RNN_PATH_WAVEFRONT;
+  } else {
+    s = plan_rec(h, false, N, &pl);
+    if (s != RNN_OK) return s;
+    *fwd = kind(pl);
+  }
+  s = plan_rec(h, true, N, &pl);
+  if (s != RNN_OK) return s;
+  *bwd = kind(pl);
   return RNN_OK;
 }
 

@@ -94,7 +94,7 @@ struct RecDirArgs {
 
 struct RecPlan {
   int direct = 0;       // 1: per-warp dataflow path (one batch chunk)
-  int tc = 0;           // 1: tensor-core forward path (recurrent_tc.cu)
+  int tc = 0;           // 1: tensor-core forward path (recurrent_tc.cu), 2: backward (recurrent_tc_bwd.cu)
   int shape = 0;        // register-tile shape id (see recurrent.cu)
   int P = 0;            // blocks per direction
   int U = 0;            // hidden units per block (last block may have fewer)
@@ -147,6 +147,13 @@ bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t sm
 cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st);
 // co-resident clusters of `cluster` blocks of the cluster kernels with `smem` bytes
 int rec_cluster_capacity(int cluster, size_t smem);
+// Tensor-core backward path (recurrent_tc_bwd.cu): plan (false if the problem
+// does not qualify; caps[c] = co-resident clusters of c blocks, c <= 16) and
+// launch; capacity of its kernel for clusters of up to 16 blocks.
+bool rec_tc_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
+                     const int* caps, RecPlan* out);
+cudaError_t rec_tc_bwd_launch(const RecParams& p, cudaStream_t st);
+int rec_tc_bwd_capacity(int cluster, size_t smem);
 
 // ---------------------------------------------------------------------------
 // layer wavefront (unidirectional bf16 stacks): one persistent launch runs all

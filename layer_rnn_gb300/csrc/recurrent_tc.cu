@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 #ifdef LAYER_RNN_TRACE
 __device__ unsigned long long g_ttrace[4][1024][8];
@@ -36,135 +37,10 @@ namespace lr {
 
 namespace {
 
+using namespace tc;
+
 constexpr int kTThreads = 256;
 constexpr int kTM = 128;  // MMA M (rows of W per block, padded)
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned cl_size() {
-  unsigned n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-__device__ __forceinline__ unsigned cl_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cl_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void st_peer(float* local_ptr, unsigned rank, float v) {
-  unsigned raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(raddr)
-               : "r"(smem_addr(local_ptr)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// B tile descriptor: K-major rows of 128 bytes, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (tile base 1024-byte aligned)
-__device__ __forceinline__ uint64_t b_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// byte offset of the 16-byte chunk `c` (0..7) of row `n` inside one K atom
-// (rows x 128 bytes, 128-byte swizzle: chunk index XOR row index within the
-// 8-row group)
-__device__ __forceinline__ uint32_t sw_off(int n, int c) {
-  return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
-}
-
-__device__ __forceinline__ void mma_a_tmem(bool bf, uint32_t d, uint32_t a, uint64_t b,
-                                           uint32_t idesc, uint32_t acc) {
-  if (bf)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// bounded; false once the limit passed or another block recorded a failure
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* status,
-                                                  long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  unsigned it = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++it & 63u) == 0) {
-      if (ld_volatile_int(status) != kDevOk) return false;
-      if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
-        atomicCAS(status, kDevOk, kDevTimeout);
-        return false;
-      }
-    }
-  }
-  return true;
-}
 
 __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
   const int r = j / Ur;
@@ -429,10 +305,15 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
         if (!row_ok || owner >= Pk) continue;
+        // 16-byte pieces (row starts are 64-byte aligned, Nm % 16 == 0); columns
+        // N .. Nm-1 of D are zero (the staged rows beyond N are zero) and unread
         float* dst = recv + ((size_t)q * G * Uq + g * Uq + uo) * Nm + c0;
+        const bool ok = have && mma_ok;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c0 + i < N) st_peer(dst + i, (unsigned)owner, (have && mma_ok) ? v[i] : 0.f);
+        for (int i = 0; i < 32; i += 4)
+          if (c0 + i < N)
+            st_peer4(dst + i, (unsigned)owner, ok ? v[i] : 0.f, ok ? v[i + 1] : 0.f,
+                     ok ? v[i + 2] : 0.f, ok ? v[i + 3] : 0.f);
       }
     }
     fence_before();

@@ -168,29 +168,15 @@ __device__ __forceinline__ void store_bf16(void* base, int64_t i, float v) {
   reinterpret_cast<bf16*>(base)[i] = __float2bfloat16_rn(v);
 }
 
-// pointwise of one (unit, batch) item; gate pre-activations a0..a3 include
-// the bias.  Returns h; updates the state (LSTM c, GRU fp32 h).
-__device__ __forceinline__ float wf_cell(int mode, float a0, float a1, float a2, float a3,
-                                         float& state, float* gp, int64_t H) {
-  if (mode == 1) {
-    const float ig = sigmoidf_(a0), fg = sigmoidf_(a1), gg = tanhf(a2), og = sigmoidf_(a3);
-    const float c = fg * state + ig * gg;
-    state = c;
-    if (gp) {
-      gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
-    }
-    return og * tanhf(c);
-  }
-  // GRU: a2 = W_in x + b_in, a3 = W_hn h + b_hn
-  const float rg = sigmoidf_(a0), z = sigmoidf_(a1);
-  const float nv = tanhf(a2 + rg * a3);
-  const float h = (1.f - z) * nv + z * state;
-  state = h;
-  if (gp) {
-    gp[0] = rg; gp[H] = z; gp[2 * H] = nv; gp[3 * H] = a3;
-  }
-  return h;
+// Gate nonlinearities on the bf16 path: the hardware tanh (tanh.approx.f32,
+// relative error about 2^-11, below the bf16 resolution of the stored h) and
+// the identity sigmoid(x) = (1 + tanh(x / 2)) / 2.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+__device__ __forceinline__ float sigm_hw(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
 
 __global__ void __launch_bounds__(kWThreads, 1)
     rec_wf_kernel(const __grid_constant__ WfMaps maps, const __grid_constant__ WfParams p) {
@@ -411,35 +397,62 @@ __global__ void __launch_bounds__(kWThreads, 1)
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ci * 16), v);
         if (R == 4) {
+          // lanes 4u .. 4u+3 hold gates 0..3 of unit u for columns 4*j4 ..
+          // 4*j4+3; lane 4u+g collects all gates of column 4*j4+g.  The four
+          // columns of this thread are independent chains: exchange, gate math
+          // and cell update run for all of them before any (predicated) store.
+          float ga[4][4];
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
-            // lanes 4u .. 4u+3 hold gates 0..3 of unit u for columns
-            // 4*j4 .. 4*j4+3; lane 4u+g collects all gates of column 4*j4+g
-            const float x0 = v[4 * j4], x1 = v[4 * j4 + 1], x2 = v[4 * j4 + 2], x3 = v[4 * j4 + 3];
             float got[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float send = pick4(x0, x1, x2, x3, (g - k) & 3);
+              const float send =
+                  pick4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3], (g - k) & 3);
               got[k] = __shfl_sync(0xffffffffu, send, (lane & ~3) | ((g + k) & 3));
             }
             // got[k] is gate (g + k) & 3; gate i is got[(i - g) & 3]
-            const float a0 = pick4(got[0], got[1], got[2], got[3], (0 - g) & 3) + bias[0];
-            const float a1 = pick4(got[0], got[1], got[2], got[3], (1 - g) & 3) + bias[1];
-            const float a2 = pick4(got[0], got[1], got[2], got[3], (2 - g) & 3) + bias[2];
-            const float a3 = pick4(got[0], got[1], got[2], got[3], (3 - g) & 3) + bias[3];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              ga[j4][i] = pick4(got[0], got[1], got[2], got[3], (i - g) & 3) + bias[i];
+          }
+          float hv[4], o0[4], o1[4], o2[4], o3[4];
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            float& stv = state[sl * 4 + j4];
+            if (p.mode == 1) {  // LSTM: i, f, g, o
+              o0[j4] = sigm_hw(ga[j4][0]);
+              o1[j4] = sigm_hw(ga[j4][1]);
+              o2[j4] = tanh_hw(ga[j4][2]);
+              o3[j4] = sigm_hw(ga[j4][3]);
+              stv = fmaf(o1[j4], stv, o0[j4] * o2[j4]);
+              hv[j4] = o3[j4] * tanh_hw(stv);
+            } else {  // GRU: r, z, W_in x + b_in, W_hn h + b_hn
+              o0[j4] = sigm_hw(ga[j4][0]);
+              o1[j4] = sigm_hw(ga[j4][1]);
+              o2[j4] = tanh_hw(fmaf(o0[j4], ga[j4][3], ga[j4][2]));
+              o3[j4] = ga[j4][3];
+              stv = fmaf(o1[j4], stv - o2[j4], o2[j4]);  // (1 - z) n + z h
+              hv[j4] = stv;
+            }
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
             const int n = ci * 16 + 4 * j4 + g;
             if (!unit_ok || n >= N) continue;
             const int64_t row = row0 + n;
-            float* gp = a.gates ? a.gates + row * GsH + j : nullptr;
-            float& stv = state[sl * 4 + j4];
-            const float h = wf_cell(p.mode, a0, a1, a2, a3, stv, gp, H);
             const int64_t o = (int64_t)n * H + j;
+            const float h = hv[j4];
+            if (a.gates) {
+              float* gp = a.gates + row * GsH + j;
+              gp[0] = o0[j4]; gp[H] = o1[j4]; gp[2 * H] = o2[j4]; gp[3 * H] = o3[j4];
+            }
             hs[o] = __float2bfloat16_rn(h);
             if (a.y) store_bf16(a.y, row * H + j, h);
-            if (a.cseq) a.cseq[(int64_t)(t + 1) * N * H + o] = stv;
+            if (p.mode == 1 && a.cseq) a.cseq[(int64_t)(t + 1) * N * H + o] = state[sl * 4 + j4];
             if (last) {
               if (a.hy) store_bf16(a.hy, o, h);
-              if (a.cy) a.cy[o] = stv;
+              if (a.cy) a.cy[o] = state[sl * 4 + j4];
             }
           }
         } else {
@@ -448,7 +461,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const int n = ci * 16 + i;
             if (!unit_ok || n >= N) continue;
             const int64_t row = row0 + n;
-            const float h = tanhf(v[i] + bias[0]);
+            const float h = tanh_hw(v[i] + bias[0]);
             const int64_t o = (int64_t)n * H + j;
             hs[o] = __float2bfloat16_rn(h);
             if (a.y) store_bf16(a.y, row * H + j, h);

@@ -135,3 +135,52 @@ def test_barrier_timeout_is_reported_and_context_survives():
         torch.cuda.synchronize()
     finally:
         r.close()
+
+
+@pytest.mark.parametrize("case", [("lstm", 1, False, 9, 20, 48, 96, "f32"),
+                                  ("gru", 2, True, 5, 7, 24, 40, "f32"),
+                                  ("lstm", 2, False, 6, 12, 32, 64, "bf16")],
+                         ids=["lstm-f32", "gru-bi-f32", "lstm-bf16"])
+def test_cuda_core_recurrent_flag_parity(case):
+    # the CUDA-core recurrent kernels (forward and backward), selected by flag
+    from layer_rnn_gb300 import binding as B
+    mode, L, bidir, T, N, I, H, dt = case
+    cfg = wl.make_config(mode, L, bidir, T, N, I, H, dt, 0.4, seed=78)
+    inp = wl.make_inputs(cfg)
+    gpu = harness.run_gpu(cfg, inp, flags=B.RNN_FLAG_SIMT_RECURRENT)
+    ref = harness.run_oracle(cfg, inp)
+    harness.assert_parity(cfg, gpu, ref)
+
+
+def test_backward_timeout_is_reported_and_context_survives():
+    import torch
+    from layer_rnn_gb300 import binding as B
+    cfg = wl.make_config("lstm", 1, False, 7, 8, 32, 64, "f32", 0.3, seed=6)
+    inp = wl.make_inputs(cfg)
+    T, N, I, H = cfg["T"], cfg["N"], cfg["I"], cfg["H"]
+    r = B.Rnn("lstm", 1, False, I, H, "f32", 0)
+    try:
+        x = harness.to_dev(inp["x"], "f32")
+        W = harness.to_dev(inp["w"], "f32")
+        dy = harness.to_dev(inp["dy"], "f32")
+        y = harness.empty((T, N, H), "f32")
+        dx = harness.empty((T, N, I), "f32")
+        ws = r.alloc_workspace(T, N)
+        r.forward_training(x, None, None, W, y, None, None, ws)
+        assert r.check_status() == 0
+        # block 0 never announces backward step 2: the rest give up after 50 ms
+        B.rnn_set_debug(r.h, 0, 2, 50_000_000)
+        r.backward_data(W, dy, None, None, dx, None, None, ws)
+        assert r.check_status() == 6  # RNN_ERR_TIMEOUT
+        assert r.check_status() == 0
+        B.rnn_set_debug(r.h, -1, -1, 2_000_000_000)
+        r.backward_data(W, dy, None, None, dx, None, None, ws)
+        assert r.check_status() == 0
+        import oracle
+        params = oracle.unflatten_weights(inp["w"], "lstm", 1, False, I, H)
+        _, _, _, cache = oracle.forward("lstm", inp["x"], None, None, params, 1, False)
+        dx_ref, _, _, _ = oracle.backward(params, cache, inp["dy"])
+        assert harness.rel_err(harness.from_dev(dx), dx_ref) < harness.TOL_F32_GRAD
+        torch.cuda.synchronize()
+    finally:
+        r.close()
