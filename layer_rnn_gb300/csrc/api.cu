@@ -366,6 +366,11 @@ rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
                   h->max_clusters, pl))
     return RNN_OK;
   if (backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
+      rec_tcm_bwd_plan(h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
+                       h->max_clusters, pl) &&
+      (size_t)pl->P * h->D * 128 <= kSyncBytes - 64)
+    return RNN_OK;
+  if (backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
       rec_tc_bwd_plan(h->mode, bf, h->D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
                       h->bwd_caps, pl) &&
       (size_t)pl->P * h->D * 128 <= kSyncBytes - 64)
@@ -769,7 +774,8 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
-      s = cuda_status(rp.plan.tc        ? rec_tc_bwd_launch(rp, st)
+      s = cuda_status(rp.plan.tc == 3   ? rec_tcm_bwd_launch(rp, st)
+                      : rp.plan.tc      ? rec_tc_bwd_launch(rp, st)
                       : rp.plan.cluster ? rec_cluster_launch(true, rp, st)
                                         : rec_backward(rp, st));
       if (s != RNN_OK) return finish(h, st, s);

@@ -94,7 +94,8 @@ struct RecDirArgs {
 
 struct RecPlan {
   int direct = 0;       // 1: per-warp dataflow path (one batch chunk)
-  int tc = 0;           // 1: tensor-core forward path (recurrent_tc.cu), 2: backward (recurrent_tc_bwd.cu)
+  int tc = 0;           // 1: tensor-core forward (recurrent_tc.cu), 2: backward
+                        // (recurrent_tc_bwd.cu), 3: batch-as-M backward (recurrent_tc_bwdm.cu)
   int shape = 0;        // register-tile shape id (see recurrent.cu)
   int P = 0;            // blocks per direction
   int U = 0;            // hidden units per block (last block may have fewer)
@@ -154,6 +155,11 @@ bool rec_tc_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_
                      const int* caps, RecPlan* out);
 cudaError_t rec_tc_bwd_launch(const RecParams& p, cudaStream_t st);
 int rec_tc_bwd_capacity(int cluster, size_t smem);
+// Tensor-core backward with the batch as the MMA's M (recurrent_tc_bwdm.cu;
+// bf16, batch 64..128): plan (false if the problem does not qualify) and launch.
+bool rec_tcm_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
+                      const int* max_clusters, RecPlan* out);
+cudaError_t rec_tcm_bwd_launch(const RecParams& p, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // layer wavefront (unidirectional bf16 stacks): one persistent launch runs all

@@ -51,9 +51,9 @@ __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
 struct TcLayout {
   uint32_t b_hi, b_lo;      // staged B tiles: n_atoms x (Nm x 128 bytes)
   uint32_t recv;            // [2][Pk][G*Uq][Nm] f32
-  uint32_t outs;            // [G*Uq][Nm] f32
-  uint32_t hst, cst;        // [Uq][N] f32 state of the own units
-  uint32_t gxs;             // [G][Uq][N] f32 next projection values
+  uint32_t outs;            // [G][N][Uq] f32 summed partials
+  uint32_t hst, cst;        // [N][Uq] f32 state of the own units
+  uint32_t gxs;             // [G][N][Uq] f32 next projection values
   uint32_t total;
 };
 
@@ -69,7 +69,7 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
   L.recv = off;
   off += 2u * pl.cluster * G * pl.Uq * pl.nbp * 4u;
   L.outs = off;
-  off += (uint32_t)G * pl.Uq * pl.nbp * 4u;
+  off += (uint32_t)G * pl.Uq * N * 4u;
   L.hst = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.cst = off;
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     const int64_t o = (int64_t)n * H + j;
     const float hv = a.h0 ? to_f(reinterpret_cast<const T*>(a.h0)[o]) : 0.f;
     const float cv = a.c0 ? a.c0[o] : 0.f;
-    hst[uu * N + n] = hv;
-    cst[uu * N + n] = cv;
+    hst[n * Uq + uu] = hv;
+    cst[n * Uq + uu] = cv;
     const int slot0 = d ? nT : 0;
     if (a.hseq) reinterpret_cast<T*>(a.hseq)[(int64_t)slot0 * N * H + o] = from_f<T>(hv);
     if (a.cseq) a.cseq[(int64_t)slot0 * N * H + o] = cv;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     for (int it = tid; it < G * items; it += kTThreads) {
       const int g = it / items, rem = it - g * items;
       const int uu = rem % Uqc, n = rem / Uqc;
-      cp_async4(gxs + (g * Uq + uu) * N + n,
+      cp_async4(gxs + (g * N + n) * Uq + uu,
                 a.gx + ((int64_t)t * N + n) * GH + (int64_t)g * H + u0 + uq0 + uu);
     }
     cp_async_commit();
@@ -319,13 +319,14 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     fence_before();
     cl_sync();
     if (!failed) {
+      // batch index fastest: consecutive threads read consecutive partials
       for (int idx = tid; idx < G * items; idx += kTThreads) {
-        const int g = idx / items, rem = idx - g * items;
-        const int uu = rem % Uqc, n = rem / Uqc;
+        const int n = idx % N, gu = idx / N;
+        const int g = gu / Uqc, uu = gu - g * Uqc;
         float v = 0.f;
         for (int rank = 0; rank < Pk; ++rank)
           v += recv[((size_t)rank * G * Uq + g * Uq + uu) * Nm + n];
-        outs[(g * Uq + uu) * Nm + n] = v;
+        outs[(g * N + n) * Uq + uu] = v;
       }
     }
     cp_async_wait_all();
@@ -336,36 +337,37 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         const int slot = d ? t : t + 1;
-        const float* gv = gxs + uu * N + n;     // gate g at gv[g * Uq * N]
+        const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
+        const float* ov = outs + n * Uq + uu;   // likewise
         float h;
         if (p.mode == 1) {
-          const float ig = sigmoidf_(gv[0] + outs[(0 * Uq + uu) * Nm + n]);
-          const float fg = sigmoidf_(gv[Uq * N] + outs[(1 * Uq + uu) * Nm + n]);
-          const float gg = tanhf(gv[2 * Uq * N] + outs[(2 * Uq + uu) * Nm + n]);
-          const float og = sigmoidf_(gv[3 * Uq * N] + outs[(3 * Uq + uu) * Nm + n]);
-          const float c = fg * cst[uu * N + n] + ig * gg;
+          const float ig = sigmoidf_(gv[0] + ov[0]);
+          const float fg = sigmoidf_(gv[N * Uq] + ov[N * Uq]);
+          const float gg = tanhf(gv[2 * N * Uq] + ov[2 * N * Uq]);
+          const float og = sigmoidf_(gv[3 * N * Uq] + ov[3 * N * Uq]);
+          const float c = fg * cst[n * Uq + uu] + ig * gg;
           h = og * tanhf(c);
-          cst[uu * N + n] = c;
+          cst[n * Uq + uu] = c;
           if (a.gates) {
             float* gp = a.gates + row * 4 * H + j;
             gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
           }
           if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
         } else if (p.mode == 2) {
-          const float ghn = outs[(2 * Uq + uu) * Nm + n] + s_bhn[uu];
-          const float rg = sigmoidf_(gv[0] + outs[(0 * Uq + uu) * Nm + n]);
-          const float z = sigmoidf_(gv[Uq * N] + outs[(1 * Uq + uu) * Nm + n]);
+          const float ghn = ov[2 * N * Uq] + s_bhn[uu];
+          const float rg = sigmoidf_(gv[0] + ov[0]);
+          const float z = sigmoidf_(gv[N * Uq] + ov[N * Uq]);
           const float nv = tanhf(gv[2 * Uq * N] + rg * ghn);
-          h = (1.f - z) * nv + z * hst[uu * N + n];
+          h = (1.f - z) * nv + z * hst[n * Uq + uu];
           if (a.gates) {
             float* gp = a.gates + row * 4 * H + j;
             gp[0] = rg; gp[H] = z; gp[2 * H] = nv; gp[3 * H] = ghn;
           }
         } else {
-          h = tanhf(gv[0] + outs[uu * Nm + n]);
+          h = tanhf(gv[0] + ov[0]);
           if (a.gates) a.gates[row * H + j] = h;
         }
-        hst[uu * N + n] = h;
+        hst[n * Uq + uu] = h;
         y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
         if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
       }
@@ -381,8 +383,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     for (int it = tid; it < items; it += kTThreads) {
       const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
       const int64_t o = (int64_t)n * H + j;
-      if (a.hy) reinterpret_cast<T*>(a.hy)[o] = from_f<T>(hst[uu * N + n]);
-      if (a.cy) a.cy[o] = cst[uu * N + n];
+      if (a.hy) reinterpret_cast<T*>(a.hy)[o] = from_f<T>(hst[n * Uq + uu]);
+      if (a.cy) a.cy[o] = cst[n * Uq + uu];
     }
   }
   fence_before();

@@ -54,7 +54,7 @@ __device__ __forceinline__ int owner_flag_b(int u, int Ur, int Uq, int Pk) {
 struct BLayout {
   uint32_t b_hi, b_lo;   // staged B tiles: KC atoms x (Nm rows x 128 bytes)
   uint32_t recv;         // [2][Pk][Uq][Nm] f32
-  uint32_t outs;         // [Uq][Nm] f32
+  uint32_t outs;         // [N][Uq] f32 summed partials
   uint32_t st_dc, st_carry;  // [Uq*N] f32: LSTM dc, GRU dh*z
   uint32_t pin;          // [kNIn][Uq*N] f32
   uint32_t total;
@@ -72,7 +72,7 @@ __host__ __device__ inline BLayout b_layout(const RecPlan& pl, int N, bool bf) {
   L.recv = off;
   off += 2u * pl.cluster * pl.Uq * pl.nbp * 4u;
   L.outs = off;
-  off += (uint32_t)pl.Uq * pl.nbp * 4u;
+  off += (uint32_t)pl.Uq * N * 4u;
   L.st_dc = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.st_carry = off;
@@ -324,11 +324,12 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     fence_before();
     cl_sync();
     if (!failed && s > 0) {
-      for (int it = tid; it < items; it += kBThreads) {
-        const int uu = it % Uqc, n = it / Uqc;
+      // batch index fastest: consecutive threads read consecutive partials
+      for (int idx = tid; idx < items; idx += kBThreads) {
+        const int n = idx % N, uu = idx / N;
         float v = 0.f;
         for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * Uq + uu) * Nm + n];
-        outs[uu * Nm + n] = v;
+        outs[n * Uq + uu] = v;
       }
     }
     cp_async_wait_all();
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         if (s == 0)
           dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
         else
-          dhf = outs[uu * Nm + n] + st_carry[it];
+          dhf = outs[n * Uq + uu] + st_carry[it];
         if (s == nT) {
           if (a.dh0) reinterpret_cast<T*>(a.dh0)[(int64_t)n * H + j] = from_f<T>(dhf);
           if (a.dc0) a.dc0[(int64_t)n * H + j] = st_dc[it];

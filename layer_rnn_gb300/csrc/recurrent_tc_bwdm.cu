@@ -1,0 +1,545 @@
+// Tensor-core recurrent backward for large batches (bf16): the batch is the
+// MMA's M dimension.
+//
+// Per step the backward contraction is
+//     dh_{t-1}[n][k] = sum_j dG_h[t][n][j] * W_hh[j][k]
+// (reverse-mode through the recurrences of the "rnn training example?" thread,
+// reading 13 of the design notes).  With a batch of 64..128 sequences the
+// batch fills the 128 rows of a tcgen05 MMA, so here A = dG_h[t] (batch rows,
+// K-major along the G*H gate rows, exactly as the workspace stores it) and
+// B = W_hh^T (hidden units as the MMA's N).  Clusters of Pk blocks own row
+// groups of Ur units; the blocks of a cluster split the G*H contraction:
+//   * B, the block's W_hh^T slice [Ur units][Kk gate rows] in bf16, stays in
+//     shared memory for the whole sequence (128-byte-swizzled K-major atoms);
+//   * A, the previous step's dG_h slice [N][Kk], streams from L2 through a
+//     TMA ring (cp.async.bulk.tensor.3d over [T][N][G*H]; batch rows beyond N
+//     read as zeros) while one thread issues the MMAs;
+//   * the accumulator D[n][u] (tensor memory, lane = batch row) is pushed, 4
+//     units per 16-byte DSMEM store, to the block that owns the units'
+//     pointwise step; the owners sum the Pk partials in a fixed order, run the
+//     gate-gradient chain and store dG (bf16), then release their step flag.
+// The loads read what other blocks stored, so the writer fences its stores to
+// the async proxy before its release and the reader after its acquire.  All
+// waits are bounded; cluster barriers run on every step, work or not.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+#ifdef LAYER_RNN_TRACE
+__device__ unsigned long long g_mtrace[4][1024][8];
+#define MTRACE(s, k)                                                                          \
+  do {                                                                                        \
+    const int nb_ = gridDim.x;                                                                \
+    const int b_ = blockIdx.x == 0 ? 0 : blockIdx.x == nb_ / 3 ? 1 : blockIdx.x == (2 * nb_) / 3 \
+                 ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
+    if (b_ >= 0 && threadIdx.x == 0 && (s) < 1024) g_mtrace[b_][(s)][(k)] = lr::globaltimer_ns();\
+  } while (0)
+#else
+#define MTRACE(s, k) ((void)0)
+#endif
+
+namespace lr {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kMThreads = 256;
+constexpr int kMRows = 128;     // MMA M (batch rows)
+constexpr int kMChunk = 64;     // bf16 elements of K per ring stage / B atom
+constexpr int kMStages = 4;
+constexpr int kMNIn = 7;        // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1}
+
+struct MMaps {
+  CUtensorMap a[2];  // dG_h of each direction: [T][N][G*H] bf16, box 64 x 128 x 1
+};
+
+__device__ __forceinline__ int owner_flag_m(int u, int Ur, int Uq, int Pk) {
+  const int r = u / Ur;
+  return r * Pk + (u - r * Ur) / Uq;
+}
+
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                     uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4m(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct MLayout {
+  uint32_t b;         // resident B: KC atoms x (Urp rows x 128 bytes)
+  uint32_t ring;      // kMStages x (128 rows x 128 bytes)
+  uint32_t recv;      // [2][Pk][N][Uq] f32
+  uint32_t outs;      // [N][Uq] f32
+  uint32_t st_dc, st_carry;  // [Uq*N] f32
+  uint32_t pin;       // [kMNIn][Uq*N] f32
+  uint32_t total;
+};
+
+__host__ __device__ inline MLayout m_layout(const RecPlan& pl, int N) {
+  MLayout L;
+  uint32_t off = 0;
+  L.b = off;
+  off += (uint32_t)pl.KC * pl.nbp * 128u;
+  L.ring = off;
+  off += (uint32_t)kMStages * kMRows * 128u;
+  L.recv = off;
+  off += 2u * pl.cluster * N * pl.Uq * 4u;
+  L.outs = off;
+  off += (uint32_t)N * pl.Uq * 4u;
+  L.st_dc = off;
+  off += (uint32_t)pl.Uq * N * 4u;
+  L.st_carry = off;
+  off += (uint32_t)pl.Uq * N * 4u;
+  L.pin = off;
+  off += (uint32_t)kMNIn * pl.Uq * N * 4u;
+  L.total = (off + 1023u) & ~1023u;
+  return L;
+}
+
+__global__ void __launch_bounds__(kMThreads, 1)
+    rec_bwd_tcm(const __grid_constant__ MMaps maps, const __grid_constant__ RecParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * kMStages + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_fail, s_stop, s_issued;
+  const RecPlan& pl = p.plan;
+  const int P = pl.P, Pk = pl.cluster;
+  const int d = blockIdx.x / P;
+  const int b = blockIdx.x - d * P;
+  const int r = b / Pk, q = b - r * Pk;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, nT = p.T, G = p.G, Ur = pl.Ur, Uq = pl.Uq;
+  const int64_t GH = (int64_t)G * H;
+  const int Urp = pl.nbp;
+  const int u0 = r * Ur, Urc = min(Ur, H - u0);
+  const int uq0 = q * Uq, Uqc = max(0, min(Uq, Urc - uq0));
+  const int k0 = q * pl.Kk;
+  const int Kc = (int)max((int64_t)0, min((int64_t)pl.Kk, GH - k0));
+  const int nch = (Kc + kMChunk - 1) / kMChunk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  const uint32_t base_s = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
+  const MLayout Lo = m_layout(pl, N);
+  float* recv0 = reinterpret_cast<float*>(base + Lo.recv);
+  float* outs = reinterpret_cast<float*>(base + Lo.outs);
+  float* st_dc = reinterpret_cast<float*>(base + Lo.st_dc);
+  float* st_carry = reinterpret_cast<float*>(base + Lo.st_carry);
+  float* pin = reinterpret_cast<float*>(base + Lo.pin);
+  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[kMStages]);
+  const uint32_t done = smem_addr(&bars[2 * kMStages]);
+  const uint32_t ncols = (uint32_t)pl.lda;
+  const uint32_t bytesA = kMRows * 128u;
+  const int items = Uqc * N;
+  const int icap = Uq * N;
+
+  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || N > kMRows ||
+                       Urp % 16 != 0 || Urp > 256 || Urp < Ur || (uint32_t)Urp > ncols ||
+                       ncols > 512u || (ncols & (ncols - 1u)) != 0 || ncols < 32u ||
+                       pl.Kk % kMChunk != 0 || Uq % 4 != 0 || Uq * Pk < Ur || d >= 2;
+  if (tid == 0) {
+    s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
+    if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
+    s_stop = 0;
+    s_issued = 0;
+    for (int s = 0; s < kMStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s) : "memory");
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2 && !cfg_bad) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // resident B = W_hh^T slice: element (unit u, gate row k0 + jj) at atom jj/64,
+  // row u, 16-byte chunk (jj%64)/8 (swizzled), 2-byte lane jj%8; consecutive
+  // threads read consecutive units of one W_hh row
+  {
+    const bf16* W = reinterpret_cast<const bf16*>(a.whh);
+    const int total = pl.KC * kMChunk * Urp;
+    for (int idx = tid; idx < total; idx += kMThreads) {
+      const int jj = idx / Urp, u = idx - jj * Urp;
+      const bf16 v = (!cfg_bad && u < Urc && jj < Kc) ? W[(int64_t)(k0 + jj) * H + u0 + u]
+                                                      : __float2bfloat16_rn(0.f);
+      const uint32_t off = (uint32_t)(jj / kMChunk) * (uint32_t)Urp * 128u +
+                           sw_off(u, (jj % kMChunk) / 8) + (uint32_t)(jj % 8) * 2u;
+      *reinterpret_cast<bf16*>(base + Lo.b + off) = v;
+    }
+  }
+  for (int it = tid; it < items; it += kMThreads) {
+    const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+    st_dc[it] = a.dcy ? a.dcy[(int64_t)n * H + j] : 0.f;
+    st_carry[it] = 0.f;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_slot;
+  unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
+  bf16* dgx = reinterpret_cast<bf16*>(a.dgx);
+  bf16* dgh = reinterpret_cast<bf16*>(a.dgh);
+  const bf16* hseq = reinterpret_cast<const bf16*>(a.hseq);
+  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(Urp >> 3) << 17) |
+                         ((uint32_t)(kMRows >> 4) << 24);
+  bool failed = s_fail != 0;
+  uint32_t chunk_it = 0;  // ring position (chunks issued over all steps)
+  uint32_t done_ph = 0;
+  const int q4 = warp & 3, half = warp >> 2;
+  const int nrow = q4 * 32 + lane;  // batch row of this thread's tensor-memory lane
+
+  for (int s = 0; s <= nT; ++s) {
+    const int t = d ? s : nT - 1 - s;
+    const int tp = d ? s - 1 : nT - s;
+    MTRACE(s, 0);
+    if (!failed && s < nT) {
+      const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+      for (int it = tid; it < items; it += kMThreads) {
+        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        const int64_t row = (int64_t)t * N + n;
+        if (!a.dy_bf16)
+          cp_async4(pin + it,
+                    reinterpret_cast<const float*>(a.dy) + row * p.lddy + (int64_t)d * H + j);
+        if (p.mode == 0) {
+          cp_async4(pin + 1 * icap + it, a.gates + row * H + j);
+        } else {
+          const float* gp = a.gates + row * 4 * H + j;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) cp_async4(pin + (1 + g) * icap + it, gp + (int64_t)g * H);
+          if (p.mode == 1) {
+            cp_async4(pin + 5 * icap + it, a.cseq + ((int64_t)sc * N + n) * H + j);
+            cp_async4(pin + 6 * icap + it, a.cseq + ((int64_t)sp * N + n) * H + j);
+          }
+        }
+      }
+    }
+    cp_async_commit();
+    const bool have = !failed && s > 0 && Kc > 0;
+    if (have) {
+      if (warp == 0) {
+        // wait for the owners of this block's gate rows, then stream the slice
+        bool ok = true;
+        for (int g = 0; g < G && ok; ++g) {
+          const int lo = max(k0, g * H), hi = min(k0 + Kc, (g + 1) * H);
+          if (lo < hi)
+            ok = warp_wait_flags(flags, p.flag_stride, owner_flag_m(lo - g * H, Ur, Uq, Pk),
+                                 owner_flag_m(hi - 1 - g * H, Ur, Uq, Pk), (unsigned)s, p.status,
+                                 p.timeout_ns, p.spin_ns);
+        }
+        __syncwarp();
+        int c = 0;
+        for (; ok && c < nch; ++c) {
+          const uint32_t it = chunk_it + (uint32_t)c;
+          const uint32_t st = it % kMStages, ph = (it / kMStages) & 1u;
+          int okl = 1;
+          if (lane == 0) {
+            okl = mbar_try_wait(empty0 + 8 * st, ph ^ 1u) ? 1 : 0;
+            if (!okl) {
+              const unsigned long long t0 = globaltimer_ns();
+              unsigned spins = 0;
+              while (!(okl = mbar_try_wait(empty0 + 8 * st, ph ^ 1u) ? 1 : 0)) {
+                if ((++spins & 63u) == 0 && (long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+                  atomicCAS(p.status, kDevOk, kDevTimeout);
+                  break;
+                }
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) {
+            if (c == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t fb = full0 + 8 * st;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                         "r"(bytesA)
+                         : "memory");
+            tma3(base_s + Lo.ring + st * bytesA, &maps.a[d], k0 + c * kMChunk, 0, tp, fb);
+          }
+          __syncwarp();
+        }
+        if (lane == 0 && c < nch) {
+          s_issued = c;
+          __threadfence_block();
+          s_stop = 1;
+          s_fail = 1;
+        }
+        __syncwarp();
+      } else if (warp == 1 && lane == 0) {
+        int c = 0;
+        for (; c < nch; ++c) {
+          const uint32_t it = chunk_it + (uint32_t)c;
+          const uint32_t st = it % kMStages, ph = (it / kMStages) & 1u;
+          bool got = mbar_try_wait(full0 + 8 * st, ph);
+          if (!got) {
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned spins = 0;
+            while (!(got = mbar_try_wait(full0 + 8 * st, ph))) {
+              if (ld_volatile_int(&s_stop) && c >= ld_volatile_int(&s_issued)) break;
+              if ((++spins & 63u) == 0 && (long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+                atomicCAS(p.status, kDevOk, kDevTimeout);
+                s_fail = 1;
+                break;
+              }
+            }
+          }
+          if (!got) break;
+          fence_after();
+          const uint64_t ad = b_desc(base_s + Lo.ring + st * bytesA);
+          const uint64_t bd = b_desc(base_s + Lo.b + (uint32_t)c * (uint32_t)Urp * 128u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                        (c > 0 || kk > 0) ? 1u : 0u);
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                  empty0 + 8 * st)
+              : "memory");
+        }
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                done)
+            : "memory");
+      }
+      __syncwarp();
+      // the commit above always arrives: every thread waits for it
+      const unsigned long long t0 = globaltimer_ns();
+      unsigned spins = 0;
+      while (!mbar_try_wait(done, done_ph)) {
+        if ((++spins & 63u) == 0 && (long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+          atomicCAS(p.status, kDevOk, kDevTimeout);
+          s_fail = 1;
+          break;
+        }
+      }
+      done_ph ^= 1u;
+      chunk_it += (uint32_t)nch;
+      fence_after();
+    }
+    __syncthreads();
+    failed = s_fail != 0;
+    MTRACE(s, 1);
+    // push the accumulator rows (batch n) to the owners of the units, 4 units
+    // per 16-byte store (Uq is a multiple of 4)
+    float* recv = recv0 + (size_t)(s & 1) * Pk * N * Uq;
+    if (!failed && s > 0) {
+      for (int cg = half; cg < Urp / 4; cg += 2) {
+        float v[4];
+        tmem_ld4m(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(cg * 4), v);
+        const int u = cg * 4;
+        if (nrow >= N || u >= Urc) continue;
+        const int owner = u / Uq, uo = u - owner * Uq;
+        if (owner >= Pk) continue;
+        st_peer4(recv + ((size_t)q * N + nrow) * Uq + uo, (unsigned)owner, have ? v[0] : 0.f,
+                 have ? v[1] : 0.f, have ? v[2] : 0.f, have ? v[3] : 0.f);
+      }
+    }
+    fence_before();
+    cl_sync();
+    if (!failed && s > 0) {
+      for (int it = tid; it < items; it += kMThreads) {
+        const int uu = it % Uqc, n = it / Uqc;
+        float v = 0.f;
+        for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * N + n) * Uq + uu];
+        outs[n * Uq + uu] = v;
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    MTRACE(s, 2);
+    if (!failed) {
+      for (int it = tid; it < items; it += kMThreads) {
+        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        float dhf;
+        if (s == 0)
+          dhf = a.dhy ? __bfloat162float(reinterpret_cast<const bf16*>(a.dhy)[(int64_t)n * H + j])
+                      : 0.f;
+        else
+          dhf = outs[n * Uq + uu] + st_carry[it];
+        if (s == nT) {
+          if (a.dh0) reinterpret_cast<bf16*>(a.dh0)[(int64_t)n * H + j] = __float2bfloat16_rn(dhf);
+          if (a.dc0) a.dc0[(int64_t)n * H + j] = st_dc[it];
+          continue;
+        }
+        const int64_t row = (int64_t)t * N + n;
+        const float dyv =
+            a.dy_bf16 ? __bfloat162float(
+                            reinterpret_cast<const bf16*>(a.dy)[row * p.lddy + (int64_t)d * H + j])
+                      : pin[it];
+        const float dh = dyv + dhf;
+        const float g0 = pin[1 * icap + it];
+        bf16* gxo = dgx + row * GH + j;
+        if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
+          const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
+          const float cc = pin[5 * icap + it], cpv = pin[6 * icap + it];
+          const float tc = tanhf(cc);
+          const float dc = st_dc[it] + dh * g3 * (1.f - tc * tc);
+          gxo[0] = __float2bfloat16_rn(dc * g2 * g0 * (1.f - g0));
+          gxo[H] = __float2bfloat16_rn(dc * cpv * g1 * (1.f - g1));
+          gxo[2 * H] = __float2bfloat16_rn(dc * g0 * (1.f - g2 * g2));
+          gxo[3 * H] = __float2bfloat16_rn(dh * tc * g3 * (1.f - g3));
+          st_dc[it] = dc * g1;
+        } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
+          const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
+          const int sp = d ? t + 1 : t;
+          const float hp = __bfloat162float(hseq[((int64_t)sp * N + n) * H + j]);
+          const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
+          const float daz = dh * (hp - g2) * g1 * (1.f - g1);
+          const float dar = dan * g3 * g0 * (1.f - g0);
+          gxo[0] = __float2bfloat16_rn(dar);
+          gxo[H] = __float2bfloat16_rn(daz);
+          gxo[2 * H] = __float2bfloat16_rn(dan);
+          bf16* gho = dgh + row * GH + j;
+          gho[0] = __float2bfloat16_rn(dar);
+          gho[H] = __float2bfloat16_rn(daz);
+          gho[2 * H] = __float2bfloat16_rn(dan * g0);
+          st_carry[it] = dh * g1;
+        } else {  // tanh RNN: g0 = h_t
+          gxo[0] = __float2bfloat16_rn(dh * (1.f - g0 * g0));
+        }
+      }
+    }
+    fence_before();
+    __syncthreads();
+    MTRACE(s, 3);
+    if (!failed && tid == 0 && s < nT && !(blockIdx.x == p.fault_block && s == p.fault_step)) {
+      // this block's dG stores (ordered before this thread by the barrier)
+      // become visible to the other blocks' tensor loads: proxy fence, release
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
+    }
+    MTRACE(s, 4);
+  }
+  cl_sync();  // no block leaves while a peer may still store into it
+  fence_before();
+  __syncthreads();
+  if (warp == 2 && !cfg_bad)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols)
+                 : "memory");
+}
+
+}  // namespace
+
+bool rec_tcm_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
+                      const int* max_clusters, RecPlan* out) {
+  if (!bf16 || N < 64 || N > kMRows || H % 8 != 0) return false;
+  const int G = mode == 1 ? 4 : mode == 2 ? 3 : 1;
+  const int GH = G * H;
+  bool found = false;
+  double best = 0;
+  RecPlan bp;
+  for (int Pk : {4, 8, 2}) {
+    const int cap = max_clusters[Pk];
+    const int Pr_max = std::min(cap / D, (num_sms / D) / Pk);
+    if (Pr_max < 1) continue;
+    const int Ur = (H + Pr_max - 1) / Pr_max;
+    const int Urp = (Ur + 15) / 16 * 16;
+    if (Urp > 256) continue;
+    const int Pr = (H + Ur - 1) / Ur;
+    const int Uq = ((Ur + Pk - 1) / Pk + 3) / 4 * 4;
+    const int Kk = ((GH + Pk - 1) / Pk + kMChunk - 1) / kMChunk * kMChunk;
+    int cols = 32;
+    while (cols < Urp) cols *= 2;
+    RecPlan pl;
+    pl.direct = 0;
+    pl.cluster = Pk; pl.Pr = Pr; pl.P = Pr * Pk; pl.Ur = Ur; pl.Uq = Uq;
+    pl.Kk = Kk;
+    pl.K = Kk;
+    pl.KC = Kk / kMChunk;
+    pl.nbp = Urp;
+    pl.lda = cols;
+    pl.Mloc = Ur; pl.Mp = kMRows; pl.nb = N;
+    pl.tc = 3;
+    const MLayout L = m_layout(pl, N);
+    pl.smem = std::max<size_t>(L.total + 1024, 120 * 1024);
+    if (pl.smem > smem_limit) continue;
+    if (D * pl.P > num_sms) continue;
+    // streamed slice per step, the owners' reduction and pointwise items
+    const double cost = (double)Kk * 2.0 + (double)Uq * N * (Pk / 4.0 + 6.0) / 8.0;
+    if (!found || cost < best) {
+      found = true;
+      best = cost;
+      bp = pl;
+    }
+  }
+  if (found) *out = bp;
+  return found;
+}
+
+#ifdef LAYER_RNN_TRACE
+extern "C" int rnn_debug_mtrace_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mtrace)) bytes = sizeof(g_mtrace);
+  return (int)cudaMemcpyFromSymbol(host, g_mtrace, bytes);
+}
+extern "C" int rnn_debug_mtrace_clear() {
+  static unsigned long long zeros[4][1024][8];
+  return (int)cudaMemcpyToSymbol(g_mtrace, zeros, sizeof(zeros));
+}
+#endif
+
+cudaError_t rec_tcm_bwd_launch(const RecParams& p, cudaStream_t st) {
+  const RecPlan& pl = p.plan;
+  MMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const uint64_t GH = (uint64_t)p.G * p.H, N = (uint64_t)p.N, T = (uint64_t)p.T;
+  for (int d = 0; d < p.D; ++d) {
+    const uint64_t dims[3] = {GH, N, T}, strides[2] = {GH * 2, N * GH * 2};
+    const uint32_t box[3] = {(uint32_t)kMChunk, (uint32_t)kMRows, 1u};
+    if (!tma_encode(&maps.a[d], 3, true, p.dir[d].dgh, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  void* fn = (void*)rec_bwd_tcm;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
+  if (e != cudaSuccess) return e;
+  RecParams copy = p;
+  void* args[] = {&maps, &copy};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.D * pl.P);
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace lr

@@ -68,7 +68,8 @@ constexpr int kWThreads = 256;
 constexpr int kRows = 128;       // MMA M
 constexpr int kChunk = 64;       // bf16 elements of K per ring stage (128 bytes)
 constexpr int kMaxStages = 8;
-constexpr int kMaxNm = 128;      // batch columns per block (fp32 state in registers)
+constexpr int kMaxNm = 128;      // batch columns per block
+constexpr int kStateSlots = kMaxNm / 8;  // fp32 state items per thread (4-column groups / 2)
 
 struct WfMaps {
   CUtensorMap a[kWfMaxLayers];   // packed weights [rows][kp], box 64 x 128
@@ -146,18 +147,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ float pick4(float a, float b, float c, float d, int i) {
@@ -250,36 +247,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
   }
   // fp32 state of this thread's (unit, batch) items: LSTM c, GRU h
-  float state[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) state[i] = 0.f;
+  // kept in shared memory (slot i of thread tid at st_s[i * kWThreads + tid]):
+  // the epilogue below is a loop, not unrolled, to stay small in the
+  // instruction cache
+  float* st_s = reinterpret_cast<float*>(smem_raw + (base - su32(smem_raw)) + S * stage);
+  for (int i = 0; i < kStateSlots; ++i) st_s[i * kWThreads + tid] = 0.f;
   // slot 0 of hseq (and cseq) and the initial state
   const bf16* h0 = reinterpret_cast<const bf16*>(a.h0);
-#pragma unroll
-  for (int sl = 0; sl < 4; ++sl) {
-    const int ci = half + 2 * sl;
-    if (ci >= nci) break;
-    if (R == 4) {
-#pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4) {
-        const int n = ci * 16 + 4 * j4 + g;
-        if (failed || !unit_ok || n >= N) continue;
-        const int64_t o = (int64_t)n * H + j;
-        const float hv = h0 ? __bfloat162float(h0[o]) : 0.f;
-        const float cv = a.c0 ? a.c0[o] : 0.f;
-        state[sl * 4 + j4] = p.mode == 1 ? cv : hv;
-        store_bf16(a.hseq, o, hv);
-        if (a.cseq) a.cseq[o] = cv;
-      }
-    } else {
-#pragma unroll
+  if (R == 4) {
+    // the epilogue's item mapping: column n = 4*cg + g, cg = half, half + 2, ...
+    for (int cg = half; cg < Nm / 4; cg += 2) {
+      const int n = cg * 4 + g;
+      if (failed || !unit_ok || n >= N) continue;
+      const int64_t o = (int64_t)n * H + j;
+      const float hv = h0 ? __bfloat162float(h0[o]) : 0.f;
+      const float cv = a.c0 ? a.c0[o] : 0.f;
+      st_s[(cg >> 1) * kWThreads + tid] = p.mode == 1 ? cv : hv;
+      store_bf16(a.hseq, o, hv);
+      if (a.cseq) a.cseq[o] = cv;
+    }
+  } else {
+    for (int ci = half; ci < nci; ci += 2)
       for (int i = 0; i < 16; ++i) {
         const int n = ci * 16 + i;
         if (failed || !unit_ok || n >= N) continue;
         const int64_t o = (int64_t)n * H + j;
         store_bf16(a.hseq, o, h0 ? __bfloat162float(h0[o]) : 0.f);
       }
-    }
   }
   __syncthreads();
   unsigned* flags = p.flags;
@@ -390,75 +384,68 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const bool last = t == nT - 1;
       const int64_t row0 = (int64_t)t * N;
       bf16* hs = reinterpret_cast<bf16*>(a.hseq) + (int64_t)(t + 1) * N * H;
+      if (R == 4) {
+        // 4-column groups, alternating between the two warp halves.  Lanes
+        // 4u .. 4u+3 hold gates 0..3 of unit u for the group's 4 columns; lane
+        // 4u+g collects all gates of column 4*cg+g with three shuffles.  The
+        // loop body stays small (it runs from the instruction cache).
+#pragma unroll 2
+        for (int cg = half; cg < Nm / 4; cg += 2) {
+          float v[4];
+          tmem_ld4(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * 4), v);
+          float got[4];
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        const int ci = half + 2 * sl;
-        if (ci >= nci) break;
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ci * 16), v);
-        if (R == 4) {
-          // lanes 4u .. 4u+3 hold gates 0..3 of unit u for columns 4*j4 ..
-          // 4*j4+3; lane 4u+g collects all gates of column 4*j4+g.  The four
-          // columns of this thread are independent chains: exchange, gate math
-          // and cell update run for all of them before any (predicated) store.
-          float ga[4][4];
-#pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            float got[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float send =
-                  pick4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3], (g - k) & 3);
-              got[k] = __shfl_sync(0xffffffffu, send, (lane & ~3) | ((g + k) & 3));
-            }
-            // got[k] is gate (g + k) & 3; gate i is got[(i - g) & 3]
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ga[j4][i] = pick4(got[0], got[1], got[2], got[3], (i - g) & 3) + bias[i];
+          for (int k = 0; k < 4; ++k) {
+            const float send = pick4(v[0], v[1], v[2], v[3], (g - k) & 3);
+            got[k] = __shfl_sync(0xffffffffu, send, (lane & ~3) | ((g + k) & 3));
           }
-          float hv[4], o0[4], o1[4], o2[4], o3[4];
-#pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            float& stv = state[sl * 4 + j4];
-            if (p.mode == 1) {  // LSTM: i, f, g, o
-              o0[j4] = sigm_hw(ga[j4][0]);
-              o1[j4] = sigm_hw(ga[j4][1]);
-              o2[j4] = tanh_hw(ga[j4][2]);
-              o3[j4] = sigm_hw(ga[j4][3]);
-              stv = fmaf(o1[j4], stv, o0[j4] * o2[j4]);
-              hv[j4] = o3[j4] * tanh_hw(stv);
-            } else {  // GRU: r, z, W_in x + b_in, W_hn h + b_hn
-              o0[j4] = sigm_hw(ga[j4][0]);
-              o1[j4] = sigm_hw(ga[j4][1]);
-              o2[j4] = tanh_hw(fmaf(o0[j4], ga[j4][3], ga[j4][2]));
-              o3[j4] = ga[j4][3];
-              stv = fmaf(o1[j4], stv - o2[j4], o2[j4]);  // (1 - z) n + z h
-              hv[j4] = stv;
-            }
+          // got[k] is gate (g + k) & 3; gate i is got[(i - g) & 3]
+          const float a0 = pick4(got[0], got[1], got[2], got[3], (0 - g) & 3) + bias[0];
+          const float a1 = pick4(got[0], got[1], got[2], got[3], (1 - g) & 3) + bias[1];
+          const float a2 = pick4(got[0], got[1], got[2], got[3], (2 - g) & 3) + bias[2];
+          const float a3 = pick4(got[0], got[1], got[2], got[3], (3 - g) & 3) + bias[3];
+          const int n = cg * 4 + g;
+          float& stv = st_s[(cg >> 1) * kWThreads + tid];
+          float o0, o1, o2, o3, h;
+          if (p.mode == 1) {  // LSTM: i, f, g, o
+            o0 = sigm_hw(a0);
+            o1 = sigm_hw(a1);
+            o2 = tanh_hw(a2);
+            o3 = sigm_hw(a3);
+            const float c = fmaf(o1, stv, o0 * o2);
+            h = o3 * tanh_hw(c);
+            stv = c;
+          } else {  // GRU: r, z, W_in x + b_in, W_hn h + b_hn
+            o0 = sigm_hw(a0);
+            o1 = sigm_hw(a1);
+            o2 = tanh_hw(fmaf(o0, a3, a2));
+            o3 = a3;
+            h = fmaf(o1, stv - o2, o2);  // (1 - z) n + z h
+            stv = h;
           }
-#pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const int n = ci * 16 + 4 * j4 + g;
-            if (!unit_ok || n >= N) continue;
-            const int64_t row = row0 + n;
-            const int64_t o = (int64_t)n * H + j;
-            const float h = hv[j4];
-            if (a.gates) {
-              float* gp = a.gates + row * GsH + j;
-              gp[0] = o0[j4]; gp[H] = o1[j4]; gp[2 * H] = o2[j4]; gp[3 * H] = o3[j4];
-            }
-            hs[o] = __float2bfloat16_rn(h);
-            if (a.y) store_bf16(a.y, row * H + j, h);
-            if (p.mode == 1 && a.cseq) a.cseq[(int64_t)(t + 1) * N * H + o] = state[sl * 4 + j4];
-            if (last) {
-              if (a.hy) store_bf16(a.hy, o, h);
-              if (a.cy) a.cy[o] = state[sl * 4 + j4];
-            }
+          if (!unit_ok || n >= N) continue;
+          const int64_t row = row0 + n;
+          const int64_t o = (int64_t)n * H + j;
+          if (a.gates) {
+            float* gp = a.gates + row * GsH + j;
+            gp[0] = o0; gp[H] = o1; gp[2 * H] = o2; gp[3 * H] = o3;
           }
-        } else {
+          hs[o] = __float2bfloat16_rn(h);
+          if (a.y) store_bf16(a.y, row * H + j, h);
+          if (p.mode == 1 && a.cseq) a.cseq[(int64_t)(t + 1) * N * H + o] = stv;
+          if (last) {
+            if (a.hy) store_bf16(a.hy, o, h);
+            if (a.cy) a.cy[o] = stv;
+          }
+        }
+      } else {
+#pragma unroll 2
+        for (int cg = half; cg < Nm / 4; cg += 2) {
+          float v[4];
+          tmem_ld4(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * 4), v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = ci * 16 + i;
+          for (int i = 0; i < 4; ++i) {
+            const int n = cg * 4 + i;
             if (!unit_ok || n >= N) continue;
             const int64_t row = row0 + n;
             const float h = tanh_hw(v[i] + bias[0]);
@@ -555,10 +542,11 @@ bool wf_plan(int mode, int bf16, int L, int D, int64_t I, int64_t H, int64_t N, 
   while (cols < pl.Nm) cols *= 2;
   pl.tmem_cols = cols;
   const size_t stage = (size_t)kRows * 128 + (size_t)pl.Nm * 128;
-  const size_t budget = std::min<size_t>(smem_optin, 227 * 1024) - 1024 - 1024;
+  const size_t state_bytes = (size_t)kStateSlots * kWThreads * 4;
+  const size_t budget = std::min<size_t>(smem_optin, 227 * 1024) - 1024 - 1024 - state_bytes;
   pl.stages = (int)std::min<size_t>(kMaxStages, budget / stage);
   if (pl.stages < 2) return false;
-  pl.smem = pl.stages * stage + 1024;
+  pl.smem = pl.stages * stage + 1024 + state_bytes;
   // more than half of the shared memory: one block per SM, so each block's
   // tensor-memory allocation never waits for another's
   pl.smem = std::max<size_t>(pl.smem, 120 * 1024);
