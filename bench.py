@@ -475,10 +475,15 @@ def main():
     ap.add_argument("--workload", default="ds2_lstm", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override T of the workload (small cases for profiler captures; "
+                         "the default workload sizes are the benchmark)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     cfg = wl.WORKLOADS[args.workload]
+    if args.seq_len > 0:
+        cfg = wl.with_sizes(cfg, T=args.seq_len)
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -860,11 +860,21 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       g2.in_bf16 = bf; g2.out_bf16 = bf;
       s = run_gemm(h, g2, sc, st);
       if (s != RNN_OK) return s;
-      if (colsum(mp<char>(dW, weight_offset(h, l, d, 2) * e), bf, dgx, bf, T * N, GH, GH, st) !=
-              cudaSuccess ||
-          colsum(mp<char>(dW, weight_offset(h, l, d, 3) * e), bf, dgh, bf, T * N, GH, GH, st) !=
-              cudaSuccess)
+      // db_ih = sum of dG_x over (t, n); db_hh likewise over dG_h, which is
+      // dG_x itself except for the GRU: then one sum serves both
+      Scratch cs = sc;
+      const int64_t cs_bytes = std::min<int64_t>(cs.cap - align256(cs.off), (int64_t)64 << 20);
+      float* part = cs_bytes > 0 ? static_cast<float*>(cs.take(cs_bytes)) : nullptr;
+      char* db_ih = mp<char>(dW, weight_offset(h, l, d, 2) * e);
+      char* db_hh = mp<char>(dW, weight_offset(h, l, d, 3) * e);
+      if (colsum(db_ih, bf, dgx, bf, T * N, GH, GH, part, part ? cs_bytes : 0, h->num_sms, st) !=
+          cudaSuccess)
         return RNN_ERR_CUDA;
+      const cudaError_t ce =
+          dgh == dgx ? cudaMemcpyAsync(db_hh, db_ih, GH * e, cudaMemcpyDeviceToDevice, st)
+                     : colsum(db_hh, bf, dgh, bf, T * N, GH, GH, part, part ? cs_bytes : 0,
+                              h->num_sms, st);
+      if (ce != cudaSuccess) return RNN_ERR_CUDA;
     }
   }
   return finish(h, st, RNN_OK);

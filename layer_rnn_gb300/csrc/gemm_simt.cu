@@ -2,6 +2,8 @@
 // operand strides, fp32 accumulation, fused bias and optional second product.
 // 128x128 block tile, K step 16, 256 threads, 8x8 outputs per thread, operands
 // converted to fp32 in shared memory, register-prefetched double buffering.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -183,6 +185,53 @@ __global__ void __launch_bounds__(1024) colsum_kernel(void* dst, int dst_bf16, c
   }
 }
 
+// Column sums in two passes: pass 1 gives every block a 16-byte column
+// vector per thread and a chunk of rows (coalesced: a warp reads 512
+// consecutive bytes of a row, four rows in flight), writing fp32 partials
+// [chunk][cols]; pass 2 adds the chunks in a fixed order.  Deterministic.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_part_kernel(const T* src, int64_t rows, int64_t cols,
+                                                          int64_t ld, int64_t rows_per_chunk,
+                                                          float* part) {
+  constexpr int VE = 16 / (int)sizeof(T);
+  const int64_t cv = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VE;  // first column
+  if (cv >= cols) return;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_chunk;
+  const int64_t r1 = min(rows, r0 + rows_per_chunk);
+  float acc[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) acc[e] = 0.f;
+  int64_t r = r0;
+  for (; r + 3 < r1; r += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(src + (r + q) * ld + cv));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) acc[e] += sizeof(T) == 4 ? lane_f32(v[q], e) : lane_bf16(v[q], e);
+  }
+  for (; r < r1; ++r) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * ld + cv));
+#pragma unroll
+    for (int e = 0; e < VE; ++e) acc[e] += sizeof(T) == 4 ? lane_f32(v, e) : lane_bf16(v, e);
+  }
+  float* out = part + (int64_t)blockIdx.y * cols + cv;
+#pragma unroll
+  for (int e = 0; e < VE; ++e)
+    if (cv + e < cols) out[e] = acc[e];
+}
+
+__global__ void colsum_final_kernel(const float* part, int64_t chunks, int64_t cols, void* dst,
+                                    int dst_bf16) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float t = 0.f;
+  for (int64_t k = 0; k < chunks; ++k) t += part[k * cols + c];
+  if (dst_bf16) reinterpret_cast<bf16*>(dst)[c] = __float2bfloat16_rn(t);
+  else reinterpret_cast<float*>(dst)[c] = t;
+}
+
 }  // namespace
 
 std::atomic<int64_t> g_kernel_launches{0};
@@ -210,8 +259,34 @@ cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st) {
 }
 
 cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16, int64_t rows,
-                   int64_t cols, int64_t ld, cudaStream_t st) {
+                   int64_t cols, int64_t ld, float* scratch, int64_t scratch_bytes,
+                   int num_sms, cudaStream_t st) {
   if (cols <= 0) return cudaSuccess;
+  const int e = src_bf16 ? 2 : 4;
+  const int VE = 16 / e;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld * e) % 16 == 0 &&
+                   cols % VE == 0;
+  if (vec && scratch && rows > 0) {
+    const int64_t vecs = cols / VE;
+    const int64_t bx = (vecs + 255) / 256;
+    // about four waves of blocks, at least 16 rows per chunk
+    int64_t chunks = std::max<int64_t>(1, ((int64_t)num_sms * 4 + bx - 1) / bx);
+    chunks = std::min<int64_t>(chunks, (rows + 15) / 16);
+    while (chunks > 1 && chunks * cols * 4 > scratch_bytes) chunks /= 2;
+    const int64_t rpc = (rows + chunks - 1) / chunks;
+    chunks = (rows + rpc - 1) / rpc;
+    dim3 grid((unsigned)bx, (unsigned)chunks);
+    if (src_bf16)
+      colsum_part_kernel<bf16><<<grid, 256, 0, st>>>(reinterpret_cast<const bf16*>(src), rows,
+                                                     cols, ld, rpc, scratch);
+    else
+      colsum_part_kernel<float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(src), rows,
+                                                      cols, ld, rpc, scratch);
+    colsum_final_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(scratch, chunks, cols, dst,
+                                                                        dst_bf16);
+    g_kernel_launches.fetch_add(2, std::memory_order_relaxed);
+    return cudaGetLastError();
+  }
   colsum_kernel<<<(unsigned)((cols + 31) / 32), 1024, 0, st>>>(dst, dst_bf16, src, src_bf16, rows,
                                                               cols, ld);
   g_kernel_launches.fetch_add(1, std::memory_order_relaxed);

@@ -466,14 +466,33 @@ bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Split of K that minimises a wave model: the grid runs in ceil(units / SMs)
+// waves of ceil(nkt / ks) 128-byte K blocks each, plus the fp32 partial sums
+// (written and read once per split) at HBM speed, in K-block time units.
 int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms) {
   const int BN = N > 64 ? 128 : 64;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int64_t nkt = (K_total * (tf32 ? 4 : 2) + 127) / 128;
-  if (tiles >= (int64_t)num_sms * 3 / 2 || nkt < 8) return 1;
-  int ks = (int)((2 * (int64_t)num_sms + tiles - 1) / tiles);
-  ks = (int)std::min<int64_t>(ks, nkt / 4);
-  return std::max(1, std::min(ks, 8));
+  if (nkt < 8 || num_sms < 1) return 1;
+  // one K block of one tile: 2*128*BN*(128/e) flop (x3 passes for fp32) on
+  // one SM at about 1/152 of the dense rate (bf16 2.25, tf32 1.1 PFLOP/s)
+  const double kb_flop = 2.0 * BM * BN * (tf32 ? 32.0 * 3.0 : 64.0);
+  const double sm_rate = (tf32 ? 1.1e15 : 2.25e15) / 152.0;
+  const double t_kb = kb_flop / sm_rate;
+  const double red_per_split = 8.0 * (double)M * N / 6.0e12 / t_kb;
+  int best_ks = 1;
+  double best = 0;
+  for (int ks = 1; ks <= 8; ++ks) {
+    if (ks > 1 && nkt / ks < 4) break;
+    const int64_t units = tiles * ks;
+    const double waves = (double)((units + num_sms - 1) / num_sms);
+    const double cost = waves * (double)((nkt + ks - 1) / ks) + (ks > 1 ? red_per_split * ks : 0.0);
+    if (ks == 1 || cost < best) {
+      best = cost;
+      best_ks = ks;
+    }
+  }
+  return best_ks;
 }
 
 bool gemm_tc_supported(const TcGemm& g) {

@@ -61,9 +61,11 @@ cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t 
 cudaError_t transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
                            int64_t ldd, cudaStream_t st);
 
-// column sums: dst[c] = sum_r src[r*ld + c], r < rows (fp32 accumulate, fixed order)
+// column sums: dst[c] = sum_r src[r*ld + c], r < rows (fp32 accumulate, fixed
+// order); with `scratch` (fp32 partials) in two coalesced passes
 cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16,
-                   int64_t rows, int64_t cols, int64_t ld, cudaStream_t st);
+                   int64_t rows, int64_t cols, int64_t ld, float* scratch,
+                   int64_t scratch_bytes, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // persistent recurrent kernels

@@ -157,8 +157,18 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// element i (0..3, may differ per lane) of (a, b, c, d) with predicated
+// selects, never a branch: lanes of a warp take different i here
+__device__ __forceinline__ float sel_if(unsigned cond, float if_set, float if_clear) {
+  float r;
+  asm("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\tselp.f32 %0, %1, %2, p;\n\t}"
+      : "=f"(r)
+      : "f"(if_set), "f"(if_clear), "r"(cond));
+  return r;
+}
 __device__ __forceinline__ float pick4(float a, float b, float c, float d, int i) {
-  return i == 0 ? a : i == 1 ? b : i == 2 ? c : d;
+  const unsigned b0 = (unsigned)i & 1u, b1 = (unsigned)i & 2u;
+  return sel_if(b1, sel_if(b0, d, c), sel_if(b0, b, a));
 }
 
 __device__ __forceinline__ void store_bf16(void* base, int64_t i, float v) {
