@@ -191,12 +191,33 @@ bool prep_operand(const void* p, int64_t rows, int64_t K, int64_t sr, int64_t sk
 
 // A dense phase: tensor-core GEMM when the operands can be presented to it
 // (alignment, scratch room), otherwise the CUDA-core GEMM.
-rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaStream_t st) {
+// A GEMM operand already presented K-major (and split for fp32) in scratch,
+// reused by the GEMMs that share it (dW_ih and dW_hh both read dG_x^T unless
+// the mode is GRU)
+struct PreparedA {
+  bool valid = false;
+  const void* src = nullptr;
+  int64_t M = 0, K = 0, sam = 0, sak = 0;
+  const void* hi = nullptr;
+  const void* lo = nullptr;
+  int64_t ld = 0;
+};
+
+rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaStream_t st,
+                      const PreparedA* pa = nullptr) {
   if (!(h->flags & RNN_FLAG_SIMT_GEMM)) {
     const bool tf = !g.in_bf16;
     TcGemm t;
     t.M = g.M; t.N = g.N; t.K = g.K; t.tf32 = tf ? 1 : 0;
-    bool ok = prep_operand(g.A, g.M, g.K, g.sam, g.sak, tf, &sc, &t.A_hi, &t.A_lo, &t.lda, st) &&
+    const bool reuse = pa && pa->valid && pa->src == g.A && pa->M == g.M && pa->K == g.K &&
+                       pa->sam == g.sam && pa->sak == g.sak;
+    if (reuse) {
+      t.A_hi = pa->hi;
+      t.A_lo = pa->lo;
+      t.lda = pa->ld;
+    }
+    bool ok = (reuse ||
+               prep_operand(g.A, g.M, g.K, g.sam, g.sak, tf, &sc, &t.A_hi, &t.A_lo, &t.lda, st)) &&
               prep_operand(g.B, g.N, g.K, g.sbn, g.sbk, tf, &sc, &t.B_hi, &t.B_lo, &t.ldb, st);
     if (ok && g.K2 > 0) {
       t.K2 = g.K2;
@@ -844,13 +865,21 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       const void* dgh = h->mode == RNN_GRU ? ws + lay.at(RNN_WS_DGH, l, d).off : dgx;
       const char* hseq = ws + lay.at(RNN_WS_HSEQ, l, d).off;
       const void* hprev = hseq + (d == 1 ? N * H * e : 0);
+      // dG_x^T, presented once for both weight GEMMs when dG_h is dG_x
+      Scratch scl = sc;
+      PreparedA pa;
+      if (!(h->flags & RNN_FLAG_SIMT_GEMM) && dgh == dgx) {
+        pa.src = dgx; pa.M = GH; pa.K = T * N; pa.sam = 1; pa.sak = GH;
+        pa.valid = prep_operand(dgx, GH, T * N, 1, GH, !bf, &scl, &pa.hi, &pa.lo, &pa.ld, st);
+        if (!pa.valid) scl = sc;
+      }
       GemmArgs g;
       g.M = GH; g.N = I_l; g.K = T * N;
       g.A = dgx; g.sam = 1; g.sak = GH;
       g.B = in; g.sbk = I_l; g.sbn = 1;
       g.C = mp<char>(dW, weight_offset(h, l, d, 0) * e); g.ldc = I_l;
       g.in_bf16 = bf; g.out_bf16 = bf;
-      s = run_gemm(h, g, sc, st);
+      s = run_gemm(h, g, scl, st, &pa);
       if (s != RNN_OK) return s;
       GemmArgs g2;
       g2.M = GH; g2.N = H; g2.K = T * N;
@@ -858,7 +887,7 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       g2.B = hprev; g2.sbk = H; g2.sbn = 1;
       g2.C = mp<char>(dW, weight_offset(h, l, d, 1) * e); g2.ldc = H;
       g2.in_bf16 = bf; g2.out_bf16 = bf;
-      s = run_gemm(h, g2, sc, st);
+      s = run_gemm(h, g2, scl, st, &pa);
       if (s != RNN_OK) return s;
       // db_ih = sum of dG_x over (t, n); db_hh likewise over dG_h, which is
       // dG_x itself except for the GRU: then one sum serves both
