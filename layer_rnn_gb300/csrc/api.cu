@@ -230,7 +230,7 @@ rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaSt
       t.bias_bf16 = g.bias_bf16;
       t.status = h->d_status;
       t.timeout_ns = h->timeout_ns;
-      const int ks = gemm_tc_splitk(g.M, g.N, g.K + g.K2, tf, h->num_sms);
+      const int ks = g.no_split ? 1 : gemm_tc_splitk(g.M, g.N, g.K + g.K2, tf, h->num_sms);
       if (ks > 1) {
         t.part = static_cast<float*>(sc.take(ks * g.M * g.N * 4));
         if (t.part) t.ksplit = ks;
@@ -450,6 +450,9 @@ rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, 
     g.bias2_limit = h->mode == RNN_GRU ? 2 * h->H : GH;
     g.in_bf16 = g.bias_bf16 = h->dtype == RNN_BF16;
     g.out_bf16 = 0;
+    // training and inference (different scratch room) must produce the same
+    // G_x bit for bit: one fixed summation order, no K split
+    g.no_split = 1;
     rnn_status_t s = run_gemm(h, g, sc, st);
     if (s != RNN_OK) return s;
   }

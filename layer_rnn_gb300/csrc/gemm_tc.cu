@@ -466,11 +466,20 @@ bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output tile width: 256 columns when the output is wide enough.  A 128 x 256
+// tile reads each A tile once for twice the MMA work of a 128 x 128 tile,
+// which matters because the operand stream from L2 (about 64 bytes per clock
+// per SM) otherwise limits the tensor pipe (bf16 128 x 128 tiles need ~117).
+int gemm_tc_bn(int64_t N, bool tf32) {
+  (void)tf32;
+  return N >= 192 ? 256 : N > 64 ? 128 : 64;
+}
+
 // Split of K that minimises a wave model: the grid runs in ceil(units / SMs)
 // waves of ceil(nkt / ks) 128-byte K blocks each, plus the fp32 partial sums
 // (written and read once per split) at HBM speed, in K-block time units.
 int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms) {
-  const int BN = N > 64 ? 128 : 64;
+  const int BN = gemm_tc_bn(N, tf32);
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int64_t nkt = (K_total * (tf32 ? 4 : 2) + 127) / 128;
   if (nkt < 8 || num_sms < 1) return 1;
@@ -510,7 +519,7 @@ bool gemm_tc_supported(const TcGemm& g) {
 
 cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   const bool tf32 = g.tf32 != 0;
-  const int BN = g.N > 64 ? 128 : 64;
+  const int BN = gemm_tc_bn(g.N, tf32);
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
   bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, !tf32, BM) &&
@@ -554,10 +563,13 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)kp.ksplit);
   cudaError_t e;
   if (tf32)
-    e = BN == 128 ? launch_tc<128, true>(maps, kp, grid, st) : launch_tc<64, true>(maps, kp, grid, st);
+    e = BN == 256   ? launch_tc<256, true>(maps, kp, grid, st)
+        : BN == 128 ? launch_tc<128, true>(maps, kp, grid, st)
+                    : launch_tc<64, true>(maps, kp, grid, st);
   else
-    e = BN == 128 ? launch_tc<128, false>(maps, kp, grid, st)
-                  : launch_tc<64, false>(maps, kp, grid, st);
+    e = BN == 256   ? launch_tc<256, false>(maps, kp, grid, st)
+        : BN == 128 ? launch_tc<128, false>(maps, kp, grid, st)
+                    : launch_tc<64, false>(maps, kp, grid, st);
   if (e != cudaSuccess || kp.ksplit == 1) return e;
   const int64_t total = g.M * g.N;
   const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);

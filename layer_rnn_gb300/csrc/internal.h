@@ -30,6 +30,7 @@ struct GemmArgs {
   int out_bf16 = 0;   // C element type
   int bias_bf16 = 0;  // bias element type
   int accumulate = 0; // C += result instead of C = result
+  int no_split = 0;   // never split K (the result must not depend on scratch room)
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
