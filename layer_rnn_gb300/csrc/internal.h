@@ -117,6 +117,9 @@ struct RecPlan {
   int Kk = 0;           // K elements per cluster rank (multiple of 16 bytes)
   int Wm = 0, Wk = 0;   // warps along rows x along K inside a block
   int ldbs = 0;         // shared-memory row stride of the staged K slice (elements)
+  // batch-as-M backward: TMA ring stages, pointwise inputs prefetched into
+  // shared memory (1) or read in the pointwise step (0), partial-sum buffers
+  int ring = 0, pin = 1, rbufs = 2;
   size_t smem = 0;
 };
 

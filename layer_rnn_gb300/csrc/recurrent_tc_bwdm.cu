@@ -51,8 +51,10 @@ using namespace tc;
 constexpr int kMThreads = 256;
 constexpr int kMRows = 128;     // MMA M (batch rows)
 constexpr int kMChunk = 64;     // bf16 elements of K per ring stage / B atom
-constexpr int kMStages = 4;
+constexpr int kMStages = 8;      // most ring stages the kernel supports
+constexpr int kRingUse = 4;      // stages the plan uses
 constexpr int kMNIn = 7;        // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1}
+constexpr int kRegItems = 4;    // items per thread when the inputs are prefetched to registers
 
 struct MMaps {
   CUtensorMap a[2];  // dG_h of each direction: [T][N][G*H] bf16, box 64 x 128 x 1
@@ -93,11 +95,11 @@ __device__ __forceinline__ void tmem_ld4m(uint32_t taddr, float (&v)[4]) {
 
 struct MLayout {
   uint32_t b;         // resident B: KC atoms x (Urp rows x 128 bytes)
-  uint32_t ring;      // kMStages x (128 rows x 128 bytes)
-  uint32_t recv;      // [2][Pk][N][Uq] f32
+  uint32_t ring;      // pl.ring stages x (128 rows x 128 bytes)
+  uint32_t recv;      // [rbufs][Pk][N][Uq] f32
   uint32_t outs;      // [N][Uq] f32
   uint32_t st_dc, st_carry;  // [Uq*N] f32
-  uint32_t pin;       // [kMNIn][Uq*N] f32
+  uint32_t pin;       // [kMNIn][Uq*N] f32 (when pl.pin == 1)
   uint32_t total;
 };
 
@@ -107,9 +109,9 @@ __host__ __device__ inline MLayout m_layout(const RecPlan& pl, int N) {
   L.b = off;
   off += (uint32_t)pl.KC * pl.nbp * 128u;
   L.ring = off;
-  off += (uint32_t)kMStages * kMRows * 128u;
+  off += (uint32_t)pl.ring * kMRows * 128u;
   L.recv = off;
-  off += 2u * pl.cluster * N * pl.Uq * 4u;
+  off += (uint32_t)pl.rbufs * pl.cluster * N * pl.Uq * 4u;
   L.outs = off;
   off += (uint32_t)N * pl.Uq * 4u;
   L.st_dc = off;
@@ -117,7 +119,7 @@ __host__ __device__ inline MLayout m_layout(const RecPlan& pl, int N) {
   L.st_carry = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.pin = off;
-  off += (uint32_t)kMNIn * pl.Uq * N * 4u;
+  off += pl.pin == 1 ? (uint32_t)kMNIn * pl.Uq * N * 4u : 0u;
   L.total = (off + 1023u) & ~1023u;
   return L;
 }
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const int k0 = q * pl.Kk;
   const int Kc = (int)max((int64_t)0, min((int64_t)pl.Kk, GH - k0));
   const int nch = (Kc + kMChunk - 1) / kMChunk;
+  const int S = pl.ring;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   const uint32_t base_s = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -162,7 +165,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || N > kMRows ||
                        Urp % 16 != 0 || Urp > 256 || Urp < Ur || (uint32_t)Urp > ncols ||
                        ncols > 512u || (ncols & (ncols - 1u)) != 0 || ncols < 32u ||
-                       pl.Kk % kMChunk != 0 || Uq % 4 != 0 || Uq * Pk < Ur || d >= 2;
+                       pl.Kk % kMChunk != 0 || Uq % 4 != 0 || Uq * Pk < Ur || d >= 2 ||
+                       S < 2 || S > kMStages || pl.rbufs < 1 || pl.rbufs > 2;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
@@ -223,8 +227,37 @@ __global__ void __launch_bounds__(kMThreads, 1)
     const int t = d ? s : nT - 1 - s;
     const int tp = d ? s - 1 : nT - s;
     MTRACE(s, 0);
-    if (!failed && s < nT) {
-      const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+    const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+    // the pointwise inputs of item it at time t: dy, the saved gates, c_t,
+    // c_{t-1}
+    auto fetch_inputs = [&](int it, float (&v)[kMNIn]) {
+      const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+      const int64_t row = (int64_t)t * N + n;
+      const int64_t dyo = row * p.lddy + (int64_t)d * H + j;
+      v[0] = a.dy_bf16 ? __bfloat162float(reinterpret_cast<const bf16*>(a.dy)[dyo])
+                       : reinterpret_cast<const float*>(a.dy)[dyo];
+      if (p.mode == 0) {
+        v[1] = a.gates[row * H + j];
+      } else {
+        const float* gp = a.gates + row * 4 * H + j;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) v[1 + g] = gp[(int64_t)g * H];
+        if (p.mode == 1) {
+          v[5] = a.cseq[((int64_t)sc * N + n) * H + j];
+          v[6] = a.cseq[((int64_t)sp * N + n) * H + j];
+        }
+      }
+    };
+    // prefetch: into registers (loads in flight during the contraction), or
+    // with cp.async into shared memory
+    float rin[kRegItems][kMNIn];
+    if (!failed && s < nT && pl.pin == 2) {
+#pragma unroll
+      for (int k = 0; k < kRegItems; ++k) {
+        const int it = tid + k * kMThreads;
+        if (it < items) fetch_inputs(it, rin[k]);
+      }
+    } else if (!failed && s < nT && pl.pin == 1) {
       for (int it = tid; it < items; it += kMThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
@@ -261,7 +294,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         int c = 0;
         for (; ok && c < nch; ++c) {
           const uint32_t it = chunk_it + (uint32_t)c;
-          const uint32_t st = it % kMStages, ph = (it / kMStages) & 1u;
+          const uint32_t st = it % (uint32_t)S, ph = (it / (uint32_t)S) & 1u;
           int okl = 1;
           if (lane == 0) {
             okl = mbar_try_wait(empty0 + 8 * st, ph ^ 1u) ? 1 : 0;
@@ -299,7 +332,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         int c = 0;
         for (; c < nch; ++c) {
           const uint32_t it = chunk_it + (uint32_t)c;
-          const uint32_t st = it % kMStages, ph = (it / kMStages) & 1u;
+          const uint32_t st = it % (uint32_t)S, ph = (it / (uint32_t)S) & 1u;
           bool got = mbar_try_wait(full0 + 8 * st, ph);
           if (!got) {
             const unsigned long long t0 = globaltimer_ns();
@@ -351,7 +384,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     MTRACE(s, 1);
     // push the accumulator rows (batch n) to the owners of the units, 4 units
     // per 16-byte store (Uq is a multiple of 4)
-    float* recv = recv0 + (size_t)(s & 1) * Pk * N * Uq;
+    float* recv = recv0 + (size_t)(pl.rbufs == 2 ? (s & 1) : 0) * Pk * N * Uq;
     if (!failed && s > 0) {
       for (int cg = half; cg < Urp / 4; cg += 2) {
         float v[4];
@@ -374,58 +407,81 @@ __global__ void __launch_bounds__(kMThreads, 1)
         outs[n * Uq + uu] = v;
       }
     }
+    // one partial-sum buffer: nobody pushes the next step's partials before
+    // every owner has summed this step's
+    if (pl.rbufs == 1) cl_sync();
     cp_async_wait_all();
     __syncthreads();
     MTRACE(s, 2);
+    // one item's gate-gradient chain; v = its inputs (unused at s == nT)
+    auto point = [&](int it, const float (&v)[kMNIn]) {
+      const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+      float dhf;
+      if (s == 0)
+        dhf = a.dhy ? __bfloat162float(reinterpret_cast<const bf16*>(a.dhy)[(int64_t)n * H + j])
+                    : 0.f;
+      else
+        dhf = outs[n * Uq + uu] + st_carry[it];
+      if (s == nT) {
+        if (a.dh0) reinterpret_cast<bf16*>(a.dh0)[(int64_t)n * H + j] = __float2bfloat16_rn(dhf);
+        if (a.dc0) a.dc0[(int64_t)n * H + j] = st_dc[it];
+        return;
+      }
+      const int64_t row = (int64_t)t * N + n;
+      const float dh = v[0] + dhf;
+      const float g0 = v[1];
+      bf16* gxo = dgx + row * GH + j;
+      if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
+        const float g1 = v[2], g2 = v[3], g3 = v[4], cc = v[5], cpv = v[6];
+        const float tc = tanhf(cc);
+        const float dc = st_dc[it] + dh * g3 * (1.f - tc * tc);
+        gxo[0] = __float2bfloat16_rn(dc * g2 * g0 * (1.f - g0));
+        gxo[H] = __float2bfloat16_rn(dc * cpv * g1 * (1.f - g1));
+        gxo[2 * H] = __float2bfloat16_rn(dc * g0 * (1.f - g2 * g2));
+        gxo[3 * H] = __float2bfloat16_rn(dh * tc * g3 * (1.f - g3));
+        st_dc[it] = dc * g1;
+      } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
+        const float g1 = v[2], g2 = v[3], g3 = v[4];
+        const float hp = __bfloat162float(hseq[((int64_t)sp * N + n) * H + j]);
+        const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
+        const float daz = dh * (hp - g2) * g1 * (1.f - g1);
+        const float dar = dan * g3 * g0 * (1.f - g0);
+        gxo[0] = __float2bfloat16_rn(dar);
+        gxo[H] = __float2bfloat16_rn(daz);
+        gxo[2 * H] = __float2bfloat16_rn(dan);
+        bf16* gho = dgh + row * GH + j;
+        gho[0] = __float2bfloat16_rn(dar);
+        gho[H] = __float2bfloat16_rn(daz);
+        gho[2 * H] = __float2bfloat16_rn(dan * g0);
+        st_carry[it] = dh * g1;
+      } else {  // tanh RNN: g0 = h_t
+        gxo[0] = __float2bfloat16_rn(dh * (1.f - g0 * g0));
+      }
+    };
     if (!failed) {
-      for (int it = tid; it < items; it += kMThreads) {
-        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
-        float dhf;
-        if (s == 0)
-          dhf = a.dhy ? __bfloat162float(reinterpret_cast<const bf16*>(a.dhy)[(int64_t)n * H + j])
-                      : 0.f;
-        else
-          dhf = outs[n * Uq + uu] + st_carry[it];
-        if (s == nT) {
-          if (a.dh0) reinterpret_cast<bf16*>(a.dh0)[(int64_t)n * H + j] = __float2bfloat16_rn(dhf);
-          if (a.dc0) a.dc0[(int64_t)n * H + j] = st_dc[it];
-          continue;
+      if (pl.pin == 2) {
+#pragma unroll
+        for (int k = 0; k < kRegItems; ++k) {
+          const int it = tid + k * kMThreads;
+          if (it < items) point(it, rin[k]);
         }
-        const int64_t row = (int64_t)t * N + n;
-        const float dyv =
-            a.dy_bf16 ? __bfloat162float(
-                            reinterpret_cast<const bf16*>(a.dy)[row * p.lddy + (int64_t)d * H + j])
-                      : pin[it];
-        const float dh = dyv + dhf;
-        const float g0 = pin[1 * icap + it];
-        bf16* gxo = dgx + row * GH + j;
-        if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
-          const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
-          const float cc = pin[5 * icap + it], cpv = pin[6 * icap + it];
-          const float tc = tanhf(cc);
-          const float dc = st_dc[it] + dh * g3 * (1.f - tc * tc);
-          gxo[0] = __float2bfloat16_rn(dc * g2 * g0 * (1.f - g0));
-          gxo[H] = __float2bfloat16_rn(dc * cpv * g1 * (1.f - g1));
-          gxo[2 * H] = __float2bfloat16_rn(dc * g0 * (1.f - g2 * g2));
-          gxo[3 * H] = __float2bfloat16_rn(dh * tc * g3 * (1.f - g3));
-          st_dc[it] = dc * g1;
-        } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
-          const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
-          const int sp = d ? t + 1 : t;
-          const float hp = __bfloat162float(hseq[((int64_t)sp * N + n) * H + j]);
-          const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
-          const float daz = dh * (hp - g2) * g1 * (1.f - g1);
-          const float dar = dan * g3 * g0 * (1.f - g0);
-          gxo[0] = __float2bfloat16_rn(dar);
-          gxo[H] = __float2bfloat16_rn(daz);
-          gxo[2 * H] = __float2bfloat16_rn(dan);
-          bf16* gho = dgh + row * GH + j;
-          gho[0] = __float2bfloat16_rn(dar);
-          gho[H] = __float2bfloat16_rn(daz);
-          gho[2 * H] = __float2bfloat16_rn(dan * g0);
-          st_carry[it] = dh * g1;
-        } else {  // tanh RNN: g0 = h_t
-          gxo[0] = __float2bfloat16_rn(dh * (1.f - g0 * g0));
+      } else {
+        for (int it = tid; it < items; it += kMThreads) {
+          float v[kMNIn];
+          if (s < nT) {
+            if (pl.pin == 1) {
+#pragma unroll
+              for (int k = 0; k < kMNIn; ++k) v[k] = pin[k * icap + it];
+              if (a.dy_bf16) {
+                const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+                v[0] = __bfloat162float(reinterpret_cast<const bf16*>(
+                    a.dy)[((int64_t)t * N + n) * p.lddy + (int64_t)d * H + j]);
+              }
+            } else {
+              fetch_inputs(it, v);
+            }
+          }
+          point(it, v);
         }
       }
     }
@@ -480,12 +536,49 @@ bool rec_tcm_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size
     pl.lda = cols;
     pl.Mloc = Ur; pl.Mp = kMRows; pl.nb = N;
     pl.tc = 3;
+    // as many ring stages (bytes in flight on the dG_h stream) as fit: first
+    // with the prefetched pointwise inputs and double-buffered partial sums,
+    // then without the prefetch, then with one partial-sum buffer
+    // per-step time model (microseconds, fitted to step traces of this kernel):
+    // the dG_h stream, about 2 us per 64 KB of the slice; pointwise items cost
+    // 0.3 us each with prefetched inputs and 1.4 us reading them inline; a
+    // single partial-sum buffer costs a second cluster barrier
+    const bool regs = (Uq * N + kMThreads - 1) / kMThreads <= kRegItems;
+    const int cfgs[4][2] = {{regs ? 2 : 1, 2}, {1, 2}, {0, 2}, {0, 1}};
+    double best_cfg = 0;
+    int best_ring = 0, best_pin = 1, best_rb = 2;
+    for (int cfg = 0; cfg < 4; ++cfg) {
+      pl.pin = cfgs[cfg][0];
+      pl.rbufs = cfgs[cfg][1];
+      pl.ring = 0;
+      const size_t fixed = m_layout(pl, N).total + 1024;
+      // four stages: a deeper ring was measured no faster (the slice is read
+      // by every row group at once; the stream is bound by L2, not in-flight
+      // bytes)
+      const int ring = fixed < smem_limit
+                           ? (int)std::min<size_t>(kRingUse, (smem_limit - fixed) / (kMRows * 128))
+                           : 0;
+      if (ring < 2) continue;
+      const double per_thread = (double)((Uq * N + kMThreads - 1) / kMThreads);
+      const double t_stream = (double)Kk * kMRows * 2.0 / (kRingUse * kMRows * 128.0) * 2.0 *
+                              (ring < kRingUse ? (double)kRingUse / ring : 1.0);
+      const double t_point = per_thread * (pl.pin ? 0.3 : 1.4);
+      const double t_red = 1.0 + 0.02 * Pk * Uq * N / kMThreads + (pl.rbufs == 1 ? 2.0 : 0.0);
+      const double t = t_stream + t_point + t_red;
+      if (best_ring == 0 || t < best_cfg) {
+        best_cfg = t;
+        best_ring = ring;
+        best_pin = pl.pin;
+        best_rb = pl.rbufs;
+      }
+    }
+    if (best_ring < 2) continue;
+    pl.ring = best_ring; pl.pin = best_pin; pl.rbufs = best_rb;
     const MLayout L = m_layout(pl, N);
     pl.smem = std::max<size_t>(L.total + 1024, 120 * 1024);
     if (pl.smem > smem_limit) continue;
     if (D * pl.P > num_sms) continue;
-    // streamed slice per step, the owners' reduction and pointwise items
-    const double cost = (double)Kk * 2.0 + (double)Uq * N * (Pk / 4.0 + 6.0) / 8.0;
+    const double cost = best_cfg;
     if (!found || cost < best) {
       found = true;
       best = cost;
