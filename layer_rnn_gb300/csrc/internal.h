@@ -93,6 +93,10 @@ struct RecDirArgs {
   void* dgh = nullptr;           // [T][N][G*H] (compute type), == dgx unless GRU
   void* dh0 = nullptr;           // [N][H] or null
   float* dc0 = nullptr;          // [N][H] or null
+  // time order of this direction's arrays: 1 = reversed (a bidirectional
+  // layer's second direction), 0 = forward, -1 = taken from the block's
+  // direction index (both directions in one launch)
+  int rev = -1;
 };
 
 struct RecPlan {

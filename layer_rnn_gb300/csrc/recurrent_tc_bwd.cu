@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   const int b = blockIdx.x - d * P;
   const int r = b / Pk, q = b - r * Pk;
   const RecDirArgs& a = p.dir[d];
+  const int rv = a.rev >= 0 ? a.rev : d;  // reversed time order
   const int H = p.H, N = p.N, nT = p.T, G = p.G, Ur = pl.Ur, Uq = pl.Uq;
   const int64_t GH = (int64_t)G * H;
   const int Nm = pl.nbp, Kp = pl.K;
@@ -203,13 +204,13 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   uint32_t phase = 0;
 
   for (int s = 0; s <= nT; ++s) {
-    const int t = d ? s : nT - 1 - s;   // time processed at this step (s < nT)
-    const int tp = d ? s - 1 : nT - s;  // time processed at the previous step (s > 0)
+    const int t = rv ? s : nT - 1 - s;   // time processed at this step (s < nT)
+    const int tp = rv ? s - 1 : nT - s;  // time processed at the previous step (s > 0)
     BTRACE(s, 0);
     // pointwise inputs of time t (fp32 sources by cp.async; bf16 ones are read
     // in the pointwise loop)
     if (!failed && s < nT) {
-      const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+      const int sc = rv ? t : t + 1, sp = rv ? t + 1 : t;
       for (int it = tid; it < items; it += kBThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           st_dc[it] = dc * g1;
         } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
-          const int sp = d ? t + 1 : t;
+          const int sp = rv ? t + 1 : t;
           const float hp = BF ? to_f(hseq[((int64_t)sp * N + n) * H + j]) : pin[6 * icap + it];
           const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
           const float daz = dh * (hp - g2) * g1 * (1.f - g1);

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const int b = blockIdx.x - d * P;
   const int r = b / Pk, q = b - r * Pk;
   const RecDirArgs& a = p.dir[d];
+  const int rv = a.rev >= 0 ? a.rev : d;  // reversed time order
   const int H = p.H, N = p.N, nT = p.T, G = p.G, Ur = pl.Ur, Uq = pl.Uq;
   const int64_t GH = (int64_t)G * H;
   const int Urp = pl.nbp;
@@ -224,10 +225,10 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const int nrow = q4 * 32 + lane;  // batch row of this thread's tensor-memory lane
 
   for (int s = 0; s <= nT; ++s) {
-    const int t = d ? s : nT - 1 - s;
-    const int tp = d ? s - 1 : nT - s;
+    const int t = rv ? s : nT - 1 - s;
+    const int tp = rv ? s - 1 : nT - s;
     MTRACE(s, 0);
-    const int sc = d ? t : t + 1, sp = d ? t + 1 : t;
+    const int sc = rv ? t : t + 1, sp = rv ? t + 1 : t;
     // the pointwise inputs of item it at time t: dy, the saved gates, c_t,
     // c_{t-1}
     auto fetch_inputs = [&](int it, float (&v)[kMNIn]) {
