@@ -70,25 +70,38 @@ def load_peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
+def kernel_source_sha256(src):
+    """sha256 over a kernel's source file and every header of the library
+    (csrc/*.cuh, csrc/*.h, in name order): a change to any of them can change
+    the kernel."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "layer_rnn_gb300", "csrc")
+    files = [os.path.join(ROOT, src)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
+                                                glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for fn in files:
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def traffic_for(phase, cfg):
     """DRAM bytes per launch of the phase's kernel from a committed ncu summary,
-    or None when there is none for this workload or the kernel source changed
-    since the counters were taken."""
-    import hashlib
+    or None when there is none for this workload or the kernel source (or a
+    header it may include) changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         doc = json.load(f)
     ent = doc.get(cfg["name"], {}).get(phase)
-    if not ent:
+    if not ent or "sources_sha256" not in ent:
         return None
-    src = os.path.join(ROOT, ent["source"])
-    if not os.path.exists(src):
+    if not os.path.exists(os.path.join(ROOT, ent["source"])):
         return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != ent["source_sha256"]:
-            return None
+    if kernel_source_sha256(ent["source"]) != ent["sources_sha256"]:
+        return None
     return ent["dram_bytes_per_launch"]
 
 

@@ -119,15 +119,65 @@ __device__ __forceinline__ void publish_flag(unsigned* f, unsigned value) {
 }
 
 // The lanes of a warp wait, together, for the flags of blocks lo..hi
-// (inclusive; block b's flag at flags[b * stride]) to reach `value`.
+// (inclusive; block b's flag at flags[b * stride]) to reach `value`.  Lane l
+// polls flags lo + l + 32 j, all of its loads in flight at once, and re-polls
+// only the flags not yet there, so a warp sees up to 256 flags that are
+// already set in one round trip to L2 (polling them one after another costs
+// two round trips each).  The acquire side of the writers' releases: for more
+// than two flags a lane, one gpu-scope acquire fence after the relaxed loads
+// that saw the values; for fewer, an acquire load of each flag (the fence
+// also waits for the lane's own stores still in flight, which costs more than
+// one or two loads).  With at most one flag a lane, each lane runs wait_flag
+// (measured faster there than the batched loop).  Bounded like wait_flag.
 // Returns false (in every lane) if any wait gave up.
 __device__ __forceinline__ bool warp_wait_flags(const unsigned* flags, int stride, int lo, int hi,
                                                 unsigned value, int* status,
                                                 long long timeout_ns, int spin_ns) {
+  constexpr int kPer = 8;
   const int lane = threadIdx.x & 31;
   bool ok = true;
-  for (int i = lo + lane; i <= hi && ok; i += 32)
-    ok = wait_flag(flags + (size_t)i * stride, value, status, timeout_ns, spin_ns);
+  if (hi - lo < 32) {  // at most one flag a lane
+    if (lo + lane <= hi)
+      ok = wait_flag(flags + (size_t)(lo + lane) * stride, value, status, timeout_ns, spin_ns);
+    return __all_sync(0xffffffffu, ok);
+  }
+  for (int base = lo; base <= hi && ok; base += 32 * kPer) {
+    unsigned pending = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (base + lane + 32 * j <= hi) pending |= 1u << j;
+    unsigned long long t0 = 0;
+    unsigned it = 0;
+    while (pending) {
+      unsigned v[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        v[j] = (pending >> j) & 1u
+                   ? ld_relaxed_gpu(flags + (size_t)(base + lane + 32 * j) * stride)
+                   : value;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (v[j] >= value) pending &= ~(1u << j);
+      if (!pending) break;
+      if (it == 0) t0 = globaltimer_ns();
+      if (spin_ns > 0) __nanosleep(spin_ns);
+      if ((++it & 31u) == 0) {
+        if (ld_volatile_int(status) != kDevOk) {
+          ok = false;
+        } else if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+          atomicCAS(status, kDevOk, kDevTimeout);
+          ok = false;
+        }
+        if (!ok) break;
+      }
+    }
+  }
+  if (ok) {
+    if (hi - lo + 1 > 64)
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    else
+      for (int i = lo + lane; i <= hi; i += 32) (void)ld_acquire_gpu(flags + (size_t)i * stride);
+  }
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                                  p.timeout_ns, p.spin_ns);
         }
         __syncwarp();
+        MTRACE(s, 5);
         int c = 0;
         for (; ok && c < nch; ++c) {
           const uint32_t it = chunk_it + (uint32_t)c;
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
           }
           __syncwarp();
         }
+        MTRACE(s, 6);
         if (lane == 0 && c < nch) {
           s_issued = c;
           __threadfence_block();
