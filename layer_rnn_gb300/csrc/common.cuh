@@ -127,7 +127,9 @@ __device__ __forceinline__ void publish_flag(unsigned* f, unsigned value) {
 // than two flags a lane, one gpu-scope acquire fence after the relaxed loads
 // that saw the values; for fewer, an acquire load of each flag (the fence
 // also waits for the lane's own stores still in flight, which costs more than
-// one or two loads).  With at most one flag a lane, each lane runs wait_flag
+// one or two loads; it waits for the lane's loads in flight as well, so a
+// caller with a wide range issues its prefetches after the wait).  With at
+// most one flag a lane, each lane runs wait_flag
 // (measured faster there than the batched loop).  Bounded like wait_flag.
 // Returns false (in every lane) if any wait gave up.
 __device__ __forceinline__ bool warp_wait_flags(const unsigned* flags, int stride, int lo, int hi,

@@ -30,13 +30,12 @@
 #include "tc_common.cuh"
 
 #ifdef LAYER_RNN_TRACE
-__device__ unsigned long long g_mtrace[4][1024][8];
-#define MTRACE(s, k)                                                                          \
-  do {                                                                                        \
-    const int nb_ = gridDim.x;                                                                \
-    const int b_ = blockIdx.x == 0 ? 0 : blockIdx.x == nb_ / 3 ? 1 : blockIdx.x == (2 * nb_) / 3 \
-                 ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
-    if (b_ >= 0 && threadIdx.x == 0 && (s) < 1024) g_mtrace[b_][(s)][(k)] = lr::globaltimer_ns();\
+// per block (up to 160), per step (up to 1024), 8 time marks
+__device__ unsigned long long g_mtrace[160][1024][8];
+#define MTRACE(s, k)                                                                   \
+  do {                                                                                 \
+    if (blockIdx.x < 160 && threadIdx.x == 0 && (s) < 1024)                            \
+      g_mtrace[blockIdx.x][(s)][(k)] = lr::globaltimer_ns();                           \
   } while (0)
 #else
 #define MTRACE(s, k) ((void)0)
@@ -54,7 +53,11 @@ constexpr int kMChunk = 64;     // bf16 elements of K per ring stage / B atom
 constexpr int kMStages = 8;      // most ring stages the kernel supports
 constexpr int kRingUse = 4;      // stages the plan uses
 constexpr int kMNIn = 7;        // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1}
-constexpr int kRegItems = 4;    // items per thread when the inputs are prefetched to registers
+constexpr int kRegItems = 5;    // items per thread when the inputs are prefetched to registers
+// threads that prefetch the pointwise inputs, into registers or shared memory
+// (warps 1..7: the producer warp ends a wide flag wait with an acquire fence,
+// which would also wait for its own loads and copies in flight)
+constexpr int kRegThreads = kMThreads - 32;
 
 struct MMaps {
   CUtensorMap a[2];  // dG_h of each direction: [T][N][G*H] bf16, box 64 x 128 x 1
@@ -253,13 +256,15 @@ __global__ void __launch_bounds__(kMThreads, 1)
     // with cp.async into shared memory
     float rin[kRegItems][kMNIn];
     if (!failed && s < nT && pl.pin == 2) {
+      if (warp > 0) {
 #pragma unroll
-      for (int k = 0; k < kRegItems; ++k) {
-        const int it = tid + k * kMThreads;
-        if (it < items) fetch_inputs(it, rin[k]);
+        for (int k = 0; k < kRegItems; ++k) {
+          const int it = tid - 32 + k * kRegThreads;
+          if (it < items) fetch_inputs(it, rin[k]);
+        }
       }
-    } else if (!failed && s < nT && pl.pin == 1) {
-      for (int it = tid; it < items; it += kMThreads) {
+    } else if (!failed && s < nT && pl.pin == 1 && warp > 0) {
+      for (int it = tid - 32; it < items; it += kRegThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         if (!a.dy_bf16)
@@ -463,10 +468,12 @@ __global__ void __launch_bounds__(kMThreads, 1)
     };
     if (!failed) {
       if (pl.pin == 2) {
+        if (warp > 0) {
 #pragma unroll
-        for (int k = 0; k < kRegItems; ++k) {
-          const int it = tid + k * kMThreads;
-          if (it < items) point(it, rin[k]);
+          for (int k = 0; k < kRegItems; ++k) {
+            const int it = tid - 32 + k * kRegThreads;
+            if (it < items) point(it, rin[k]);
+          }
         }
       } else {
         for (int it = tid; it < items; it += kMThreads) {
@@ -539,15 +546,17 @@ bool rec_tcm_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size
     pl.lda = cols;
     pl.Mloc = Ur; pl.Mp = kMRows; pl.nb = N;
     pl.tc = 3;
-    // as many ring stages (bytes in flight on the dG_h stream) as fit: first
-    // with the prefetched pointwise inputs and double-buffered partial sums,
-    // then without the prefetch, then with one partial-sum buffer
+    // as many ring stages (bytes in flight on the dG_h stream) as fit, for
+    // each of: prefetched pointwise inputs (in registers when they fit, else
+    // in shared memory) with double-buffered partial sums, the same with one
+    // partial-sum buffer, no prefetch with two, no prefetch with one
     // per-step time model (microseconds, fitted to step traces of this kernel):
     // the dG_h stream, about 2 us per 64 KB of the slice; pointwise items cost
     // 0.3 us each with prefetched inputs and 1.4 us reading them inline; a
     // single partial-sum buffer costs a second cluster barrier
-    const bool regs = (Uq * N + kMThreads - 1) / kMThreads <= kRegItems;
-    const int cfgs[4][2] = {{regs ? 2 : 1, 2}, {1, 2}, {0, 2}, {0, 1}};
+    const bool regs = (Uq * N + kRegThreads - 1) / kRegThreads <= kRegItems;
+    // registers whenever the items fit (measured faster than shared memory)
+    const int cfgs[4][2] = {{regs ? 2 : 1, 2}, {regs ? 2 : 0, 1}, {0, 2}, {0, 1}};
     double best_cfg = 0;
     int best_ring = 0, best_pin = 1, best_rb = 2;
     for (int cfg = 0; cfg < 4; ++cfg) {
@@ -562,7 +571,8 @@ bool rec_tcm_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size
                            ? (int)std::min<size_t>(kRingUse, (smem_limit - fixed) / (kMRows * 128))
                            : 0;
       if (ring < 2) continue;
-      const double per_thread = (double)((Uq * N + kMThreads - 1) / kMThreads);
+      const int workers = pl.pin == 2 ? kRegThreads : kMThreads;
+      const double per_thread = (double)((Uq * N + workers - 1) / workers);
       const double t_stream = (double)Kk * kMRows * 2.0 / (kRingUse * kMRows * 128.0) * 2.0 *
                               (ring < kRingUse ? (double)kRingUse / ring : 1.0);
       const double t_point = per_thread * (pl.pin ? 0.3 : 1.4);
@@ -598,8 +608,10 @@ extern "C" int rnn_debug_mtrace_copy(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, g_mtrace, bytes);
 }
 extern "C" int rnn_debug_mtrace_clear() {
-  static unsigned long long zeros[4][1024][8];
-  return (int)cudaMemcpyToSymbol(g_mtrace, zeros, sizeof(zeros));
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_mtrace);
+  if (e == cudaSuccess) e = cudaMemset(ptr, 0, sizeof(g_mtrace));
+  return (int)e;
 }
 #endif
 
