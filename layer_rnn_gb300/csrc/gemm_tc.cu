@@ -392,6 +392,47 @@ __global__ void transpose_bf16_kernel(const bf16* src, int64_t rows, int64_t col
   }
 }
 
+// bf16 transpose for aligned shapes (rows % 16 == 0, cols % 8 == 0, both row
+// strides multiples of 8 elements, 16-byte aligned buffers): each thread reads
+// a 16-row x 8-column block as sixteen 16-byte row pieces (a warp reads 512
+// contiguous bytes of a row per load), transposes it in registers with byte
+// permutes and writes 8 output rows of 32 contiguous bytes (whole sectors).
+// Block = 8 warps = 128 source rows x 256 source columns.
+__device__ __forceinline__ uint32_t u4_word(const uint4& a, int k) {
+  return k == 0 ? a.x : k == 1 ? a.y : k == 2 ? a.z : a.w;
+}
+
+__global__ void __launch_bounds__(256) transpose_bf16_v_kernel(const bf16* __restrict__ src,
+                                                               int64_t rows, int64_t cols,
+                                                               int64_t lds, bf16* __restrict__ dst,
+                                                               int64_t ldd) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t r0 = (int64_t)blockIdx.y * 128 + w * 16;
+  const int64_t c0 = ((int64_t)blockIdx.x * 32 + lane) * 8;
+  if (r0 >= rows || c0 >= cols) return;
+  uint4 v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    v[i] = __ldg(reinterpret_cast<const uint4*>(src + (r0 + i) * lds + c0));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    // element j of source rows 2k and 2k+1 -> the low and high half of word k
+    const unsigned sel = (j & 1) ? 0x7632u : 0x5410u;
+    uint4 o0, o1;
+    o0.x = __byte_perm(u4_word(v[0], j >> 1), u4_word(v[1], j >> 1), sel);
+    o0.y = __byte_perm(u4_word(v[2], j >> 1), u4_word(v[3], j >> 1), sel);
+    o0.z = __byte_perm(u4_word(v[4], j >> 1), u4_word(v[5], j >> 1), sel);
+    o0.w = __byte_perm(u4_word(v[6], j >> 1), u4_word(v[7], j >> 1), sel);
+    o1.x = __byte_perm(u4_word(v[8], j >> 1), u4_word(v[9], j >> 1), sel);
+    o1.y = __byte_perm(u4_word(v[10], j >> 1), u4_word(v[11], j >> 1), sel);
+    o1.z = __byte_perm(u4_word(v[12], j >> 1), u4_word(v[13], j >> 1), sel);
+    o1.w = __byte_perm(u4_word(v[14], j >> 1), u4_word(v[15], j >> 1), sel);
+    uint4* out = reinterpret_cast<uint4*>(dst + (c0 + j) * ldd + r0);
+    out[0] = o0;
+    out[1] = o1;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -592,6 +633,16 @@ cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t 
 cudaError_t transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
                            int64_t ldd, cudaStream_t st) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const bool vec = rows % 16 == 0 && cols % 8 == 0 && lds % 8 == 0 && ldd % 8 == 0 &&
+                   reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dst) % 16 == 0 && (rows + 127) / 128 <= 65535;
+  if (vec) {
+    dim3 grid((unsigned)((cols / 8 + 31) / 32), (unsigned)((rows + 127) / 128));
+    transpose_bf16_v_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const bf16*>(src), rows, cols,
+                                                  lds, reinterpret_cast<bf16*>(dst), ldd);
+    g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+  }
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
   transpose_bf16_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const bf16*>(src), rows, cols, lds,
                                               reinterpret_cast<bf16*>(dst), ldd);
