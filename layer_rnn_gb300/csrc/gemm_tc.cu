@@ -376,11 +376,14 @@ __global__ void split_kernel(const float* src, int64_t rows, int64_t cols, int64
   }
 }
 
-// tf32 hi/lo split without transposing, for aligned shapes (16-byte aligned
-// buffers, row strides and column counts multiples of 4): one 16-byte vector
-// of 4 columns per thread and loop step.  (A register-blocked transposing
-// version, 8 x 4 per thread with 16-byte stores to 32 rows at once, measured
-// slower than the 32 x 32 shared-memory tile of split_kernel.)
+// tf32 hi/lo split for aligned shapes (16-byte aligned buffers, row strides
+// and column counts multiples of 4; rows a multiple of 4 when transposing).
+// Plain (split_v_kernel): one 16-byte vector of 4 columns per thread and loop
+// step.  Transposing (split_tt_kernel): a 64 x 64 tile through shared memory
+// (row pitch 65 floats), read and written with 16-byte accesses, a warp
+// covering two 256-byte row pieces per access on both sides.  (A
+// register-blocked transposing version, 8 x 4 per thread with 16-byte stores
+// to 32 rows at once, measured slower than the 32 x 32 tile of split_kernel.)
 __device__ __forceinline__ float4 tf32_hi4(float4 v) {
   return make_float4(__uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u),
                      __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u),
@@ -401,6 +404,40 @@ __global__ void __launch_bounds__(256) split_v_kernel(const float* __restrict__ 
     *reinterpret_cast<float4*>(hi + r * ldd + c) = h;
     if (lo)
       *reinterpret_cast<float4*>(lo + r * ldd + c) =
+          make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+  }
+}
+
+__global__ void __launch_bounds__(256) split_tt_kernel(const float* __restrict__ src, int64_t rows,
+                                                       int64_t cols, int64_t lds,
+                                                       float* __restrict__ hi,
+                                                       float* __restrict__ lo, int64_t ldd) {
+  __shared__ float tile[64][65];
+  const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+  const int tid = threadIdx.x, q = tid & 15, sub = tid >> 4;  // 16 vectors x 16 rows a pass
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int row = p * 16 + sub;
+    const int64_t r = r0 + row, c = c0 + 4 * q;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows && c < cols) v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    tile[row][4 * q + 0] = v.x;
+    tile[row][4 * q + 1] = v.y;
+    tile[row][4 * q + 2] = v.z;
+    tile[row][4 * q + 3] = v.w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int oc = p * 16 + sub;  // source column = output row within the tile
+    const int64_t orow = c0 + oc, ocol = r0 + 4 * q;
+    if (orow >= cols || ocol >= rows) continue;
+    const float4 v = make_float4(tile[4 * q + 0][oc], tile[4 * q + 1][oc], tile[4 * q + 2][oc],
+                                 tile[4 * q + 3][oc]);
+    const float4 h = tf32_hi4(v);
+    *reinterpret_cast<float4*>(hi + orow * ldd + ocol) = h;
+    if (lo)
+      *reinterpret_cast<float4*>(lo + orow * ldd + ocol) =
           make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
   }
 }
@@ -657,6 +694,12 @@ cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t 
                   reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
                   reinterpret_cast<uintptr_t>(hi) % 16 == 0 &&
                   reinterpret_cast<uintptr_t>(lo) % 16 == 0;
+  if (al && transpose && rows % 4 == 0 && (rows + 63) / 64 <= 65535) {
+    dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
+    split_tt_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd);
+    g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+  }
   if (al && !transpose) {
     const int64_t blocks = std::min<int64_t>((rows * (cols / 4) + 255) / 256, 152 * 16);
     split_v_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd);
