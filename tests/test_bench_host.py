@@ -1,0 +1,77 @@
+"""Host logic of bench.py that needs no GPU: the DRAM-traffic figure of the
+roofline line is taken from profiles/traffic.json only while the kernel's
+source and every header of the library are unchanged since the capture."""
+
+import json
+import os
+
+import pytest
+
+
+def _tree(tmp_path):
+    csrc = tmp_path / "layer_rnn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1\n")
+    (csrc / "common.cuh").write_text("header v1\n")
+    (csrc / "internal.h").write_text("decls v1\n")
+    (tmp_path / "profiles").mkdir()
+    return csrc
+
+
+def _write_traffic(tmp_path, sha, nbytes=123456):
+    doc = {"ds2_lstm": {"rec_fwd": {"kernel": "k", "source": "layer_rnn_gb300/csrc/k.cu",
+                                    "sources_sha256": sha, "dram_bytes_per_launch": nbytes}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(doc))
+
+
+@pytest.fixture
+def bench_at(tmp_path, monkeypatch):
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    return bench
+
+
+def test_traffic_reported_while_sources_match(tmp_path, bench_at):
+    _tree(tmp_path)
+    _write_traffic(tmp_path, bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu"))
+    assert bench_at.traffic_for("rec_fwd", {"name": "ds2_lstm"}) == 123456
+    # no entry for this phase or workload
+    assert bench_at.traffic_for("rec_bwd", {"name": "ds2_lstm"}) is None
+    assert bench_at.traffic_for("rec_fwd", {"name": "lstm4_bf16"}) is None
+
+
+@pytest.mark.parametrize("changed", ["k.cu", "common.cuh", "internal.h", "new.cuh"])
+def test_traffic_dropped_when_kernel_or_header_changes(tmp_path, bench_at, changed):
+    csrc = _tree(tmp_path)
+    _write_traffic(tmp_path, bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu"))
+    with open(os.path.join(csrc, changed), "a") as f:
+        f.write("edit\n")
+    assert bench_at.traffic_for("rec_fwd", {"name": "ds2_lstm"}) is None
+
+
+def test_other_sources_do_not_affect_the_hash(tmp_path, bench_at):
+    csrc = _tree(tmp_path)
+    before = bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu")
+    (csrc / "other.cu").write_text("another kernel\n")
+    assert bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu") == before
+
+
+def test_entries_without_a_source_hash_are_ignored(tmp_path, bench_at):
+    _tree(tmp_path)
+    doc = {"ds2_lstm": {"rec_fwd": {"kernel": "k", "source": "layer_rnn_gb300/csrc/k.cu",
+                                    "dram_bytes_per_launch": 1}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(doc))
+    assert bench_at.traffic_for("rec_fwd", {"name": "ds2_lstm"}) is None
+
+
+def test_committed_traffic_entries_name_existing_profiles():
+    import bench
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        doc = json.load(f)
+    for wl, phases in doc.items():
+        if wl.startswith("_"):
+            continue
+        for ph, ent in phases.items():
+            assert os.path.exists(os.path.join(bench.ROOT, ent["source"])), (wl, ph)
+            assert os.path.exists(os.path.join(bench.ROOT, ent["profile"])), (wl, ph)
+            assert ent["dram_bytes_per_launch"] > 0
