@@ -119,19 +119,18 @@ __device__ __forceinline__ void publish_flag(unsigned* f, unsigned value) {
 }
 
 // The lanes of a warp wait, together, for the flags of blocks lo..hi
-// (inclusive; block b's flag at flags[b * stride]) to reach `value`.  Lane l
-// polls flags lo + l + 32 j, all of its loads in flight at once, and re-polls
-// only the flags not yet there, so a warp sees up to 256 flags that are
-// already set in one round trip to L2 (polling them one after another costs
-// two round trips each).  The acquire side of the writers' releases: for more
-// than two flags a lane, one gpu-scope acquire fence after the relaxed loads
-// that saw the values; for fewer, an acquire load of each flag (the fence
-// also waits for the lane's own stores still in flight, which costs more than
-// one or two loads; it waits for the lane's loads in flight as well, so a
-// caller with a wide range issues its prefetches after the wait).  With at
-// most one flag a lane, each lane runs wait_flag
-// (measured faster there than the batched loop).  Bounded like wait_flag.
-// Returns false (in every lane) if any wait gave up.
+// (inclusive; block b's flag at flags[b * stride]) to reach `value`.  Bounded
+// like wait_flag; returns false (in every lane) if any wait gave up.
+// - At most one flag a lane: each lane runs wait_flag (measured fastest there).
+// - More: lane l polls flags lo + l + 32 j with all of its loads in flight at
+//   once and re-polls only the flags not yet set, so a warp sees up to 256 set
+//   flags in one round trip to L2 (one after another costs two round trips a
+//   flag: the relaxed load, then the acquire load).
+// - The acquire side of the writers' releases: with up to two flags a lane, an
+//   acquire load of each flag; with more, one gpu-scope acquire fence after
+//   the relaxed loads that saw the values.  The fence also waits for the
+//   lane's own stores and loads still in flight, so a caller with a wide range
+//   issues its prefetches after the wait or from other warps.
 __device__ __forceinline__ bool warp_wait_flags(const unsigned* flags, int stride, int lo, int hi,
                                                 unsigned value, int* status,
                                                 long long timeout_ns, int spin_ns) {
