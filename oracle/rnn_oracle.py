@@ -32,6 +32,13 @@ What it computes (sources, by page title and section):
 * Tensor shapes follow the PyTorch shapes quoted in the oneDNN issue: input in
   TNC order [T, N, I]; hx / cx / hy / cy of shape (num_layers * num_directions,
   batch, hidden), index ``layer * D + direction``.
+* Variable-length batches (optional ``lengths``).  "rnn training example?"
+  (oneDNN issue #218) names PyTorch's packed sequences as the form variable
+  lengths arrive in, and the unpacking to TNC as the integration cost.
+  Reading taken: PyTorch's packed-sequence semantics on the padded TNC batch.
+  A step t >= len_n of sequence n leaves its state unchanged and writes zero
+  output, so hy is the state after the last valid step, and the reverse
+  direction starts from h0 at step len_n - 1.
 * Backward ("reuse forward intermediate results during backward", MXNet design
   page, Operator Registration): reverse-mode differentiation of the scalar loss
       loss = sum(y * dy) + sum(hy * dhy) + sum(cy * dcy)
@@ -120,13 +127,19 @@ def flatten_weights(params, mode, num_layers, bidirectional, input_size, hidden_
 # one direction of one layer
 # ----------------------------------------------------------------------------
 
-def _direction_forward(mode, x, h0, c0, p, reverse):
+def _direction_forward(mode, x, h0, c0, p, reverse, lengths=None):
     """Run one direction over the whole sequence.
 
     x: [T, N, I_l]; h0, c0: [N, H].  Returns (out [T, N, H], h_T, c_T, tape);
     ``tape`` keeps, per processed step, the values the backward pass reuses.
+
+    lengths: None, or the valid length of each sequence [N].  Step t of a
+    sequence with t >= its length leaves the state unchanged and outputs zero,
+    so the forward direction ends on the state of the last valid step and the
+    reverse direction starts from h0 at the last valid step.
     """
     T = x.shape[0]
+    valid = None if lengths is None else np.arange(T)[:, None] < np.asarray(lengths)[None, :]
     W_ih, W_hh, b_ih, b_hh = p["W_ih"], p["W_hh"], p["b_ih"], p["b_hh"]
     H = W_hh.shape[1]
     out = np.zeros((T, x.shape[1], H))
@@ -159,7 +172,15 @@ def _direction_forward(mode, x, h0, c0, p, reverse):
             tape.append(dict(t=t, h_prev=h_prev, r=r, z=z, n=n, h_n=h_n))
         else:
             raise ValueError("unknown mode %r" % mode)
-        out[t] = h
+        if valid is None:
+            out[t] = h
+        else:
+            m = valid[t][:, None]
+            tape[-1]["m"] = m
+            out[t] = np.where(m, h, 0.0)
+            h = np.where(m, h, h_prev)
+            if c is not None:
+                c = np.where(m, c, c_prev)
     return out, h, c, tape
 
 
@@ -178,7 +199,17 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
     for rec in reversed(tape):
         t = rec["t"]
         h_prev = rec["h_prev"]
-        dh = dout[t] + dh_next
+        m = rec.get("m")
+        if m is None:
+            dh = dout[t] + dh_next
+        else:
+            # a step past the sequence's length passed h (and c) through and
+            # output zero: its incoming state gradient goes straight back
+            dh = np.where(m, dout[t] + dh_next, 0.0)
+            carry_h = np.where(m, 0.0, dh_next)
+            if mode == "lstm":
+                carry_c = np.where(m, 0.0, dc_next)
+                dc_next = np.where(m, dc_next, 0.0)
         if mode == "rnn_tanh":
             da = dh * (1.0 - rec["h"] ** 2)
             dgx = dgh = da
@@ -207,6 +238,10 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
             dgx = np.concatenate([da_r, da_z, da_n], axis=1)
             dgh = np.concatenate([da_r, da_z, da_n * r], axis=1)
             dh_next = dh * z + dgh @ W_hh
+        if m is not None:
+            dh_next = dh_next + carry_h
+            if mode == "lstm":
+                dc_next = dc_next + carry_c
         dx[t] = dgx @ W_ih
         grads["W_ih"] += dgx.T @ x[t]
         grads["W_hh"] += dgh.T @ h_prev
@@ -219,17 +254,25 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
 # whole stack
 # ----------------------------------------------------------------------------
 
-def forward(mode, x, h0, c0, params, num_layers, bidirectional):
+def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
     """Training forward of the stack.
 
     x: [T, N, I]; h0, c0: [L*D, N, H] (c0 ignored unless LSTM; None = zeros);
     params: list (index l*D+d) of dicts W_ih, W_hh, b_ih, b_hh.
+    lengths: None (every sequence has length T) or the valid length of each
+    sequence, [N] integers in 0..T, for padded variable-length batches (the
+    PyTorch packed-sequence semantics: y is zero past a sequence's length, hy
+    is the state after its last valid step in each direction).
     Returns (y [T, N, D*H], hy [L*D, N, H], cy [L*D, N, H] or None, cache).
     """
     x = np.asarray(x, dtype=np.float64)
     D = 2 if bidirectional else 1
     H = params[0]["W_hh"].shape[1]
     T, N = x.shape[0], x.shape[1]
+    if lengths is not None:
+        lengths = np.asarray(lengths)
+        if lengths.shape != (N,) or lengths.min(initial=0) < 0 or lengths.max(initial=0) > T:
+            raise ValueError("lengths must be [N] integers in 0..T")
     if h0 is None:
         h0 = np.zeros((num_layers * D, N, H))
     if c0 is None:
@@ -246,7 +289,8 @@ def forward(mode, x, h0, c0, params, num_layers, bidirectional):
         for d in range(D):
             k = l * D + d
             out, hT, cT, tape = _direction_forward(mode, layer_in, h0[k], c0[k],
-                                                   params[k], reverse=(d == 1))
+                                                   params[k], reverse=(d == 1),
+                                                   lengths=lengths)
             outs.append(out)
             hy[k] = hT
             if cy is not None:
@@ -304,14 +348,16 @@ def loss(y, hy, cy, dy, dhy=None, dcy=None):
 
 
 def run_flat(mode, num_layers, bidirectional, input_size, hidden_size,
-             x, h0, c0, w_flat, dy, dhy, dcy):
+             x, h0, c0, w_flat, dy, dhy, dcy, lengths=None):
     """Forward + backward on the canonical flat weight buffer.
 
     Returns a dict of float64 arrays: y, hy, cy, dx, dh0, dc0, dW (flat).
+    ``lengths``: as for ``forward``.
     """
     params = unflatten_weights(w_flat, mode, num_layers, bidirectional,
                                input_size, hidden_size)
-    y, hy, cy, cache = forward(mode, x, h0, c0, params, num_layers, bidirectional)
+    y, hy, cy, cache = forward(mode, x, h0, c0, params, num_layers, bidirectional,
+                               lengths)
     dx, dh0, dc0, dparams = backward(params, cache, dy, dhy,
                                      dcy if mode == "lstm" else None)
     dW = flatten_weights(dparams, mode, num_layers, bidirectional,
