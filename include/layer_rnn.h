@@ -210,6 +210,38 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N,
                                   const void* x, const void* h0, const void* y,
                                   const void* workspace, int64_t ws_bytes, void* dW);
 
+/* Variable-length (padded) batches.  The same calls with one more argument,
+ * lengths: device memory, N int32 values, the valid length of each sequence
+ * of the padded [T, N, ...] batch (the PyTorch packed-sequence layout after
+ * unpacking to TNC, which "rnn training example?" (oneDNN issue #218) raises
+ * as the way such batches arrive).  Semantics, per sequence n and direction:
+ * a step t >= lengths[n] leaves the state unchanged and writes zero output,
+ * so y is zero past the length, hy / cy are the state after the last valid
+ * step, and the reverse direction starts from h0 at step lengths[n] - 1.
+ * rnn_backward_data_varlen is the derivative of that: dy past a sequence's
+ * length is ignored, and its gate gradients are zero.  rnn_backward_weights
+ * needs no lengths (the zero gate gradients drop the padded steps); the padded
+ * entries of x must be finite, because dW_ih multiplies them by zero.
+ * Values outside 0..T act as 0 or T.  The lengths buffer is read by the
+ * enqueued kernels: keep it unchanged until they have run.  These calls run
+ * on the CUDA-core recurrent kernels (no wavefront, no tensor-core recurrence;
+ * the dense phases still use the tensor cores).
+ * Errors: as the calls without lengths, and RNN_ERR_INVALID_ARG for a NULL
+ * lengths, RNN_ERR_MISALIGNED for one not 4-byte aligned. */
+rnn_status_t rnn_forward_training_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                         const int32_t* lengths, const void* x,
+                                         const void* h0, const void* c0, const void* W,
+                                         void* y, void* hy, void* cy, void* workspace,
+                                         int64_t ws_bytes);
+rnn_status_t rnn_forward_inference_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          const int32_t* lengths, const void* x,
+                                          const void* h0, const void* c0, const void* W,
+                                          void* y, void* hy, void* cy);
+rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                      const int32_t* lengths, const void* W, const void* dy,
+                                      const void* dhy, const void* dcy, void* dx, void* dh0,
+                                      void* dc0, void* workspace, int64_t ws_bytes);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RNN_OK, RNN_ERR_TIMEOUT or RNN_ERR_DEVICE_CHECK). */
 rnn_status_t rnn_check_status(rnn_t h, void* stream);

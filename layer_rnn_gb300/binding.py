@@ -46,6 +46,12 @@ SIGNATURES = {
     "rnn_backward_data": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _i64]),
     "rnn_backward_weights": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "rnn_forward_training_varlen": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _i64]),
+    "rnn_forward_inference_varlen": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
+                                            _vp, _vp]),
+    "rnn_backward_data_varlen": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _vp, _i64]),
     "rnn_check_status": (_i32, [_vp, _vp]),
     "rnn_set_debug": (_i32, [_vp, _i32, _i32, _i64]),
     "rnn_enable_phase_timing": (_i32, [_vp, _i32]),
@@ -145,6 +151,22 @@ def rnn_backward_data(h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_byt
     _call("rnn_backward_data", h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes)
 
 
+def rnn_forward_training_varlen(h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy, ws,
+                                ws_bytes):
+    _call("rnn_forward_training_varlen", h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy, ws,
+          ws_bytes)
+
+
+def rnn_forward_inference_varlen(h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy):
+    _call("rnn_forward_inference_varlen", h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy)
+
+
+def rnn_backward_data_varlen(h, stream, T, N, lengths, W, dy, dhy, dcy, dx, dh0, dc0, ws,
+                             ws_bytes):
+    _call("rnn_backward_data_varlen", h, stream, T, N, lengths, W, dy, dhy, dcy, dx, dh0, dc0, ws,
+          ws_bytes)
+
+
 def rnn_backward_weights(h, stream, T, N, x, h0, y, ws, ws_bytes, dW):
     _call("rnn_backward_weights", h, stream, T, N, x, h0, y, ws, ws_bytes, dW)
 
@@ -239,6 +261,23 @@ class Rnn:
         T, N = dy.shape[0], dy.shape[1]
         rnn_backward_data(self.h, self._stream(stream), T, N, _p(W), _p(dy), _p(dhy), _p(dcy),
                           _p(dx), _p(dh0), _p(dc0), _p(ws), ws.numel())
+
+    # variable-length batches: lengths is a device int32 tensor [N]
+    def forward_training_varlen(self, lengths, x, h0, c0, W, y, hy, cy, ws, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_forward_training_varlen(self.h, self._stream(stream), T, N, _p(lengths), _p(x),
+                                    _p(h0), _p(c0), _p(W), _p(y), _p(hy), _p(cy), _p(ws),
+                                    ws.numel())
+
+    def forward_inference_varlen(self, lengths, x, h0, c0, W, y, hy, cy, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_forward_inference_varlen(self.h, self._stream(stream), T, N, _p(lengths), _p(x),
+                                     _p(h0), _p(c0), _p(W), _p(y), _p(hy), _p(cy))
+
+    def backward_data_varlen(self, lengths, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream=None):
+        T, N = dy.shape[0], dy.shape[1]
+        rnn_backward_data_varlen(self.h, self._stream(stream), T, N, _p(lengths), _p(W), _p(dy),
+                                 _p(dhy), _p(dcy), _p(dx), _p(dh0), _p(dc0), _p(ws), ws.numel())
 
     def backward_weights(self, x, h0, y, ws, dW, stream=None):
         T, N = x.shape[0], x.shape[1]

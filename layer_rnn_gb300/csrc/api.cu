@@ -382,8 +382,19 @@ struct PhaseScope {
 
 // Kernel choice for D directions in one launch (D = 1 also for one direction
 // of a bidirectional layer run on its own).
-rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl, int D) {
+rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl, int D,
+                      bool varlen = false) {
   const bool bf = h->dtype == RNN_BF16;
+  if (varlen) {
+    // per-sequence lengths: the staged CUDA-core kernels are the ones that
+    // read them
+    if (!rec_make_plan(backward, h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
+                       pl, false))
+      return RNN_ERR_UNSUPPORTED;
+    if (pl->P * D > h->num_sms) return RNN_ERR_NO_RESIDENCY;
+    if ((size_t)pl->P * D * 128 > kSyncBytes - 64) return RNN_ERR_UNSUPPORTED;
+    return RNN_OK;
+  }
   if (!backward && !(h->flags & RNN_FLAG_SIMT_RECURRENT) &&
       rec_tc_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
                   h->max_clusters, pl))
@@ -550,9 +561,13 @@ rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_
   return cuda_status(wf_launch(p, st));
 }
 
+// lengths: per-sequence valid lengths (device [N] int32) or null.  With
+// lengths, inference needs hseq_scratch: D * (T+1) * N * H elements for the
+// carried states.
 rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, const void* x,
                           const void* h0, const void* c0, const void* W, void* y, void* hy,
-                          void* cy, char* ws, bool training, Scratch sc) {
+                          void* cy, char* ws, bool training, Scratch sc,
+                          const int* lengths = nullptr, char* hseq_scratch = nullptr) {
   const int64_t e = esize(h), H = h->H, NH = N * H;
   WsLayout lay = ws_layout(h, T, N);
   float* gx;
@@ -567,11 +582,13 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     ybuf[1] = mp<char>(h->scratch, gx_bytes + yb);
   }
   bool wf_used = false;
-  rnn_status_t s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc,
-                                     &wf_used);
-  if (wf_used || s != RNN_OK) return s;
+  rnn_status_t s = RNN_OK;
+  if (!lengths) {
+    s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc, &wf_used);
+    if (wf_used || s != RNN_OK) return s;
+  }
   RecPlan plan;
-  s = plan_rec(h, false, N, &plan);
+  s = plan_rec(h, false, N, &plan, h->D, lengths != nullptr);
   if (s != RNN_OK) return s;
   const void* in = x;
   for (int l = 0; l < h->L; ++l) {
@@ -588,6 +605,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     fill_rec_common(h, T, N, &rp);
     rp.plan = plan;
     rp.ldy = h->D * H;
+    rp.lengths = lengths;
     for (int d = 0; d < h->D; ++d) {
       RecDirArgs& a = rp.dir[d];
       const int k = l * h->D + d;
@@ -603,6 +621,8 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
         a.hseq = mp<char>(ws, lay.at(RNN_WS_HSEQ, l, d).off);
         a.gates = mp<float>(ws, lay.at(RNN_WS_GATES, l, d).off);
         a.cseq = h->mode == RNN_LSTM ? mp<float>(ws, lay.at(RNN_WS_CSEQ, l, d).off) : nullptr;
+      } else if (lengths) {
+        a.hseq = hseq_scratch + (int64_t)d * (T + 1) * NH * e;
       }
     }
     {
@@ -707,9 +727,10 @@ rnn_status_t rnn_workspace_layout(rnn_t h, int64_t T, int64_t N, int region, int
   return RNN_OK;
 }
 
-rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
-                                  const void* h0, const void* c0, const void* W, void* y,
-                                  void* hy, void* cy, void* workspace, int64_t ws_bytes) {
+static rnn_status_t forward_training_impl(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          const int32_t* lengths, const void* x, const void* h0,
+                                          const void* c0, const void* W, void* y, void* hy,
+                                          void* cy, void* workspace, int64_t ws_bytes) {
   rnn_status_t s = check_sizes(h, T, N);
   if (s != RNN_OK) return s;
   if (!x || !W || !y || !workspace) return RNN_ERR_INVALID_ARG;
@@ -726,13 +747,32 @@ rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, c
     sc.base = static_cast<char*>(workspace) + R.off;
     sc.cap = R.bytes;
   }
-  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true, sc);
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true, sc,
+                   lengths);
   return finish(h, st, s);
 }
 
-rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
-                                   const void* h0, const void* c0, const void* W, void* y,
-                                   void* hy, void* cy) {
+rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
+                                  const void* h0, const void* c0, const void* W, void* y,
+                                  void* hy, void* cy, void* workspace, int64_t ws_bytes) {
+  return forward_training_impl(h, stream, T, N, nullptr, x, h0, c0, W, y, hy, cy, workspace,
+                               ws_bytes);
+}
+
+rnn_status_t rnn_forward_training_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                         const int32_t* lengths, const void* x, const void* h0,
+                                         const void* c0, const void* W, void* y, void* hy,
+                                         void* cy, void* workspace, int64_t ws_bytes) {
+  if (!lengths) return RNN_ERR_INVALID_ARG;
+  if (!aligned(lengths, 4)) return RNN_ERR_MISALIGNED;
+  return forward_training_impl(h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy, workspace,
+                               ws_bytes);
+}
+
+static rnn_status_t forward_inference_impl(rnn_t h, void* stream, int64_t T, int64_t N,
+                                           const int32_t* lengths, const void* x,
+                                           const void* h0, const void* c0, const void* W,
+                                           void* y, void* hy, void* cy) {
   rnn_status_t s = check_sizes(h, T, N);
   if (s != RNN_OK) return s;
   if (!x || !W || !y) return RNN_ERR_INVALID_ARG;
@@ -742,8 +782,11 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, 
   s = device_setup(h);
   if (s != RNN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t base_bytes = align256(h->D * T * N * h->G * h->H * 4) +
-                             2 * align256(T * N * h->D * h->H * esize(h));
+  const int64_t hseq_off = align256(h->D * T * N * h->G * h->H * 4) +
+                           2 * align256(T * N * h->D * h->H * esize(h));
+  // with lengths: the carried states of every step, D x (T+1) x N x H
+  const int64_t base_bytes =
+      hseq_off + (lengths ? align256(h->D * (T + 1) * N * h->H * esize(h)) : 0);
   const size_t need = (size_t)(base_bytes + gemm_scratch_bytes(h, T, N, false));
   if (need > h->scratch_bytes) {
     // the old scratch may still be in use by earlier work on the stream
@@ -762,13 +805,30 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, 
   Scratch sc;
   sc.base = static_cast<char*>(h->scratch) + base_bytes;
   sc.cap = (int64_t)h->scratch_bytes - base_bytes;
-  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false, sc);
+  s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, nullptr, false, sc, lengths,
+                   static_cast<char*>(h->scratch) + hseq_off);
   return finish(h, st, s);
 }
 
-rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, const void* W,
-                               const void* dy, const void* dhy, const void* dcy, void* dx,
-                               void* dh0, void* dc0, void* workspace, int64_t ws_bytes) {
+rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
+                                   const void* h0, const void* c0, const void* W, void* y,
+                                   void* hy, void* cy) {
+  return forward_inference_impl(h, stream, T, N, nullptr, x, h0, c0, W, y, hy, cy);
+}
+
+rnn_status_t rnn_forward_inference_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          const int32_t* lengths, const void* x, const void* h0,
+                                          const void* c0, const void* W, void* y, void* hy,
+                                          void* cy) {
+  if (!lengths) return RNN_ERR_INVALID_ARG;
+  if (!aligned(lengths, 4)) return RNN_ERR_MISALIGNED;
+  return forward_inference_impl(h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy);
+}
+
+static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t N,
+                                       const int32_t* lengths, const void* W, const void* dy,
+                                       const void* dhy, const void* dcy, void* dx, void* dh0,
+                                       void* dc0, void* workspace, int64_t ws_bytes) {
   rnn_status_t s = check_sizes(h, T, N);
   if (s != RNN_OK) return s;
   if (!W || !dy || !dx || !workspace) return RNN_ERR_INVALID_ARG;
@@ -784,8 +844,9 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
   const int64_t e = esize(h), H = h->H, NH = N * H, GH = h->G * H;
   const bool bf = h->dtype == RNN_BF16;
   RecPlan plan, plan_one;
-  s = plan_rec(h, true, N, &plan);
-  const bool in_turn = s == RNN_OK && bwd_directions_in_turn(h, N, plan, &plan_one);
+  s = plan_rec(h, true, N, &plan, h->D, lengths != nullptr);
+  const bool in_turn =
+      s == RNN_OK && !lengths && bwd_directions_in_turn(h, N, plan, &plan_one);
   if (s != RNN_OK) return finish(h, st, s);
   Scratch sc;
   sc.base = ws + lay.at(RNN_WS_GEMM, 0, 0).off;
@@ -798,6 +859,7 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     rp.plan = plan;
     rp.ldy = h->D * H;
     rp.lddy = h->D * H;
+    rp.lengths = lengths;
     for (int d = 0; d < h->D; ++d) {
       RecDirArgs& a = rp.dir[d];
       const int k = l * h->D + d;
@@ -870,6 +932,23 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
     dcur_bf16 = target_bf16;
   }
   return finish(h, st, RNN_OK);
+}
+
+rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, const void* W,
+                               const void* dy, const void* dhy, const void* dcy, void* dx,
+                               void* dh0, void* dc0, void* workspace, int64_t ws_bytes) {
+  return backward_data_impl(h, stream, T, N, nullptr, W, dy, dhy, dcy, dx, dh0, dc0, workspace,
+                            ws_bytes);
+}
+
+rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
+                                      const int32_t* lengths, const void* W, const void* dy,
+                                      const void* dhy, const void* dcy, void* dx, void* dh0,
+                                      void* dc0, void* workspace, int64_t ws_bytes) {
+  if (!lengths) return RNN_ERR_INVALID_ARG;
+  if (!aligned(lengths, 4)) return RNN_ERR_MISALIGNED;
+  return backward_data_impl(h, stream, T, N, lengths, W, dy, dhy, dcy, dx, dh0, dc0, workspace,
+                            ws_bytes);
 }
 
 rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,

@@ -139,13 +139,19 @@ struct RecParams {
   int* status = nullptr;
   long long timeout_ns = 0;
   int fault_block = -1, fault_step = -1;
+  // valid length of each sequence ([N] int32, device), or null: every sequence
+  // runs all T steps.  A step t >= lengths[n] keeps sequence n's state and
+  // outputs zero (values outside 0..T act as 0 or T).  Only the staged
+  // CUDA-core kernels (rec_make_plan with allow_direct = false) read it.
+  const int* lengths = nullptr;
   RecDirArgs dir[2];
 };
 
 // Choose the tiling for the forward (backward = false) or backward kernel.
 // Returns false when no supported tiling fits in shared memory.
+// allow_direct = false: the staged kernel only (the one that reads lengths).
 bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
-                   size_t smem_limit, RecPlan* out);
+                   size_t smem_limit, RecPlan* out, bool allow_direct = true);
 
 // Cluster path: plan (false if the problem does not qualify) and launch.
 // max_clusters[c] = co-resident clusters of c blocks (c = 1, 2, 4, 8; 0 = unknown).

@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
   T* y = reinterpret_cast<T*>(a.y);
   T* hseq = reinterpret_cast<T*>(a.hseq);
   const int64_t GH = (int64_t)G * H;
+  const int* lens = p.lengths;  // variable lengths: the host also passes hseq
 
   for (int s = 0; s < nT; ++s) {
     const int t = d ? nT - 1 - s : s;
@@ -251,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
     int64_t lds;
     if (s == 0) {
       src = reinterpret_cast<const T*>(a.h0);
+      lds = H;
+    } else if (lens) {
+      // y is zero past a sequence's length; the state it carries is in hseq
+      // (slot of the state after time tp)
+      src = hseq + (int64_t)(d ? t + 1 : t) * N * H;
       lds = H;
     } else {
       src = y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
@@ -266,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
         const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
         const int64_t row = (int64_t)t * N + n;
         const float* gxr = a.gx + row * GH + j;
+        // past the sequence's length the step keeps the state and outputs zero
+        const bool act = !lens || t < __ldg(lens + n);
         float h;
         if (p.mode == 1) {  // LSTM, gate blocks i, f, g, o
           const float ig = sigmoidf_(__ldg(gxr) + outs[(0 * U + u) * pl.nbp + nn]);
@@ -274,12 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
           const float og = sigmoidf_(__ldg(gxr + 3 * H) + outs[(3 * U + u) * pl.nbp + nn]);
           const float c = fg * cst[u * N + n] + ig * gg;
           h = og * tanhf(c);
-          cst[u * N + n] = c;
+          if (act) cst[u * N + n] = c;
           if (a.gates) {
             float* gp = a.gates + row * 4 * H + j;
             gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
           }
-          if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
+          if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = cst[u * N + n];
         } else if (p.mode == 2) {  // GRU, gate blocks r, z, n
           const float ghn = outs[(2 * U + u) * pl.nbp + nn] + to_f(bhh[2 * H + j]);
           const float r = sigmoidf_(__ldg(gxr) + outs[(0 * U + u) * pl.nbp + nn]);
@@ -294,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
           h = tanhf(__ldg(gxr) + outs[u * pl.nbp + nn]);
           if (a.gates) a.gates[row * H + j] = h;
         }
+        if (!act) h = hown[u * N + n];
         hown[u * N + n] = h;
-        y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
+        y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(act ? h : 0.f);
         if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
       }
       __syncthreads();
@@ -359,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
   T* dgx = reinterpret_cast<T*>(a.dgx);
   T* dgh = reinterpret_cast<T*>(a.dgh);
   const T* hseq = reinterpret_cast<const T*>(a.hseq);
+  const int* lens = p.lengths;
 
   for (int s = 0; s <= nT; ++s) {
     const int t = d ? s : nT - 1 - s;        // time processed at this step (s < T)
@@ -388,8 +398,19 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
           continue;
         }
         const int64_t row = (int64_t)t * N + n;
-        const float dh = load_any(a.dy, row * p.lddy + (int64_t)d * H + j, a.dy_bf16) + dhf;
         T* gxo = dgx + row * GH + j;
+        if (lens && t >= __ldg(lens + n)) {
+          // the forward kept the state at this step: no gate gradients, and
+          // the state gradients (dh here, dc in dcs) pass straight through
+          for (int g = 0; g < G; ++g) gxo[(int64_t)g * H] = from_f<T>(0.f);
+          if (p.mode == 2) {
+            T* gho = dgh + row * GH + j;
+            for (int g = 0; g < G; ++g) gho[(int64_t)g * H] = from_f<T>(0.f);
+          }
+          carry[u * N + n] = dhf;
+          continue;
+        }
+        const float dh = load_any(a.dy, row * p.lddy + (int64_t)d * H + j, a.dy_bf16) + dhf;
         if (p.mode == 1) {  // LSTM
           const float* gp = a.gates + row * 4 * H + j;
           const float ig = gp[0], fg = gp[H], gg = gp[2 * H], og = gp[3 * H];
@@ -404,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
           gxo[2 * H] = from_f<T>(dc * ig * (1.f - gg * gg));
           gxo[3 * H] = from_f<T>(dout * og * (1.f - og));
           dcs[u * N + n] = dc * fg;
+          if (lens) carry[u * N + n] = 0.f;
         } else if (p.mode == 2) {  // GRU
           const float* gp = a.gates + row * 4 * H + j;
           const float r = gp[0], z = gp[H], nv = gp[2 * H], ghn = gp[3 * H];
@@ -423,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
         } else {  // tanh RNN
           const float hv = a.gates[row * H + j];
           gxo[0] = from_f<T>(dh * (1.f - hv * hv));
+          if (lens) carry[u * N + n] = 0.f;
         }
       }
       __syncthreads();
@@ -1016,7 +1039,7 @@ extern "C" int rnn_debug_trace_copy(void* host, size_t bytes) {
 #endif
 
 bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int num_sms,
-                   size_t smem_limit, RecPlan* out) {
+                   size_t smem_limit, RecPlan* out, bool allow_direct) {
   const int G = mode == 1 ? 4 : mode == 2 ? 3 : 1;
   const int e = bf16 ? 2 : 4;
   const int VK = 16 / e;
@@ -1026,7 +1049,7 @@ bool rec_make_plan(bool backward, int mode, int bf16, int D, int H, int N, int n
   if (P > H) P = H;
   const int U = (H + P - 1) / P;
   P = (H + U - 1) / U;
-  if (make_direct_plan(backward, G, e, D, H, N, P, U, smem_limit, out)) return true;
+  if (allow_direct && make_direct_plan(backward, G, e, D, H, N, P, U, smem_limit, out)) return true;
   const int Mloc = backward ? U : G * U;
   const int K = backward ? G * H : H;
   bool found = false;

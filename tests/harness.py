@@ -80,9 +80,10 @@ def empty(shape, dtype, device="cuda"):
     return torch.empty(shape, dtype=td, device=device)
 
 
-def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None):
+def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths=None):
     """Training forward + backward_data + backward_weights (+ inference forward)
-    through the C ABI.  Returns float64 numpy arrays."""
+    through the C ABI.  Returns float64 numpy arrays.  lengths: per-sequence
+    valid lengths [N] (the *_varlen calls), or None."""
     import torch
     from layer_rnn_gb300 import binding as B
     T, N, I, H, L = cfg["T"], cfg["N"], cfg["I"], cfg["H"], cfg["L"]
@@ -106,7 +107,12 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None):
         if poison:
             ws.fill_(0xFF)  # NaN bit patterns: anything read before written shows
             y.fill_(float("nan"))
-        r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
+        lens = None
+        if lengths is not None:
+            lens = torch.tensor(np.asarray(lengths), dtype=torch.int32, device="cuda")
+            r.forward_training_varlen(lens, x, h0, c0, W, y, hy, cy, ws, stream)
+        else:
+            r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
         dx = empty((T, N, I), dt)
         dh0 = empty((L * D, N, H), dt)
         dc0 = empty((L * D, N, H), "f32") if lstm else None
@@ -114,7 +120,10 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None):
         if poison:
             dW.fill_(float("nan"))
             dx.fill_(float("nan"))
-        r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+        if lens is not None:
+            r.backward_data_varlen(lens, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+        else:
+            r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
         r.backward_weights(x, h0, y, ws, dW, stream)
         out = dict(y=from_dev(y), hy=from_dev(hy), cy=from_dev(cy), dx=from_dev(dx),
                    dh0=from_dev(dh0), dc0=from_dev(dc0), dW=from_dev(dW))
@@ -122,7 +131,10 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None):
             yi = empty((T, N, D * H), dt)
             hyi = empty((L * D, N, H), dt)
             cyi = empty((L * D, N, H), "f32") if lstm else None
-            r.forward_inference(x, h0, c0, W, yi, hyi, cyi, stream)
+            if lens is not None:
+                r.forward_inference_varlen(lens, x, h0, c0, W, yi, hyi, cyi, stream)
+            else:
+                r.forward_inference(x, h0, c0, W, yi, hyi, cyi, stream)
             out["y_inf"] = from_dev(yi)
             out["hy_inf"] = from_dev(hyi)
             out["cy_inf"] = from_dev(cyi)
@@ -132,10 +144,11 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None):
         r.close()
 
 
-def run_oracle(cfg, inp):
+def run_oracle(cfg, inp, lengths=None):
     import oracle
     return oracle.run_flat(cfg["mode"], cfg["L"], cfg["bidir"], cfg["I"], cfg["H"], inp["x"],
-                           inp["h0"], inp["c0"], inp["w"], inp["dy"], inp["dhy"], inp["dcy"])
+                           inp["h0"], inp["c0"], inp["w"], inp["dy"], inp["dhy"], inp["dcy"],
+                           lengths=lengths)
 
 
 def weight_tensors(cfg, flat):

@@ -148,3 +148,34 @@ def test_compute_calls_reject_bad_arguments_before_any_launch(B):
                                          None) == 1
     finally:
         B.rnn_destroy(h)
+
+
+def test_varlen_calls_reject_bad_arguments_before_any_launch(B):
+    # a NULL or misaligned lengths buffer, then the checks of the calls without
+    # lengths, all on the host
+    lib = B.lib()
+    h = B.rnn_create(B.RNN_GRU, 1, True, 4, 8, 0)
+    try:
+        ws = B.rnn_workspace_size(h, 5, 2)
+        assert lib.rnn_forward_training_varlen(h, None, 5, 2, None, 256, None, None, 256, 256,
+                                               None, None, 256, ws) == 1
+        assert lib.rnn_forward_inference_varlen(h, None, 5, 2, None, 256, None, None, 256, 256,
+                                                None, None) == 1
+        assert lib.rnn_backward_data_varlen(h, None, 5, 2, None, 256, 256, None, None, 256, None,
+                                            None, 256, ws) == 1
+        assert lib.rnn_forward_training_varlen(h, None, 5, 2, 258, 256, None, None, 256, 256,
+                                               None, None, 256, ws) == 4
+        assert lib.rnn_forward_inference_varlen(h, None, 5, 2, 258, 256, None, None, 256, 256,
+                                                None, None) == 4
+        assert lib.rnn_backward_data_varlen(h, None, 5, 2, 258, 256, 256, None, None, 256, None,
+                                            None, 256, ws) == 4
+        assert lib.rnn_forward_training_varlen(h, None, 5, 2, 512, None, None, None, 256, 256,
+                                               None, None, 256, ws) == 1
+        assert lib.rnn_forward_training_varlen(h, None, 5, 2, 512, 256, None, None, 256, 256,
+                                               None, None, 256, ws - 1) == 3
+        assert lib.rnn_backward_data_varlen(h, None, 5, 2, 512, 256, 256, None, None, 256, None,
+                                            None, 256, ws - 1) == 3
+        assert lib.rnn_forward_inference_varlen(h, None, 0, 2, 512, 256, None, None, 256, 256,
+                                                None, None) == 1
+    finally:
+        B.rnn_destroy(h)
