@@ -39,6 +39,13 @@ What it computes (sources, by page title and section):
   A step t >= len_n of sequence n leaves its state unchanged and writes zero
   output, so hy is the state after the last valid step, and the reverse
   direction starts from h0 at step len_n - 1.
+* Inter-layer dropout (optional ``dropout`` and ``masks``).  "rnn training
+  example?" (oneDNN issue #218) asks for dropout as cuDNN has it, without
+  spelling it out.  Reading taken: cuDNN's / PyTorch's training dropout
+  between layers.  The output of every layer but the last is multiplied by a
+  0/1 mask and by 1 / (1 - dropout) before it becomes the next layer's input;
+  y, hy and cy are not dropped.  The masks are the method's random draws and
+  are passed in.
 * Backward ("reuse forward intermediate results during backward", MXNet design
   page, Operator Registration): reverse-mode differentiation of the scalar loss
       loss = sum(y * dy) + sum(hy * dhy) + sum(cy * dcy)
@@ -254,7 +261,8 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
 # whole stack
 # ----------------------------------------------------------------------------
 
-def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
+def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None, dropout=0.0,
+            masks=None):
     """Training forward of the stack.
 
     x: [T, N, I]; h0, c0: [L*D, N, H] (c0 ignored unless LSTM; None = zeros);
@@ -263,6 +271,8 @@ def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
     sequence, [N] integers in 0..T, for padded variable-length batches (the
     PyTorch packed-sequence semantics: y is zero past a sequence's length, hy
     is the state after its last valid step in each direction).
+    dropout, masks: inter-layer dropout probability in [0, 1) and the L-1
+    masks [T, N, D*H] (0/1) drawn for it; masks None means no dropout.
     Returns (y [T, N, D*H], hy [L*D, N, H], cy [L*D, N, H] or None, cache).
     """
     x = np.asarray(x, dtype=np.float64)
@@ -273,6 +283,11 @@ def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
         lengths = np.asarray(lengths)
         if lengths.shape != (N,) or lengths.min(initial=0) < 0 or lengths.max(initial=0) > T:
             raise ValueError("lengths must be [N] integers in 0..T")
+    if masks is not None:
+        masks = [np.asarray(m, dtype=np.float64) for m in masks]
+        if not 0.0 <= dropout < 1.0 or len(masks) != num_layers - 1 or any(
+                m.shape != (T, N, D * H) or not np.isin(m, (0.0, 1.0)).all() for m in masks):
+            raise ValueError("masks must be L-1 arrays [T, N, D*H] of 0/1, dropout in [0, 1)")
     if h0 is None:
         h0 = np.zeros((num_layers * D, N, H))
     if c0 is None:
@@ -282,7 +297,8 @@ def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
     hy = np.zeros((num_layers * D, N, H))
     cy = np.zeros((num_layers * D, N, H)) if mode == "lstm" else None
     layer_in = x
-    cache = dict(mode=mode, L=num_layers, D=D, inputs=[], tapes=[])
+    cache = dict(mode=mode, L=num_layers, D=D, inputs=[], tapes=[], masks=masks,
+                 keep=1.0 / (1.0 - dropout))
     for l in range(num_layers):
         outs = []
         cache["inputs"].append(layer_in)
@@ -297,6 +313,8 @@ def forward(mode, x, h0, c0, params, num_layers, bidirectional, lengths=None):
                 cy[k] = cT
             cache["tapes"].append(tape)
         layer_in = np.concatenate(outs, axis=2)
+        if masks is not None and l < num_layers - 1:
+            layer_in = layer_in * masks[l] * cache["keep"]
     return layer_in, hy, cy, cache
 
 
@@ -334,6 +352,8 @@ def backward(params, cache, dy, dhy=None, dcy=None):
                 dc0[k] = dc_first
             dparams[k] = g
         d_out = d_in
+        if cache.get("masks") is not None and l > 0:
+            d_out = d_out * cache["masks"][l - 1] * cache["keep"]
     return d_out, dh0, dc0, dparams
 
 
@@ -348,16 +368,16 @@ def loss(y, hy, cy, dy, dhy=None, dcy=None):
 
 
 def run_flat(mode, num_layers, bidirectional, input_size, hidden_size,
-             x, h0, c0, w_flat, dy, dhy, dcy, lengths=None):
+             x, h0, c0, w_flat, dy, dhy, dcy, lengths=None, dropout=0.0, masks=None):
     """Forward + backward on the canonical flat weight buffer.
 
     Returns a dict of float64 arrays: y, hy, cy, dx, dh0, dc0, dW (flat).
-    ``lengths``: as for ``forward``.
+    ``lengths``, ``dropout``, ``masks``: as for ``forward``.
     """
     params = unflatten_weights(w_flat, mode, num_layers, bidirectional,
                                input_size, hidden_size)
     y, hy, cy, cache = forward(mode, x, h0, c0, params, num_layers, bidirectional,
-                               lengths)
+                               lengths, dropout, masks)
     dx, dh0, dc0, dparams = backward(params, cache, dy, dhy,
                                      dcy if mode == "lstm" else None)
     dW = flatten_weights(dparams, mode, num_layers, bidirectional,
