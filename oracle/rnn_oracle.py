@@ -17,6 +17,12 @@ What it computes (sources, by page title and section):
       h' = (1 - z) * n + z * h
   The same comment states that the cuDNN equations are the same recurrence
   (its "bRu" bias is read as the update gate's recurrent bias).
+* GRU, TensorFlow flavour (mode "gru_tf"; not the path's GRU, the groundwork
+  for a flag that selects it).  The same comment of "rnn training example?"
+  writes the TensorFlow equations, where the reset gate scales h before the
+  recurrent matmul of the candidate:
+      n  = tanh(W_in x + b_in + W_hn (r * h) + b_hn)
+  with r, z and h' as above.  Same weight layout as "gru".
 * LSTM -- the pages name LSTM (MXNet "Fused RNN operator for CPU" design page,
   section Performance / LSTM; Keras issue #3692 "CudnnLSTM") but never write its
   equations.  Reading taken: the standard LSTM with two biases (the two-bias
@@ -60,8 +66,8 @@ I_l = input_size for layer 0 and D*H above it.
 
 import numpy as np
 
-MODES = ("rnn_tanh", "lstm", "gru")
-GATES = {"rnn_tanh": 1, "lstm": 4, "gru": 3}
+MODES = ("rnn_tanh", "lstm", "gru", "gru_tf")
+GATES = {"rnn_tanh": 1, "lstm": 4, "gru": 3, "gru_tf": 3}
 
 
 def sigmoid(a):
@@ -177,6 +183,15 @@ def _direction_forward(mode, x, h0, c0, p, reverse, lengths=None):
             n = np.tanh(i_n + r * h_n)
             h = (1.0 - z) * n + z * h_prev
             tape.append(dict(t=t, h_prev=h_prev, r=r, z=z, n=n, h_n=h_n))
+        elif mode == "gru_tf":
+            H = W_hh.shape[1]
+            i_r, i_z, i_n = np.split(x[t] @ W_ih.T + b_ih, 3, axis=1)
+            r = sigmoid(i_r + h_prev @ W_hh[:H].T + b_hh[:H])
+            z = sigmoid(i_z + h_prev @ W_hh[H:2 * H].T + b_hh[H:2 * H])
+            rh = r * h_prev                    # the reset gate acts before the matmul
+            n = np.tanh(i_n + rh @ W_hh[2 * H:].T + b_hh[2 * H:])
+            h = (1.0 - z) * n + z * h_prev
+            tape.append(dict(t=t, h_prev=h_prev, r=r, z=z, n=n, rh=rh))
         else:
             raise ValueError("unknown mode %r" % mode)
         if valid is None:
@@ -234,7 +249,7 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
             dc_next = dc * f
             dgx = dgh = da
             dh_next = da @ W_hh
-        else:  # gru
+        elif mode == "gru":
             r, z, n, h_n = rec["r"], rec["z"], rec["n"], rec["h_n"]
             dn = dh * (1.0 - z)
             dz = dh * (h_prev - n)
@@ -245,13 +260,33 @@ def _direction_backward(mode, x, p, tape, dout, dh_last, dc_last):
             dgx = np.concatenate([da_r, da_z, da_n], axis=1)
             dgh = np.concatenate([da_r, da_z, da_n * r], axis=1)
             dh_next = dh * z + dgh @ W_hh
+        elif mode == "gru_tf":
+            H = W_hh.shape[1]
+            r, z, n, rh = rec["r"], rec["z"], rec["n"], rec["rh"]
+            dn = dh * (1.0 - z)
+            dz = dh * (h_prev - n)
+            da_n = dn * (1.0 - n ** 2)
+            d_rh = da_n @ W_hh[2 * H:]         # gradient of the loss w.r.t. r * h
+            da_r = d_rh * h_prev * r * (1.0 - r)
+            da_z = dz * z * (1.0 - z)
+            dgx = dgh = np.concatenate([da_r, da_z, da_n], axis=1)
+            dh_next = dh * z + da_r @ W_hh[:H] + da_z @ W_hh[H:2 * H] + d_rh * r
+            # the candidate's recurrent weights multiply r * h, not h
+            whh_in = np.concatenate([np.repeat(h_prev[None], 2, 0), rh[None]], 0)
+        else:
+            raise ValueError("unknown mode %r" % mode)
         if m is not None:
             dh_next = dh_next + carry_h
             if mode == "lstm":
                 dc_next = dc_next + carry_c
         dx[t] = dgx @ W_ih
         grads["W_ih"] += dgx.T @ x[t]
-        grads["W_hh"] += dgh.T @ h_prev
+        if mode == "gru_tf":
+            for g in range(3):
+                blk = slice(g * H, (g + 1) * H)
+                grads["W_hh"][blk] += dgh[:, blk].T @ whh_in[g]
+        else:
+            grads["W_hh"] += dgh.T @ h_prev
         grads["b_ih"] += dgx.sum(axis=0)
         grads["b_hh"] += dgh.sum(axis=0)
     return dx, dh_next, dc_next, grads
