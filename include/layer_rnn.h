@@ -242,6 +242,30 @@ rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t 
                                       const void* dhy, const void* dcy, void* dx, void* dh0,
                                       void* dc0, void* workspace, int64_t ws_bytes);
 
+/* Inter-layer dropout in training, as cuDNN has it (the ask of "rnn training
+ * example?", oneDNN issue #218).  The same calls with the dropout
+ * probability p in [0, 1) and masks: device memory, (L-1) x [T, N, D*H]
+ * bytes, each 0 (dropped) or 1, one block per layer boundary (the caller
+ * draws them).  The output of layer l < L-1 becomes layer l+1's input
+ * multiplied by mask_l / (1 - p); y, hy and cy are not dropped.
+ * rnn_backward_data_dropout must get the same p and masks.
+ * rnn_backward_weights needs neither, because the workspace keeps the dropped
+ * inputs.  Inference does not drop.  For L = 1, masks may be NULL.  These
+ * calls take the layer-by-layer path: no wavefront.  The masks buffer is read
+ * by the enqueued kernels: keep it unchanged until they have run.
+ * Errors: as the calls without dropout, and RNN_ERR_INVALID_ARG for p outside
+ * [0, 1) or NULL masks with L > 1. */
+rnn_status_t rnn_forward_training_dropout(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          float dropout, const uint8_t* masks, const void* x,
+                                          const void* h0, const void* c0, const void* W,
+                                          void* y, void* hy, void* cy, void* workspace,
+                                          int64_t ws_bytes);
+rnn_status_t rnn_backward_data_dropout(rnn_t h, void* stream, int64_t T, int64_t N,
+                                       float dropout, const uint8_t* masks, const void* W,
+                                       const void* dy, const void* dhy, const void* dcy,
+                                       void* dx, void* dh0, void* dc0, void* workspace,
+                                       int64_t ws_bytes);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RNN_OK, RNN_ERR_TIMEOUT or RNN_ERR_DEVICE_CHECK). */
 rnn_status_t rnn_check_status(rnn_t h, void* stream);

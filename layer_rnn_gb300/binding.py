@@ -46,6 +46,10 @@ SIGNATURES = {
     "rnn_backward_data": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _i64]),
     "rnn_backward_weights": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "rnn_forward_training_dropout": (_i32, [_vp, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp,
+                                            _vp, _vp, _vp, _vp, _vp, _vp, _i64]),
+    "rnn_backward_data_dropout": (_i32, [_vp, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _vp, _vp, _vp, _i64]),
     "rnn_forward_training_varlen": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _i64]),
     "rnn_forward_inference_varlen": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -149,6 +153,18 @@ def rnn_forward_inference_static(h, stream, T, N, x, h0, c0, W, y, hy, cy):
 
 def rnn_backward_data(h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes):
     _call("rnn_backward_data", h, stream, T, N, W, dy, dhy, dcy, dx, dh0, dc0, ws, ws_bytes)
+
+
+def rnn_forward_training_dropout(h, stream, T, N, p, masks, x, h0, c0, W, y, hy, cy, ws,
+                                 ws_bytes):
+    _call("rnn_forward_training_dropout", h, stream, T, N, p, masks, x, h0, c0, W, y, hy, cy, ws,
+          ws_bytes)
+
+
+def rnn_backward_data_dropout(h, stream, T, N, p, masks, W, dy, dhy, dcy, dx, dh0, dc0, ws,
+                              ws_bytes):
+    _call("rnn_backward_data_dropout", h, stream, T, N, p, masks, W, dy, dhy, dcy, dx, dh0, dc0,
+          ws, ws_bytes)
 
 
 def rnn_forward_training_varlen(h, stream, T, N, lengths, x, h0, c0, W, y, hy, cy, ws,
@@ -261,6 +277,19 @@ class Rnn:
         T, N = dy.shape[0], dy.shape[1]
         rnn_backward_data(self.h, self._stream(stream), T, N, _p(W), _p(dy), _p(dhy), _p(dcy),
                           _p(dx), _p(dh0), _p(dc0), _p(ws), ws.numel())
+
+    # inter-layer dropout: masks is a device uint8 tensor [L-1, T, N, D*H] of 0/1
+    def forward_training_dropout(self, p, masks, x, h0, c0, W, y, hy, cy, ws, stream=None):
+        T, N = x.shape[0], x.shape[1]
+        rnn_forward_training_dropout(self.h, self._stream(stream), T, N, p, _p(masks), _p(x),
+                                     _p(h0), _p(c0), _p(W), _p(y), _p(hy), _p(cy), _p(ws),
+                                     ws.numel())
+
+    def backward_data_dropout(self, p, masks, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream=None):
+        T, N = dy.shape[0], dy.shape[1]
+        rnn_backward_data_dropout(self.h, self._stream(stream), T, N, p, _p(masks), _p(W),
+                                  _p(dy), _p(dhy), _p(dcy), _p(dx), _p(dh0), _p(dc0), _p(ws),
+                                  ws.numel())
 
     # variable-length batches: lengths is a device int32 tensor [N]
     def forward_training_varlen(self, lengths, x, h0, c0, W, y, hy, cy, ws, stream=None):

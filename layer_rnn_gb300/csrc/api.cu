@@ -567,7 +567,8 @@ rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_
 rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, const void* x,
                           const void* h0, const void* c0, const void* W, void* y, void* hy,
                           void* cy, char* ws, bool training, Scratch sc,
-                          const int* lengths = nullptr, char* hseq_scratch = nullptr) {
+                          const int* lengths = nullptr, char* hseq_scratch = nullptr,
+                          const uint8_t* drop_masks = nullptr, float drop_p = 0.f) {
   const int64_t e = esize(h), H = h->H, NH = N * H;
   WsLayout lay = ws_layout(h, T, N);
   float* gx;
@@ -583,7 +584,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
   }
   bool wf_used = false;
   rnn_status_t s = RNN_OK;
-  if (!lengths) {
+  if (!lengths && !drop_masks) {  // the wavefront chains the layers inside one launch
     s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc, &wf_used);
     if (wf_used || s != RNN_OK) return s;
   }
@@ -630,6 +631,14 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
       s = cuda_status(rp.plan.tc        ? rec_tc_launch(rp, st)
                       : rp.plan.cluster ? rec_cluster_launch(false, rp, st)
                                         : rec_forward(rp, st));
+      if (s != RNN_OK) return s;
+    }
+    if (drop_masks && l < h->L - 1) {
+      // the next layer reads this layer's output dropped (in place: the
+      // recurrent kernels keep their own copy of the states)
+      const int64_t n = T * N * h->D * H;
+      s = cuda_status(dropout_apply(out, h->dtype == RNN_BF16, drop_masks + (int64_t)l * n, n,
+                                    1.f / (1.f - drop_p), h->num_sms, st));
       if (s != RNN_OK) return s;
     }
     in = out;
@@ -730,7 +739,9 @@ rnn_status_t rnn_workspace_layout(rnn_t h, int64_t T, int64_t N, int region, int
 static rnn_status_t forward_training_impl(rnn_t h, void* stream, int64_t T, int64_t N,
                                           const int32_t* lengths, const void* x, const void* h0,
                                           const void* c0, const void* W, void* y, void* hy,
-                                          void* cy, void* workspace, int64_t ws_bytes) {
+                                          void* cy, void* workspace, int64_t ws_bytes,
+                                          const uint8_t* drop_masks = nullptr,
+                                          float drop_p = 0.f) {
   rnn_status_t s = check_sizes(h, T, N);
   if (s != RNN_OK) return s;
   if (!x || !W || !y || !workspace) return RNN_ERR_INVALID_ARG;
@@ -748,7 +759,7 @@ static rnn_status_t forward_training_impl(rnn_t h, void* stream, int64_t T, int6
     sc.cap = R.bytes;
   }
   s = forward_impl(h, st, T, N, x, h0, c0, W, y, hy, cy, static_cast<char*>(workspace), true, sc,
-                   lengths);
+                   lengths, nullptr, drop_masks, drop_p);
   return finish(h, st, s);
 }
 
@@ -757,6 +768,17 @@ rnn_status_t rnn_forward_training(rnn_t h, void* stream, int64_t T, int64_t N, c
                                   void* hy, void* cy, void* workspace, int64_t ws_bytes) {
   return forward_training_impl(h, stream, T, N, nullptr, x, h0, c0, W, y, hy, cy, workspace,
                                ws_bytes);
+}
+
+rnn_status_t rnn_forward_training_dropout(rnn_t h, void* stream, int64_t T, int64_t N,
+                                          float dropout, const uint8_t* masks, const void* x,
+                                          const void* h0, const void* c0, const void* W, void* y,
+                                          void* hy, void* cy, void* workspace,
+                                          int64_t ws_bytes) {
+  if (!h || !(dropout >= 0.f && dropout < 1.f) || (h->L > 1 && !masks))
+    return RNN_ERR_INVALID_ARG;
+  return forward_training_impl(h, stream, T, N, nullptr, x, h0, c0, W, y, hy, cy, workspace,
+                               ws_bytes, h->L > 1 ? masks : nullptr, dropout);
 }
 
 rnn_status_t rnn_forward_training_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
@@ -828,7 +850,9 @@ rnn_status_t rnn_forward_inference_varlen(rnn_t h, void* stream, int64_t T, int6
 static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t N,
                                        const int32_t* lengths, const void* W, const void* dy,
                                        const void* dhy, const void* dcy, void* dx, void* dh0,
-                                       void* dc0, void* workspace, int64_t ws_bytes) {
+                                       void* dc0, void* workspace, int64_t ws_bytes,
+                                       const uint8_t* drop_masks = nullptr,
+                                       float drop_p = 0.f) {
   rnn_status_t s = check_sizes(h, T, N);
   if (s != RNN_OK) return s;
   if (!W || !dy || !dx || !workspace) return RNN_ERR_INVALID_ARG;
@@ -928,6 +952,13 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
       s = run_gemm(h, g, sc, st);
       if (s != RNN_OK) return s;
     }
+    if (drop_masks && l > 0) {
+      // the layer below's output reached this layer dropped
+      const int64_t n = T * N * h->D * H;
+      s = cuda_status(dropout_apply(target, 0, drop_masks + (int64_t)(l - 1) * n, n,
+                                    1.f / (1.f - drop_p), h->num_sms, st));
+      if (s != RNN_OK) return finish(h, st, s);
+    }
     dcur = target;
     dcur_bf16 = target_bf16;
   }
@@ -939,6 +970,17 @@ rnn_status_t rnn_backward_data(rnn_t h, void* stream, int64_t T, int64_t N, cons
                                void* dh0, void* dc0, void* workspace, int64_t ws_bytes) {
   return backward_data_impl(h, stream, T, N, nullptr, W, dy, dhy, dcy, dx, dh0, dc0, workspace,
                             ws_bytes);
+}
+
+rnn_status_t rnn_backward_data_dropout(rnn_t h, void* stream, int64_t T, int64_t N,
+                                       float dropout, const uint8_t* masks, const void* W,
+                                       const void* dy, const void* dhy, const void* dcy,
+                                       void* dx, void* dh0, void* dc0, void* workspace,
+                                       int64_t ws_bytes) {
+  if (!h || !(dropout >= 0.f && dropout < 1.f) || (h->L > 1 && !masks))
+    return RNN_ERR_INVALID_ARG;
+  return backward_data_impl(h, stream, T, N, nullptr, W, dy, dhy, dcy, dx, dh0, dc0, workspace,
+                            ws_bytes, h->L > 1 ? masks : nullptr, dropout);
 }
 
 rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t N,

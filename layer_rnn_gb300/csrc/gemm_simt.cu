@@ -293,4 +293,31 @@ cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16, int64
   return cudaGetLastError();
 }
 
+// Inter-layer dropout with given masks: buf[i] *= mask[i] * scale, in place
+// (fp32 or bf16 elements; mask bytes are 0 or 1).  A select, not a product
+// with the mask, so a dropped element is exactly zero whatever its value.
+__global__ void dropout_kernel(void* buf, int bf16, const uint8_t* __restrict__ mask, int64_t n,
+                               float scale) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool keep = __ldg(mask + i) != 0;
+    if (bf16) {
+      __nv_bfloat16* b = static_cast<__nv_bfloat16*>(buf);
+      b[i] = __float2bfloat16_rn(keep ? __bfloat162float(b[i]) * scale : 0.f);
+    } else {
+      float* f = static_cast<float*>(buf);
+      f[i] = keep ? f[i] * scale : 0.f;
+    }
+  }
+}
+
+cudaError_t dropout_apply(void* buf, int bf16, const uint8_t* mask, int64_t n, float scale,
+                          int num_sms, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)std::max(1, num_sms) * 8);
+  dropout_kernel<<<(unsigned)blocks, 256, 0, st>>>(buf, bf16, mask, n, scale);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
 }  // namespace lr

@@ -80,10 +80,12 @@ def empty(shape, dtype, device="cuda"):
     return torch.empty(shape, dtype=td, device=device)
 
 
-def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths=None):
+def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths=None,
+            dropout=None):
     """Training forward + backward_data + backward_weights (+ inference forward)
     through the C ABI.  Returns float64 numpy arrays.  lengths: per-sequence
-    valid lengths [N] (the *_varlen calls), or None."""
+    valid lengths [N] (the *_varlen calls), or None.  dropout: (p, masks) with
+    masks [L-1, T, N, D*H] of 0/1 (the *_dropout calls), or None."""
     import torch
     from layer_rnn_gb300 import binding as B
     T, N, I, H, L = cfg["T"], cfg["N"], cfg["I"], cfg["H"], cfg["L"]
@@ -107,10 +109,13 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths
         if poison:
             ws.fill_(0xFF)  # NaN bit patterns: anything read before written shows
             y.fill_(float("nan"))
-        lens = None
+        lens = masks = None
         if lengths is not None:
             lens = torch.tensor(np.asarray(lengths), dtype=torch.int32, device="cuda")
             r.forward_training_varlen(lens, x, h0, c0, W, y, hy, cy, ws, stream)
+        elif dropout is not None:
+            masks = torch.tensor(np.asarray(dropout[1]), dtype=torch.uint8, device="cuda")
+            r.forward_training_dropout(dropout[0], masks, x, h0, c0, W, y, hy, cy, ws, stream)
         else:
             r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
         dx = empty((T, N, I), dt)
@@ -122,6 +127,8 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths
             dx.fill_(float("nan"))
         if lens is not None:
             r.backward_data_varlen(lens, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+        elif masks is not None:
+            r.backward_data_dropout(dropout[0], masks, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
         else:
             r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
         r.backward_weights(x, h0, y, ws, dW, stream)
@@ -144,11 +151,12 @@ def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths
         r.close()
 
 
-def run_oracle(cfg, inp, lengths=None):
+def run_oracle(cfg, inp, lengths=None, dropout=None):
     import oracle
+    p, masks = dropout if dropout is not None else (0.0, None)
     return oracle.run_flat(cfg["mode"], cfg["L"], cfg["bidir"], cfg["I"], cfg["H"], inp["x"],
                            inp["h0"], inp["c0"], inp["w"], inp["dy"], inp["dhy"], inp["dcy"],
-                           lengths=lengths)
+                           lengths=lengths, dropout=p, masks=masks)
 
 
 def weight_tensors(cfg, flat):

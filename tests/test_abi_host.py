@@ -179,3 +179,20 @@ def test_varlen_calls_reject_bad_arguments_before_any_launch(B):
                                                 None, None) == 1
     finally:
         B.rnn_destroy(h)
+
+
+def test_dropout_calls_reject_bad_arguments_before_any_launch(B):
+    lib = B.lib()
+    h = B.rnn_create(B.RNN_LSTM, 2, False, 4, 8, 0)
+    try:
+        ws = B.rnn_workspace_size(h, 5, 2)
+        args = (256, None, None, 256, 256, None, None, 256, ws)
+        for p, masks in ((0.2, None), (1.0, 512), (-0.1, 512), (float("nan"), 512)):
+            assert lib.rnn_forward_training_dropout(h, None, 5, 2, p, masks, *args) == 1, p
+            assert lib.rnn_backward_data_dropout(h, None, 5, 2, p, masks, 256, 256, None, None,
+                                                 256, None, None, 256, ws) == 1, p
+        # the checks of the calls without dropout still apply
+        assert lib.rnn_forward_training_dropout(h, None, 5, 2, 0.2, 512, 256, None, None, 256,
+                                                256, None, None, 256, ws - 1) == 3
+    finally:
+        B.rnn_destroy(h)
