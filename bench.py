@@ -70,17 +70,34 @@ def load_peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
+def include_closure(src):
+    """The source file and every header it includes with #include "...",
+    transitively, resolved against the including file's folder; sorted by path
+    after the source itself."""
+    import re
+    pat = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
+    first = os.path.normpath(os.path.join(ROOT, src))
+    seen, todo = {first}, [first]
+    while todo:
+        fn = todo.pop()
+        with open(fn) as f:
+            text = f.read()
+        for inc in pat.findall(text):
+            p = os.path.normpath(os.path.join(os.path.dirname(fn), inc))
+            if os.path.exists(p) and p not in seen:
+                seen.add(p)
+                todo.append(p)
+    return [first] + sorted(seen - {first})
+
+
 def kernel_source_sha256(src):
-    """sha256 over a kernel's source file and every header of the library
-    (csrc/*.cuh, csrc/*.h, in name order): a change to any of them can change
-    the kernel."""
-    import glob
+    """sha256 over a kernel's source file and the headers it includes,
+    transitively: a change to any of them can change the kernel, a change to
+    another part's header cannot."""
     import hashlib
-    csrc = os.path.join(ROOT, "layer_rnn_gb300", "csrc")
-    files = [os.path.join(ROOT, src)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
-                                                glob.glob(os.path.join(csrc, "*.h")))
     h = hashlib.sha256()
-    for fn in files:
+    for fn in include_closure(src):
+        h.update(os.path.relpath(fn, ROOT).encode() + b"\0")
         with open(fn, "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -247,7 +264,7 @@ def time_oracle(cfg, budget_s=20.0, max_reps=3):
 def run_ours(args, cfg):
     import torch
     from layer_rnn_gb300 import binding as B
-    from tests import harness
+    from layer_rnn_gb300 import tensors as tz
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -261,20 +278,20 @@ def run_ours(args, cfg):
     paths = B.rnn_get_paths(r.h, N)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        x = harness.to_dev(inp["x"], dt, dev)
-        h0 = harness.to_dev(inp["h0"], dt, dev)
-        c0 = harness.to_dev(inp["c0"], "f32", dev) if lstm else None
-        W = harness.to_dev(inp["w"], dt, dev)
-        dy = harness.to_dev(inp["dy"], dt, dev)
-        dhy = harness.to_dev(inp["dhy"], dt, dev)
-        dcy = harness.to_dev(inp["dcy"], "f32", dev) if lstm else None
-        y = harness.empty((T, N, D * H), dt, dev)
-        hy = harness.empty((L * D, N, H), dt, dev)
-        cy = harness.empty((L * D, N, H), "f32", dev) if lstm else None
-        dx = harness.empty((T, N, I), dt, dev)
-        dh0 = harness.empty((L * D, N, H), dt, dev)
-        dc0 = harness.empty((L * D, N, H), "f32", dev) if lstm else None
-        dW = harness.empty((inp["w"].size,), dt, dev)
+        x = tz.to_dev(inp["x"], dt, dev)
+        h0 = tz.to_dev(inp["h0"], dt, dev)
+        c0 = tz.to_dev(inp["c0"], "f32", dev) if lstm else None
+        W = tz.to_dev(inp["w"], dt, dev)
+        dy = tz.to_dev(inp["dy"], dt, dev)
+        dhy = tz.to_dev(inp["dhy"], dt, dev)
+        dcy = tz.to_dev(inp["dcy"], "f32", dev) if lstm else None
+        y = tz.empty((T, N, D * H), dt, dev)
+        hy = tz.empty((L * D, N, H), dt, dev)
+        cy = tz.empty((L * D, N, H), "f32", dev) if lstm else None
+        dx = tz.empty((T, N, I), dt, dev)
+        dh0 = tz.empty((L * D, N, H), dt, dev)
+        dc0 = tz.empty((L * D, N, H), "f32", dev) if lstm else None
+        dW = tz.empty((inp["w"].size,), dt, dev)
         ws = r.alloc_workspace(T, N, dev)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream.synchronize()

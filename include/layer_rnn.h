@@ -185,8 +185,11 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N,
  * that first call before any stream capture.  Every call on a device shares
  * the array and leaves its contents behind: calls that overlap on the GPU
  * (other streams, other handles) race and must be serialised by the caller.
- * Each call clears the array's status word first, so a barrier timeout is
- * reported only by the call itself when the handle has RNN_FLAG_SYNC_CHECK. */
+ * The array has its own status word.  Each call clears it first; a barrier
+ * timeout of the call is returned by the call itself when the handle has
+ * RNN_FLAG_SYNC_CHECK, else by the next rnn_check_status on that device
+ * (which reads and clears it too) before the next static call.  A handle
+ * already bound to another device returns RNN_ERR_INVALID_ARG. */
 rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int64_t T, int64_t N,
                                           const void* x, const void* h0, const void* c0,
                                           const void* W, void* y, void* hy, void* cy);
@@ -267,7 +270,9 @@ rnn_status_t rnn_backward_data_dropout(rnn_t h, void* stream, int64_t T, int64_t
                                        int64_t ws_bytes);
 
 /* Synchronise `stream`, then return and clear the device status word
- * (RNN_OK, RNN_ERR_TIMEOUT or RNN_ERR_DEVICE_CHECK). */
+ * (RNN_OK, RNN_ERR_TIMEOUT or RNN_ERR_DEVICE_CHECK): the handle's own, and,
+ * once rnn_forward_inference_static has run on the current device, that
+ * call's (synchronise the stream it ran on first). */
 rnn_status_t rnn_check_status(rnn_t h, void* stream);
 
 /* Test hook for failure detection.  timeout_ns > 0 sets the step-barrier

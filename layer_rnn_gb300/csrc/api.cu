@@ -338,18 +338,23 @@ rnn_status_t cuda_status(cudaError_t e) {
   return RNN_ERR_CUDA;
 }
 
-rnn_status_t read_status(rnn_handle* h, cudaStream_t st) {
-  if (cudaStreamSynchronize(st) != cudaSuccess) return RNN_ERR_CUDA;
-  if (!h->d_status) return RNN_OK;
+// read a device status word and clear it when it holds a failure
+rnn_status_t take_status_word(int* word) {
   int v = 0;
-  if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return RNN_ERR_CUDA;
   if (v != 0) {
     const int zero = 0;
-    if (cudaMemcpy(h->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    if (cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return RNN_ERR_CUDA;
   }
   return (rnn_status_t)v;
+}
+
+rnn_status_t read_status(rnn_handle* h, cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RNN_ERR_CUDA;
+  if (!h->d_status) return RNN_OK;
+  return take_status_word(h->d_status);
 }
 
 rnn_status_t finish(rnn_handle* h, cudaStream_t st, rnn_status_t s) {
@@ -1067,9 +1072,22 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
   return finish(h, st, RNN_OK);
 }
 
+namespace {
+int* static_status_word(int dev);
+}
+
 rnn_status_t rnn_check_status(rnn_t h, void* stream) {
   if (!h) return RNN_ERR_INVALID_ARG;
-  return read_status(h, static_cast<cudaStream_t>(stream));
+  rnn_status_t s = read_status(h, static_cast<cudaStream_t>(stream));
+  // the status word of rnn_forward_inference_static's array on this device,
+  // when a static call has run here
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
+  if (int* w = static_status_word(dev)) {
+    const rnn_status_t s2 = take_status_word(w);
+    if (s == RNN_OK) s = s2;
+  }
+  return s;
 }
 
 rnn_status_t rnn_set_debug(rnn_t h, int fault_block, int fault_step, int64_t timeout_ns) {
@@ -1165,7 +1183,7 @@ const char* rnn_status_string(rnn_status_t s) {
 // do it: code running while a memory pool owns the whole device, allocators
 // that must not be re-entered, or processes with a fixed memory budget set at
 // start-up.  rnn_forward_inference keeps its scratch in handle-owned memory
-// that it allocates on first use (and the handle allocates 4 KB of barrier
+// that it allocates on first use (and the handle allocates 64 KB of barrier
 // flags on its first compute call); this entry point instead places all of its
 // scratch -- the step flags and status word, the input projection and the two
 // intermediate layer outputs -- in one file-scope device array, so the call
@@ -1199,6 +1217,15 @@ rnn_status_t static_scratch_address(int dev, void** out) {
   return RNN_OK;
 }
 
+// the array's status word on device `dev`, or null before the first static
+// call there
+int* static_status_word(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) return nullptr;
+  return reinterpret_cast<int*>(static_cast<char*>(g_static_addr[dev]) + kSyncBytes - 64);
+}
+
 }  // namespace
 
 extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int64_t T, int64_t N,
@@ -1218,6 +1245,7 @@ extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int6
   if (need > (int64_t)kStaticScratchBytes) return RNN_ERR_WORKSPACE_TOO_SMALL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
+  if (h->device >= 0 && h->device != dev) return RNN_ERR_INVALID_ARG;  // one device per handle
   void* base = nullptr;
   s = static_scratch_address(dev, &base);
   if (s != RNN_OK) return s;

@@ -5,7 +5,7 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "internal.h"
+#include "gemm.h"
 
 namespace lr {
 

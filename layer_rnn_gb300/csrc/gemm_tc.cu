@@ -22,7 +22,7 @@
 #include <mutex>
 
 #include "common.cuh"
-#include "internal.h"
+#include "gemm.h"
 
 namespace lr {
 

@@ -24,7 +24,7 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "internal.h"
+#include "rec.h"
 
 namespace lr {
 

@@ -21,7 +21,7 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "internal.h"
+#include "rec.h"
 
 #ifdef LAYER_RNN_TRACE
 __device__ unsigned long long g_ctrace[4][1024][8];

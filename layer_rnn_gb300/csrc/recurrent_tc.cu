@@ -17,7 +17,7 @@
 #include <type_traits>
 
 #include "common.cuh"
-#include "internal.h"
+#include "rec.h"
 #include "tc_common.cuh"
 
 #ifdef LAYER_RNN_TRACE

@@ -26,7 +26,7 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "internal.h"
+#include "rec.h"
 #include "tc_common.cuh"
 
 #ifdef LAYER_RNN_TRACE

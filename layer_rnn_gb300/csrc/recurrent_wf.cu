@@ -46,7 +46,7 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "internal.h"
+#include "wf.h"
 
 #ifdef LAYER_RNN_TRACE
 __device__ unsigned long long g_wtrace[4][1024][8];

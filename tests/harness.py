@@ -54,30 +54,7 @@ def tolerances(cfg):
 # device marshalling (torch is used for device memory and streams only)
 # ----------------------------------------------------------------------------
 
-def to_dev(a, dtype, device="cuda"):
-    import torch
-    if a is None:
-        return None
-    st = wl.to_storage(a, dtype)
-    if dtype == "bf16":
-        return torch.from_numpy(st.view(np.int16)).to(device).view(torch.bfloat16)
-    return torch.from_numpy(st).to(device)
-
-
-def from_dev(t):
-    import torch
-    if t is None:
-        return None
-    if t.dtype == torch.bfloat16:
-        bits = t.view(torch.int16).cpu().numpy().view(np.uint16)
-        return wl.bf16_to_float(bits).astype(np.float64)
-    return t.cpu().numpy().astype(np.float64)
-
-
-def empty(shape, dtype, device="cuda"):
-    import torch
-    td = torch.bfloat16 if dtype == "bf16" else torch.float32
-    return torch.empty(shape, dtype=td, device=device)
+from layer_rnn_gb300.tensors import empty, from_dev, to_dev  # noqa: E402,F401
 
 
 def run_gpu(cfg, inp, flags=0, poison=True, inference=True, stream=None, lengths=None,

@@ -1,6 +1,7 @@
 """Host logic of bench.py that needs no GPU: the DRAM-traffic figure of the
 roofline line is taken from profiles/traffic.json only while the kernel's
-source and every header of the library are unchanged since the capture."""
+source and every header it includes (transitively) are unchanged since the
+capture."""
 
 import json
 import os
@@ -11,9 +12,11 @@ import pytest
 def _tree(tmp_path):
     csrc = tmp_path / "layer_rnn_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "k.cu").write_text("kernel v1\n")
+    (csrc / "k.cu").write_text('#include "common.cuh"\n#include "rec.h"\nkernel v1\n')
     (csrc / "common.cuh").write_text("header v1\n")
-    (csrc / "internal.h").write_text("decls v1\n")
+    (csrc / "rec.h").write_text('#include "host_common.h"\ndecls v1\n')
+    (csrc / "host_common.h").write_text("shared decls v1\n")
+    (csrc / "wf.h").write_text("another part's decls v1\n")
     (tmp_path / "profiles").mkdir()
     return csrc
 
@@ -40,8 +43,8 @@ def test_traffic_reported_while_sources_match(tmp_path, bench_at):
     assert bench_at.traffic_for("rec_fwd", {"name": "lstm4_bf16"}) is None
 
 
-@pytest.mark.parametrize("changed", ["k.cu", "common.cuh", "internal.h", "new.cuh"])
-def test_traffic_dropped_when_kernel_or_header_changes(tmp_path, bench_at, changed):
+@pytest.mark.parametrize("changed", ["k.cu", "common.cuh", "rec.h", "host_common.h"])
+def test_traffic_dropped_when_kernel_or_included_header_changes(tmp_path, bench_at, changed):
     csrc = _tree(tmp_path)
     _write_traffic(tmp_path, bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu"))
     with open(os.path.join(csrc, changed), "a") as f:
@@ -49,11 +52,20 @@ def test_traffic_dropped_when_kernel_or_header_changes(tmp_path, bench_at, chang
     assert bench_at.traffic_for("rec_fwd", {"name": "ds2_lstm"}) is None
 
 
-def test_other_sources_do_not_affect_the_hash(tmp_path, bench_at):
+@pytest.mark.parametrize("changed", ["wf.h", "other.cu", "new.cuh"])
+def test_sources_not_included_do_not_affect_the_hash(tmp_path, bench_at, changed):
     csrc = _tree(tmp_path)
     before = bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu")
-    (csrc / "other.cu").write_text("another kernel\n")
+    with open(os.path.join(csrc, changed), "a") as f:
+        f.write("edit\n")
     assert bench_at.kernel_source_sha256("layer_rnn_gb300/csrc/k.cu") == before
+
+
+def test_include_closure_is_transitive(tmp_path, bench_at):
+    _tree(tmp_path)
+    names = [os.path.basename(p)
+             for p in bench_at.include_closure("layer_rnn_gb300/csrc/k.cu")]
+    assert names == ["k.cu", "common.cuh", "host_common.h", "rec.h"]
 
 
 def test_entries_without_a_source_hash_are_ignored(tmp_path, bench_at):

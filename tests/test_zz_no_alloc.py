@@ -101,3 +101,33 @@ def test_static_scratch_rejects_oversized_problems():
         assert code == 3  # RNN_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
     finally:
         r.close()
+
+
+def test_static_call_timeout_is_reported_by_check_status():
+    """A step barrier that runs out of time inside a static call (one block
+    skips its flag release, so the others wait until the short limit) is
+    recorded in the array's own status word: rnn_check_status returns it and
+    clears it, and the next static call is correct again."""
+    import torch
+    from layer_rnn_gb300 import binding as B
+    cfg = CASES[0]
+    r = B.Rnn(cfg["mode"], cfg["L"], cfg["bidir"], cfg["I"], cfg["H"], cfg["dtype"], 0)
+    try:
+        i = _inputs(cfg, cfg["seed"])
+        ref = _outputs(cfg)
+        _call(B, B.rnn_forward_inference, r, cfg, i, ref)
+        assert B.rnn_check_status(r.h, r._stream(None)) == 0
+        B.rnn_set_debug(r.h, 0, 3, 50_000_000)  # block 0 skips step 3; 50 ms limit
+        got = _outputs(cfg)
+        _call(B, B.rnn_forward_inference_static, r, cfg, i, got)
+        torch.cuda.synchronize()
+        assert B.rnn_check_status(r.h, r._stream(None)) == 6  # RNN_ERR_TIMEOUT
+        assert B.rnn_check_status(r.h, r._stream(None)) == 0  # cleared
+        B.rnn_set_debug(r.h, -1, -1, 2_000_000_000)
+        _call(B, B.rnn_forward_inference_static, r, cfg, i, got)
+        assert B.rnn_check_status(r.h, r._stream(None)) == 0
+        for k in ("y", "hy"):
+            a, b = harness.from_dev(got[k]), harness.from_dev(ref[k])
+            assert harness.rel_err(a, b) <= harness.tolerances(cfg)[0], k
+    finally:
+        r.close()
