@@ -23,8 +23,8 @@ import math
 
 import numpy as np
 
-GATES = {"rnn_tanh": 1, "lstm": 4, "gru": 3}
-MODE_IDS = {"rnn_tanh": 0, "lstm": 1, "gru": 2}
+GATES = {"rnn_tanh": 1, "lstm": 4, "gru": 3, "gru_tf": 3}
+MODE_IDS = {"rnn_tanh": 0, "lstm": 1, "gru": 2, "gru_tf": 3}
 DTYPE_IDS = {"f32": 0, "bf16": 1}
 
 

@@ -143,6 +143,11 @@ def run(mode, L, bidir, x, h0, c0, params, dy, dhy, dcy):
                         return _dot(p["W_hh"][row], hn) + p["b_hh"][row]
 
                     hv, cv = [], []
+                    if mode == "gru_tf":
+                        # TensorFlow flavour: every unit's reset gate first,
+                        # then the candidate's recurrent product over r * h
+                        rs = [vsigmoid(gi(j) + gh(j)) for j in range(H)]
+                        rh = [rs[k] * hn[k] for k in range(H)]
                     for j in range(H):
                         if mode == "rnn_tanh":
                             hv.append(vtanh(gi(j) + gh(j)))
@@ -154,6 +159,11 @@ def run(mode, L, bidir, x, h0, c0, params, dy, dhy, dcy):
                             cj = fg * c[n][j] + ig * gg
                             cv.append(cj)
                             hv.append(og * vtanh(cj))
+                        elif mode == "gru_tf":
+                            inputgate = vsigmoid(gi(H + j) + gh(H + j))
+                            newgate = vtanh(gi(2 * H + j) + _dot(p["W_hh"][2 * H + j], rh) +
+                                            p["b_hh"][2 * H + j])
+                            hv.append(newgate + inputgate * (hn[j] - newgate))
                         else:
                             resetgate = vsigmoid(gi(j) + gh(j))
                             inputgate = vsigmoid(gi(H + j) + gh(H + j))

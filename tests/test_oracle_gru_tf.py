@@ -8,7 +8,11 @@ its own code:
 * on the first step from a zero state with b_hn = 0 both flavours give
   n = tanh(W_in x + b_in);
 * central finite differences of the loss (also with variable lengths);
-* on generic inputs the flavours differ.
+* on generic inputs the flavours differ;
+* one step with two units evaluated exactly outside the oracle (literal
+  expected values), and the unrolled scalar graph of tests/scalar_graph.py,
+  which differentiates the TensorFlow equation node by node -- both tell
+  W_hn (r * h) from r * (W_hn h).
 """
 
 import numpy as np
@@ -99,3 +103,40 @@ def test_gru_tf_gradients_match_finite_differences(L, bidir, lengths):
         scale = max(1.0, np.abs(num).max())
         np.testing.assert_allclose(g.ravel(), num, rtol=0, atol=2e-7 * scale,
                                    err_msg="gradient of %s" % name)
+
+
+def test_one_step_by_hand_two_units():
+    """One TensorFlow-flavour step ("rnn training example?", the TensorFlow GRU
+    equations: n = tanh(W_in x + b_in + W_hn (r * h) + b_hn)) with H = 2, a
+    full (non-diagonal) W_hn, both reset gates strictly between 0 and 1, h != 0
+    and b_hn != 0.  The expected values are that equation evaluated exactly
+    (rational inputs, 25 significant digits) outside the oracle and written
+    here as literals.  At H = 1 the product would be a scalar and could not
+    tell W_hn (r * h) from r * (W_hn h); here the two differ in the second
+    decimal."""
+    x = 0.7
+    h = [-0.4, 0.6]
+    W_ih = np.array([0.3, -0.2, 0.5, 0.1, -0.3, 0.4]).reshape(6, 1)  # r0 r1 z0 z1 n0 n1
+    W_hh = np.array([[-0.6, 0.4], [0.2, 0.5],      # W_hr
+                     [-0.3, 0.25], [0.1, -0.4],    # W_hz
+                     [0.7, -0.9], [0.5, 0.8]])     # W_hn
+    b_ih = np.array([0.05, -0.1, 0.2, 0.0, -0.25, 0.15])
+    b_hh = np.array([0.1, 0.3, -0.2, 0.15, 0.4, -0.3])
+    p = [dict(W_ih=W_ih, W_hh=W_hh, b_ih=b_ih, b_hh=b_hh)]
+    y, hy, _, cache = oracle.forward("gru_tf", np.array([[[x]]]), np.array([[h]]), None, p, 1,
+                                     False)
+    rec = cache["tapes"][0][0]  # layer 0, direction 0, step 0
+    r_exact = [0.6984652160025387754745268, 0.5695462239392290158986344]
+    z_exact = [0.6502185485738270628302611, 0.4850044983805899277070476]
+    n_exact = [-0.5102925359619838186435149, 0.2577428642137648597495013]
+    h_exact = [-0.4385782833102560749224672, 0.4237391146729452878227584]
+    np.testing.assert_allclose(y[0, 0], h_exact, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(hy[0, 0], h_exact, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(rec["r"][0], r_exact, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(rec["z"][0], z_exact, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(rec["n"][0], n_exact, rtol=0, atol=1e-15)
+    # the candidates of the other placements of r differ by far more than the
+    # tolerance: r * (W_hn h + b_hn) (PyTorch flavour) and r * (W_hn h) + b_hn
+    for wrong in ([-0.6371464663287032615489948, 0.3957580063783218927540946],
+                  [-0.5599370473363979272877778, 0.2816496370598662883406038]):
+        assert np.abs(np.array(wrong) - np.array(n_exact)).max() > 1e-2

@@ -180,6 +180,7 @@ def test_single_scalar_step_by_hand():
 UNROLLED_CASES = [
     ("lstm", 1, False), ("gru", 1, False), ("rnn_tanh", 1, False),
     ("lstm", 2, True), ("gru", 2, True), ("rnn_tanh", 2, True),
+    ("gru_tf", 1, False), ("gru_tf", 2, True),
 ]
 
 
