@@ -4,15 +4,40 @@
 // hidden units, the blocks of a cluster split the contraction length K), but
 // each block's per-step product
 //     D[m][n] = sum_k W_hh[row m][k0 + k] * h_{t-1}[n][k0 + k]      (m < 128)
-// runs on the tensor cores: the block's W_hh slice stays for the whole
-// sequence in tensor memory as the MMA's A operand (fp32: tf32 hi and lo
-// parts, three passes hi*hi + hi*lo + lo*hi as in the dense phases; bf16: one
-// pass, two elements per 32-bit column), the step's h slice is staged into
-// shared memory in the 128-byte-swizzled K-major layout the MMA reads as B,
-// and the accumulator D lands in tensor memory.  D's rows are pushed over
-// distributed shared memory to the blocks that own the units' pointwise math,
-// as in the cluster path.  All waits are bounded; the cluster barriers are
-// executed by every block on every step, work or not.
+// runs on the tensor cores with W_hh's slice resident in tensor memory for the
+// whole sequence.
+//
+// fp32 operands are split into fp16 pairs, x = (hi + lo * 2^-11) / scale, with
+// hi = fp16(x * scale), lo = fp16((x * scale - hi) * 2^11) and a power-of-two
+// scale per block and operand (W: its slice's largest magnitude maps just
+// below 2^14; h: every |h_t| is at most max(1, max |h0|) -- LSTM and tanh
+// outputs lie in (-1, 1), a GRU state is a convex mix of its candidate and the
+// previous state -- so one scale from h0's slice holds for the whole
+// sequence).  The product keeps hi*hi + hi*lo + lo*hi, three MMA passes of 16
+// K each: about 22 significant bits per operand, as three tf32 passes on
+// tf32 hi / lo splits, in half the MMA instructions (an MMA's issue, not the
+// tensor pipe, bounds these small N = batch products).  bf16 runs one pass.
+//
+// Step pipeline (one step = one time step of one direction):
+//   1. staging, K atoms (128 bytes of every batch row) spread over the warps:
+//      a warp waits only for the step flags of the blocks that produced its
+//      atom's hidden units, loads its rows of the atom of h_{t-1} from L2,
+//      splits them (fp32) and stores them in the 128-byte-swizzled K-major
+//      layout the MMA reads as B;
+//   2. MMA issue after one block barrier: fp32 has one issuing thread per
+//      pass, each with its own accumulator in tensor memory, so the three
+//      passes issue in parallel;
+//   3. the accumulators' rows are combined in a fixed order and pushed over
+//      distributed shared memory to the block that owns each unit's pointwise
+//      step; every pushing warp then arrives (release, cluster scope) on the
+//      owner's exchange barrier, so an owner waits only for its own inputs
+//      instead of a cluster-wide barrier;
+//   4. the owner sums the partials in rank order (deterministic), runs the
+//      fused gate math, stores the step's h (what the other blocks read) and
+//      releases its step flag; the workspace stores (gates, c, h sequence) go
+//      out after the release, so the release does not wait for them.
+// The next step's input projection values are fetched with cp.async at the
+// start of each step (the pages' ping-pong prefetch).  All waits are bounded.
 #include <algorithm>
 #include <type_traits>
 
@@ -29,8 +54,19 @@ __device__ unsigned long long g_ttrace[4][1024][8];
                  ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
     if (b_ >= 0 && threadIdx.x == 0 && (s) < 1024) g_ttrace[b_][(s)][(k)] = lr::globaltimer_ns();\
   } while (0)
+// per-warp stamps of the step pipeline: [block][step][0..15 atom staged,
+// 16..18 issuer i done]
+__device__ unsigned long long g_wtrace[4][1024][32];
+#define WTRACE(s, k)                                                                          \
+  do {                                                                                        \
+    const int nb_ = gridDim.x;                                                                \
+    const int b_ = blockIdx.x == 0 ? 0 : blockIdx.x == nb_ / 3 ? 1 : blockIdx.x == (2 * nb_) / 3 \
+                 ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
+    if (b_ >= 0 && (threadIdx.x & 31) == 0 && (s) < 1024) g_wtrace[b_][(s)][(k)] = lr::globaltimer_ns();\
+  } while (0)
 #else
 #define TTRACE(s, k) ((void)0)
+#define WTRACE(s, k) ((void)0)
 #endif
 
 namespace lr {
@@ -40,7 +76,9 @@ namespace {
 using namespace tc;
 
 constexpr int kTThreads = 256;
-constexpr int kTM = 128;  // MMA M (rows of W per block, padded)
+constexpr int kTWarps = kTThreads / 32;
+constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
+constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
 
 __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
   const int r = j / Ur;
@@ -49,11 +87,11 @@ __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
 
 // shared memory layout (offsets in bytes from a 1024-aligned base)
 struct TcLayout {
-  uint32_t b_hi, b_lo;      // staged B tiles: n_atoms x (Nm x 128 bytes)
-  uint32_t recv;            // [2][Pk][G*Uq][Nm] f32
-  uint32_t outs;            // [G][N][Uq] f32 summed partials
+  uint32_t b_hi, b_lo;      // staged B tiles: KC atoms x (Nm rows x 128 bytes)
+  uint32_t recv;            // [2][Pk][G*Uq][Nm] f32 partial sums pushed by the cluster
+  uint32_t stash;           // [4][N][Uq] f32 saved activations, stored after the release
   uint32_t hst, cst;        // [N][Uq] f32 state of the own units
-  uint32_t gxs;             // [G][N][Uq] f32 next projection values
+  uint32_t gxs;             // [G][N][Uq] f32 this step's projection values
   uint32_t total;
 };
 
@@ -67,9 +105,9 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
   L.b_lo = off;
   off += bf ? 0 : ntile;
   L.recv = off;
-  off += 2u * pl.cluster * G * pl.Uq * pl.nbp * 4u;
-  L.outs = off;
-  off += (uint32_t)G * pl.Uq * N * 4u;
+  off += 2u * pl.cluster * G * pl.Uq * (pl.nbp + 4) * 4u;
+  L.stash = off;
+  off += 4u * pl.Uq * N * 4u;
   L.hst = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.cst = off;
@@ -83,11 +121,16 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
 template <bool BF>
 __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant__ RecParams p) {
   typedef typename std::conditional<BF, bf16, float>::type T;
+  constexpr int NI = BF ? 1 : 3;   // issuing threads = accumulators (one per pass)
+  constexpr int EPA = 64;            // K elements (16-bit) per 128-byte atom
+  constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t xbar[2];  // partial-sum exchange, by step parity
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_fail;
+  __shared__ int s_fail, s_mma_bad, s_x_bad;
   __shared__ float s_bhn[kTM];
+  __shared__ float s_red[kTThreads / 32][2];
   const RecPlan& pl = p.plan;
   const int P = pl.P, Pk = pl.cluster;
   const int d = blockIdx.x / P;
@@ -100,6 +143,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   const int u0 = r * Ur, Urc = min(Ur, H - u0);
   const int uq0 = q * Uq, Uqc = max(0, min(Uq, Urc - uq0));
   const int k0 = q * pl.Kk, Kc = max(0, min(pl.Kk, H - k0));
+  const int KCu = (Kc + EPA - 1) / EPA;        // atoms this block stages and multiplies
   const int Mb = G * Ur;                       // rows of the block's A (<= 128)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t GH = (int64_t)G * H;
@@ -108,28 +152,35 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
   const TcLayout Lo = tc_layout(pl, G, N, BF);
   float* recv0 = reinterpret_cast<float*>(base + Lo.recv);
-  float* outs = reinterpret_cast<float*>(base + Lo.outs);
+  float* stash = reinterpret_cast<float*>(base + Lo.stash);
   float* hst = reinterpret_cast<float*>(base + Lo.hst);
   float* cst = reinterpret_cast<float*>(base + Lo.cst);
   float* gxs = reinterpret_cast<float*>(base + Lo.gxs);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
-  const uint32_t bar = smem_addr(&mma_bar);
-  // tensor memory: D at column 0 (Nm columns), A after it
-  const uint32_t a_col = (uint32_t)Nm;
-  const uint32_t a_lo_col = (uint32_t)(Nm + Kp);
+  const uint32_t mbar = smem_addr(&mma_bar);
+  const uint32_t xbar0 = smem_addr(&xbar[0]);
+  // tensor memory: accumulator i at column i * Nm, then the A operands, two
+  // 16-bit elements per column: W (bf16) or W_hi and W_lo (fp32 split)
+  const uint32_t a_col = (uint32_t)(NI * Nm);
+  const uint32_t a_lo_col = a_col + (uint32_t)(Kp / 2);
   const uint32_t ncols = (uint32_t)pl.lda;     // allocated columns (power of two)
 
-  // the launch formed the planned clusters, the tensor-memory columns hold D
-  // and A, D's rows fit the MMA's M and N the staged tile: otherwise the block
-  // touches neither tensor memory nor a peer's shared memory
+  // the launch formed the planned clusters, the tensor-memory columns hold the
+  // accumulators and A, D's rows fit the MMA's M and N the staged tile:
+  // otherwise the block touches neither tensor memory nor a peer's memory
   const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q ||
-                       (uint32_t)(Nm + (BF ? Kp / 2 : 2 * Kp)) > ncols || ncols > 512u ||
+                       a_col + (uint32_t)(BF ? Kp / 2 : Kp) > ncols || ncols > 512u ||
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Mb > kTM || N > Nm ||
-                       Nm % 16 != 0 || Nm > 256 || Kp % (BF ? 64 : 32) != 0 || pl.Kk > Kp;
+                       Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
+                       pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > 32;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
+    s_mma_bad = 0;
+    s_x_bad = 0;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    mbar_init(mbar, NI);
+    mbar_init(xbar0, (unsigned)(kTWarps * Pk));
+    mbar_init(xbar0 + 8u, (unsigned)(kTWarps * Pk));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && !cfg_bad) {
@@ -139,16 +190,61 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // zero the staged B tiles (rows >= N and columns >= Kc stay zero) and state
-  for (uint32_t i = tid; i < (Lo.recv) / 16u; i += kTThreads)
+  // zero the staged B tiles and the W_lo tile (rows >= N / >= Mb and columns
+  // >= Kc stay zero)
+  for (uint32_t i = tid; i < Lo.recv / 16u; i += kTThreads)
     reinterpret_cast<uint4*>(base)[i] = make_uint4(0, 0, 0, 0);
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // A (this block's W_hh slice) into tensor memory: lane m = row g*Ur + u,
-  // column chunks of 32; warp w serves lanes 32*(w%4) .. +31
+  // the split's scales (fp32): largest |W| of the slice and largest |h0| of
+  // the staged K slice, each mapped just below 2^14 by a power of two
+  float w_scale = 1.f, h_scale = 1.f, out_scale = 1.f;
+  if (!BF) {
+    const T* W = reinterpret_cast<const T*>(a.whh);
+    float wm = 0.f, hm = 1.f;
+    if (!cfg_bad) {
+      for (int idx = tid; idx < Mb * Kc; idx += kTThreads) {
+        const int m = idx / Kc, k = idx - m * Kc;
+        const int g = m / Ur, u = m - g * Ur;
+        if (g < G && u < Urc) wm = fmaxf(wm, fabsf(to_f(W[(int64_t)(g * H + u0 + u) * H + k0 + k])));
+      }
+      if (a.h0)
+        for (int idx = tid; idx < N * Kc; idx += kTThreads) {
+          const int n = idx / Kc, k = idx - n * Kc;
+          hm = fmaxf(hm, fabsf(to_f(reinterpret_cast<const T*>(a.h0)[(int64_t)n * H + k0 + k])));
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, o));
+    }
+    if (lane == 0) {
+      s_red[warp][0] = wm;
+      s_red[warp][1] = hm;
+    }
+    __syncthreads();
+    wm = 0.f;
+    hm = 1.f;
+    for (int w = 0; w < kTThreads / 32; ++w) {
+      wm = fmaxf(wm, s_red[w][0]);
+      hm = fmaxf(hm, s_red[w][1]);
+    }
+    int ew = 0, eh = 0;
+    if (wm > 0.f) (void)frexpf(wm, &ew);  // wm < 2^ew
+    (void)frexpf(hm, &eh);
+    ew = min(max(14 - ew, -100), 100);
+    eh = min(max(14 - eh, -100), 100);
+    w_scale = ldexpf(1.f, ew);
+    h_scale = ldexpf(1.f, eh);
+    out_scale = ldexpf(1.f, -(ew + eh));
+  }
+
+  // A (this block's W_hh slice) into tensor memory: lane / row m = g*Ur + u,
+  // 32-column chunks of 64 K elements (two 16-bit elements per column); warp w
+  // serves lanes 32*(w%4) .. +31.  fp32: W_hi at a_col, W_lo at a_lo_col.
   if (!cfg_bad) {
     const T* W = reinterpret_cast<const T*>(a.whh);
     const int quarter = warp & 3;
@@ -156,25 +252,19 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     const int g = m / Ur, u = m - g * Ur;
     const bool row_ok = m < Mb && g < G && u < Urc;
     const T* wrow = row_ok ? W + (int64_t)(g * H + u0 + u) * H + k0 : W;
-    const int epc = BF ? 64 : 32;              // elements per 32-column chunk
-    const int nchunk = Kp / epc;
+    const int nchunk = pl.KC;                  // one 32-column chunk per atom
     for (int ci = warp >> 2; ci < nchunk; ci += kTThreads / 128) {
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
+        const int k = ci * 64 + 2 * i;
+        const float e0 = (row_ok && k < Kc) ? to_f(wrow[k]) : 0.f;
+        const float e1 = (row_ok && k + 1 < Kc) ? to_f(wrow[k + 1]) : 0.f;
         if (BF) {
-          const int k = ci * 64 + 2 * i;
-          float e0 = (row_ok && k < Kc) ? to_f(wrow[k]) : 0.f;
-          float e1 = (row_ok && k + 1 < Kc) ? to_f(wrow[k + 1]) : 0.f;
-          const uint32_t b0 = __float_as_uint(e0) >> 16, b1 = __float_as_uint(e1) >> 16;
-          hi[i] = b0 | (b1 << 16);
+          hi[i] = (__float_as_uint(e0) >> 16) | ((__float_as_uint(e1) >> 16) << 16);
           lo[i] = 0;
         } else {
-          const int k = ci * 32 + i;
-          const float v = (row_ok && k < Kc) ? to_f(wrow[k]) : 0.f;
-          const uint32_t hb = __float_as_uint(v) & 0xFFFFE000u;
-          hi[i] = hb;
-          lo[i] = __float_as_uint(v - __uint_as_float(hb));
+          split_f16x2(e0 * w_scale, e1 * w_scale, hi[i], lo[i]);
         }
       }
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -199,187 +289,257 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   }
   for (int uu = tid; uu < Uqc; uu += kTThreads)
     s_bhn[uu] = p.mode == 2 ? to_f(reinterpret_cast<const T*>(a.bhh)[2 * H + u0 + uq0 + uu]) : 0.f;
-  const int flo = Kc > 0 ? owner_of(k0, Ur, Uq, Pk) : 0;
-  const int fhi = Kc > 0 ? owner_of(k0 + Kc - 1, Ur, Uq, Pk) : -1;
   unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
   T* y = reinterpret_cast<T*>(a.y);
   T* hseq = reinterpret_cast<T*>(a.hseq);
-  const uint32_t idesc = (1u << 4) | ((BF ? 1u : 2u) << 7) | ((BF ? 1u : 2u) << 10) |
+  // kind::f16 with bf16 (1) or fp16 (0) operands, fp32 accumulate
+  const uint32_t idesc = (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) |
                          ((uint32_t)(Nm >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
-  const int kstep = BF ? 16 : 8;               // K per MMA
-  const int nsteps = (Kc + kstep - 1) / kstep;
   fence_before();
   __syncthreads();
   fence_after();
-  bool failed = s_fail != 0;
-  uint32_t phase = 0;  // parity of the next completion of the MMA barrier
+  uint32_t mma_phase = 0;  // parity of the next completion of the MMA barrier
 
   for (int s = 0; s < nT; ++s) {
     const int t = d ? nT - 1 - s : s;
     const int tp = d ? t + 1 : t - 1;
+    const bool failed = s_fail != 0;  // read after the previous step's barrier
     TTRACE(s, 0);
     // this step's input projection values of the own items (consumed after the
     // contraction, so their latency hides behind it)
-    for (int it = tid; it < G * items; it += kTThreads) {
-      const int g = it / items, rem = it - g * items;
-      const int uu = rem % Uqc, n = rem / Uqc;
-      cp_async4(gxs + (g * N + n) * Uq + uu,
-                a.gx + ((int64_t)t * N + n) * GH + (int64_t)g * H + u0 + uq0 + uu);
+    if (!failed) {
+      for (int it = tid; it < G * items; it += kTThreads) {
+        const int g = it / items, rem = it - g * items;
+        const int uu = rem % Uqc, n = rem / Uqc;
+        cp_async4(gxs + (g * N + n) * Uq + uu,
+                  a.gx + ((int64_t)t * N + n) * GH + (int64_t)g * H + u0 + uq0 + uu);
+      }
     }
     cp_async_commit();
-    if (!failed && s > 0 && Kc > 0 && warp == 0) {
-      if (!warp_wait_flags(flags, p.flag_stride, flo, fhi, (unsigned)s, p.status, p.timeout_ns,
-                           p.spin_ns) &&
-          lane == 0)
-        s_fail = 1;
-    }
-    __syncthreads();
-    TTRACE(s, 1);
-    failed = s_fail != 0;
+    const bool have = !failed && Kc > 0;
     const T* src = s == 0 ? reinterpret_cast<const T*>(a.h0)
                           : y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
     const int64_t ldsrc = s == 0 ? H : p.ldy;
-    const bool have = !failed && src != nullptr && Kc > 0;
-    // stage B = h_{t-1}[n][k0 .. k0+Kc) into the swizzled K-major tiles
+    // 1. staging: task (atom, row part) -> warp; each warp waits only for the
+    // producers of its atom's units, then stages its rows of h_{t-1}[n][atom]
+    // as B (fp16 hi / lo for fp32)
+    const int parts = max(1, kTWarps / max(1, KCu));
     if (have) {
-      constexpr int VE = 16 / (int)sizeof(T);
-      const int nv = Kc / VE;
-      for (int idx = tid; idx < N * nv; idx += kTThreads) {
-        const int n = idx / nv, c16 = idx - n * nv;
-        const uint4 v = ldcg16(src + k0 + (int64_t)n * ldsrc + c16 * VE);
-        const int atom = c16 >> 3, c = c16 & 7;
-        const uint32_t off = (uint32_t)atom * atom_bytes + sw_off(n, c);
-        if (BF) {
-          *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = v;
-        } else {
-          uint4 h4, l4;
-          h4.x = v.x & 0xFFFFE000u; l4.x = __float_as_uint(__uint_as_float(v.x) - __uint_as_float(h4.x));
-          h4.y = v.y & 0xFFFFE000u; l4.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h4.y));
-          h4.z = v.z & 0xFFFFE000u; l4.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h4.z));
-          h4.w = v.w & 0xFFFFE000u; l4.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h4.w));
-          *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = h4;
-          *reinterpret_cast<uint4*>(base + Lo.b_lo + off) = l4;
+      for (int task = warp; task < KCu * parts; task += kTWarps) {
+        const int at = task % KCu, part = task / KCu;
+        const int ka = at * EPA, kn = min(EPA, Kc - ka);
+        if (s > 0 &&
+            !warp_wait_flags(flags, p.flag_stride, owner_of(k0 + ka, Ur, Uq, Pk),
+                             owner_of(k0 + ka + kn - 1, Ur, Uq, Pk), (unsigned)s, p.status,
+                             p.timeout_ns, p.spin_ns) &&
+            lane == 0)
+          s_fail = 1;  // the data is not used: the status word already holds the failure
+        unsigned char* bh = base + Lo.b_hi + (uint32_t)at * atom_bytes;
+        unsigned char* bl = base + Lo.b_lo + (uint32_t)at * atom_bytes;
+        // 16-byte chunk c of row n holds K elements ka + 8c .. +7; this task
+        // takes rows part, part + parts, ...
+        for (int idx = lane; idx < ((N - part + parts - 1) / parts) * 8; idx += 32) {
+          const int n = part + (idx >> 3) * parts, c = idx & 7;
+          const uint32_t off = sw_off(n, c);
+          const bool in = src != nullptr && c * 8 < kn;
+          const T* sp = src + k0 + ka + c * 8 + (int64_t)n * ldsrc;
+          if (BF) {
+            const uint4 v = in ? ldcg16(sp) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(bh + off) = v;
+          } else {
+            // K slices are multiples of 4 fp32 elements: the last chunk of a
+            // slice may hold only its first half
+            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+            if (in) {
+              v0 = ldcg16(sp);
+              if (c * 8 + 4 < kn) v1 = ldcg16(sp + 4);
+            }
+            uint4 h4, l4;
+            split_f16x2(__uint_as_float(v0.x) * h_scale, __uint_as_float(v0.y) * h_scale, h4.x, l4.x);
+            split_f16x2(__uint_as_float(v0.z) * h_scale, __uint_as_float(v0.w) * h_scale, h4.y, l4.y);
+            split_f16x2(__uint_as_float(v1.x) * h_scale, __uint_as_float(v1.y) * h_scale, h4.z, l4.z);
+            split_f16x2(__uint_as_float(v1.z) * h_scale, __uint_as_float(v1.w) * h_scale, h4.w, l4.w);
+            *reinterpret_cast<uint4*>(bh + off) = h4;
+            *reinterpret_cast<uint4*>(bl + off) = l4;
+          }
         }
+        WTRACE(s, at);
       }
     }
+    // the staged tiles to the tensor cores' (async) proxy, then one barrier: a
+    // per-atom mbarrier measured slower (each wait costs about 100 ns)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    TTRACE(s, 1);
+    if (have) {
+      // 2. MMA issue: issuer i is lane 0 of warp kTWarps-1-i and runs pass i
+      // into accumulator i (pass 0: W_hi h_hi, 1: W_hi h_lo, 2: W_lo h_hi);
+      // descriptors advance by whole atoms and 32-byte K steps inside the
+      // start-address field; the padded tail of the last atom multiplies
+      // zeros (B columns >= Kc are staged as zeros, W columns >= Kc are zero)
+      const int iss = kTWarps - 1 - warp;
+      if (iss >= 0 && iss < NI && lane == 0) {
+        const uint32_t dcol = tmem + (uint32_t)(iss * Nm);
+        const uint64_t bd0 = b_desc(base_s + ((!BF && iss == 1) ? Lo.b_lo : Lo.b_hi));
+        const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
+        const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
+        fence_after();
+        for (int at = 0; at < KCu; ++at) {
+          const uint64_t bd = bd0 + (uint64_t)at * bstep;
+          const uint32_t acol = acol0 + (uint32_t)(at * 32);
+#pragma unroll
+          for (int kk = 0; kk < EPA / KSTEP; ++kk)
+            mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
+                       (at | kk) ? 1u : 0u);
+        }
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                mbar)
+            : "memory");
+        WTRACE(s, 16 + iss);
+      }
+      TTRACE(s, 6);
+    }
+    // wait for the products: the first issuer's warp polls the barrier, the
+    // other warps sleep in the block barrier meanwhile
+    if (have && warp == kTWarps - 1) {
+      const bool ok = mbar_wait_bounded(mbar, mma_phase, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok) && lane == 0) s_mma_bad = 1;
+    }
+    if (have) mma_phase ^= 1u;
     fence_before();
     __syncthreads();
     fence_after();
-    TTRACE(s, 6);
-    if (have && tid == 0) {
-      for (int ks = 0; ks < nsteps; ++ks) {
-        const uint32_t atom = (uint32_t)(ks >> 2), kk = (uint32_t)(ks & 3);
-        const uint64_t bh = b_desc(base_s + Lo.b_hi + atom * atom_bytes) + kk * 2;
-        const uint32_t acc0 = ks > 0 ? 1u : 0u;
-        if (BF) {
-          mma_a_tmem(true, tmem, tmem + a_col + (uint32_t)(ks * 8), bh, idesc, acc0);
-        } else {
-          const uint64_t bl = b_desc(base_s + Lo.b_lo + atom * atom_bytes) + kk * 2;
-          mma_a_tmem(false, tmem, tmem + a_col + (uint32_t)(ks * 8), bh, idesc, acc0);
-          mma_a_tmem(false, tmem, tmem + a_col + (uint32_t)(ks * 8), bl, idesc, 1u);
-          mma_a_tmem(false, tmem, tmem + a_lo_col + (uint32_t)(ks * 8), bh, idesc, 1u);
-        }
-      }
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-          : "memory");
-    }
-    // wait for the products (every thread: the phase of this step)
-    bool mma_ok = true;
-    if (have) {
-      mma_ok = mbar_wait_bounded(bar, phase, p.status, p.timeout_ns);
-      phase ^= 1u;
-    }
-    fence_after();
+    const bool mma_ok = s_mma_bad == 0;
     TTRACE(s, 2);
-    // push D's rows (partials over this block's K slice) to the owners
-    float* recv = recv0 + (size_t)(s & 1) * Pk * G * Uq * Nm;
+    // 3. push D's rows (partials over this block's K slice, accumulators summed
+    // in a fixed order) to the owners; warps 0-3 take columns 0-15, warps 4-7
+    // columns 16-31 (then 32-47 and 48-63, ...)
+    const int Rs = Nm + 4;  // exchange row stride (floats): 16-byte rows, fewer bank conflicts
+    float* recv = recv0 + (size_t)(s & 1) * Pk * G * Uq * Rs;
+    const uint32_t xb = xbar0 + 8u * (uint32_t)(s & 1);
     if (!failed) {
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
       const int g = m / Ur, u = m - g * Ur;
       const bool row_ok = m < Mb && g < G && u < Urc;
       const int owner = row_ok ? u / Uq : 0, uo = u - owner * Uq;
-      for (int c0 = (warp >> 2) * 32; c0 < Nm; c0 += (kTThreads / 128) * 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
-        if (!row_ok || owner >= Pk) continue;
-        // 16-byte pieces (row starts are 64-byte aligned, Nm % 16 == 0); columns
-        // N .. Nm-1 of D are zero (the staged rows beyond N are zero) and unread
-        float* dst = recv + ((size_t)q * G * Uq + g * Uq + uo) * Nm + c0;
-        const bool ok = have && mma_ok;
+      const bool ok = have && mma_ok;
+      const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);
+      for (int c0 = (warp >> 2) * 16; c0 < N; c0 += (kTWarps / 4) * 16) {
+        float v[NI][16];
+        if (ok) {
+          if constexpr (NI == 3) {
+            // the three accumulators' loads in flight together, one wait
+            tmem_ld16x3(lrow + (uint32_t)c0, lrow + (uint32_t)(Nm + c0),
+                        lrow + (uint32_t)(2 * Nm + c0), v[0], v[1], v[2]);
+            // (hi hi + (hi lo + lo hi) 2^-11) / (w_scale h_scale), powers of two
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
+            for (int e = 0; e < 16; ++e)
+              v[0][e] = fmaf(v[1][e] + v[2][e], 1.f / 2048.f, v[0][e]) * out_scale;
+          } else {
+            tmem_ld16(lrow + (uint32_t)c0, v[0]);
+          }
+          if (warp == 0 && c0 == 0) WTRACE(s, 24);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[0][e] = 0.f;
+        }
+        if (!row_ok || owner >= Pk) continue;
+        // 16-byte pieces (rows of Nm + 4 floats, Nm % 16 == 0); columns N .. Nm-1
+        // of D are zero (the staged rows beyond N are zero) and unread
+        float* dst = recv + ((size_t)q * G * Uq + g * Uq + uo) * Rs + c0;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
           if (c0 + i < N)
-            st_peer4(dst + i, (unsigned)owner, ok ? v[i] : 0.f, ok ? v[i + 1] : 0.f,
-                     ok ? v[i + 2] : 0.f, ok ? v[i + 3] : 0.f);
+            st_peer4(dst + i, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2], v[0][i + 3]);
       }
+      __syncwarp();
+      if (warp == 0) WTRACE(s, 25);
+      if (lane < Pk) mbar_arrive_peer(xb, (unsigned)lane);
+      WTRACE(s, 20 + (warp & 1));
     }
     fence_before();
-    cl_sync();
-    if (!failed) {
-      // batch index fastest: consecutive threads read consecutive partials
-      for (int idx = tid; idx < G * items; idx += kTThreads) {
-        const int n = idx % N, gu = idx / N;
-        const int g = gu / Uqc, uu = gu - g * Uqc;
-        float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank)
-          v += recv[((size_t)rank * G * Uq + g * Uq + uu) * Nm + n];
-        outs[(g * N + n) * Uq + uu] = v;
-      }
-    }
+    // 4. the owner's partial sums: every rank's pushes of this step
+    bool x_ok = true;
+    if (!failed) x_ok = mbar_wait_cluster_bounded(xb, (uint32_t)((s >> 1) & 1), p.status,
+                                                  p.timeout_ns);
+    WTRACE(s, 22 + (warp & 1));
+    if (!x_ok) s_x_bad = 1;
     cp_async_wait_all();
     __syncthreads();
     TTRACE(s, 3);
-    if (!failed) {
+    const bool live = !failed && x_ok && s_x_bad == 0;
+    if (live) {
+      // the partial sums of each gate (rank order, fixed) feed the gate math
+      const size_t rstride = (size_t)G * Uq * Rs;
       for (int it = tid; it < items; it += kTThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
-        const int slot = d ? t : t + 1;
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
-        const float* ov = outs + n * Uq + uu;   // likewise
+        float* sv = stash + n * Uq + uu;        // likewise
+        float ov[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          ov[g] = 0.f;
+          if (g < G) {
+            const float* rp = recv + ((size_t)g * Uq + uu) * Rs + n;
+            for (int rank = 0; rank < Pk; ++rank) ov[g] += rp[rank * rstride];
+          }
+        }
         float h;
         if (p.mode == 1) {
           const float ig = sigmoidf_(gv[0] + ov[0]);
-          const float fg = sigmoidf_(gv[N * Uq] + ov[N * Uq]);
-          const float gg = tanhf(gv[2 * N * Uq] + ov[2 * N * Uq]);
-          const float og = sigmoidf_(gv[3 * N * Uq] + ov[3 * N * Uq]);
+          const float fg = sigmoidf_(gv[N * Uq] + ov[1]);
+          const float gg = tanhf(gv[2 * N * Uq] + ov[2]);
+          const float og = sigmoidf_(gv[3 * N * Uq] + ov[3]);
           const float c = fg * cst[n * Uq + uu] + ig * gg;
           h = og * tanhf(c);
           cst[n * Uq + uu] = c;
-          if (a.gates) {
-            float* gp = a.gates + row * 4 * H + j;
-            gp[0] = ig; gp[H] = fg; gp[2 * H] = gg; gp[3 * H] = og;
-          }
-          if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
+          sv[0] = ig; sv[N * Uq] = fg; sv[2 * N * Uq] = gg; sv[3 * N * Uq] = og;
         } else if (p.mode == 2) {
-          const float ghn = ov[2 * N * Uq] + s_bhn[uu];
+          const float ghn = ov[2] + s_bhn[uu];
           const float rg = sigmoidf_(gv[0] + ov[0]);
-          const float z = sigmoidf_(gv[N * Uq] + ov[N * Uq]);
+          const float z = sigmoidf_(gv[N * Uq] + ov[1]);
           const float nv = tanhf(gv[2 * Uq * N] + rg * ghn);
           h = (1.f - z) * nv + z * hst[n * Uq + uu];
-          if (a.gates) {
-            float* gp = a.gates + row * 4 * H + j;
-            gp[0] = rg; gp[H] = z; gp[2 * H] = nv; gp[3 * H] = ghn;
-          }
+          sv[0] = rg; sv[N * Uq] = z; sv[2 * N * Uq] = nv; sv[3 * N * Uq] = ghn;
         } else {
           h = tanhf(gv[0] + ov[0]);
-          if (a.gates) a.gates[row * H + j] = h;
         }
         hst[n * Uq + uu] = h;
         y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
-        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
       }
     }
     __syncthreads();
     TTRACE(s, 4);
-    if (!failed && tid == 0 && s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
+    if (live && tid == 0 && s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
       publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
     TTRACE(s, 5);
+    // workspace stores of the step, after the release
+    if (live) {
+      for (int it = tid; it < items; it += kTThreads) {
+        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        const int64_t row = (int64_t)t * N + n;
+        const int slot = d ? t : t + 1;
+        const float* sv = stash + n * Uq + uu;
+        if (a.gates) {
+          if (p.mode == 0) {
+            a.gates[row * H + j] = hst[n * Uq + uu];
+          } else {
+            float* gp = a.gates + row * 4 * H + j;
+            gp[0] = sv[0]; gp[H] = sv[N * Uq]; gp[2 * H] = sv[2 * N * Uq]; gp[3 * H] = sv[3 * N * Uq];
+          }
+        }
+        if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = cst[n * Uq + uu];
+        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(hst[n * Uq + uu]);
+      }
+    }
+    if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
+    __syncthreads();
   }
   cl_sync();  // no block leaves while a peer may still store into it
-  if (!failed) {
+  if (s_fail == 0) {
     for (int it = tid; it < items; it += kTThreads) {
       const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
       const int64_t o = (int64_t)n * H + j;
@@ -403,6 +563,7 @@ bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t sm
   if ((H * e) % 16 != 0 || N < 1 || N > 256) return false;
   const int Nm = (N + 15) / 16 * 16;
   const int Ur_max = kTM / G;
+  const int NI = bf16 ? 1 : 3;
   bool found = false;
   double best = 0;
   RecPlan bp;
@@ -414,19 +575,20 @@ bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t sm
     if (Ur > Ur_max) continue;
     const int Pr = (H + Ur - 1) / Ur;
     const int Uq = (Ur + Pk - 1) / Pk;
-    const int epc = bf16 ? 64 : 32;                       // elements per 32 TMEM columns
+    const int epc = 64;                                   // 16-bit elements per 128-byte atom
     const int Kk = (((H + Pk - 1) / Pk) + 7) / 8 * 8;     // 16-byte aligned slices
     const int Kp = (Kk + epc - 1) / epc * epc;
-    const int acols = bf16 ? Kp / 2 : 2 * Kp;
+    if (Kp / epc > kMaxAtoms) continue;
+    const int acols = bf16 ? Kp / 2 : Kp;                 // W (bf16) / W_hi and W_lo (fp32 split)
     int cols = 32;
-    while (cols < Nm + acols) cols *= 2;
+    while (cols < NI * Nm + acols) cols *= 2;
     if (cols > 512) continue;
     RecPlan pl;
     pl.direct = 0;
     pl.cluster = Pk; pl.Pr = Pr; pl.P = Pr * Pk; pl.Ur = Ur; pl.Uq = Uq;
     pl.Kk = Kk;
     pl.K = Kp;                       // padded K slice
-    pl.KC = Kp / (bf16 ? 64 : 32);   // K atoms of 128 bytes
+    pl.KC = Kp / epc;                // K atoms of 128 bytes
     pl.nbp = Nm;                     // MMA N
     pl.lda = cols;                   // tensor memory columns
     pl.Mloc = G * Ur; pl.Mp = kTM; pl.nb = N;
@@ -453,6 +615,10 @@ bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t sm
 extern "C" int rnn_debug_ttrace_copy(void* host, size_t bytes) {
   if (bytes > sizeof(g_ttrace)) bytes = sizeof(g_ttrace);
   return (int)cudaMemcpyFromSymbol(host, g_ttrace, bytes);
+}
+extern "C" int rnn_debug_fwtrace_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_wtrace)) bytes = sizeof(g_wtrace);
+  return (int)cudaMemcpyFromSymbol(host, g_wtrace, bytes);
 }
 extern "C" int rnn_debug_ttrace_clear() {
   static unsigned long long zeros[4][1024][8];

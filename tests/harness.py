@@ -5,7 +5,8 @@ Parity metric (per output tensor): normwise maximum relative error
 ``max|gpu - ref| / max|ref|`` -- robust to entries of the reference near zero.
 Bars: 1e-4 for fp32 forward outputs (y, hy, cy), 1e-3 for fp32 gradients
 (dx, dh0, dc0, every weight / bias gradient tensor), 2e-2 for every output of
-a bf16 workload.
+a bf16 workload.  Reported beside it: the elementwise relative error
+``|gpu - ref| / max(|ref|, 1e-6 max|ref|)`` at its 99.9th percentile.
 """
 
 import os
@@ -42,6 +43,21 @@ def rel_err(gpu, ref):
     if scale == 0.0:
         return float(diff)
     return float(diff / scale)
+
+
+def elementwise_err(gpu, ref, q=99.9):
+    """The q-th percentile over the entries of |gpu - ref| / max(|ref|,
+    1e-6 * max|ref|): the elementwise relative error reported beside the
+    normwise one, which a few large entries can dominate."""
+    gpu = np.asarray(gpu, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    floor = 1e-6 * np.abs(ref).max()
+    if floor == 0.0:
+        return float(np.percentile(np.abs(gpu - ref), q))
+    return float(np.percentile(np.abs(gpu - ref) / np.maximum(np.abs(ref), floor), q))
 
 
 def tolerances(cfg):
@@ -163,6 +179,20 @@ def compare(cfg, gpu, ref):
     rw = weight_tensors(cfg, ref["dW"])
     for k in rw:
         res["d" + k] = (rel_err(gw[k], rw[k]), tg)
+    return res
+
+
+def elementwise_report(cfg, gpu, ref):
+    """Dict name -> 99.9th-percentile elementwise relative error, for every
+    output compare() covers."""
+    res = {}
+    for k in ("y", "hy", "cy", "dx", "dh0", "dc0"):
+        if ref[k] is not None:
+            res[k] = elementwise_err(gpu[k], ref[k])
+    gw = weight_tensors(cfg, gpu["dW"])
+    rw = weight_tensors(cfg, ref["dW"])
+    for k in rw:
+        res["d" + k] = elementwise_err(gw[k], rw[k])
     return res
 
 
