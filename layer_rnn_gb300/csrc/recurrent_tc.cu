@@ -126,9 +126,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
-  __shared__ __align__(8) uint64_t xbar[2];  // partial-sum exchange, by step parity
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_fail, s_mma_bad, s_x_bad;
+  __shared__ int s_fail, s_mma_bad;
   __shared__ float s_bhn[kTM];
   __shared__ float s_red[kTThreads / 32][2];
   const RecPlan& pl = p.plan;
@@ -158,7 +157,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   float* gxs = reinterpret_cast<float*>(base + Lo.gxs);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
   const uint32_t mbar = smem_addr(&mma_bar);
-  const uint32_t xbar0 = smem_addr(&xbar[0]);
   // tensor memory: accumulator i at column i * Nm, then the A operands, two
   // 16-bit elements per column: W (bf16) or W_hi and W_lo (fp32 split)
   const uint32_t a_col = (uint32_t)(NI * Nm);
@@ -176,11 +174,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     s_mma_bad = 0;
-    s_x_bad = 0;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
     mbar_init(mbar, NI);
-    mbar_init(xbar0, (unsigned)(kTWarps * Pk));
-    mbar_init(xbar0 + 8u, (unsigned)(kTWarps * Pk));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && !cfg_bad) {
@@ -378,46 +373,46 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       // start-address field; the padded tail of the last atom multiplies
       // zeros (B columns >= Kc are staged as zeros, W columns >= Kc are zero)
       const int iss = kTWarps - 1 - warp;
-      if (iss >= 0 && iss < NI && lane == 0) {
-        const uint32_t dcol = tmem + (uint32_t)(iss * Nm);
-        const uint64_t bd0 = b_desc(base_s + ((!BF && iss == 1) ? Lo.b_lo : Lo.b_hi));
-        const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
-        const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
-        fence_after();
-        for (int at = 0; at < KCu; ++at) {
-          const uint64_t bd = bd0 + (uint64_t)at * bstep;
-          const uint32_t acol = acol0 + (uint32_t)(at * 32);
-#pragma unroll
-          for (int kk = 0; kk < EPA / KSTEP; ++kk)
-            mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
-                       (at | kk) ? 1u : 0u);
+      if (iss >= 0 && iss < NI) {
+        if (lane == 0) {
+          const uint32_t dcol = tmem + (uint32_t)(iss * Nm);
+          const uint64_t bd0 = b_desc(base_s + ((!BF && iss == 1) ? Lo.b_lo : Lo.b_hi));
+          const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
+          const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
+          fence_after();
+          for (int at = 0; at < KCu; ++at) {
+            const uint64_t bd = bd0 + (uint64_t)at * bstep;
+            const uint32_t acol = acol0 + (uint32_t)(at * 32);
+  #pragma unroll
+            for (int kk = 0; kk < EPA / KSTEP; ++kk)
+              mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
+                         (at | kk) ? 1u : 0u);
+          }
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                  mbar)
+              : "memory");
+          WTRACE(s, 16 + iss);
         }
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                mbar)
-            : "memory");
-        WTRACE(s, 16 + iss);
+        __syncwarp();
       }
       TTRACE(s, 6);
     }
-    // wait for the products: the first issuer's warp polls the barrier, the
-    // other warps sleep in the block barrier meanwhile
-    if (have && warp == kTWarps - 1) {
-      const bool ok = mbar_wait_bounded(mbar, mma_phase, p.status, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, ok) && lane == 0) s_mma_bad = 1;
+    // wait for the products (every thread, the phase of this step)
+    bool mma_ok = true;
+    if (have) {
+      mma_ok = mbar_wait_bounded(mbar, mma_phase, p.status, p.timeout_ns);
+      if (!mma_ok) s_mma_bad = 1;
+      mma_phase ^= 1u;
     }
-    if (have) mma_phase ^= 1u;
-    fence_before();
-    __syncthreads();
+    mma_ok = __all_sync(0xffffffffu, mma_ok);
     fence_after();
-    const bool mma_ok = s_mma_bad == 0;
     TTRACE(s, 2);
     // 3. push D's rows (partials over this block's K slice, accumulators summed
     // in a fixed order) to the owners; warps 0-3 take columns 0-15, warps 4-7
     // columns 16-31 (then 32-47 and 48-63, ...)
     const int Rs = Nm + 4;  // exchange row stride (floats): 16-byte rows, fewer bank conflicts
     float* recv = recv0 + (size_t)(s & 1) * Pk * G * Uq * Rs;
-    const uint32_t xb = xbar0 + 8u * (uint32_t)(s & 1);
     if (!failed) {
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
@@ -454,22 +449,17 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           if (c0 + i < N)
             st_peer4(dst + i, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2], v[0][i + 3]);
       }
-      __syncwarp();
       if (warp == 0) WTRACE(s, 25);
-      if (lane < Pk) mbar_arrive_peer(xb, (unsigned)lane);
-      WTRACE(s, 20 + (warp & 1));
     }
-    fence_before();
-    // 4. the owner's partial sums: every rank's pushes of this step
-    bool x_ok = true;
-    if (!failed) x_ok = mbar_wait_cluster_bounded(xb, (uint32_t)((s >> 1) & 1), p.status,
-                                                  p.timeout_ns);
-    WTRACE(s, 22 + (warp & 1));
-    if (!x_ok) s_x_bad = 1;
+    // 4. one cluster barrier per step, executed by every block, work or not:
+    // after it every owner holds every rank's partials of this step (and
+    // every thread's projection prefetch has landed)
     cp_async_wait_all();
-    __syncthreads();
+    fence_before();
+    cl_sync();
+    WTRACE(s, 22 + (warp & 1));
     TTRACE(s, 3);
-    const bool live = !failed && x_ok && s_x_bad == 0;
+    const bool live = !failed && s_mma_bad == 0;
     if (live) {
       // the partial sums of each gate (rank order, fixed) feed the gate math
       const size_t rstride = (size_t)G * Uq * Rs;
