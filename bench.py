@@ -263,12 +263,36 @@ def time_oracle(cfg, budget_s=20.0, max_reps=3):
 # ----------------------------------------------------------------------------
 def run_ours(args, cfg):
     import torch
-    from layer_rnn_gb300 import binding as B
-    from layer_rnn_gb300 import tensors as tz
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = dist_init("nccl")
+    line = measure(args, cfg, dist, dev, rank, ws_n, local)
+    if cfg["name"] == "ds2_lstm" and not args.no_gru:
+        # the metric is LSTM/GRU at the DS2 shape: the GRU layer of the same
+        # shape, timed the same way, rides along in the same line
+        g = measure(args, wl.WORKLOADS["ds2_gru"], dist, dev, rank, ws_n, local)
+        line["gru"] = {k: g[k] for k in ("value", "unit", "ms_per_step", "effective_tflops",
+                                         "phases", "recurrent_paths", "roofline", "e2e",
+                                         "gpu_launches", "clocks")}
+        line["gru"]["config"] = g["config"]
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, spent = time_oracle(cfg, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "sequences/s",
+                                "cores": os.cpu_count(), "kind": "oracle", "sample": sample,
+                                "seconds": round(spent, 2)}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure(args, cfg, dist, dev, rank, ws_n, local):
+    """Time one workload (device-resident steps, per-phase events, end to end
+    through pinned host buffers) and return its bench line (no CPU baseline)."""
+    import torch
+    from layer_rnn_gb300 import binding as B
+    from layer_rnn_gb300 import tensors as tz
     T, N, I, H, L = cfg["T"], cfg["N"], cfg["I"], cfg["H"], cfg["L"]
     D = wl.num_directions(cfg)
     dt = cfg["dtype"]
@@ -372,6 +396,15 @@ def run_ours(args, cfg):
     barrier(dist)
     ms_e2e = timed(args.steps, e2e_step)
     ms_e2e_max = max_over_ranks(statistics.mean(ms_e2e), dist, dev)
+    # the step protocol of the tensor-core recurrent forward alone (flag waits,
+    # cluster barrier, release; no work): the barrier term of the recurrence's
+    # latency bound
+    empty_us = None
+    if paths[0] == "tensor":
+        try:
+            empty_us = B.rnn_measure_step_protocol(r.h, stream.cuda_stream, N, T)
+        except B.RnnError:
+            empty_us = None
     r.close()
 
     peaks, peak_src = load_peaks()
@@ -393,6 +426,11 @@ def run_ours(args, cfg):
         if on_tensor:
             if dt == "bf16":
                 return "tensor", bf16_sus, "%s bf16 dense, sustained (cuBLAS loop)" % peak_src
+            if ph == "rec_fwd" and paths[0] == "tensor":
+                return ("tensor", bf16_sus / 3.0,
+                        "%s bf16 sustained / 3 passes: fp32 as three fp16 passes on "
+                        "scaled hi / lo splits (fp16 and bf16 share the kind::f16 rate)"
+                        % peak_src)
             return ("tensor", bf16_sus * 1.1 / 2.25 / 3.0,
                     "%s bf16 sustained x 1.1/2.25 (nominal tf32/bf16) / 3 passes: fp32 as "
                     "3xTF32" % peak_src)
@@ -416,6 +454,22 @@ def run_ours(args, cfg):
             nsteps = (T + L - 1) if wave else L * T
             per_phase[ph]["path"] = paths[0] if ph == "rec_fwd" else paths[1]
             per_phase[ph]["us_per_step"] = round(ms_ph * 1e3 / nsteps, 3)
+            if empty_us is not None and per_phase[ph]["path"] == "tensor" and L == 1:
+                # latency bound of one serial step: max(W_hh streamed once
+                # from on-chip memory at 128 B/clk/SM, the step's MMA work at
+                # the phase's tensor peak) + the measured empty-step protocol
+                G = gates(cfg["mode"])
+                e = 2 if dt == "bf16" else 4
+                w_us = G * H * H * e / (num_sms * 128.0 * sm_clk * 1e6) * 1e6
+                mma_us = D * 2.0 * N * G * H * H / (pk_ * 1e12) * 1e6
+                bound = max(w_us, mma_us) + empty_us
+                per_phase[ph]["bound_us"] = {
+                    "w_hh_stream_us": round(w_us, 3), "mma_us": round(mma_us, 3),
+                    "empty_step_us": round(empty_us, 3), "bound_us": round(bound, 3),
+                    "frac_of_bound": round(bound / per_phase[ph]["us_per_step"], 3),
+                    "note": "empty step = the forward kernel's flag waits, cluster barrier "
+                            "and release alone (rnn_measure_step_protocol), used for both "
+                            "directions of the recurrence"}
     # dominant phase by time share
     dom = max(PHASE_NAMES, key=lambda p: phases[p][0])
     avg_ms = phases[dom][0] / max(1, args.steps)
@@ -457,15 +511,7 @@ def run_ours(args, cfg):
         "wall_s_timed_region": round(wall, 3),
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        v, sample, spent = time_oracle(cfg, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "sequences/s",
-                                "cores": os.cpu_count(), "kind": "oracle", "sample": sample,
-                                "seconds": round(spent, 2)}
-    if dist is not None:
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def run_reference(args, cfg):
@@ -505,6 +551,9 @@ def main():
     ap.add_argument("--workload", default="ds2_lstm", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gru", action="store_true",
+                    help="time only the named workload (by default the ds2_lstm line also "
+                         "carries the ds2_gru layer of the same shape)")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override T of the workload (small cases for profiler captures; "
                          "the default workload sizes are the benchmark)")

@@ -304,6 +304,60 @@ typedef enum {
 } rnn_path_t;
 rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
 
+/* The step protocol of the tensor-core recurrent forward, timed alone.  The
+ * pages have no counterpart of this call: it measures the part of a
+ * recurrent step's latency that no arithmetic removes, the term a latency
+ * bound of the recurrence adds to the time of streaming W_hh and of the MMA.
+ * It runs `steps` (2 .. 2^20) empty steps of the forward kernel's protocol for
+ * batch N with one direction -- the same grid and clusters, the same waits
+ * for the producers' step flags, the per-step cluster barrier and the flag
+ * release, with no loads, no MMA and no gate math -- once to warm up and once
+ * between two CUDA events on `stream`, synchronises `stream`, and returns the
+ * average microseconds per step.  It touches only the handle's step flags and
+ * status word.  RNN_ERR_UNSUPPORTED when the forward of batch N does not run
+ * on the tensor-core recurrent kernel; a barrier timeout returns
+ * RNN_ERR_TIMEOUT. */
+rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t steps,
+                                       double* us_per_step);
+
+/* Test hooks for the packed operand forms.  The pages have no counterpart:
+ * the forms are this library's own (the "matrix pre-transposition" of the
+ * cuDNN table in Keras issue #3692 names the idea, not a layout).  Each runs
+ * the library's packing kernel asynchronously on `stream` into caller
+ * buffers, so a test can check that the packing loses and invents nothing.
+ *
+ * rnn_debug_split_tf32: the tf32 hi / lo split of the dense phases' fp32
+ * operands.  src [rows][cols] (row stride lds floats) -> hi, lo (lo may be
+ * NULL) [rows][cols] (transpose = 0) or [cols][rows] (transpose = 1), row
+ * stride ldd floats.  hi keeps the top 10 mantissa bits of each value, lo =
+ * value - hi (both fp32, so hi + lo reproduces the value exactly).
+ *
+ * rnn_debug_transpose_bf16: the K-major bf16 operand copy of the dense
+ * phases.  src [rows][cols] (row stride lds elements) -> dst [cols][rows]
+ * (row stride ldd elements), bit for bit.
+ *
+ * rnn_debug_wf_pack: the layer wavefront's packed rows of one layer (bf16
+ * handles of a unidirectional stack with 2..8 layers only, as the wavefront;
+ * RNN_ERR_UNSUPPORTED otherwise) for batch N, from the canonical buffer W.
+ * layout[0..4] receives Pr (blocks of the layer), Ur (units per block), R
+ * (packed rows per unit: 4 for LSTM i, f, g, o and GRU r, z, n_x, n_h; 1 for
+ * tanh), kp (packed row length, elements) and Kxp (the x part's padded
+ * length).  Row (r*Ur + u)*R + g of wp [Pr*Ur*R][kp] bf16 is, for unit
+ * j = r*Ur + u < H: [W_ih row of gate g of unit j | zeros to Kxp | W_hh row |
+ * zeros to kp], with the GRU's n_x row taking only W_in and its n_h row only
+ * W_hn (n_h is W_hn's row in the h part, zeros in the x part); bias[row] (fp32)
+ * = b_ih + b_hh of that row (GRU: b_in on n_x, b_hn on n_h).  Rows of units
+ * j >= H are zero.  wp_bytes / bias_bytes are the buffers' sizes:
+ * RNN_ERR_WORKSPACE_TOO_SMALL when they are short. */
+rnn_status_t rnn_debug_split_tf32(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                                  float* hi, float* lo, int64_t ldd, int transpose,
+                                  void* stream);
+rnn_status_t rnn_debug_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds,
+                                      void* dst, int64_t ldd, void* stream);
+rnn_status_t rnn_debug_wf_pack(rnn_t h, void* stream, int64_t N, int layer, const void* W,
+                               void* wp, int64_t wp_bytes, float* bias, int64_t bias_bytes,
+                               int64_t* layout);
+
 /* Static description of the status code. */
 const char* rnn_status_string(rnn_status_t s);
 

@@ -62,6 +62,10 @@ SIGNATURES = {
     "rnn_get_phase_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _pi64]),
     "rnn_get_paths": (_i32, [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_int)]),
+    "rnn_measure_step_protocol": (_i32, [_vp, _vp, _i64, _i64, ctypes.POINTER(ctypes.c_double)]),
+    "rnn_debug_split_tf32": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp]),
+    "rnn_debug_transpose_bf16": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp]),
+    "rnn_debug_wf_pack": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _pi64]),
     "rnn_status_string": (ctypes.c_char_p, [_i32]),
 }
 
@@ -185,6 +189,28 @@ def rnn_backward_data_varlen(h, stream, T, N, lengths, W, dy, dhy, dcy, dx, dh0,
 
 def rnn_backward_weights(h, stream, T, N, x, h0, y, ws, ws_bytes, dW):
     _call("rnn_backward_weights", h, stream, T, N, x, h0, y, ws, ws_bytes, dW)
+
+
+def rnn_measure_step_protocol(h, stream, N, steps):
+    """Microseconds per empty step of the tensor-core forward's protocol."""
+    us = ctypes.c_double()
+    _call("rnn_measure_step_protocol", h, stream, N, steps, ctypes.byref(us))
+    return us.value
+
+
+def rnn_debug_split_tf32(src, rows, cols, lds, hi, lo, ldd, transpose, stream):
+    _call("rnn_debug_split_tf32", src, rows, cols, lds, hi, lo, ldd, int(transpose), stream)
+
+
+def rnn_debug_transpose_bf16(src, rows, cols, lds, dst, ldd, stream):
+    _call("rnn_debug_transpose_bf16", src, rows, cols, lds, dst, ldd, stream)
+
+
+def rnn_debug_wf_pack(h, stream, N, layer, W, wp, wp_bytes, bias, bias_bytes):
+    """Returns (Pr, Ur, R, kp, Kxp)."""
+    lay = (ctypes.c_int64 * 5)()
+    _call("rnn_debug_wf_pack", h, stream, N, layer, W, wp, wp_bytes, bias, bias_bytes, lay)
+    return tuple(lay)
 
 
 def rnn_check_status(h, stream):

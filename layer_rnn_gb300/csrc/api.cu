@@ -1159,6 +1159,100 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
   return RNN_OK;
 }
 
+// ----------------------------------------------------------------------------
+// test hooks: the packed operand forms, produced by the library's own kernels
+// ----------------------------------------------------------------------------
+rnn_status_t rnn_debug_split_tf32(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                                  float* hi, float* lo, int64_t ldd, int transpose,
+                                  void* stream) {
+  if (!src || !hi || rows < 1 || cols < 1 || lds < cols || ldd < (transpose ? rows : cols))
+    return RNN_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || !aligned(hi, 16) || !aligned(lo, 16)) return RNN_ERR_MISALIGNED;
+  return cuda_status(split_operand(src, rows, cols, lds, hi, lo, ldd, transpose != 0,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+rnn_status_t rnn_debug_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds,
+                                      void* dst, int64_t ldd, void* stream) {
+  if (!src || !dst || rows < 1 || cols < 1 || lds < cols || ldd < rows)
+    return RNN_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || !aligned(dst, 16)) return RNN_ERR_MISALIGNED;
+  return cuda_status(
+      transpose_bf16(src, rows, cols, lds, dst, ldd, static_cast<cudaStream_t>(stream)));
+}
+
+rnn_status_t rnn_debug_wf_pack(rnn_t h, void* stream, int64_t N, int layer, const void* W,
+                               void* wp, int64_t wp_bytes, float* bias, int64_t bias_bytes,
+                               int64_t* layout) {
+  if (!h || !W || !wp || !bias || !layout || N < 1 || layer < 0 || layer >= h->L)
+    return RNN_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(wp, 16) || !aligned(bias, 16)) return RNN_ERR_MISALIGNED;
+  rnn_status_t s = device_setup(h);
+  if (s != RNN_OK) return s;
+  WfPlan pl;
+  if (!wf_candidate(h, N) ||
+      !wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &pl))
+    return RNN_ERR_UNSUPPORTED;
+  const int64_t I_l = layer_in(h, layer), H = h->H;
+  const int64_t kp = wf_kp(I_l, H);
+  const int64_t rows = (int64_t)pl.Pr * pl.R * pl.Ur;
+  if (wp_bytes < rows * kp * 2 || bias_bytes < rows * 4) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t e = 2;
+  const cudaError_t ce =
+      wf_pack(pl, h->mode, I_l, H, cp<char>(W, weight_offset(h, layer, 0, 0) * e),
+              cp<char>(W, weight_offset(h, layer, 0, 1) * e),
+              cp<char>(W, weight_offset(h, layer, 0, 2) * e),
+              cp<char>(W, weight_offset(h, layer, 0, 3) * e), wp, bias,
+              static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return RNN_ERR_CUDA;
+  layout[0] = pl.Pr;
+  layout[1] = pl.Ur;
+  layout[2] = pl.R;
+  layout[3] = kp;
+  layout[4] = (I_l + 63) / 64 * 64;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t steps,
+                                       double* us_per_step) {
+  if (!h || !us_per_step || N < 1 || steps < 2 || steps > (1 << 20)) return RNN_ERR_INVALID_ARG;
+  rnn_status_t s = device_setup(h);
+  if (s != RNN_OK) return s;
+  RecPlan pl;
+  s = plan_rec(h, false, N, &pl, 1);
+  if (s != RNN_OK) return s;
+  if (pl.tc != 1) return RNN_ERR_UNSUPPORTED;
+  RecParams rp;
+  fill_rec_common(h, steps, N, &rp);
+  rp.D = 1;
+  rp.plan = pl;
+  rp.fault_block = -1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return RNN_ERR_CUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return RNN_ERR_CUDA;
+  }
+  s = RNN_OK;
+  // the flag memset of the launch sits outside the events: one warm-up launch,
+  // then a timed one
+  for (int rep = 0; rep < 2 && s == RNN_OK; ++rep) {
+    if (rep == 1 && cudaEventRecord(e0, st) != cudaSuccess) s = RNN_ERR_CUDA;
+    if (s == RNN_OK) s = cuda_status(rec_tc_probe_launch(rp, st));
+    if (rep == 1 && s == RNN_OK && cudaEventRecord(e1, st) != cudaSuccess) s = RNN_ERR_CUDA;
+  }
+  float ms = 0.f;
+  if (s == RNN_OK && (cudaEventSynchronize(e1) != cudaSuccess ||
+                      cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+    s = RNN_ERR_CUDA;
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (s == RNN_OK) s = read_status(h, st);
+  if (s == RNN_OK) *us_per_step = (double)ms * 1e3 / (double)steps;
+  return s;
+}
+
 const char* rnn_status_string(rnn_status_t s) {
   switch (s) {
     case RNN_OK: return "ok";

@@ -99,6 +99,9 @@ cudaError_t rec_cluster_launch(bool backward, const RecParams& p, cudaStream_t s
 bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
                  const int* max_clusters, RecPlan* out);
 cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st);
+// The tensor-core forward's step protocol with no work (flag waits, cluster
+// barrier, flag release), p.T steps, same plan and grid as rec_tc_launch.
+cudaError_t rec_tc_probe_launch(const RecParams& p, cudaStream_t st);
 // co-resident clusters of `cluster` blocks of the cluster kernels with `smem` bytes
 int rec_cluster_capacity(int cluster, size_t smem);
 // Tensor-core backward path (recurrent_tc_bwd.cu): plan (false if the problem

@@ -544,7 +544,78 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                  : "memory");
 }
 
+// The forward kernel's step protocol with no work: per step, each warp waits
+// for the flags of its atoms' producers, one block barrier, the cluster
+// barrier, one block barrier and the flag release -- the part of a step's
+// latency that no arithmetic removes.  Same grid, clusters and waits as
+// rec_fwd_tc; bounded like it.
+__global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_constant__ RecParams p) {
+  __shared__ int s_fail;
+  const RecPlan& pl = p.plan;
+  const int P = pl.P, Pk = pl.cluster;
+  const int d = blockIdx.x / P;
+  const int b = blockIdx.x - d * P;
+  const int q = b % Pk;
+  const int H = p.H, Ur = pl.Ur, Uq = pl.Uq;
+  const int k0 = q * pl.Kk, Kc = max(0, min(pl.Kk, H - k0));
+  const int EPA = 64, KCu = (Kc + EPA - 1) / EPA;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q;
+  if (threadIdx.x == 0) {
+    s_fail = cfg_bad;
+    if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
+  }
+  __syncthreads();
+  unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
+  const int parts = max(1, kTWarps / max(1, KCu));
+  for (int s = 0; s < p.T; ++s) {
+    const bool failed = s_fail != 0;
+    if (!failed && s > 0) {
+      for (int task = warp; task < KCu * parts; task += kTWarps) {
+        const int ka = (task % KCu) * EPA, kn = min(EPA, Kc - ka);
+        if (!warp_wait_flags(flags, p.flag_stride, owner_of(k0 + ka, Ur, Uq, Pk),
+                             owner_of(k0 + ka + kn - 1, Ur, Uq, Pk), (unsigned)s, p.status,
+                             p.timeout_ns, p.spin_ns) &&
+            lane == 0)
+          s_fail = 1;
+      }
+    }
+    __syncthreads();
+    cl_sync();
+    __syncthreads();
+    if (!failed && s_fail == 0 && threadIdx.x == 0 && s + 1 < p.T)
+      publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
+  }
+  cl_sync();
+}
+
 }  // namespace
+
+cudaError_t rec_tc_probe_launch(const RecParams& p, cudaStream_t st) {
+  const RecPlan& pl = p.plan;
+  void* fn = (void*)rec_step_probe;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
+  if (e != cudaSuccess) return e;
+  RecParams copy = p;
+  void* args[] = {&copy};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.D * pl.P);
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = pl.smem;  // the forward's size: one block per SM, as there
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
 
 bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
                  const int* max_clusters, RecPlan* out) {
