@@ -44,9 +44,10 @@
  *     call synchronises and returns it itself.
  *   - One handle serves one stream at a time (it owns the step-barrier
  *     counters its kernels use).  No call allocates device memory except
- *     rnn_forward_inference (first call per (T, N) growth, see there) and the
- *     first compute call of a handle (its 64 KB of step flags);
- *     rnn_forward_inference_static never allocates.
+ *     rnn_forward_inference (first call per (T, N) growth, see there),
+ *     rnn_measure_step_protocol (a temporary buffer) and the first compute
+ *     call of a handle (its 64 KB of step flags); rnn_forward_inference_static
+ *     never allocates.
  */
 #ifndef LAYER_RNN_H
 #define LAYER_RNN_H
@@ -177,9 +178,9 @@ rnn_status_t rnn_forward_inference(rnn_t h, void* stream, int64_t T, int64_t N,
  * rnn_forward_inference.  All scratch -- step flags and status word, the input
  * projection, two intermediate layer outputs -- lives in one static device
  * array of 32 MiB per device, held by every GPU that loads the library until
- * the process exits.  A call needs 65536 + A(D*T*N*G*H*4) bytes, plus
- * 2*A(T*N*D*H*elem) when num_layers > 1 (A = round up to 256, elem = 4 for
- * RNN_F32, 2 for RNN_BF16); larger problems return
+ * the process exits.  A call needs 65536 + A(D*T*N*G*H*4) + D*A(24*N*H)
+ * bytes, plus 2*A(T*N*D*H*elem) when num_layers > 1 (A = round up to 256,
+ * elem = 4 for RNN_F32, 2 for RNN_BF16); larger problems return
  * RNN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.  Every call on a device shares
@@ -309,13 +310,14 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
  * recurrent step's latency that no arithmetic removes, the term a latency
  * bound of the recurrence adds to the time of streaming W_hh and of the MMA.
  * It runs `steps` (2 .. 2^20) empty steps of the forward kernel's protocol for
- * batch N with one direction -- the same grid and clusters, the same waits
- * for the producers' step flags, the per-step cluster barrier and the flag
- * release, with no loads, no MMA and no gate math -- once to warm up and once
- * between two CUDA events on `stream`, synchronises `stream`, and returns the
- * average microseconds per step.  It touches only the handle's step flags and
+ * batch N with one direction -- the same grid and clusters, each block
+ * writing the exchange words of its units and polling those of its K slice,
+ * the per-step cluster barrier, with no MMA and no gate math -- once to warm
+ * up and once between two CUDA events on `stream`, synchronises `stream`, and
+ * returns the average microseconds per step.  It allocates (cudaMalloc) and
+ * frees a temporary exchange buffer of 24*N*H bytes and uses the handle's
  * status word.  RNN_ERR_UNSUPPORTED when the forward of batch N does not run
- * on the tensor-core recurrent kernel; a barrier timeout returns
+ * on the tensor-core recurrent kernel; a wait that runs out of time returns
  * RNN_ERR_TIMEOUT. */
 rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t steps,
                                        double* us_per_step);

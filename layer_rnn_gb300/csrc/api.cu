@@ -123,6 +123,12 @@ int64_t wf_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool trainin
   return b + 4096;
 }
 
+// exchange words of the tensor-core recurrent forward (every direction), taken
+// from the front of a call's scratch
+int64_t xchg_bytes(const rnn_handle* h, int64_t N) {
+  return h->D * align256((int64_t)rec_tc_xchg_bytes((int)N, (int)(h->G * h->H)));
+}
+
 // scratch the GEMM phases of one call need (maximum over the phases)
 int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool training) {
   const bool tf = h->dtype != RNN_BF16;
@@ -141,7 +147,7 @@ int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool train
     need = std::max(need, dgt + opnd_bytes(std::max(I_l, h->H), TN, tf) +
                               align256((int64_t)kMaxKsplit * GH * std::max(I_l, h->H) * 4));
   }
-  return std::max(need, wf_scratch_bytes(h, T, N, training)) + 4096;
+  return std::max(need, wf_scratch_bytes(h, T, N, training)) + 4096 + xchg_bytes(h, N);
 }
 
 struct Scratch {
@@ -596,6 +602,13 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
   RecPlan plan;
   s = plan_rec(h, false, N, &plan, h->D, lengths != nullptr);
   if (s != RNN_OK) return s;
+  unsigned long long* hx[2] = {nullptr, nullptr};
+  if (plan.tc) {
+    for (int d = 0; d < h->D; ++d) {
+      hx[d] = static_cast<unsigned long long*>(sc.take(rec_tc_xchg_bytes((int)N, (int)H)));
+      if (!hx[d]) return RNN_ERR_WORKSPACE_TOO_SMALL;
+    }
+  }
   const void* in = x;
   for (int l = 0; l < h->L; ++l) {
     void* out;
@@ -621,6 +634,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
       a.h0 = h0 ? cp<char>(h0, k * NH * e) : nullptr;
       a.c0 = (c0 && h->mode == RNN_LSTM) ? cp<float>(c0, k * NH * 4) : nullptr;
       a.y = out;
+      a.hx = hx[d];
       a.hy = hy ? mp<char>(hy, k * NH * e) : nullptr;
       a.cy = (cy && h->mode == RNN_LSTM) ? mp<float>(cy, k * NH * 4) : nullptr;
       if (training) {
@@ -880,6 +894,14 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
   Scratch sc;
   sc.base = ws + lay.at(RNN_WS_GEMM, 0, 0).off;
   sc.cap = lay.at(RNN_WS_GEMM, 0, 0).bytes;
+  // exchange words of the tensor-core backward, from the front of the scratch
+  unsigned long long* gxw[2] = {nullptr, nullptr};
+  if (plan.tc == 2 || (in_turn && plan_one.tc == 2)) {
+    for (int d = 0; d < h->D; ++d) {
+      gxw[d] = static_cast<unsigned long long*>(sc.take(rec_tc_xchg_bytes((int)N, (int)GH)));
+      if (!gxw[d]) return finish(h, st, RNN_ERR_WORKSPACE_TOO_SMALL);
+    }
+  }
   const void* dcur = dy;
   int dcur_bf16 = bf;
   for (int l = h->L - 1; l >= 0; --l) {
@@ -904,6 +926,7 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
       a.dgh = h->mode == RNN_GRU ? mp<char>(ws, lay.at(RNN_WS_DGH, l, d).off) : a.dgx;
       a.dh0 = dh0 ? mp<char>(dh0, k * NH * e) : nullptr;
       a.dc0 = (dc0 && h->mode == RNN_LSTM) ? mp<float>(dc0, k * NH * 4) : nullptr;
+      a.hx = gxw[d];
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
@@ -1228,10 +1251,17 @@ rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t
   rp.plan = pl;
   rp.fault_block = -1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* xbuf = nullptr;
+  if (cudaMalloc(&xbuf, rec_tc_xchg_bytes((int)N, (int)h->H)) != cudaSuccess) return RNN_ERR_CUDA;
+  rp.dir[0].hx = static_cast<unsigned long long*>(xbuf);
   cudaEvent_t e0, e1;
-  if (cudaEventCreate(&e0) != cudaSuccess) return RNN_ERR_CUDA;
+  if (cudaEventCreate(&e0) != cudaSuccess) {
+    cudaFree(xbuf);
+    return RNN_ERR_CUDA;
+  }
   if (cudaEventCreate(&e1) != cudaSuccess) {
     cudaEventDestroy(e0);
+    cudaFree(xbuf);
     return RNN_ERR_CUDA;
   }
   s = RNN_OK;
@@ -1249,6 +1279,8 @@ rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
   if (s == RNN_OK) s = read_status(h, st);
+  if (cudaStreamSynchronize(st) != cudaSuccess && s == RNN_OK) s = RNN_ERR_CUDA;
+  cudaFree(xbuf);
   if (s == RNN_OK) *us_per_step = (double)ms * 1e3 / (double)steps;
   return s;
 }
@@ -1336,7 +1368,7 @@ extern "C" rnn_status_t rnn_forward_inference_static(rnn_t h, void* stream, int6
   const int64_t gx_bytes = align256(h->D * T * N * h->G * h->H * 4);
   const int64_t yb = align256(T * N * h->D * h->H * esize(h));
   const int64_t need = (int64_t)kSyncBytes + gx_bytes + (h->L > 1 ? 2 * yb : 0);
-  if (need > (int64_t)kStaticScratchBytes) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  if (need + xchg_bytes(h, N) > (int64_t)kStaticScratchBytes) return RNN_ERR_WORKSPACE_TOO_SMALL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_CUDA;
   if (h->device >= 0 && h->device != dev) return RNN_ERR_INVALID_ARG;  // one device per handle

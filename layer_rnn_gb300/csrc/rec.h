@@ -21,6 +21,11 @@ struct RecDirArgs {
   float* cseq = nullptr;         // [T+1][N][H] or null
   void* hy = nullptr;            // [N][H] or null
   float* cy = nullptr;           // [N][H] or null
+  // tensor-core kernels: exchange words of the step outputs the other blocks
+  // read, value bits | step << 32 -- forward h [3][N][H]
+  // (rec_tc_xchg_bytes(N, H) bytes), backward dG_h [3][N][G*H]
+  // (rec_tc_xchg_bytes(N, G*H) bytes)
+  unsigned long long* hx = nullptr;
   // backward
   const void* dy = nullptr;      // row (t*N+n)*lddy, column d*H + j
   int dy_bf16 = 0;
@@ -99,6 +104,9 @@ cudaError_t rec_cluster_launch(bool backward, const RecParams& p, cudaStream_t s
 bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
                  const int* max_clusters, RecPlan* out);
 cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st);
+// bytes of one direction's exchange words of a tensor-core recurrent kernel
+// whose step output is [N][width] (forward width = H, backward G*H)
+size_t rec_tc_xchg_bytes(int N, int width);
 // The tensor-core forward's step protocol with no work (flag waits, cluster
 // barrier, flag release), p.T steps, same plan and grid as rec_tc_launch.
 cudaError_t rec_tc_probe_launch(const RecParams& p, cudaStream_t st);

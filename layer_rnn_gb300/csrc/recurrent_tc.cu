@@ -79,6 +79,7 @@ constexpr int kTThreads = 256;
 constexpr int kTWarps = kTThreads / 32;
 constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
 constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
+constexpr int kPollRows = 16;   // exchange rows a lane polls at once
 
 __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
   const int r = j / Ur;
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                        a_col + (uint32_t)(BF ? Kp / 2 : Kp) > ncols || ncols > 512u ||
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Mb > kTM || N > Nm ||
                        Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
-                       pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > 32;
+                       pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > 32 || a.hx == nullptr ||
+                       (H & 1) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     s_mma_bad = 0;
@@ -284,7 +286,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   }
   for (int uu = tid; uu < Uqc; uu += kTThreads)
     s_bhn[uu] = p.mode == 2 ? to_f(reinterpret_cast<const T*>(a.bhh)[2 * H + u0 + uq0 + uu]) : 0.f;
-  unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
   T* y = reinterpret_cast<T*>(a.y);
   T* hseq = reinterpret_cast<T*>(a.hseq);
   // kind::f16 with bf16 (1) or fp16 (0) operands, fp32 accumulate
@@ -294,6 +295,19 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   __syncthreads();
   fence_after();
   uint32_t mma_phase = 0;  // parity of the next completion of the MMA barrier
+  // step-invariant index work, once: this thread's accumulator row (the
+  // epilogue) and its first pointwise item
+  int e_g, e_uo, e_owner;
+  bool e_row_ok;
+  {
+    const int m = (warp & 3) * 32 + lane;
+    e_g = m / Ur;
+    const int u = m - e_g * Ur;
+    e_row_ok = m < Mb && e_g < G && u < Urc;
+    e_owner = e_row_ok ? u / Uq : 0;
+    e_uo = u - e_owner * Uq;
+  }
+  const int i_uu = Uqc > 0 ? tid % Uqc : 0, i_n = Uqc > 0 ? tid / Uqc : 0;
 
   for (int s = 0; s < nT; ++s) {
     const int t = d ? nT - 1 - s : s;
@@ -315,47 +329,80 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     const T* src = s == 0 ? reinterpret_cast<const T*>(a.h0)
                           : y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
     const int64_t ldsrc = s == 0 ? H : p.ldy;
-    // 1. staging: task (atom, row part) -> warp; each warp waits only for the
-    // producers of its atom's units, then stages its rows of h_{t-1}[n][atom]
-    // as B (fp16 hi / lo for fp32)
+    // 1. staging: task (atom, row part) -> warp.  Step 0 stages h0 from
+    // memory; later steps poll the tagged exchange words of h_{t-1} written by
+    // the producers of the atom's units (value and step in one 8-byte word, so
+    // the data is its own flag: no release fence on the writer's side, no
+    // second round trip on the reader's) and stage them as B (fp16 hi / lo
+    // for fp32).
     const int parts = max(1, kTWarps / max(1, KCu));
     if (have) {
+      const unsigned long long* hxp = a.hx + (size_t)((s + 2) % 3) * N * H + k0;
       for (int task = warp; task < KCu * parts; task += kTWarps) {
         const int at = task % KCu, part = task / KCu;
         const int ka = at * EPA, kn = min(EPA, Kc - ka);
-        if (s > 0 &&
-            !warp_wait_flags(flags, p.flag_stride, owner_of(k0 + ka, Ur, Uq, Pk),
-                             owner_of(k0 + ka + kn - 1, Ur, Uq, Pk), (unsigned)s, p.status,
-                             p.timeout_ns, p.spin_ns) &&
-            lane == 0)
-          s_fail = 1;  // the data is not used: the status word already holds the failure
+        const int nr = (N - part + parts - 1) / parts;  // rows part, part + parts, ...
         unsigned char* bh = base + Lo.b_hi + (uint32_t)at * atom_bytes;
         unsigned char* bl = base + Lo.b_lo + (uint32_t)at * atom_bytes;
-        // 16-byte chunk c of row n holds K elements ka + 8c .. +7; this task
-        // takes rows part, part + parts, ...
-        for (int idx = lane; idx < ((N - part + parts - 1) / parts) * 8; idx += 32) {
-          const int n = part + (idx >> 3) * parts, c = idx & 7;
-          const uint32_t off = sw_off(n, c);
-          const bool in = src != nullptr && c * 8 < kn;
-          const T* sp = src + k0 + ka + c * 8 + (int64_t)n * ldsrc;
-          if (BF) {
-            const uint4 v = in ? ldcg16(sp) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(bh + off) = v;
-          } else {
-            // K slices are multiples of 4 fp32 elements: the last chunk of a
-            // slice may hold only its first half
-            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-            if (in) {
-              v0 = ldcg16(sp);
-              if (c * 8 + 4 < kn) v1 = ldcg16(sp + 4);
+        if (s == 0) {
+          // 16-byte chunk c of row n holds K elements ka + 8c .. +7
+          for (int idx = lane; idx < nr * 8; idx += 32) {
+            const int n = part + (idx >> 3) * parts, c = idx & 7;
+            const uint32_t off = sw_off(n, c);
+            const bool in = src != nullptr && c * 8 < kn;
+            const T* sp = src + k0 + ka + c * 8 + (int64_t)n * ldsrc;
+            if (BF) {
+              const uint4 v = in ? ldcg16(sp) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(bh + off) = v;
+            } else {
+              // K slices are multiples of 4 fp32 elements: the last chunk of a
+              // slice may hold only its first half
+              uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+              if (in) {
+                v0 = ldcg16(sp);
+                if (c * 8 + 4 < kn) v1 = ldcg16(sp + 4);
+              }
+              uint4 h4, l4;
+              split_f16x2(__uint_as_float(v0.x) * h_scale, __uint_as_float(v0.y) * h_scale, h4.x, l4.x);
+              split_f16x2(__uint_as_float(v0.z) * h_scale, __uint_as_float(v0.w) * h_scale, h4.y, l4.y);
+              split_f16x2(__uint_as_float(v1.x) * h_scale, __uint_as_float(v1.y) * h_scale, h4.z, l4.z);
+              split_f16x2(__uint_as_float(v1.z) * h_scale, __uint_as_float(v1.w) * h_scale, h4.w, l4.w);
+              *reinterpret_cast<uint4*>(bh + off) = h4;
+              *reinterpret_cast<uint4*>(bl + off) = l4;
             }
-            uint4 h4, l4;
-            split_f16x2(__uint_as_float(v0.x) * h_scale, __uint_as_float(v0.y) * h_scale, h4.x, l4.x);
-            split_f16x2(__uint_as_float(v0.z) * h_scale, __uint_as_float(v0.w) * h_scale, h4.y, l4.y);
-            split_f16x2(__uint_as_float(v1.x) * h_scale, __uint_as_float(v1.y) * h_scale, h4.z, l4.z);
-            split_f16x2(__uint_as_float(v1.z) * h_scale, __uint_as_float(v1.w) * h_scale, h4.w, l4.w);
-            *reinterpret_cast<uint4*>(bh + off) = h4;
-            *reinterpret_cast<uint4*>(bl + off) = l4;
+          }
+        } else {
+          // lane l holds units 2l, 2l+1 of the atom (the 4-byte word l & 3 of
+          // 16-byte chunk l >> 2 in the swizzled row), up to kPollRows rows in
+          // flight at once
+          const bool lane_in = 2 * lane < kn;
+          const uint32_t woff = (uint32_t)(lane & 3) * 4u;
+          for (int r0 = 0; r0 < nr; r0 += kPollRows) {
+            const int nb = min(kPollRows, nr - r0);
+            unsigned long long w0[kPollRows], w1[kPollRows];
+            if (!poll_tagged<kPollRows>(hxp + ka + 2 * lane, part + r0 * parts, parts, H, nb,
+                                        lane_in, (unsigned)s, w0, w1, p.status, p.timeout_ns) &&
+                lane == 0)
+              s_fail = 1;  // the data is not used: the status word holds the failure
+            if (lane_in) {
+#pragma unroll
+              for (int j = 0; j < kPollRows; ++j) {
+                if (j >= nb) break;
+                const int n = part + (r0 + j) * parts;
+                const uint32_t off = sw_off(n, lane >> 2) + woff;
+                const float f0 = __uint_as_float((uint32_t)w0[j]);
+                const float f1 = __uint_as_float((uint32_t)w1[j]);
+                if (BF) {
+                  *reinterpret_cast<uint32_t*>(bh + off) =
+                      (__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16);
+                } else {
+                  uint32_t hw, lw;
+                  split_f16x2(f0 * h_scale, f1 * h_scale, hw, lw);
+                  *reinterpret_cast<uint32_t*>(bh + off) = hw;
+                  *reinterpret_cast<uint32_t*>(bl + off) = lw;
+                }
+              }
+            }
           }
         }
         WTRACE(s, at);
@@ -415,10 +462,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     float* recv = recv0 + (size_t)(s & 1) * Pk * G * Uq * Rs;
     if (!failed) {
       const int quarter = warp & 3;
-      const int m = quarter * 32 + lane;
-      const int g = m / Ur, u = m - g * Ur;
-      const bool row_ok = m < Mb && g < G && u < Urc;
-      const int owner = row_ok ? u / Uq : 0, uo = u - owner * Uq;
+      const int g = e_g, uo = e_uo, owner = e_owner;
+      const bool row_ok = e_row_ok;
       const bool ok = have && mma_ok;
       const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);
       for (int c0 = (warp >> 2) * 16; c0 < N; c0 += (kTWarps / 4) * 16) {
@@ -464,7 +509,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       // the partial sums of each gate (rank order, fixed) feed the gate math
       const size_t rstride = (size_t)G * Uq * Rs;
       for (int it = tid; it < items; it += kTThreads) {
-        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
+        const int j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
         float* sv = stash + n * Uq + uu;        // likewise
@@ -498,18 +544,23 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           h = tanhf(gv[0] + ov[0]);
         }
         hst[n * Uq + uu] = h;
-        y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(h);
+        const T hs = from_f<T>(h);
+        y[row * p.ldy + (int64_t)d * H + j] = hs;
+        // the exchange word of h_t: its value as stored (what y holds) and the
+        // step that reads it
+        if (s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
+          st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + j,
+                         ((unsigned long long)(s + 1) << 32) | __float_as_uint(to_f(hs)));
       }
     }
     __syncthreads();
     TTRACE(s, 4);
-    if (live && tid == 0 && s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
-      publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
     TTRACE(s, 5);
     // workspace stores of the step, after the release
     if (live) {
       for (int it = tid; it < items; it += kTThreads) {
-        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
+        const int j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         const int slot = d ? t : t + 1;
         const float* sv = stash + n * Uq + uu;
@@ -544,47 +595,59 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                  : "memory");
 }
 
-// The forward kernel's step protocol with no work: per step, each warp waits
-// for the flags of its atoms' producers, one block barrier, the cluster
-// barrier, one block barrier and the flag release -- the part of a step's
-// latency that no arithmetic removes.  Same grid, clusters and waits as
-// rec_fwd_tc; bounded like it.
+// The forward kernel's step protocol with no work: per step, each block
+// writes the exchange words of its units, each warp polls the words of its
+// atoms' units, one block barrier, the cluster barrier, one block barrier --
+// the part of a step's latency that no arithmetic removes.  Same grid,
+// clusters, exchange words and waits as rec_fwd_tc; bounded like it.
 __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_constant__ RecParams p) {
   __shared__ int s_fail;
   const RecPlan& pl = p.plan;
   const int P = pl.P, Pk = pl.cluster;
   const int d = blockIdx.x / P;
   const int b = blockIdx.x - d * P;
-  const int q = b % Pk;
-  const int H = p.H, Ur = pl.Ur, Uq = pl.Uq;
+  const int r = b / Pk, q = b % Pk;
+  const RecDirArgs& a = p.dir[d];
+  const int H = p.H, N = p.N, Ur = pl.Ur, Uq = pl.Uq;
+  const int u0 = r * Ur, Urc = min(Ur, H - u0);
+  const int uq0 = q * Uq, Uqc = max(0, min(Uq, Urc - uq0));
   const int k0 = q * pl.Kk, Kc = max(0, min(pl.Kk, H - k0));
   const int EPA = 64, KCu = (Kc + EPA - 1) / EPA;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q;
+  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || a.hx == nullptr;
   if (threadIdx.x == 0) {
     s_fail = cfg_bad;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
   }
   __syncthreads();
-  unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
   const int parts = max(1, kTWarps / max(1, KCu));
   for (int s = 0; s < p.T; ++s) {
     const bool failed = s_fail != 0;
     if (!failed && s > 0) {
+      const unsigned long long* hxp = a.hx + (size_t)((s + 2) % 3) * N * H + k0;
       for (int task = warp; task < KCu * parts; task += kTWarps) {
-        const int ka = (task % KCu) * EPA, kn = min(EPA, Kc - ka);
-        if (!warp_wait_flags(flags, p.flag_stride, owner_of(k0 + ka, Ur, Uq, Pk),
-                             owner_of(k0 + ka + kn - 1, Ur, Uq, Pk), (unsigned)s, p.status,
-                             p.timeout_ns, p.spin_ns) &&
-            lane == 0)
-          s_fail = 1;
+        const int at = task % KCu, part = task / KCu;
+        const int ka = at * EPA, kn = min(EPA, Kc - ka);
+        const int nr = (N - part + parts - 1) / parts;
+        for (int r0 = 0; r0 < nr; r0 += kPollRows) {
+          unsigned long long w0[kPollRows], w1[kPollRows];
+          if (!poll_tagged<kPollRows>(hxp + ka + 2 * lane, part + r0 * parts, parts, H,
+                                      min(kPollRows, nr - r0), 2 * lane < kn, (unsigned)s, w0,
+                                      w1, p.status, p.timeout_ns) &&
+              lane == 0)
+            s_fail = 1;
+        }
       }
     }
     __syncthreads();
     cl_sync();
     __syncthreads();
-    if (!failed && s_fail == 0 && threadIdx.x == 0 && s + 1 < p.T)
-      publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
+    if (!failed && s_fail == 0 && s + 1 < p.T)
+      for (int it = threadIdx.x; it < Uqc * N; it += kTThreads) {
+        const int uu = it % Uqc, n = it / Uqc;
+        st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + u0 + uq0 + uu,
+                       (unsigned long long)(s + 1) << 32);
+      }
   }
   cl_sync();
 }
@@ -597,8 +660,11 @@ cudaError_t rec_tc_probe_launch(const RecParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
-  if (e != cudaSuccess) return e;
+  for (int d = 0; d < p.D; ++d) {
+    if (!p.dir[d].hx) return cudaErrorInvalidValue;
+    e = cudaMemsetAsync(p.dir[d].hx, 0, rec_tc_xchg_bytes(p.N, p.H), st);
+    if (e != cudaSuccess) return e;
+  }
   RecParams copy = p;
   void* args[] = {&copy};
   cudaLaunchConfig_t cfg = {};
@@ -616,6 +682,8 @@ cudaError_t rec_tc_probe_launch(const RecParams& p, cudaStream_t st) {
   g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
+
+size_t rec_tc_xchg_bytes(int N, int H) { return (size_t)3 * N * H * 8; }
 
 bool rec_tc_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_t smem_limit,
                  const int* max_clusters, RecPlan* out) {
@@ -693,8 +761,12 @@ cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
-  if (e != cudaSuccess) return e;
+  // exchange words from an earlier launch must not look current: tags start at 1
+  for (int d = 0; d < p.D; ++d) {
+    if (!p.dir[d].hx) return cudaErrorInvalidValue;
+    e = cudaMemsetAsync(p.dir[d].hx, 0, rec_tc_xchg_bytes(p.N, p.H), st);
+    if (e != cudaSuccess) return e;
+  }
   RecParams copy = p;
   void* args[] = {&copy};
   cudaLaunchConfig_t cfg = {};

@@ -7,15 +7,27 @@
 // with j over the G*H gate rows.  The contraction is K = G*H long, so the
 // blocks of a cluster (up to 16, a non-portable cluster size) split it: block
 // (r, q) keeps W_hh^T for the Ur units of row group r and the gate rows
-// k0 .. k0+Kk-1 in tensor memory as the MMA's A operand (fp32: tf32 hi and lo
-// parts, three passes; bf16: one pass, two elements per 32-bit column), stages
-// the previous step's dG_h slice as the swizzled K-major B operand, and pushes
-// each row of the accumulator over distributed shared memory (16-byte stores)
-// to the block that owns the unit's pointwise step.  The owners sum the Pk
-// partials in a fixed order, run the gate-gradient chain, store dG_x (and
-// dG_h for the GRU) and release their step flag.  The pointwise inputs of the
-// step (dy, the saved gates, c_t and c_{t-1}) are fetched with cp.async at
-// the start of the step, so their latency hides behind the contraction.
+// k0 .. k0+Kk-1 in tensor memory as the MMA's A operand and stages the
+// previous step's dG_h slice as the swizzled K-major B operand.
+//
+// fp32 operands are split into fp16 pairs, x = (hi + lo * 2^-11) / scale
+// (hi = fp16(x * scale), lo = fp16((x * scale - hi) * 2^11)), with power-of-
+// two scales per block: W_hh^T's from its slice once, dG_h's from the staged
+// slice of every step (gradients have no fixed range), so the slice's largest
+// magnitude maps just below 2^14.  The product keeps hi*hi + hi*lo + lo*hi:
+// three passes of 16 K, each issued by its own thread into its own
+// accumulator, about 22 significant bits per operand as three tf32 passes,
+// in half the MMA instructions.  bf16 runs one pass.
+//
+// Per step: warps poll the exchange words of their K atoms -- each 8-byte word
+// holds a dG_h value and the step that reads it, written by the owner of the
+// gate row, so the data is its own flag -- and stage them; one block barrier;
+// the MMAs; the accumulator rows go over distributed shared memory (16-byte
+// stores) to the block that owns each unit's pointwise step; one cluster
+// barrier; the owners sum the Pk partials in a fixed order, run the gate-
+// gradient chain, and write dG_h with its exchange words (GRU: dG_x, which no
+// block of this launch reads, after the step's barrier).  The step's pointwise inputs (dy, the saved gates, c_t
+// and c_{t-1}) are fetched with cp.async at the start of the step.
 #include <algorithm>
 #include <type_traits>
 
@@ -43,8 +55,11 @@ namespace {
 using namespace tc;
 
 constexpr int kBThreads = 256;
+constexpr int kBWarps = kBThreads / 32;
 constexpr int kBM = 128;    // MMA M: output units per row group (padded)
 constexpr int kNIn = 7;     // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1} / h_{t-1}
+constexpr int kBMaxAtoms = 16;
+constexpr int kBPollRows = 16;  // exchange rows a lane polls at once
 
 __device__ __forceinline__ int owner_flag_b(int u, int Ur, int Uq, int Pk) {
   const int r = u / Ur;
@@ -53,9 +68,10 @@ __device__ __forceinline__ int owner_flag_b(int u, int Ur, int Uq, int Pk) {
 
 struct BLayout {
   uint32_t b_hi, b_lo;   // staged B tiles: KC atoms x (Nm rows x 128 bytes)
-  uint32_t recv;         // [2][Pk][Uq][Nm] f32
-  uint32_t outs;         // [N][Uq] f32 summed partials
+  uint32_t raw;          // fp32: the staged dG_h slice before its split, [N][Kp + 4]
+  uint32_t recv;         // [2][Pk][Uq][Nm + 4] f32
   uint32_t st_dc, st_carry;  // [Uq*N] f32: LSTM dc, GRU dh*z
+  uint32_t stash;        // [3][Uq*N] f32: GRU dG_x, stored after the release
   uint32_t pin;          // [kNIn][Uq*N] f32
   uint32_t total;
 };
@@ -69,14 +85,16 @@ __host__ __device__ inline BLayout b_layout(const RecPlan& pl, int N, bool bf) {
   off += ntile;
   L.b_lo = off;
   off += bf ? 0 : ntile;
+  L.raw = off;
+  off += bf ? 0 : (uint32_t)N * (pl.K + 4) * 4u;
   L.recv = off;
-  off += 2u * pl.cluster * pl.Uq * pl.nbp * 4u;
-  L.outs = off;
-  off += (uint32_t)pl.Uq * N * 4u;
+  off += 2u * pl.cluster * pl.Uq * (pl.nbp + 4) * 4u;
   L.st_dc = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.st_carry = off;
   off += (uint32_t)pl.Uq * N * 4u;
+  L.stash = off;
+  off += 3u * pl.Uq * N * 4u;
   L.pin = off;
   off += (uint32_t)kNIn * pl.Uq * N * 4u;
   L.total = (off + 1023u) & ~1023u;
@@ -86,10 +104,14 @@ __host__ __device__ inline BLayout b_layout(const RecPlan& pl, int N, bool bf) {
 template <bool BF>
 __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant__ RecParams p) {
   typedef typename std::conditional<BF, bf16, float>::type T;
+  constexpr int NI = BF ? 1 : 3;     // issuing threads = accumulators (one per pass)
+  constexpr int EPA = 64;            // K elements (16-bit) per 128-byte atom
+  constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_fail;
+  __shared__ int s_fail, s_mma_bad;
+  __shared__ float s_red[kBWarps];
   const RecPlan& pl = p.plan;
   const int P = pl.P, Pk = pl.cluster;
   const int d = blockIdx.x / P;
@@ -104,33 +126,41 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   const int uq0 = q * Uq, Uqc = max(0, min(Uq, Urc - uq0));
   const int k0 = q * pl.Kk;
   const int Kc = (int)max((int64_t)0, min((int64_t)pl.Kk, GH - k0));
+  const int KCu = (Kc + EPA - 1) / EPA;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   const uint32_t base_s = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
   const BLayout Lo = b_layout(pl, N, BF);
+  float* raw = reinterpret_cast<float*>(base + Lo.raw);
   float* recv0 = reinterpret_cast<float*>(base + Lo.recv);
-  float* outs = reinterpret_cast<float*>(base + Lo.outs);
   float* st_dc = reinterpret_cast<float*>(base + Lo.st_dc);
   float* st_carry = reinterpret_cast<float*>(base + Lo.st_carry);
+  float* stash = reinterpret_cast<float*>(base + Lo.stash);
   float* pin = reinterpret_cast<float*>(base + Lo.pin);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
-  const uint32_t bar = smem_addr(&mma_bar);
-  const uint32_t a_col = (uint32_t)Nm;
-  const uint32_t a_lo_col = (uint32_t)(Nm + Kp);
+  const uint32_t mbar = smem_addr(&mma_bar);
+  // tensor memory: accumulator i at column i * Nm, then the A operands, two
+  // 16-bit elements per column: W^T (bf16) or its hi and lo halves (fp32)
+  const uint32_t a_col = (uint32_t)(NI * Nm);
+  const uint32_t a_lo_col = a_col + (uint32_t)(Kp / 2);
   const uint32_t ncols = (uint32_t)pl.lda;
   const int items = Uqc * N;
   const int icap = Uq * N;  // stride of one input array in pin
+  const int Rs = Nm + 4;    // exchange row stride (floats)
+  const int Ks = Kp + 4;    // raw staging row stride (floats)
 
   const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q ||
-                       (uint32_t)(Nm + (BF ? Kp / 2 : 2 * Kp)) > ncols || ncols > 512u ||
+                       a_col + (uint32_t)(BF ? Kp / 2 : Kp) > ncols || ncols > 512u ||
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Ur > kBM || N > Nm ||
-                       Nm % 16 != 0 || Nm > 256 || Kp % (BF ? 64 : 32) != 0 || pl.Kk > Kp ||
-                       Uq * Pk < Ur;
+                       Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
+                       pl.KC > kBMaxAtoms || pl.Kk > Kp || Uq * Pk < Ur || Pk > 32 ||
+                       a.hx == nullptr || (GH & 1) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
+    s_mma_bad = 0;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    mbar_init(mbar, NI);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && !cfg_bad) {
@@ -140,39 +170,57 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // staged tiles zero: rows >= N and columns >= Kc stay zero
   for (uint32_t i = tid; i < Lo.recv / 16u; i += kBThreads)
     reinterpret_cast<uint4*>(base)[i] = make_uint4(0, 0, 0, 0);
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
+  const T* W = reinterpret_cast<const T*>(a.whh);
 
-  // A = W_hh^T slice into tensor memory: lane m = unit u0 + m, columns = gate
-  // rows k0 + jj; lanes of a warp read consecutive units of one W_hh row
+  // W^T's split scale (fp32): its slice's largest magnitude just below 2^14
+  int ew = 0;
+  float w_scale = 1.f;
+  if (!BF) {
+    float wm = 0.f;
+    if (!cfg_bad)
+      for (int idx = tid; idx < Kc * Urc; idx += kBThreads) {
+        const int jj = idx / Urc, m = idx - jj * Urc;
+        wm = fmaxf(wm, fabsf(to_f(W[(int64_t)(k0 + jj) * H + u0 + m])));
+      }
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+    if (lane == 0) s_red[warp] = wm;
+    __syncthreads();
+    wm = 0.f;
+    for (int w = 0; w < kBWarps; ++w) wm = fmaxf(wm, s_red[w]);
+    __syncthreads();
+    if (wm > 0.f) (void)frexpf(wm, &ew);
+    ew = min(max(14 - ew, -100), 100);
+    w_scale = ldexpf(1.f, ew);
+  }
+
+  // A = W_hh^T slice into tensor memory: lane m = unit u0 + m, columns =
+  // gate-row pairs (k0 + jj, k0 + jj + 1); lanes of a warp read consecutive
+  // units of one W_hh row
   if (!cfg_bad) {
-    const T* W = reinterpret_cast<const T*>(a.whh);
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const bool row_ok = m < Urc;
-    const int epc = BF ? 64 : 32;
-    const int nchunk = Kp / epc;
+    const int nchunk = pl.KC;  // 32 columns = 64 gate rows per chunk
     for (int ci = warp >> 2; ci < nchunk; ci += kBThreads / 128) {
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
+        const int jj = ci * 64 + 2 * i;
+        const float e0 = (row_ok && jj < Kc) ? to_f(W[(int64_t)(k0 + jj) * H + u0 + m]) : 0.f;
+        const float e1 =
+            (row_ok && jj + 1 < Kc) ? to_f(W[(int64_t)(k0 + jj + 1) * H + u0 + m]) : 0.f;
         if (BF) {
-          const int jj = ci * 64 + 2 * i;
-          const float e0 = (row_ok && jj < Kc) ? to_f(W[(int64_t)(k0 + jj) * H + u0 + m]) : 0.f;
-          const float e1 =
-              (row_ok && jj + 1 < Kc) ? to_f(W[(int64_t)(k0 + jj + 1) * H + u0 + m]) : 0.f;
           hi[i] = (__float_as_uint(e0) >> 16) | ((__float_as_uint(e1) >> 16) << 16);
           lo[i] = 0;
         } else {
-          const int jj = ci * 32 + i;
-          const float v = (row_ok && jj < Kc) ? to_f(W[(int64_t)(k0 + jj) * H + u0 + m]) : 0.f;
-          const uint32_t hb = __float_as_uint(v) & 0xFFFFE000u;
-          hi[i] = hb;
-          lo[i] = __float_as_uint(v - __uint_as_float(hb));
+          split_f16x2(e0 * w_scale, e1 * w_scale, hi[i], lo[i]);
         }
       }
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -189,23 +237,22 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     st_dc[it] = a.dcy ? a.dcy[(int64_t)n * H + j] : 0.f;
     st_carry[it] = 0.f;
   }
-  unsigned* flags = p.flags + (size_t)d * P * p.flag_stride;
   T* dgx = reinterpret_cast<T*>(a.dgx);
   T* dgh = reinterpret_cast<T*>(a.dgh);
   const T* hseq = reinterpret_cast<const T*>(a.hseq);
-  const uint32_t idesc = (1u << 4) | ((BF ? 1u : 2u) << 7) | ((BF ? 1u : 2u) << 10) |
+  // kind::f16 with bf16 (1) or fp16 (0) operands, fp32 accumulate
+  const uint32_t idesc = (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) |
                          ((uint32_t)(Nm >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-  const int kstep = BF ? 16 : 8;
-  const int nsteps = (Kc + kstep - 1) / kstep;
+  const int parts = max(1, kBWarps / max(1, KCu));
   fence_before();
   __syncthreads();
   fence_after();
-  bool failed = s_fail != 0;
-  uint32_t phase = 0;
+  uint32_t mma_phase = 0;
 
   for (int s = 0; s <= nT; ++s) {
     const int t = rv ? s : nT - 1 - s;   // time processed at this step (s < nT)
     const int tp = rv ? s - 1 : nT - s;  // time processed at the previous step (s > 0)
+    const bool failed = s_fail != 0;     // read after the previous step's barrier
     BTRACE(s, 0);
     // pointwise inputs of time t (fp32 sources by cp.async; bf16 ones are read
     // in the pointwise loop)
@@ -234,116 +281,171 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
       }
     }
     cp_async_commit();
-    // the previous step's dG_h slice: wait for the blocks that own its units
-    if (!failed && s > 0 && Kc > 0 && warp == 0) {
-      bool ok = true;
-      for (int g = 0; g < G && ok; ++g) {
-        const int lo = max(k0, g * H), hi = min(k0 + Kc, (g + 1) * H);
-        if (lo < hi)
-          ok = warp_wait_flags(flags, p.flag_stride, owner_flag_b(lo - g * H, Ur, Uq, Pk),
-                               owner_flag_b(hi - 1 - g * H, Ur, Uq, Pk), (unsigned)s, p.status,
-                               p.timeout_ns, p.spin_ns);
-      }
-      if (!ok && lane == 0) s_fail = 1;
-    }
-    __syncthreads();
-    BTRACE(s, 1);
-    failed = s_fail != 0;
     const bool have = !failed && s > 0 && Kc > 0;
+    // 1. staging of the previous step's dG_h slice: task (atom, row part) ->
+    // warp; the warp polls the exchange words of its atom (value and step in
+    // one 8-byte word, written by the owners of those gate rows: the data is
+    // its own flag) and stages them as B (bf16) or as raw fp32 until the
+    // step's scale is known
+    float lmax = 0.f;
     if (have) {
-      constexpr int VE = 16 / (int)sizeof(T);
-      const int nv = Kc / VE;
-      const T* src = dgh + (int64_t)tp * N * GH + k0;
-      for (int idx = tid; idx < N * nv; idx += kBThreads) {
-        const int n = idx / nv, c16 = idx - n * nv;
-        const uint4 v = ldcg16(src + (int64_t)n * GH + c16 * VE);
-        const int atom = c16 >> 3, c = c16 & 7;
-        const uint32_t off = (uint32_t)atom * atom_bytes + sw_off(n, c);
-        if (BF) {
-          *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = v;
-        } else {
+      const unsigned long long* gxp = a.hx + (size_t)((s + 2) % 3) * N * GH + k0;
+      for (int task = warp; task < KCu * parts; task += kBWarps) {
+        const int at = task % KCu, part = task / KCu;
+        const int ka = at * EPA, kn = min(EPA, Kc - ka);
+        const int nr = (N - part + parts - 1) / parts;  // rows part, part + parts, ...
+        const bool lane_in = 2 * lane < kn;  // lane l: gate rows ka + 2l, ka + 2l + 1
+        for (int r0 = 0; r0 < nr; r0 += kBPollRows) {
+          const int nb = min(kBPollRows, nr - r0);
+          unsigned long long w0[kBPollRows], w1[kBPollRows];
+          if (!poll_tagged<kBPollRows>(gxp + ka + 2 * lane, part + r0 * parts, parts, GH, nb,
+                                       lane_in, (unsigned)s, w0, w1, p.status, p.timeout_ns) &&
+              lane == 0)
+            s_fail = 1;  // the data is not used: the status word holds the failure
+          if (!lane_in) continue;
+#pragma unroll
+          for (int j = 0; j < kBPollRows; ++j) {
+            if (j >= nb) break;
+            const int n = part + (r0 + j) * parts;
+            const float f0 = __uint_as_float((uint32_t)w0[j]);
+            const float f1 = __uint_as_float((uint32_t)w1[j]);
+            if (BF) {
+              *reinterpret_cast<uint32_t*>(base + Lo.b_hi + (uint32_t)at * atom_bytes +
+                                           sw_off(n, lane >> 2) + (uint32_t)(lane & 3) * 4u) =
+                  (__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16);
+            } else {
+              *reinterpret_cast<float2*>(raw + n * Ks + ka + 2 * lane) = make_float2(f0, f1);
+              lmax = fmaxf(lmax, fmaxf(fabsf(f0), fabsf(f1)));
+            }
+          }
+        }
+      }
+    }
+    float out_scale = 1.f;
+    if (!BF) {
+      // the step's dG_h scale, then the split into the B tiles
+      for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+      if (lane == 0) s_red[warp] = lmax;
+      __syncthreads();
+      if (have) {
+        float hm = 0.f;
+        for (int w = 0; w < kBWarps; ++w) hm = fmaxf(hm, s_red[w]);
+        int eh = 0;
+        if (hm > 0.f) (void)frexpf(hm, &eh);
+        eh = min(max(14 - eh, -100), 100);
+        const float h_scale = ldexpf(1.f, eh);
+        out_scale = ldexpf(1.f, -(ew + eh));
+        for (int idx = tid; idx < N * KCu * 8; idx += kBThreads) {
+          const int c = idx & 7, at = (idx >> 3) % KCu, n = (idx >> 3) / KCu;
+          const float* rp = raw + n * Ks + at * EPA + c * 8;
+          const float4 v0 = *reinterpret_cast<const float4*>(rp);
+          const float4 v1 = *reinterpret_cast<const float4*>(rp + 4);
           uint4 h4, l4;
-          h4.x = v.x & 0xFFFFE000u; l4.x = __float_as_uint(__uint_as_float(v.x) - __uint_as_float(h4.x));
-          h4.y = v.y & 0xFFFFE000u; l4.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h4.y));
-          h4.z = v.z & 0xFFFFE000u; l4.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h4.z));
-          h4.w = v.w & 0xFFFFE000u; l4.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h4.w));
+          split_f16x2(v0.x * h_scale, v0.y * h_scale, h4.x, l4.x);
+          split_f16x2(v0.z * h_scale, v0.w * h_scale, h4.y, l4.y);
+          split_f16x2(v1.x * h_scale, v1.y * h_scale, h4.z, l4.z);
+          split_f16x2(v1.z * h_scale, v1.w * h_scale, h4.w, l4.w);
+          const uint32_t off = (uint32_t)at * atom_bytes + sw_off(n, c);
           *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = h4;
           *reinterpret_cast<uint4*>(base + Lo.b_lo + off) = l4;
         }
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    fence_before();
     __syncthreads();
-    fence_after();
-    BTRACE(s, 6);
-    if (have && tid == 0) {
-      for (int ks = 0; ks < nsteps; ++ks) {
-        const uint32_t atom = (uint32_t)(ks >> 2), kk = (uint32_t)(ks & 3);
-        const uint64_t bh = b_desc(base_s + Lo.b_hi + atom * atom_bytes) + kk * 2;
-        const uint32_t acc0 = ks > 0 ? 1u : 0u;
-        if (BF) {
-          mma_a_tmem(true, tmem, tmem + a_col + (uint32_t)(ks * 8), bh, idesc, acc0);
-        } else {
-          const uint64_t bl = b_desc(base_s + Lo.b_lo + atom * atom_bytes) + kk * 2;
-          mma_a_tmem(false, tmem, tmem + a_col + (uint32_t)(ks * 8), bh, idesc, acc0);
-          mma_a_tmem(false, tmem, tmem + a_col + (uint32_t)(ks * 8), bl, idesc, 1u);
-          mma_a_tmem(false, tmem, tmem + a_lo_col + (uint32_t)(ks * 8), bh, idesc, 1u);
+    BTRACE(s, 1);
+    // 2. MMA issue: issuer i is lane 0 of warp kBWarps-1-i and runs pass i
+    // into accumulator i (pass 0: W_hi g_hi, 1: W_hi g_lo, 2: W_lo g_hi); the
+    // padded tail of the last atom multiplies zeros
+    if (have) {
+      const int iss = kBWarps - 1 - warp;
+      if (iss >= 0 && iss < NI) {
+        if (lane == 0) {
+          const uint32_t dcol = tmem + (uint32_t)(iss * Nm);
+          const uint64_t bd0 = b_desc(base_s + ((!BF && iss == 1) ? Lo.b_lo : Lo.b_hi));
+          const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
+          const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
+          fence_after();
+          for (int at = 0; at < KCu; ++at) {
+            const uint64_t bd = bd0 + (uint64_t)at * bstep;
+            const uint32_t acol = acol0 + (uint32_t)(at * 32);
+#pragma unroll
+            for (int kk = 0; kk < EPA / KSTEP; ++kk)
+              mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
+                         (at | kk) ? 1u : 0u);
+          }
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                  mbar)
+              : "memory");
         }
+        __syncwarp();
       }
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-          : "memory");
     }
+    BTRACE(s, 6);
     bool mma_ok = true;
     if (have) {
-      mma_ok = mbar_wait_bounded(bar, phase, p.status, p.timeout_ns);
-      phase ^= 1u;
+      mma_ok = mbar_wait_bounded(mbar, mma_phase, p.status, p.timeout_ns);
+      if (!mma_ok) s_mma_bad = 1;
+      mma_phase ^= 1u;
     }
+    mma_ok = __all_sync(0xffffffffu, mma_ok);
     fence_after();
     BTRACE(s, 2);
-    // push each accumulator row (unit u0 + m) to the block that owns the unit
-    float* recv = recv0 + (size_t)(s & 1) * Pk * Uq * Nm;
+    // 3. push each accumulator row (unit u0 + m) to the block that owns the
+    // unit: warps 0-3 take columns 0-15, warps 4-7 columns 16-31, ...
+    float* recv = recv0 + (size_t)(s & 1) * Pk * Uq * Rs;
     if (!failed && s > 0) {
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
       const bool row_ok = m < Urc;
       const int owner = row_ok ? m / Uq : 0, uo = m - owner * Uq;
-      for (int c0 = (warp >> 2) * 32; c0 < Nm; c0 += (kBThreads / 128) * 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
-        if (!row_ok || owner >= Pk) continue;
-        float* dst = recv + ((size_t)q * Uq + uo) * Nm + c0;
-        const bool ok = have && mma_ok;
+      const bool ok = have && mma_ok;
+      const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);
+      for (int c0 = (warp >> 2) * 16; c0 < N; c0 += (kBWarps / 4) * 16) {
+        float v[NI][16];
+        if (ok) {
+          if constexpr (NI == 3) {
+            tmem_ld16x3(lrow + (uint32_t)c0, lrow + (uint32_t)(Nm + c0),
+                        lrow + (uint32_t)(2 * Nm + c0), v[0], v[1], v[2]);
+            // (hi hi + (hi lo + lo hi) 2^-11) / (w_scale g_scale), powers of two
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
+            for (int e = 0; e < 16; ++e)
+              v[0][e] = fmaf(v[1][e] + v[2][e], 1.f / 2048.f, v[0][e]) * out_scale;
+          } else {
+            tmem_ld16(lrow + (uint32_t)c0, v[0]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[0][e] = 0.f;
+        }
+        if (!row_ok || owner >= Pk) continue;
+        float* dst = recv + ((size_t)q * Uq + uo) * Rs + c0;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
           if (c0 + i < N)
-            st_peer4(dst + i, (unsigned)owner, ok ? v[i] : 0.f, ok ? v[i + 1] : 0.f,
-                     ok ? v[i + 2] : 0.f, ok ? v[i + 3] : 0.f);
+            st_peer4(dst + i, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2], v[0][i + 3]);
       }
     }
+    // 4. one cluster barrier per step, executed by every block, work or not
+    cp_async_wait_all();
     fence_before();
     cl_sync();
-    if (!failed && s > 0) {
-      // batch index fastest: consecutive threads read consecutive partials
-      for (int idx = tid; idx < items; idx += kBThreads) {
-        const int n = idx % N, uu = idx / N;
-        float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * Uq + uu) * Nm + n];
-        outs[n * Uq + uu] = v;
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
     BTRACE(s, 3);
-    if (!failed) {
+    const bool live = !failed && s_mma_bad == 0;
+    if (live) {
       for (int it = tid; it < items; it += kBThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         float dhf;
-        if (s == 0)
+        if (s == 0) {
           dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
-        else
-          dhf = outs[n * Uq + uu] + st_carry[it];
+        } else {
+          // the Pk partials in rank order (fixed), then the GRU's direct term
+          const float* rp = recv + (size_t)uu * Rs + n;
+          float v = 0.f;
+          for (int rank = 0; rank < Pk; ++rank) v += rp[(size_t)rank * Uq * Rs];
+          dhf = v + st_carry[it];
+        }
         if (s == nT) {
           if (a.dh0) reinterpret_cast<T*>(a.dh0)[(int64_t)n * H + j] = from_f<T>(dhf);
           if (a.dc0) a.dc0[(int64_t)n * H + j] = st_dc[it];
@@ -356,15 +458,24 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         const float dh = dyv + dhf;
         const float g0 = pin[1 * icap + it];
         T* gxo = dgx + row * GH + j;
+        // the exchange words of this step's dG_h (value as stored, and the
+        // step that reads it: every step below nT, the last one included,
+        // has a successor that multiplies it)
+        const bool xw = !(blockIdx.x == p.fault_block && s == p.fault_step);
+        unsigned long long* xo = a.hx + ((size_t)(s % 3) * N + n) * GH + j;
+        const unsigned long long tag = (unsigned long long)(s + 1) << 32;
+        float gh[4];
+        int ng = 1;
         if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
           const float cc = pin[5 * icap + it], cpv = pin[6 * icap + it];
           const float tc = tanhf(cc);
           const float dc = st_dc[it] + dh * g3 * (1.f - tc * tc);
-          gxo[0] = from_f<T>(dc * g2 * g0 * (1.f - g0));
-          gxo[H] = from_f<T>(dc * cpv * g1 * (1.f - g1));
-          gxo[2 * H] = from_f<T>(dc * g0 * (1.f - g2 * g2));
-          gxo[3 * H] = from_f<T>(dh * tc * g3 * (1.f - g3));
+          gh[0] = dc * g2 * g0 * (1.f - g0);
+          gh[1] = dc * cpv * g1 * (1.f - g1);
+          gh[2] = dc * g0 * (1.f - g2 * g2);
+          gh[3] = dh * tc * g3 * (1.f - g3);
+          ng = 4;
           st_dc[it] = dc * g1;
         } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
@@ -373,24 +484,42 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           const float dan = dh * (1.f - g1) * (1.f - g2 * g2);
           const float daz = dh * (hp - g2) * g1 * (1.f - g1);
           const float dar = dan * g3 * g0 * (1.f - g0);
-          gxo[0] = from_f<T>(dar);
-          gxo[H] = from_f<T>(daz);
-          gxo[2 * H] = from_f<T>(dan);
-          T* gho = dgh + row * GH + j;
-          gho[0] = from_f<T>(dar);
-          gho[H] = from_f<T>(daz);
-          gho[2 * H] = from_f<T>(dan * g0);
+          gh[0] = dar;
+          gh[1] = daz;
+          gh[2] = dan * g0;
+          ng = 3;
+          stash[it] = dar;
+          stash[icap + it] = daz;
+          stash[2 * icap + it] = dan;
           st_carry[it] = dh * g1;
         } else {  // tanh RNN: g0 = h_t
-          gxo[0] = from_f<T>(dh * (1.f - g0 * g0));
+          gh[0] = dh * (1.f - g0 * g0);
+        }
+        T* gho = dgh + row * GH + j;  // dG_x itself, except for the GRU
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          if (g >= ng) break;
+          const T v = from_f<T>(gh[g]);
+          if (xw) st_relaxed_u64(xo + (int64_t)g * H, tag | __float_as_uint(to_f(v)));
+          gho[(int64_t)g * H] = v;
         }
       }
     }
     __syncthreads();
     BTRACE(s, 4);
-    if (!failed && tid == 0 && s < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
-      publish_flag(flags + (size_t)b * p.flag_stride, (unsigned)(s + 1));
     BTRACE(s, 5);
+    // GRU: dG_x (read by the dense phases only) after the release
+    if (live && p.mode == 2 && s < nT) {
+      for (int it = tid; it < items; it += kBThreads) {
+        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        T* gxo = dgx + ((int64_t)t * N + n) * GH + j;
+        gxo[0] = from_f<T>(stash[it]);
+        gxo[H] = from_f<T>(stash[icap + it]);
+        gxo[2 * H] = from_f<T>(stash[2 * icap + it]);
+      }
+    }
+    if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
+    __syncthreads();
   }
   cl_sync();  // no block leaves while a peer may still store into it
   fence_before();
@@ -451,19 +580,21 @@ bool rec_tc_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_
     if (Ur > kBM) continue;
     const int Pr = (H + Ur - 1) / Ur;
     const int Uq = (Ur + Pk - 1) / Pk;
-    const int epc = bf16 ? 64 : 32;
+    const int epc = 64;  // 16-bit elements per 128-byte atom
     const int Kk = (((GH + Pk - 1) / Pk) + 7) / 8 * 8;
     const int Kp = (Kk + epc - 1) / epc * epc;
-    const int acols = bf16 ? Kp / 2 : 2 * Kp;
+    if (Kp / epc > kBMaxAtoms) continue;
+    const int NI = bf16 ? 1 : 3;
+    const int acols = bf16 ? Kp / 2 : Kp;
     int cols = 32;
-    while (cols < Nm + acols) cols *= 2;
+    while (cols < NI * Nm + acols) cols *= 2;
     if (cols > 512) continue;
     RecPlan pl;
     pl.direct = 0;
     pl.cluster = Pk; pl.Pr = Pr; pl.P = Pr * Pk; pl.Ur = Ur; pl.Uq = Uq;
     pl.Kk = Kk;
     pl.K = Kp;
-    pl.KC = Kp / (bf16 ? 64 : 32);
+    pl.KC = Kp / epc;
     pl.nbp = Nm;
     pl.lda = cols;
     pl.Mloc = Ur; pl.Mp = kBM; pl.nb = N;
@@ -474,7 +605,7 @@ bool rec_tc_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_
     if (D * pl.P > num_sms) continue;
     // MMA issue (K slice, passes), the push of Ur rows, the owners' reduction
     // over Pk partials and their pointwise items
-    const double cost = (double)Kp * (bf16 ? 1 : 3) * (Nm / 32.0) * 2.0 + (double)Ur * N / 16.0 +
+    const double cost = (double)Kp * (Nm / 32.0) * 2.0 + (double)Ur * N / 16.0 +
                         (double)Uq * N * (Pk / 4.0 + 8.0);
     if (!found || cost < best) {
       found = true;
@@ -507,8 +638,12 @@ cudaError_t rec_tc_bwd_launch(const RecParams& p, cudaStream_t st) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (size_t)p.D * pl.P * p.flag_stride, st);
-  if (e != cudaSuccess) return e;
+  // exchange words from an earlier launch must not look current: tags start at 1
+  for (int d = 0; d < p.D; ++d) {
+    if (!p.dir[d].hx) return cudaErrorInvalidValue;
+    e = cudaMemsetAsync(p.dir[d].hx, 0, rec_tc_xchg_bytes(p.N, p.G * p.H), st);
+    if (e != cudaSuccess) return e;
+  }
   RecParams copy = p;
   void* args[] = {&copy};
   cudaLaunchConfig_t cfg = {};

@@ -163,6 +163,57 @@ __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Poll nb (<= R) rows of tagged exchange words: row j's pair of 8-byte words
+// (value in the low half, step tag in the high half) at p + (row0 + j *
+// rstep) * ld, loaded 16 bytes at a time, all pending rows in flight at once;
+// returns when every pair carries `tag` (lanes with active = false return at
+// once).  Each 8-byte word is single-copy atomic, so a word with the right tag
+// holds the right value.  Bounded like warp_wait_flags; every lane of the
+// warp must call it.
+template <int R>
+__device__ __forceinline__ bool poll_tagged(const unsigned long long* p, int row0, int rstep,
+                                            int64_t ld, int nb, bool active, unsigned tag,
+                                            unsigned long long (&w0)[R],
+                                            unsigned long long (&w1)[R], int* status,
+                                            long long timeout_ns) {
+  unsigned pending = active ? ((1u << nb) - 1u) : 0u;
+  unsigned long long t0 = 0;
+  unsigned it = 0;
+  bool ok = true;
+  while (pending) {
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if ((pending >> j) & 1u) {
+        const unsigned long long* q = p + (int64_t)(row0 + j * rstep) * ld;
+        asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];"
+                     : "=l"(w0[j]), "=l"(w1[j])
+                     : "l"(q)
+                     : "memory");
+      }
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (((pending >> j) & 1u) && (unsigned)(w0[j] >> 32) == tag &&
+          (unsigned)(w1[j] >> 32) == tag)
+        pending &= ~(1u << j);
+    if (!pending) break;
+    if (it == 0) t0 = globaltimer_ns();
+    if ((++it & 31u) == 0) {
+      if (ld_volatile_int(status) != kDevOk) {
+        ok = false;
+      } else if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+        atomicCAS(status, kDevOk, kDevTimeout);
+        ok = false;
+      }
+      if (!ok) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
