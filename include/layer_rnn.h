@@ -60,7 +60,15 @@ extern "C" {
 
 typedef struct rnn_handle* rnn_t;
 
-typedef enum { RNN_TANH = 0, RNN_LSTM = 1, RNN_GRU = 2 } rnn_mode_t;
+/* RNN_GRU_TF: the GRU flavour with the reset gate applied before the
+ * recurrent product of the candidate (TensorFlow's equations quoted in "rnn
+ * training example?", oneDNN issue #218; oneDNN's linear_before_reset = 0):
+ *   n = tanh(W_in x + b_in + W_hn (r*h) + b_hn), r, z and h' as RNN_GRU.
+ * Same weight layout as RNN_GRU (gate blocks r, z, n).  Each step needs r
+ * before the candidate's product, so it runs on the CUDA-core recurrent
+ * kernels with two barriers per step (the dense phases still use the tensor
+ * cores); the workspace's fourth gate slot keeps r*h for dW_hn. */
+typedef enum { RNN_TANH = 0, RNN_LSTM = 1, RNN_GRU = 2, RNN_GRU_TF = 3 } rnn_mode_t;
 typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 
 typedef enum {
@@ -90,8 +98,8 @@ typedef enum {
 /* regions for rnn_workspace_layout */
 typedef enum {
   RNN_WS_GATES = 0,   /* per (l,d): [T, N, G'*H] f32 saved activations; G' = 4 for
-                         LSTM (i,f,g,o) and GRU (r,z,n, W_hn h + b_hn), 1 for tanh
-                         RNN (h); time-indexed                                      */
+                         LSTM (i,f,g,o), GRU (r,z,n, W_hn h + b_hn) and TF-flavour
+                         GRU (r,z,n, r*h), 1 for tanh RNN (h); time-indexed         */
   RNN_WS_CSEQ = 1,    /* per (l,d): [T+1, N, H] f32 cell states (LSTM only); slot
                          0 (dir 0) or T (dir 1) holds c0, slot t+1 / t holds c_t    */
   RNN_WS_HSEQ = 2,    /* per (l,d): [T+1, N, H] hidden states, same slots as CSEQ,

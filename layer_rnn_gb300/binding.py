@@ -15,7 +15,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblayer_rnn.so")
 
-RNN_TANH, RNN_LSTM, RNN_GRU = 0, 1, 2
+RNN_TANH, RNN_LSTM, RNN_GRU, RNN_GRU_TF = 0, 1, 2, 3
 RNN_F32, RNN_BF16 = 0, 1
 RNN_FLAG_SYNC_CHECK, RNN_FLAG_SIMT_GEMM, RNN_FLAG_SIMT_RECURRENT = 0x1, 0x2, 0x4
 RNN_FLAG_NO_WAVEFRONT = 0x8
@@ -25,7 +25,7 @@ PHASES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_WORKSPACE_TOO_SMALL", 4: "RNN_ERR_MISALIGNED", 5: "RNN_ERR_CUDA",
           6: "RNN_ERR_TIMEOUT", 7: "RNN_ERR_NO_RESIDENCY", 8: "RNN_ERR_DEVICE_CHECK"}
-MODES = {"rnn_tanh": RNN_TANH, "lstm": RNN_LSTM, "gru": RNN_GRU}
+MODES = {"rnn_tanh": RNN_TANH, "lstm": RNN_LSTM, "gru": RNN_GRU, "gru_tf": RNN_GRU_TF}
 DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 
 # exported symbol -> (restype, argtypes)

@@ -109,7 +109,8 @@ int64_t opnd_bytes(int64_t rows, int64_t K, bool tf32) {
 // whether a call may take the layer-wavefront path (host-side conditions; the
 // device-dependent plan can still decline)
 bool wf_candidate(const rnn_handle* h, int64_t N) {
-  return h->dtype == RNN_BF16 && h->D == 1 && h->L >= 2 && h->L <= kWfMaxLayers && N <= 128 &&
+  return h->dtype == RNN_BF16 && h->mode != RNN_GRU_TF && h->D == 1 && h->L >= 2 &&
+         h->L <= kWfMaxLayers && N <= 128 &&
          h->H % 8 == 0 && h->I % 8 == 0 &&
          !(h->flags & (RNN_FLAG_NO_WAVEFRONT | RNN_FLAG_SIMT_RECURRENT));
 }
@@ -147,7 +148,9 @@ int64_t gemm_scratch_bytes(const rnn_handle* h, int64_t T, int64_t N, bool train
     need = std::max(need, dgt + opnd_bytes(std::max(I_l, h->H), TN, tf) +
                               align256((int64_t)kMaxKsplit * GH * std::max(I_l, h->H) * 4));
   }
-  return std::max(need, wf_scratch_bytes(h, T, N, training)) + 4096 + xchg_bytes(h, N);
+  // the TensorFlow-flavour GRU's bf16 copy of r * h_{t-1} for dW_hn
+  const int64_t rh_copy = (training && h->mode == RNN_GRU_TF && !tf) ? align256(TN * h->H * 2) : 0;
+  return std::max(need, wf_scratch_bytes(h, T, N, training)) + 4096 + xchg_bytes(h, N) + rh_copy;
 }
 
 struct Scratch {
@@ -396,11 +399,13 @@ struct PhaseScope {
 rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl, int D,
                       bool varlen = false) {
   const bool bf = h->dtype == RNN_BF16;
-  if (varlen) {
-    // per-sequence lengths: the staged CUDA-core kernels are the ones that
-    // read them
-    if (!rec_make_plan(backward, h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
-                       pl, false))
+  if (varlen || h->mode == RNN_GRU_TF) {
+    // per-sequence lengths, and the TensorFlow-flavour GRU's two dependent
+    // contractions per step: the staged CUDA-core kernels are the ones that
+    // run them
+    // (the TensorFlow-flavour GRU has the GRU's sizes: three gate blocks)
+    if (!rec_make_plan(backward, h->mode == RNN_GRU_TF ? RNN_GRU : h->mode, bf, D, (int)h->H,
+                       (int)N, h->num_sms, h->smem_optin, pl, false))
       return RNN_ERR_UNSUPPORTED;
     if (pl->P * D > h->num_sms) return RNN_ERR_NO_RESIDENCY;
     if ((size_t)pl->P * D * 128 > kSyncBytes - 64) return RNN_ERR_UNSUPPORTED;
@@ -486,6 +491,8 @@ rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, 
     g.C = gx + (int64_t)d * T * N * GH; g.ldc = GH;
     g.bias1 = cp<char>(W, weight_offset(h, l, d, 2) * e);
     g.bias2 = cp<char>(W, weight_offset(h, l, d, 3) * e);
+    // GRU: b_hn stays inside r * (W_hn h + b_hn); the TensorFlow flavour's
+    // b_hn is outside its product and folds like the others
     g.bias2_limit = h->mode == RNN_GRU ? 2 * h->H : GH;
     g.in_bf16 = g.bias_bf16 = h->dtype == RNN_BF16;
     g.out_bf16 = 0;
@@ -609,6 +616,13 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
       if (!hx[d]) return RNN_ERR_WORKSPACE_TOO_SMALL;
     }
   }
+  void* xrows[2] = {nullptr, nullptr};
+  if (h->mode == RNN_GRU_TF) {
+    for (int d = 0; d < h->D; ++d) {
+      xrows[d] = sc.take(N * H * e);
+      if (!xrows[d]) return RNN_ERR_WORKSPACE_TOO_SMALL;
+    }
+  }
   const void* in = x;
   for (int l = 0; l < h->L; ++l) {
     void* out;
@@ -635,6 +649,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
       a.c0 = (c0 && h->mode == RNN_LSTM) ? cp<float>(c0, k * NH * 4) : nullptr;
       a.y = out;
       a.hx = hx[d];
+      a.xbuf = xrows[d];
       a.hy = hy ? mp<char>(hy, k * NH * e) : nullptr;
       a.cy = (cy && h->mode == RNN_LSTM) ? mp<float>(cy, k * NH * 4) : nullptr;
       if (training) {
@@ -677,7 +692,7 @@ rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
                         int64_t input_size, int64_t hidden_size, int dtype, uint32_t flags) {
   if (!out) return RNN_ERR_INVALID_ARG;
   *out = nullptr;
-  if (mode < RNN_TANH || mode > RNN_GRU) return RNN_ERR_INVALID_ARG;
+  if (mode < RNN_TANH || mode > RNN_GRU_TF) return RNN_ERR_INVALID_ARG;
   if (num_layers < 1 || (bidirectional != 0 && bidirectional != 1)) return RNN_ERR_INVALID_ARG;
   if (input_size < 1 || hidden_size < 1) return RNN_ERR_INVALID_ARG;
   if (dtype != RNN_F32 && dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
@@ -695,7 +710,7 @@ rnn_status_t rnn_create(rnn_t* out, int mode, int num_layers, int bidirectional,
   h->H = hidden_size;
   h->dtype = dtype;
   h->flags = flags;
-  h->G = mode == RNN_LSTM ? 4 : mode == RNN_GRU ? 3 : 1;
+  h->G = mode == RNN_LSTM ? 4 : (mode == RNN_GRU || mode == RNN_GRU_TF) ? 3 : 1;
   h->Gs = mode == RNN_TANH ? 1 : 4;
   *out = h;
   return RNN_OK;
@@ -902,6 +917,13 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
       if (!gxw[d]) return finish(h, st, RNN_ERR_WORKSPACE_TOO_SMALL);
     }
   }
+  void* xrows[2] = {nullptr, nullptr};
+  if (h->mode == RNN_GRU_TF) {
+    for (int d = 0; d < h->D; ++d) {
+      xrows[d] = sc.take(N * GH * e);
+      if (!xrows[d]) return finish(h, st, RNN_ERR_WORKSPACE_TOO_SMALL);
+    }
+  }
   const void* dcur = dy;
   int dcur_bf16 = bf;
   for (int l = h->L - 1; l >= 0; --l) {
@@ -927,6 +949,7 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
       a.dh0 = dh0 ? mp<char>(dh0, k * NH * e) : nullptr;
       a.dc0 = (dc0 && h->mode == RNN_LSTM) ? mp<float>(dc0, k * NH * 4) : nullptr;
       a.hx = gxw[d];
+      a.xbuf = xrows[d];
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_BWD);
@@ -1021,6 +1044,25 @@ rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t 
                             ws_bytes);
 }
 
+namespace {
+// The B operand r * h_{t-1} of the TensorFlow-flavour GRU's dW_hn: rows x cols
+// fp32 with row stride lds in the workspace; bf16 handles contract in bf16,
+// so those get a bf16 copy from the scratch.
+rnn_status_t rh_operand(const rnn_handle* h, const void* rh, int64_t rows, int64_t cols,
+                        int64_t lds, GemmArgs* g, Scratch* sc, cudaStream_t st) {
+  if (h->dtype != RNN_BF16) {
+    g->B = rh; g->sbk = lds; g->sbn = 1;
+    return RNN_OK;
+  }
+  void* dst = sc->take(rows * cols * 2);
+  if (!dst) return RNN_ERR_WORKSPACE_TOO_SMALL;
+  if (to_bf16(static_cast<const float*>(rh), rows, cols, lds, dst, h->num_sms, st) != cudaSuccess)
+    return RNN_ERR_CUDA;
+  g->B = dst; g->sbk = cols; g->sbn = 1;
+  return RNN_OK;
+}
+}  // namespace
+
 rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, const void* x,
                                   const void* h0, const void* y, const void* workspace,
                                   int64_t ws_bytes, void* dW) {
@@ -1073,7 +1115,25 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       g2.B = hprev; g2.sbk = H; g2.sbn = 1;
       g2.C = mp<char>(dW, weight_offset(h, l, d, 1) * e); g2.ldc = H;
       g2.in_bf16 = bf; g2.out_bf16 = bf;
-      s = run_gemm(h, g2, scl, st, &pa);
+      if (h->mode == RNN_GRU_TF) {
+        // the TensorFlow-flavour GRU's W_hn multiplies r * h_{t-1}: its rows
+        // of dW_hh contract da_n with that product (saved in the fourth gate
+        // slot of the workspace, fp32), the r and z rows with h_{t-1}
+        g2.M = 2 * H;
+        s = run_gemm(h, g2, scl, st);
+        if (s != RNN_OK) return s;
+        const void* rh = ws + lay.at(RNN_WS_GATES, l, d).off + 3 * H * 4;
+        GemmArgs g3;
+        g3.M = H; g3.N = H; g3.K = T * N;
+        g3.A = static_cast<const char*>(dgh) + 2 * H * e; g3.sam = 1; g3.sak = GH;
+        g3.in_bf16 = bf; g3.out_bf16 = bf;
+        g3.C = mp<char>(dW, (weight_offset(h, l, d, 1) + 2 * H * H) * e); g3.ldc = H;
+        s = rh_operand(h, rh, T * N, H, 4 * H, &g3, &scl, st);
+        if (s != RNN_OK) return s;
+        s = run_gemm(h, g3, scl, st);
+      } else {
+        s = run_gemm(h, g2, scl, st, &pa);
+      }
       if (s != RNN_OK) return s;
       // db_ih = sum of dG_x over (t, n); db_hh likewise over dG_h, which is
       // dG_x itself except for the GRU: then one sum serves both

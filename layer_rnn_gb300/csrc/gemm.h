@@ -60,6 +60,10 @@ cudaError_t transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t 
 cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16,
                    int64_t rows, int64_t cols, int64_t ld, float* scratch,
                    int64_t scratch_bytes, int num_sms, cudaStream_t st);
+// dst [rows][cols] bf16 (round to nearest even) <- src [rows][cols] fp32 with
+// row stride lds
+cudaError_t to_bf16(const float* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
+                    int num_sms, cudaStream_t st);
 // buf[i] = mask[i] ? buf[i] * scale : 0 for i < n (inter-layer dropout)
 cudaError_t dropout_apply(void* buf, int bf16, const uint8_t* mask, int64_t n, float scale,
                           int num_sms, cudaStream_t st);

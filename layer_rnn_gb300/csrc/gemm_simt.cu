@@ -311,6 +311,27 @@ __global__ void dropout_kernel(void* buf, int bf16, const uint8_t* __restrict__ 
   }
 }
 
+__global__ void to_bf16_kernel(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                               bf16* dst) {
+  const int64_t n = rows * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cols, c = i - r * cols;
+    dst[i] = __float2bfloat16_rn(src[r * lds + c]);
+  }
+}
+
+cudaError_t to_bf16(const float* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
+                    int num_sms, cudaStream_t st) {
+  const int64_t n = rows * cols;
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)std::max(1, num_sms) * 8);
+  to_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, rows, cols, lds,
+                                                   reinterpret_cast<bf16*>(dst));
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
 cudaError_t dropout_apply(void* buf, int bf16, const uint8_t* mask, int64_t n, float scale,
                           int num_sms, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;

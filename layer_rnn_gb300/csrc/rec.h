@@ -26,6 +26,10 @@ struct RecDirArgs {
   // (rec_tc_xchg_bytes(N, H) bytes), backward dG_h [3][N][G*H]
   // (rec_tc_xchg_bytes(N, G*H) bytes)
   unsigned long long* hx = nullptr;
+  // staged kernels, TensorFlow-flavour GRU (mode 3): the direction's exchange
+  // rows of the second contraction of each step -- forward r * h_{t-1} [N][H],
+  // backward [N][G*H] (da_r, da_z, da_n) -- in the storage type
+  void* xbuf = nullptr;
   // backward
   const void* dy = nullptr;      // row (t*N+n)*lddy, column d*H + j
   int dy_bf16 = 0;
@@ -70,7 +74,7 @@ struct RecPlan {
 };
 
 struct RecParams {
-  int mode = 0, T = 0, N = 0, H = 0, G = 0, Gs = 0, D = 1;
+  int mode = 0, T = 0, N = 0, H = 0, G = 0, Gs = 0, D = 1;  // mode: rnn_mode_t
   int bf16 = 0;
   int64_t ldy = 0, lddy = 0;
   RecPlan plan;

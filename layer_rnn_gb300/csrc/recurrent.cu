@@ -160,10 +160,13 @@ __device__ __forceinline__ Smem carve(unsigned char* smem, const RecPlan& pl, in
 }
 
 // One batch chunk of the per-step contraction: outs[m][n] = sum_k A[m][k] B[n][k]
-// with B[n][k] = src[(n0 + n) * lds + k] (src == nullptr: zeros).
+// with B[n][k] = src[(n0 + n) * lds + k] (src == nullptr: zeros), k over
+// [kb, ke) (the whole K by default).
 template <typename T, int RM, int RN, int LM, int LN>
 __device__ __forceinline__ void step_contract(const Smem& sm, const RecPlan& pl, const T* src,
-                                              int64_t lds, int nbc, bool vec) {
+                                              int64_t lds, int nbc, bool vec, int kb = 0,
+                                              int ke = -1) {
+  if (ke < 0) ke = pl.K;
   constexpr int VK = 16 / (int)sizeof(T);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ntile = pl.tiles_m * pl.tiles_n;
@@ -177,8 +180,8 @@ __device__ __forceinline__ void step_contract(const Smem& sm, const RecPlan& pl,
   for (int i = 0; i < RM; ++i)
 #pragma unroll
     for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < pl.K; k0 += pl.KC) {
-    const int kc = min(pl.KC, pl.K - k0);
+  for (int k0 = kb; k0 < ke; k0 += pl.KC) {
+    const int kc = min(pl.KC, ke - k0);
     stage_rows<T>(Bs, pl.ldb, src ? src + k0 : nullptr, lds, nbc, kc, vec);
     __syncthreads();
     if (active) {
@@ -263,6 +266,66 @@ __global__ void __launch_bounds__(kThreads, 1) rec_fwd_kernel(const __grid_const
       lds = p.ldy;
     }
     const int slot = d ? t : t + 1;
+    if (p.mode == 3) {
+      // TensorFlow-flavour GRU ("rnn training example?", the TensorFlow GRU
+      // equations: n = tanh(W_in x + b_in + W_hn (r * h) + b_hn)).  Phase 1:
+      // r and z from h_{t-1}, and r * h_{t-1} of the own units into the
+      // direction's exchange buffer; a barrier over the direction's blocks;
+      // phase 2: W_hn (r * h_{t-1}) for the own units, the candidate and the
+      // new state.  b_hn is folded into G_x (it is outside the product).
+      T* rh = reinterpret_cast<T*>(a.xbuf);
+      for (int n0 = 0; n0 < N; n0 += pl.nb) {
+        const int nbc = min(pl.nb, N - n0);
+        step_contract<T, RM, RN, LM, LN>(sm, pl, src ? src + (int64_t)n0 * lds : nullptr, lds,
+                                         nbc, vec);
+        const float* outs = sm.outs;
+        for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+          const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+          const int64_t row = (int64_t)t * N + n;
+          const float* gxr = a.gx + row * GH + j;
+          const float r = sigmoidf_(__ldg(gxr) + outs[(0 * U + u) * pl.nbp + nn]);
+          const float z = sigmoidf_(__ldg(gxr + H) + outs[(1 * U + u) * pl.nbp + nn]);
+          const T rhv = from_f<T>(r * hown[u * N + n]);
+          rh[(int64_t)n * H + j] = rhv;
+          cst[u * N + n] = z;  // kept for phase 2 (the GRU has no cell state)
+          if (a.gates) {
+            float* gp = a.gates + row * 4 * H + j;
+            gp[0] = r; gp[H] = z; gp[3 * H] = to_f(rhv);
+          }
+        }
+        __syncthreads();
+      }
+      if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
+                        (unsigned)(2 * s + 1), p.status, p.timeout_ns, p.spin_ns, false))
+        return;
+      const bool vrh = (H * (int)sizeof(T)) % 16 == 0;
+      for (int n0 = 0; n0 < N; n0 += pl.nb) {
+        const int nbc = min(pl.nb, N - n0);
+        step_contract<T, RM, RN, LM, LN>(sm, pl, rh + (int64_t)n0 * H, H, nbc, vrh);
+        const float* outs = sm.outs;
+        for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+          const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+          const int64_t row = (int64_t)t * N + n;
+          const bool act = !lens || t < __ldg(lens + n);
+          const float z = cst[u * N + n];
+          const float nv = tanhf(__ldg(a.gx + row * GH + 2 * H + j) + outs[(2 * U + u) * pl.nbp + nn]);
+          float h = (1.f - z) * nv + z * hown[u * N + n];
+          if (a.gates) a.gates[row * 4 * H + 2 * H + j] = nv;
+          if (!act) h = hown[u * N + n];
+          hown[u * N + n] = h;
+          y[row * p.ldy + (int64_t)d * H + j] = from_f<T>(act ? h : 0.f);
+          if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(h);
+        }
+        __syncthreads();
+      }
+      if (s + 1 < nT) {
+        const bool skip = (blockIdx.x == p.fault_block) && (s == p.fault_step);
+        if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
+                          (unsigned)(2 * s + 2), p.status, p.timeout_ns, p.spin_ns, skip))
+          return;
+      }
+      continue;
+    }
     for (int n0 = 0; n0 < N; n0 += pl.nb) {
       const int nbc = min(pl.nb, N - n0);
       step_contract<T, RM, RN, LM, LN>(sm, pl, src ? src + (int64_t)n0 * lds : nullptr, lds, nbc,
@@ -370,14 +433,101 @@ __global__ void __launch_bounds__(kThreads, 1) rec_bwd_kernel(const __grid_const
   const T* hseq = reinterpret_cast<const T*>(a.hseq);
   const int* lens = p.lengths;
 
+  const bool tf = p.mode == 3;
+  T* xb = reinterpret_cast<T*>(a.xbuf);  // TF-flavour GRU: [N][G*H] exchange rows
+
   for (int s = 0; s <= nT; ++s) {
     const int t = d ? s : nT - 1 - s;        // time processed at this step (s < T)
     const int tp = d ? s - 1 : nT - s;       // time processed at the previous step (s > 0)
     if (s > 0) {
       const bool skip = (blockIdx.x == p.fault_block) && (s - 1 == p.fault_step);
       if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
-                        (unsigned)s, p.status, p.timeout_ns, p.spin_ns, skip))
+                        (unsigned)(tf ? 2 * s : s), p.status, p.timeout_ns, p.spin_ns, skip))
         return;
+    }
+    if (tf) {
+      // TensorFlow-flavour GRU, reverse mode through n = tanh(a_n + W_hn (r*h)):
+      //   dh_{t-1} = dh z + r * W_hn^T da_n + W_hr^T da_r + W_hz^T da_z,
+      //   da_r = (W_hn^T da_n) * h_{t-1} * r (1 - r).
+      // Part A: dh from the previous step's W_hr^T da_r + W_hz^T da_z (K rows
+      // 0 .. 2H of the exchange rows) and the carried dh z + r * W_hn^T da_n;
+      // da_n, da_z of the own units out; barrier; part B: W_hn^T da_n (K rows
+      // 2H .. 3H), da_r out.
+      for (int n0 = 0; n0 < N; n0 += pl.nb) {
+        const int nbc = min(pl.nb, N - n0);
+        if (s > 0)
+          step_contract<T, RM, RN, LM, LN>(sm, pl, xb + (int64_t)n0 * GH, GH, nbc, vec, 0, 2 * H);
+        const float* outs = sm.outs;
+        for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+          const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+          float dhf;
+          if (s == 0)
+            dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
+          else
+            dhf = outs[u * pl.nbp + nn] + carry[u * N + n];
+          if (s == nT) {
+            if (a.dh0) reinterpret_cast<T*>(a.dh0)[(int64_t)n * H + j] = from_f<T>(dhf);
+            continue;
+          }
+          const int64_t row = (int64_t)t * N + n;
+          T* gxo = dgx + row * GH + j;
+          if (lens && t >= __ldg(lens + n)) {
+            // a step the forward skipped: no gate gradients, dh passes through
+            gxo[H] = from_f<T>(0.f);
+            gxo[2 * H] = from_f<T>(0.f);
+            xb[(int64_t)n * GH + 2 * H + j] = from_f<T>(0.f);
+            dcs[u * N + n] = 0.f;
+            carry[u * N + n] = dhf;
+            continue;
+          }
+          const float dh = load_any(a.dy, row * p.lddy + (int64_t)d * H + j, a.dy_bf16) + dhf;
+          const float* gp = a.gates + row * 4 * H + j;
+          const float z = gp[H], nv = gp[2 * H];
+          const float hp = to_f(hseq[((int64_t)(d ? t + 1 : t) * N + n) * H + j]);
+          const float dan = dh * (1.f - z) * (1.f - nv * nv);
+          const float daz = dh * (hp - nv) * z * (1.f - z);
+          const T dant = from_f<T>(dan);
+          gxo[H] = from_f<T>(daz);
+          gxo[2 * H] = dant;
+          xb[(int64_t)n * GH + 2 * H + j] = dant;
+          dcs[u * N + n] = daz;          // for part B (no cell state in a GRU)
+          carry[u * N + n] = dh * z;     // part B adds r * W_hn^T da_n
+        }
+        __syncthreads();
+      }
+      if (s == nT) continue;
+      if (!step_barrier(p.flags + (size_t)d * pl.P * p.flag_stride, p.flag_stride, pl.P, blk,
+                        (unsigned)(2 * s + 1), p.status, p.timeout_ns, p.spin_ns, false))
+        return;
+      for (int n0 = 0; n0 < N; n0 += pl.nb) {
+        const int nbc = min(pl.nb, N - n0);
+        step_contract<T, RM, RN, LM, LN>(sm, pl, xb + (int64_t)n0 * GH, GH, nbc, vec, 2 * H,
+                                         3 * H);
+        const float* outs = sm.outs;
+        for (int idx = tid; idx < Uc * nbc; idx += kThreads) {
+          const int u = idx % Uc, nn = idx / Uc, n = n0 + nn, j = j0 + u;
+          const int64_t row = (int64_t)t * N + n;
+          T* gxo = dgx + row * GH + j;
+          T* xr = xb + (int64_t)n * GH + j;
+          if (lens && t >= __ldg(lens + n)) {
+            gxo[0] = from_f<T>(0.f);
+            xr[0] = from_f<T>(0.f);
+            xr[H] = from_f<T>(0.f);
+            continue;
+          }
+          const float drh = outs[u * pl.nbp + nn];
+          const float r = a.gates[row * 4 * H + j];
+          const float hp = to_f(hseq[((int64_t)(d ? t + 1 : t) * N + n) * H + j]);
+          const float dar = drh * hp * r * (1.f - r);
+          const T dart = from_f<T>(dar);
+          gxo[0] = dart;
+          xr[0] = dart;
+          xr[H] = from_f<T>(dcs[u * N + n]);
+          carry[u * N + n] += r * drh;
+        }
+        __syncthreads();
+      }
+      continue;
     }
     for (int n0 = 0; n0 < N; n0 += pl.nb) {
       const int nbc = min(pl.nb, N - n0);

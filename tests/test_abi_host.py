@@ -52,7 +52,7 @@ def test_library_exports_every_declared_symbol(B):
 def test_create_validates_arguments(B):
     h = ctypes.c_void_p()
     lib = B.lib()
-    bad = [(3, 1, 0, 4, 4, 0), (1, 0, 0, 4, 4, 0), (1, 1, 2, 4, 4, 0), (1, 1, 0, 0, 4, 0),
+    bad = [(4, 1, 0, 4, 4, 0), (-1, 1, 0, 4, 4, 0), (1, 0, 0, 4, 4, 0), (1, 1, 2, 4, 4, 0), (1, 1, 0, 0, 4, 0),
            (1, 1, 0, 4, 0, 0), (1, 1, 0, 4, 4, 2)]
     for args in bad:
         assert lib.rnn_create(ctypes.byref(h), *args, 0) == 1, args
@@ -64,6 +64,7 @@ def test_create_validates_arguments(B):
 
 
 @pytest.mark.parametrize("mode,L,bidir,I,H", [("lstm", 1, False, 4, 8), ("gru", 3, True, 5, 7),
+                                              ("gru_tf", 2, True, 5, 7),
                                               ("rnn_tanh", 2, True, 800, 800),
                                               ("lstm", 4, False, 1024, 1024)])
 def test_weight_layout_matches_oracle_layout(B, mode, L, bidir, I, H):
@@ -91,6 +92,7 @@ def test_weight_layout_matches_oracle_layout(B, mode, L, bidir, I, H):
 
 
 @pytest.mark.parametrize("mode,L,bidir,dtype", [("lstm", 1, False, 0), ("gru", 2, True, 0),
+                                                ("gru_tf", 2, False, 1),
                                                 ("rnn_tanh", 3, True, 1), ("lstm", 4, False, 1)])
 def test_workspace_regions_disjoint_and_aligned(B, mode, L, bidir, dtype):
     T, N, I, H = 7, 3, 5, 6
@@ -114,7 +116,7 @@ def test_workspace_regions_disjoint_and_aligned(B, mode, L, bidir, dtype):
         for a, b in zip(spans, spans[1:]):
             assert a[1] <= b[0], (a, b)
         e = 2 if dtype else 4
-        G = {"lstm": 4, "gru": 3, "rnn_tanh": 1}[mode]
+        G = {"lstm": 4, "gru": 3, "gru_tf": 3, "rnn_tanh": 1}[mode]
         assert B.rnn_workspace_layout(h, T, N, B.RNN_WS_DGX, 0, 0)[1] == T * N * G * H * e
         assert B.rnn_workspace_layout(h, T, N, B.RNN_WS_HSEQ, 0, 0)[1] == (T + 1) * N * H * e
         assert (B.rnn_workspace_layout(h, T, N, B.RNN_WS_CSEQ, 0, 0)[1] > 0) == (mode == "lstm")
