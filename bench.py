@@ -7,9 +7,11 @@ backward_weights) on the Deep Speech 2 LSTM layer shape, 1 GPU per rank.
 One JSON line on rank 0.  A step is one pass of the whole hot path over one
 batch (N=20 sequences of T=300) with inputs resident in HBM; L2 is flushed
 (256 MiB write, untimed) before every timed step; each step is bracketed by
-CUDA events on the launching stream.  Under torchrun every rank runs an
-independent replica (the operator has no data-path exchange on one GPU);
-value = sequences of all ranks / max-over-ranks step time.
+CUDA events on the launching stream.  Under torchrun the ranks run data
+parallel over the batch: each rank takes its own N sequences (weak scaling)
+and the step ends with one all-reduce (sum) of the weight gradients
+(layer_rnn_gb300.dp); value = sequences of all ranks / max-over-ranks step
+time.
 
 ``--impl reference`` times the float64 CPU oracle (the only other
 implementation) on a bounded sample of the same workload on the host cores.
@@ -185,7 +187,8 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# distributed plumbing (replicas; barrier and max over ranks only)
+# distributed plumbing (barrier and max over ranks; the data path's one
+# collective, the dW all-reduce, is layer_rnn_gb300.dp)
 # ----------------------------------------------------------------------------
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -292,6 +295,7 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
     through pinned host buffers) and return its bench line (no CPU baseline)."""
     import torch
     from layer_rnn_gb300 import binding as B
+    from layer_rnn_gb300 import dp
     from layer_rnn_gb300 import tensors as tz
     T, N, I, H, L = cfg["T"], cfg["N"], cfg["I"], cfg["H"], cfg["L"]
     D = wl.num_directions(cfg)
@@ -324,6 +328,11 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
         r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
         r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
         r.backward_weights(x, h0, y, ws, dW, stream)
+        if dist is not None:
+            # data parallel over the batch: the one exchange, the sum of the
+            # ranks' weight gradients (NCCL, on the launching stream)
+            with torch.cuda.stream(stream):
+                dp.allreduce_grads(dW, dist)
 
     def timed(n, fn):
         evs = []
@@ -493,7 +502,9 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
         "config": {"workload": cfg["name"], "mode": cfg["mode"], "layers": L,
                    "bidirectional": cfg["bidir"], "T": T, "N": N, "I": I, "H": H,
                    "global_batch": N * ws_n, "seq_len": T,
-                   "parallelism": "replicas x%d" % ws_n if ws_n > 1 else "single GPU",
+                   "parallelism": ("dp%d (batch shards of %d sequences per GPU, dW/db "
+                                   "all-reduce every step)" % (ws_n, N)) if ws_n > 1
+                   else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, untimed)"},
         "effective_tflops": round(total_flop * ws_n / (ms_step_max * 1e-3) / 1e12, 3),
         "phases": per_phase,
