@@ -46,6 +46,27 @@ __device__ __forceinline__ float lane_bf16(const uint4& v, int e) {
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// The gate nonlinearities of the tensor-core recurrent kernels with the
+// hardware exponential (ex2.approx, a few ulp) and approximate division, at a
+// relative error near 1e-6 or better.  sigmoid = 1 / (1 + e^{-a}) has no
+// cancellation.  tanh = 1 - 2 / (1 + e^{2a}) cancels near 0, so |a| < 1/4 takes
+// the Taylor series of tanh to a^9 (x - x^3/3 + 2x^5/15 - 17x^7/315 +
+// 62x^9/2835; the first omitted term, 1382x^11/155925, is below 2e-9 there).
+// Large |a| saturates cleanly: e^{|a|} overflows to inf and the division
+// gives 0.
+__device__ __forceinline__ float sigmoid_fast(float a) {
+  return __fdividef(1.0f, 1.0f + __expf(-a));
+}
+__device__ __forceinline__ float tanh_fast(float a) {
+  const float big = 1.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * a));
+  const float x2 = a * a;
+  float poly = fmaf(x2, 62.0f / 2835.0f, -17.0f / 315.0f);
+  poly = fmaf(x2, poly, 2.0f / 15.0f);
+  poly = fmaf(x2, poly, -1.0f / 3.0f);
+  const float small = fmaf(a * x2, poly, a);
+  return fabsf(a) < 0.25f ? small : big;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -33,9 +33,9 @@
 //      owner's exchange barrier, so an owner waits only for its own inputs
 //      instead of a cluster-wide barrier;
 //   4. the owner sums the partials in rank order (deterministic), runs the
-//      fused gate math, stores the step's h (what the other blocks read) and
-//      releases its step flag; the workspace stores (gates, c, h sequence) go
-//      out after the release, so the release does not wait for them.
+//      fused gate math, and writes the exchange word of each h first (value
+//      and step in one 8-byte word: the data is its own flag, the other
+//      blocks poll it), then y and the workspace (gates, c, h sequence).
 // The next step's input projection values are fetched with cp.async at the
 // start of each step (the pages' ping-pong prefetch).  All waits are bounded.
 #include <algorithm>
@@ -90,7 +90,6 @@ __device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
 struct TcLayout {
   uint32_t b_hi, b_lo;      // staged B tiles: KC atoms x (Nm rows x 128 bytes)
   uint32_t recv;            // [2][Pk][G*Uq][Nm] f32 partial sums pushed by the cluster
-  uint32_t stash;           // [4][N][Uq] f32 saved activations, stored after the release
   uint32_t hst, cst;        // [N][Uq] f32 state of the own units
   uint32_t gxs;             // [G][N][Uq] f32 this step's projection values
   uint32_t total;
@@ -107,8 +106,6 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
   off += bf ? 0 : ntile;
   L.recv = off;
   off += 2u * pl.cluster * G * pl.Uq * (pl.nbp + 4) * 4u;
-  L.stash = off;
-  off += 4u * pl.Uq * N * 4u;
   L.hst = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.cst = off;
@@ -152,7 +149,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
   const TcLayout Lo = tc_layout(pl, G, N, BF);
   float* recv0 = reinterpret_cast<float*>(base + Lo.recv);
-  float* stash = reinterpret_cast<float*>(base + Lo.stash);
   float* hst = reinterpret_cast<float*>(base + Lo.hst);
   float* cst = reinterpret_cast<float*>(base + Lo.cst);
   float* gxs = reinterpret_cast<float*>(base + Lo.gxs);
@@ -506,14 +502,15 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     TTRACE(s, 3);
     const bool live = !failed && s_mma_bad == 0;
     if (live) {
-      // the partial sums of each gate (rank order, fixed) feed the gate math
+      // the partial sums of each gate (rank order, fixed) feed the gate math;
+      // the exchange word of h_t goes out first, the workspace stores after it
       const size_t rstride = (size_t)G * Uq * Rs;
+      const int slot = d ? t : t + 1;
       for (int it = tid; it < items; it += kTThreads) {
         const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
         const int j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
-        float* sv = stash + n * Uq + uu;        // likewise
         float ov[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -523,59 +520,46 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
             for (int rank = 0; rank < Pk; ++rank) ov[g] += rp[rank * rstride];
           }
         }
-        float h;
+        float h, g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, c = 0.f;
         if (p.mode == 1) {
-          const float ig = sigmoidf_(gv[0] + ov[0]);
-          const float fg = sigmoidf_(gv[N * Uq] + ov[1]);
-          const float gg = tanhf(gv[2 * N * Uq] + ov[2]);
-          const float og = sigmoidf_(gv[3 * N * Uq] + ov[3]);
-          const float c = fg * cst[n * Uq + uu] + ig * gg;
-          h = og * tanhf(c);
-          cst[n * Uq + uu] = c;
-          sv[0] = ig; sv[N * Uq] = fg; sv[2 * N * Uq] = gg; sv[3 * N * Uq] = og;
+          g0 = sigmoid_fast(gv[0] + ov[0]);
+          g1 = sigmoid_fast(gv[N * Uq] + ov[1]);
+          g2 = tanh_fast(gv[2 * N * Uq] + ov[2]);
+          g3 = sigmoid_fast(gv[3 * N * Uq] + ov[3]);
+          c = g1 * cst[n * Uq + uu] + g0 * g2;
+          h = g3 * tanh_fast(c);
         } else if (p.mode == 2) {
-          const float ghn = ov[2] + s_bhn[uu];
-          const float rg = sigmoidf_(gv[0] + ov[0]);
-          const float z = sigmoidf_(gv[N * Uq] + ov[1]);
-          const float nv = tanhf(gv[2 * Uq * N] + rg * ghn);
-          h = (1.f - z) * nv + z * hst[n * Uq + uu];
-          sv[0] = rg; sv[N * Uq] = z; sv[2 * N * Uq] = nv; sv[3 * N * Uq] = ghn;
+          g3 = ov[2] + s_bhn[uu];  // W_hn h + b_hn
+          g0 = sigmoid_fast(gv[0] + ov[0]);
+          g1 = sigmoid_fast(gv[N * Uq] + ov[1]);
+          g2 = tanh_fast(gv[2 * Uq * N] + g0 * g3);
+          h = (1.f - g1) * g2 + g1 * hst[n * Uq + uu];
         } else {
-          h = tanhf(gv[0] + ov[0]);
+          h = tanh_fast(gv[0] + ov[0]);
         }
-        hst[n * Uq + uu] = h;
         const T hs = from_f<T>(h);
-        y[row * p.ldy + (int64_t)d * H + j] = hs;
         // the exchange word of h_t: its value as stored (what y holds) and the
         // step that reads it
         if (s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
           st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + j,
                          ((unsigned long long)(s + 1) << 32) | __float_as_uint(to_f(hs)));
-      }
-    }
-    __syncthreads();
-    TTRACE(s, 4);
-    TTRACE(s, 5);
-    // workspace stores of the step, after the release
-    if (live) {
-      for (int it = tid; it < items; it += kTThreads) {
-        const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
-        const int j = u0 + uq0 + uu;
-        const int64_t row = (int64_t)t * N + n;
-        const int slot = d ? t : t + 1;
-        const float* sv = stash + n * Uq + uu;
+        y[row * p.ldy + (int64_t)d * H + j] = hs;
+        hst[n * Uq + uu] = h;
+        if (p.mode == 1) cst[n * Uq + uu] = c;
         if (a.gates) {
           if (p.mode == 0) {
-            a.gates[row * H + j] = hst[n * Uq + uu];
+            a.gates[row * H + j] = h;
           } else {
             float* gp = a.gates + row * 4 * H + j;
-            gp[0] = sv[0]; gp[H] = sv[N * Uq]; gp[2 * H] = sv[2 * N * Uq]; gp[3 * H] = sv[3 * N * Uq];
+            gp[0] = g0; gp[H] = g1; gp[2 * H] = g2; gp[3 * H] = g3;
           }
         }
-        if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = cst[n * Uq + uu];
-        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = from_f<T>(hst[n * Uq + uu]);
+        if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
+        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = hs;
       }
     }
+    TTRACE(s, 4);
+    TTRACE(s, 5);
     if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
     __syncthreads();
   }

@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
           const float cc = pin[5 * icap + it], cpv = pin[6 * icap + it];
-          const float tc = tanhf(cc);
+          const float tc = tanh_fast(cc);
           const float dc = st_dc[it] + dh * g3 * (1.f - tc * tc);
           gh[0] = dc * g2 * g0 * (1.f - g0);
           gh[1] = dc * cpv * g1 * (1.f - g1);
