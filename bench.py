@@ -405,9 +405,9 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
     barrier(dist)
     ms_e2e = timed(args.steps, e2e_step)
     ms_e2e_max = max_over_ranks(statistics.mean(ms_e2e), dist, dev)
-    # the step protocol of the tensor-core recurrent forward alone (flag waits,
-    # cluster barrier, release; no work): the barrier term of the recurrence's
-    # latency bound
+    # the step protocol of the tensor-core recurrent forward alone (exchange
+    # words written and polled, cluster barrier; no work): the term of the
+    # recurrence's latency bound that no arithmetic removes
     empty_us = None
     if paths[0] == "tensor":
         try:
@@ -476,9 +476,9 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
                     "w_hh_stream_us": round(w_us, 3), "mma_us": round(mma_us, 3),
                     "empty_step_us": round(empty_us, 3), "bound_us": round(bound, 3),
                     "frac_of_bound": round(bound / per_phase[ph]["us_per_step"], 3),
-                    "note": "empty step = the forward kernel's flag waits, cluster barrier "
-                            "and release alone (rnn_measure_step_protocol), used for both "
-                            "directions of the recurrence"}
+                    "note": "empty step = the forward kernel's step protocol alone (exchange "
+                            "words written and polled, cluster barrier; "
+                            "rnn_measure_step_protocol), used for the backward too"}
     # dominant phase by time share
     dom = max(PHASE_NAMES, key=lambda p: phases[p][0])
     avg_ms = phases[dom][0] / max(1, args.steps)
