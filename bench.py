@@ -477,7 +477,8 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
                     "empty_step_us": round(empty_us, 3), "bound_us": round(bound, 3),
                     "frac_of_bound": round(bound / per_phase[ph]["us_per_step"], 3),
                     "note": "empty step = the forward kernel's step protocol alone (exchange "
-                            "words written and polled, cluster barrier; "
+                            "words written and polled, one block barrier, partial-sum "
+                            "pushes completing the owners' barriers; "
                             "rnn_measure_step_protocol), used for the backward too"}
     # dominant phase by time share
     dom = max(PHASE_NAMES, key=lambda p: phases[p][0])

@@ -320,7 +320,8 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
  * It runs `steps` (2 .. 2^20) empty steps of the forward kernel's protocol for
  * batch N with one direction -- the same grid and clusters, each block
  * writing the exchange words of its units and polling those of its K slice,
- * the per-step cluster barrier, with no MMA and no gate math -- once to warm
+ * one block barrier, one push per owner that completes the owner's receive
+ * barrier and the owners' wait for it, with no MMA and no gate math -- once to warm
  * up and once between two CUDA events on `stream`, synchronises `stream`, and
  * returns the average microseconds per step.  It allocates (cudaMalloc) and
  * frees a temporary exchange buffer of 24*N*H bytes and uses the handle's

@@ -29,9 +29,11 @@
 //      passes issue in parallel;
 //   3. the accumulators' rows are combined in a fixed order and pushed over
 //      distributed shared memory to the block that owns each unit's pointwise
-//      step; every pushing warp then arrives (release, cluster scope) on the
-//      owner's exchange barrier, so an owner waits only for its own inputs
-//      instead of a cluster-wide barrier;
+//      step, as asynchronous stores that complete the transaction count of
+//      the owner's receive barrier (one per buffer of the double-buffered
+//      partials): an owner waits only for its own inputs, and no block waits
+//      for a cluster barrier whose release would also drain its earlier
+//      global stores;
 //   4. the owner sums the partials in rank order (deterministic), runs the
 //      fused gate math, and writes the exchange word of each h first (value
 //      and step in one 8-byte word: the data is its own flag, the other
@@ -64,9 +66,18 @@ __device__ unsigned long long g_wtrace[4][1024][32];
                  ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
     if (b_ >= 0 && (threadIdx.x & 31) == 0 && (s) < 1024) g_wtrace[b_][(s)][(k)] = lr::globaltimer_ns();\
   } while (0)
+// a stamp of warp 0 taken only once v is computed (the shared store waits for v)
+#define PTRACE(s, k, v)                                                                       \
+  do {                                                                                        \
+    if (warp == 0) {                                                                          \
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(&s_tsink)), "f"(v) : "memory");  \
+      WTRACE(s, k);                                                                           \
+    }                                                                                         \
+  } while (0)
 #else
 #define TTRACE(s, k) ((void)0)
 #define WTRACE(s, k) ((void)0)
+#define PTRACE(s, k, v) ((void)0)
 #endif
 
 namespace lr {
@@ -80,11 +91,6 @@ constexpr int kTWarps = kTThreads / 32;
 constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
 constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
 constexpr int kPollRows = 16;   // exchange rows a lane polls at once
-
-__device__ __forceinline__ int owner_of(int j, int Ur, int Uq, int Pk) {
-  const int r = j / Ur;
-  return r * Pk + (j - r * Ur) / Uq;
-}
 
 // shared memory layout (offsets in bytes from a 1024-aligned base)
 struct TcLayout {
@@ -124,10 +130,14 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t recv_bar[2];  // partial sums of steps s (s & 1) landed
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail, s_mma_bad;
   __shared__ float s_bhn[kTM];
   __shared__ float s_red[kTThreads / 32][2];
+#ifdef LAYER_RNN_TRACE
+  __shared__ float s_tsink;
+#endif
   const RecPlan& pl = p.plan;
   const int P = pl.P, Pk = pl.cluster;
   const int d = blockIdx.x / P;
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   float* gxs = reinterpret_cast<float*>(base + Lo.gxs);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
   const uint32_t mbar = smem_addr(&mma_bar);
+  const uint32_t rbar0 = smem_addr(&recv_bar[0]);
   // tensor memory: accumulator i at column i * Nm, then the A operands, two
   // 16-bit elements per column: W (bf16) or W_hi and W_lo (fp32 split)
   const uint32_t a_col = (uint32_t)(NI * Nm);
@@ -174,6 +185,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     s_mma_bad = 0;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
     mbar_init(mbar, NI);
+    mbar_init(rbar0, 1);
+    mbar_init(rbar0 + 8u, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && !cfg_bad) {
@@ -287,8 +300,19 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   // kind::f16 with bf16 (1) or fp16 (0) operands, fp32 accumulate
   const uint32_t idesc = (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) |
                          ((uint32_t)(Nm >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
+  // bytes of partial sums pushed to this block per step: G rows per own unit,
+  // N columns in 16-byte pieces, from each block of the cluster (this one
+  // included) whose K slice is not empty.  A block with an empty slice pushes
+  // nothing: it polls nothing either, so it runs ahead of the exchange, and
+  // its zeros could land in a later step's phase.  Every pusher polls its
+  // slice each step, which keeps it within one step of the blocks that read
+  // its owners' units: its step-s pushes land only after every owner of its
+  // cluster consumed the partials of step s - 2, the other buffer's use.
+  const int pushers = min(Pk, (H + max(1, pl.Kk) - 1) / max(1, pl.Kk));
+  const uint32_t rx_bytes = (uint32_t)(pushers * G * Uqc * ((N + 3) / 4) * 16);
+  // every block's barriers are initialised before any peer pushes into them
   fence_before();
-  __syncthreads();
+  cl_sync();
   fence_after();
   uint32_t mma_phase = 0;  // parity of the next completion of the MMA barrier
   // step-invariant index work, once: this thread's accumulator row (the
@@ -309,7 +333,11 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     const int t = d ? nT - 1 - s : s;
     const int tp = d ? t + 1 : t - 1;
     const bool failed = s_fail != 0;  // read after the previous step's barrier
+    const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
     TTRACE(s, 0);
+    // this step's partial sums: one arrival plus the bytes the peers push (a
+    // peer's bytes may land first; the phase cannot complete before this)
+    if (!failed && tid == 0) mbar_arrive_expect_tx(rbar, rx_bytes);
     // this step's input projection values of the own items (consumed after the
     // contraction, so their latency hides behind it)
     if (!failed) {
@@ -405,7 +433,9 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
     }
     // the staged tiles to the tensor cores' (async) proxy, then one barrier: a
-    // per-atom mbarrier measured slower (each wait costs about 100 ns)
+    // per-atom mbarrier measured slower (each wait costs about 100 ns); the
+    // barrier also publishes every thread's projection prefetch (long landed)
+    cp_async_wait_all();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     TTRACE(s, 1);
@@ -456,7 +486,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     // columns 16-31 (then 32-47 and 48-63, ...)
     const int Rs = Nm + 4;  // exchange row stride (floats): 16-byte rows, fewer bank conflicts
     float* recv = recv0 + (size_t)(s & 1) * Pk * G * Uq * Rs;
-    if (!failed) {
+    if (!failed && Kc > 0) {
       const int quarter = warp & 3;
       const int g = e_g, uo = e_uo, owner = e_owner;
       const bool row_ok = e_row_ok;
@@ -488,21 +518,24 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
           if (c0 + i < N)
-            st_peer4(dst + i, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2], v[0][i + 3]);
+            st_async4(dst + i, rbar, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2],
+                      v[0][i + 3]);
       }
       if (warp == 0) WTRACE(s, 25);
     }
-    // 4. one cluster barrier per step, executed by every block, work or not:
-    // after it every owner holds every rank's partials of this step (and
-    // every thread's projection prefetch has landed)
-    cp_async_wait_all();
-    fence_before();
-    cl_sync();
+    // 4. the threads with pointwise items wait for this step's partials: the
+    // pushes complete the owner's barrier themselves, so no cluster barrier
+    // and no release of this block's earlier global stores is waited for
+    bool live = !failed && mma_ok;
+    if (live && tid < items) {
+      live = mbar_wait_cluster_bounded(rbar, (uint32_t)(s >> 1) & 1u, p.status, p.timeout_ns);
+      if (!live) s_fail = 1;
+    }
     WTRACE(s, 22 + (warp & 1));
     TTRACE(s, 3);
-    const bool live = !failed && s_mma_bad == 0;
     if (live) {
-      // the partial sums of each gate (rank order, fixed) feed the gate math;
+      // the partial sums of each gate (rank order, fixed; ranks with an empty K
+      // slice push nothing) feed the gate math;
       // the exchange word of h_t goes out first, the workspace stores after it
       const size_t rstride = (size_t)G * Uq * Rs;
       const int slot = d ? t : t + 1;
@@ -517,9 +550,10 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           ov[g] = 0.f;
           if (g < G) {
             const float* rp = recv + ((size_t)g * Uq + uu) * Rs + n;
-            for (int rank = 0; rank < Pk; ++rank) ov[g] += rp[rank * rstride];
+            for (int rank = 0; rank < pushers; ++rank) ov[g] += rp[rank * rstride];
           }
         }
+        if (it == tid) PTRACE(s, 26, ov[0] + ov[1] + ov[2] + ov[3] + gv[0]);
         float h, g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, c = 0.f;
         if (p.mode == 1) {
           g0 = sigmoid_fast(gv[0] + ov[0]);
@@ -538,11 +572,13 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           h = tanh_fast(gv[0] + ov[0]);
         }
         const T hs = from_f<T>(h);
+        if (it == tid) PTRACE(s, 27, h);
         // the exchange word of h_t: its value as stored (what y holds) and the
         // step that reads it
         if (s + 1 < nT && !(blockIdx.x == p.fault_block && s == p.fault_step))
           st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + j,
                          ((unsigned long long)(s + 1) << 32) | __float_as_uint(to_f(hs)));
+        if (it == tid) PTRACE(s, 28, h);
         y[row * p.ldy + (int64_t)d * H + j] = hs;
         hst[n * Uq + uu] = h;
         if (p.mode == 1) cst[n * Uq + uu] = c;
@@ -556,13 +592,16 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         }
         if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
         if (hseq) hseq[((int64_t)slot * N + n) * H + j] = hs;
+        if (it == tid) PTRACE(s, 29, h);
       }
     }
+    PTRACE(s, 30, 0.f);
     TTRACE(s, 4);
     TTRACE(s, 5);
     if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
     __syncthreads();
   }
+  fence_before();
   cl_sync();  // no block leaves while a peer may still store into it
   if (s_fail == 0) {
     for (int it = tid; it < items; it += kTThreads) {
@@ -579,13 +618,17 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                  : "memory");
 }
 
-// The forward kernel's step protocol with no work: per step, each block
-// writes the exchange words of its units, each warp polls the words of its
-// atoms' units, one block barrier, the cluster barrier, one block barrier --
-// the part of a step's latency that no arithmetic removes.  Same grid,
-// clusters, exchange words and waits as rec_fwd_tc; bounded like it.
+// The forward kernel's step protocol with no work: per step, each warp polls
+// the exchange words of its atoms' units, one block barrier, each block with
+// a K slice pushes 16 bytes to every owner of its cluster (completing the
+// owner's receive barrier), the owners' threads wait for their barrier and
+// write the exchange words of their units -- the part of a step's latency
+// that no arithmetic removes.  Same grid, clusters, exchange words, barriers
+// and waits as rec_fwd_tc; bounded like it.
 __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_constant__ RecParams p) {
   __shared__ int s_fail;
+  __shared__ __align__(8) uint64_t recv_bar[2];
+  __shared__ __align__(16) float recv[2][32][4];
   const RecPlan& pl = p.plan;
   const int P = pl.P, Pk = pl.cluster;
   const int d = blockIdx.x / P;
@@ -595,18 +638,28 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_cons
   const int H = p.H, N = p.N, Ur = pl.Ur, Uq = pl.Uq;
   const int u0 = r * Ur, Urc = min(Ur, H - u0);
   const int uq0 = q * Uq, Uqc = max(0, min(Uq, Urc - uq0));
-  const int k0 = q * pl.Kk, Kc = max(0, min(pl.Kk, H - k0));
+  const int Kk = max(1, pl.Kk);
+  const int k0 = q * Kk, Kc = max(0, min(Kk, H - k0));
   const int EPA = 64, KCu = (Kc + EPA - 1) / EPA;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || a.hx == nullptr;
-  if (threadIdx.x == 0) {
+  const int tid = threadIdx.x, items = Uqc * N;
+  const int pushers = min(Pk, (H + Kk - 1) / Kk);
+  const uint32_t rbar0 = smem_addr(&recv_bar[0]);
+  const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || a.hx == nullptr ||
+                       Pk > 32;
+  if (tid == 0) {
     s_fail = cfg_bad;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
+    mbar_init(rbar0, 1);
+    mbar_init(rbar0 + 8u, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  cl_sync();
   const int parts = max(1, kTWarps / max(1, KCu));
   for (int s = 0; s < p.T; ++s) {
     const bool failed = s_fail != 0;
+    const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
+    if (!failed && tid == 0) mbar_arrive_expect_tx(rbar, Uqc > 0 ? (uint32_t)pushers * 16u : 0u);
     if (!failed && s > 0) {
       const unsigned long long* hxp = a.hx + (size_t)((s + 2) % 3) * N * H + k0;
       for (int task = warp; task < KCu * parts; task += kTWarps) {
@@ -624,14 +677,21 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_cons
       }
     }
     __syncthreads();
-    cl_sync();
-    __syncthreads();
-    if (!failed && s_fail == 0 && s + 1 < p.T)
-      for (int it = threadIdx.x; it < Uqc * N; it += kTThreads) {
+    // one 16-byte piece to each owner of the cluster that has units
+    if (!failed && Kc > 0 && tid < Pk && min(Uq, Urc - tid * Uq) > 0)
+      st_async4(&recv[s & 1][q][0], rbar, (unsigned)tid, 0.f, 0.f, 0.f, 0.f);
+    bool live = !failed;
+    if (live && tid < items) {
+      live = mbar_wait_cluster_bounded(rbar, (uint32_t)(s >> 1) & 1u, p.status, p.timeout_ns);
+      if (!live) s_fail = 1;
+    }
+    if (live && s + 1 < p.T)
+      for (int it = tid; it < items; it += kTThreads) {
         const int uu = it % Uqc, n = it / Uqc;
         st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + u0 + uq0 + uu,
                        (unsigned long long)(s + 1) << 32);
       }
+    __syncthreads();
   }
   cl_sync();
 }

@@ -41,6 +41,31 @@ __device__ __forceinline__ void st_peer4(float* local_ptr, unsigned rank, float 
                : "memory");
 }
 
+// 16-byte asynchronous store into cluster block `rank`'s shared memory (same
+// offset as local_ptr) that completes 16 bytes of the transaction count of
+// the barrier at local_bar's offset in that block: the receiver learns of the
+// data from its own barrier, the sender waits for nothing
+__device__ __forceinline__ void st_async4(float* local_ptr, uint32_t local_bar, unsigned rank,
+                                          float a, float b, float c, float d) {
+  unsigned raddr, rbar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(raddr)
+               : "r"(smem_addr(local_ptr)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(local_bar), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          raddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+      : "memory");
+}
+
+// one arrival on a barrier of this block that also expects `bytes` more
+// transaction bytes in the current phase
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
