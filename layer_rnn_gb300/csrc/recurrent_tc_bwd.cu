@@ -23,10 +23,11 @@
 // holds a dG_h value and the step that reads it, written by the owner of the
 // gate row, so the data is its own flag -- and stage them; one block barrier;
 // the MMAs; the accumulator rows go over distributed shared memory (16-byte
-// stores) to the block that owns each unit's pointwise step; one cluster
-// barrier; the owners sum the Pk partials in a fixed order, run the gate-
-// gradient chain, and write dG_h with its exchange words (GRU: dG_x, which no
-// block of this launch reads, after the step's barrier).  The step's pointwise inputs (dy, the saved gates, c_t
+// asynchronous stores that complete the owner's receive barrier) to the block
+// that owns each unit's pointwise step; the owners wait for their barrier,
+// sum the partials in a fixed order, run the gate-gradient chain, and write
+// dG_h with its exchange words (GRU: then dG_x, which no block of this launch
+// reads).  The step's pointwise inputs (dy, the saved gates, c_t
 // and c_{t-1}) are fetched with cp.async at the start of the step.
 #include <algorithm>
 #include <type_traits>
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t recv_bar[2];  // partials of steps s (s & 1) landed
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail, s_mma_bad;
   __shared__ float s_red[kBWarps];
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   float* pin = reinterpret_cast<float*>(base + Lo.pin);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
   const uint32_t mbar = smem_addr(&mma_bar);
+  const uint32_t rbar0 = smem_addr(&recv_bar[0]);
   // tensor memory: accumulator i at column i * Nm, then the A operands, two
   // 16-bit elements per column: W^T (bf16) or its hi and lo halves (fp32)
   const uint32_t a_col = (uint32_t)(NI * Nm);
@@ -161,6 +164,8 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     s_mma_bad = 0;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
     mbar_init(mbar, NI);
+    mbar_init(rbar0, 1);
+    mbar_init(rbar0 + 8u, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && !cfg_bad) {
@@ -244,8 +249,17 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   const uint32_t idesc = (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) |
                          ((uint32_t)(Nm >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   const int parts = max(1, kBWarps / max(1, KCu));
+  // bytes of partial sums pushed to this block per step (s >= 1): one row per
+  // own unit, N columns in 16-byte pieces, from each block of the cluster
+  // whose K slice is not empty (a block with an empty slice polls nothing and
+  // would run ahead of the exchange, so it pushes nothing); every pusher
+  // polls its slice each step, so its step-s pushes land only after every
+  // owner of its cluster consumed the partials of step s - 2
+  const int pushers = (int)min((int64_t)Pk, (GH + max(1, pl.Kk) - 1) / max(1, pl.Kk));
+  const uint32_t rx_bytes = (uint32_t)(pushers * Uqc * ((N + 3) / 4) * 16);
+  // every block's barriers are initialised before any peer pushes into them
   fence_before();
-  __syncthreads();
+  cl_sync();
   fence_after();
   uint32_t mma_phase = 0;
 
@@ -253,6 +267,10 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     const int t = rv ? s : nT - 1 - s;   // time processed at this step (s < nT)
     const int tp = rv ? s - 1 : nT - s;  // time processed at the previous step (s > 0)
     const bool failed = s_fail != 0;     // read after the previous step's barrier
+    // the partials of step s >= 1 land in buffer and barrier s & 1 (use
+    // (s - 1) >> 1 of that barrier): one arrival plus the peers' bytes
+    const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
+    if (!failed && s > 0 && tid == 0) mbar_arrive_expect_tx(rbar, rx_bytes);
     BTRACE(s, 0);
     // pointwise inputs of time t (fp32 sources by cp.async; bf16 ones are read
     // in the pointwise loop)
@@ -351,6 +369,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         }
       }
     }
+    cp_async_wait_all();  // this thread's pointwise inputs (it reads only its own)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     BTRACE(s, 1);
@@ -395,7 +414,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     // 3. push each accumulator row (unit u0 + m) to the block that owns the
     // unit: warps 0-3 take columns 0-15, warps 4-7 columns 16-31, ...
     float* recv = recv0 + (size_t)(s & 1) * Pk * Uq * Rs;
-    if (!failed && s > 0) {
+    if (!failed && s > 0 && Kc > 0) {
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
       const bool row_ok = m < Urc;
@@ -424,15 +443,19 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
           if (c0 + i < N)
-            st_peer4(dst + i, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2], v[0][i + 3]);
+            st_async4(dst + i, rbar, (unsigned)owner, v[0][i], v[0][i + 1], v[0][i + 2],
+                      v[0][i + 3]);
       }
     }
-    // 4. one cluster barrier per step, executed by every block, work or not
-    cp_async_wait_all();
-    fence_before();
-    cl_sync();
+    // 4. the threads with pointwise items wait for this step's partials (the
+    // pushes complete the owner's barrier: no cluster barrier)
+    bool live = !failed && mma_ok;
+    if (live && s > 0 && tid < items) {
+      live = mbar_wait_cluster_bounded(rbar, (uint32_t)((s - 1) >> 1) & 1u, p.status,
+                                       p.timeout_ns);
+      if (!live) s_fail = 1;
+    }
     BTRACE(s, 3);
-    const bool live = !failed && s_mma_bad == 0;
     if (live) {
       for (int it = tid; it < items; it += kBThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
@@ -443,7 +466,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           // the Pk partials in rank order (fixed), then the GRU's direct term
           const float* rp = recv + (size_t)uu * Rs + n;
           float v = 0.f;
-          for (int rank = 0; rank < Pk; ++rank) v += rp[(size_t)rank * Uq * Rs];
+          for (int rank = 0; rank < pushers; ++rank) v += rp[(size_t)rank * Uq * Rs];
           dhf = v + st_carry[it];
         }
         if (s == nT) {
@@ -505,10 +528,10 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         }
       }
     }
-    __syncthreads();
     BTRACE(s, 4);
     BTRACE(s, 5);
-    // GRU: dG_x (read by the dense phases only) after the release
+    // GRU: dG_x (read by the dense phases only) after the exchange words, by
+    // the thread that computed it
     if (live && p.mode == 2 && s < nT) {
       for (int it = tid; it < items; it += kBThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
@@ -521,6 +544,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
     __syncthreads();
   }
+  fence_before();
   cl_sync();  // no block leaves while a peer may still store into it
   fence_before();
   __syncthreads();
