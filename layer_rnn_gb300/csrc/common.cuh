@@ -220,4 +220,18 @@ __device__ __forceinline__ bool step_barrier(unsigned* flags, int stride, int nb
   return __syncthreads_or(fail) == 0;
 }
 
+// sum of p[0], p[stride], ..., p[(n-1)*stride] (n <= MAX) in index order, with
+// every load issued before the first addition: a loop with a runtime trip
+// count would wait for each load before the next
+template <int MAX>
+__device__ __forceinline__ float sum_strided(const float* p, size_t stride, int n) {
+  float v[MAX];
+#pragma unroll
+  for (int i = 0; i < MAX; ++i) v[i] = i < n ? p[(size_t)i * stride] : 0.f;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAX; ++i) acc += v[i];
+  return acc;
+}
+
 }  // namespace lr

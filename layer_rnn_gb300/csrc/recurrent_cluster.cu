@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_fail = ld_volatile_int(p.status) != kDevOk;
     // the launch must have formed the planned clusters, with this block at rank
     // q: otherwise no peer shared memory is touched at all
-    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q) {
+    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q || Pk > 8) {
       atomicCAS(p.status, kDevOk, kDevCheck);
       s_fail = 1;
     }
@@ -329,10 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int idx = tid; idx < G * Uqc * N; idx += kThreads) {
         const int g = idx / (Uqc * N), rem = idx - g * (Uqc * N);
         const int u = rem / N, nn = rem - u * N;
-        float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank)
-          v += recv[((size_t)rank * G * Uq + g * Uq + u) * kNB + nn];
-        outs[(g * Uq + u) * kNB + nn] = v;
+        outs[(g * Uq + u) * kNB + nn] =
+            sum_strided<8>(recv + ((size_t)g * Uq + u) * kNB + nn, (size_t)G * Uq * kNB, Pk);
       }
     }
     __syncthreads();
@@ -420,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_fail = ld_volatile_int(p.status) != kDevOk;
     // the launch must have formed the planned clusters, with this block at rank
     // q: otherwise no peer shared memory is touched at all
-    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q) {
+    if (cluster_size() != (unsigned)Pk || cluster_rank() != (unsigned)q || Pk > 8) {
       atomicCAS(p.status, kDevOk, kDevCheck);
       s_fail = 1;
     }
@@ -510,9 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed) {
       for (int idx = tid; idx < Uqc * N; idx += kThreads) {
         const int u = idx / N, nn = idx - u * N;
-        float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * Uq + u) * kNB + nn];
-        outs[u * kNB + nn] = v;
+        outs[u * kNB + nn] = sum_strided<8>(recv + (size_t)u * kNB + nn, (size_t)Uq * kNB, Pk);
       }
     }
     __syncthreads();

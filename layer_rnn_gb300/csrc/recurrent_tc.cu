@@ -91,6 +91,7 @@ constexpr int kTWarps = kTThreads / 32;
 constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
 constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
 constexpr int kPollRows = 16;   // exchange rows a lane polls at once
+constexpr int kMaxPushers = 8;  // largest cluster of the plan
 
 // shared memory layout (offsets in bytes from a 1024-aligned base)
 struct TcLayout {
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                        a_col + (uint32_t)(BF ? Kp / 2 : Kp) > ncols || ncols > 512u ||
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Mb > kTM || N > Nm ||
                        Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
-                       pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > 32 || a.hx == nullptr ||
+                       pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > kMaxPushers || a.hx == nullptr ||
                        (H & 1) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
@@ -544,13 +545,23 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         const int j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
-        float ov[4];
+        // all partials loaded first (independent shared loads in flight
+        // together), then summed in rank order
+        float ov[4], pv[4][kMaxPushers];
+        {
+          const uint32_t rp0 = smem_addr(recv + (size_t)uu * Rs + n);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          ov[g] = 0.f;
-          if (g < G) {
-            const float* rp = recv + ((size_t)g * Uq + uu) * Rs + n;
-            for (int rank = 0; rank < pushers; ++rank) ov[g] += rp[rank * rstride];
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int rank = 0; rank < kMaxPushers; ++rank)
+              pv[g][rank] = (g < G && rank < pushers)
+                                ? ld_shared_f32(rp0 + 4u * (uint32_t)(g * Uq * Rs + rank * rstride))
+                                : 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            ov[g] = 0.f;
+#pragma unroll
+            for (int rank = 0; rank < kMaxPushers; ++rank) ov[g] += pv[g][rank];
           }
         }
         if (it == tid) PTRACE(s, 26, ov[0] + ov[1] + ov[2] + ov[3] + gv[0]);

@@ -61,6 +61,7 @@ constexpr int kBM = 128;    // MMA M: output units per row group (padded)
 constexpr int kNIn = 7;     // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1} / h_{t-1}
 constexpr int kBMaxAtoms = 16;
 constexpr int kBPollRows = 16;  // exchange rows a lane polls at once
+constexpr int kBMaxPushers = 16;  // largest cluster of the plan
 
 __device__ __forceinline__ int owner_flag_b(int u, int Ur, int Uq, int Pk) {
   const int r = u / Ur;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
                        a_col + (uint32_t)(BF ? Kp / 2 : Kp) > ncols || ncols > 512u ||
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Ur > kBM || N > Nm ||
                        Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
-                       pl.KC > kBMaxAtoms || pl.Kk > Kp || Uq * Pk < Ur || Pk > 32 ||
+                       pl.KC > kBMaxAtoms || pl.Kk > Kp || Uq * Pk < Ur || Pk > kBMaxPushers ||
                        a.hx == nullptr || (GH & 1) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
@@ -463,10 +464,16 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         if (s == 0) {
           dhf = a.dhy ? to_f(reinterpret_cast<const T*>(a.dhy)[(int64_t)n * H + j]) : 0.f;
         } else {
-          // the Pk partials in rank order (fixed), then the GRU's direct term
-          const float* rp = recv + (size_t)uu * Rs + n;
+          // the partials in rank order (fixed; all loads in flight together),
+          // then the GRU's direct term
+          const uint32_t rp0 = smem_addr(recv + (size_t)uu * Rs + n);
+          float pv[kBMaxPushers];
+#pragma unroll
+          for (int rank = 0; rank < kBMaxPushers; ++rank)
+            pv[rank] = rank < pushers ? ld_shared_f32(rp0 + 4u * (uint32_t)(rank * Uq * Rs)) : 0.f;
           float v = 0.f;
-          for (int rank = 0; rank < pushers; ++rank) v += rp[(size_t)rank * Uq * Rs];
+#pragma unroll
+          for (int rank = 0; rank < kBMaxPushers; ++rank) v += pv[rank];
           dhf = v + st_carry[it];
         }
         if (s == nT) {

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                        Urp % 16 != 0 || Urp > 256 || Urp < Ur || (uint32_t)Urp > ncols ||
                        ncols > 512u || (ncols & (ncols - 1u)) != 0 || ncols < 32u ||
                        pl.Kk % kMChunk != 0 || Uq % 4 != 0 || Uq * Pk < Ur || d >= 2 ||
-                       S < 2 || S > kMStages || pl.rbufs < 1 || pl.rbufs > 2;
+                       S < 2 || S > kMStages || pl.rbufs < 1 || pl.rbufs > 2 || Pk > 8;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
@@ -410,9 +410,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     if (!failed && s > 0) {
       for (int it = tid; it < items; it += kMThreads) {
         const int uu = it % Uqc, n = it / Uqc;
-        float v = 0.f;
-        for (int rank = 0; rank < Pk; ++rank) v += recv[((size_t)rank * N + n) * Uq + uu];
-        outs[n * Uq + uu] = v;
+        outs[n * Uq + uu] = sum_strided<8>(recv + (size_t)n * Uq + uu, (size_t)N * Uq, Pk);
       }
     }
     // one partial-sum buffer: nobody pushes the next step's partials before
