@@ -38,8 +38,9 @@
 //      fused gate math, and writes the exchange word of each h first (value
 //      and step in one 8-byte word: the data is its own flag, the other
 //      blocks poll it), then y and the workspace (gates, c, h sequence).
-// The next step's input projection values are fetched with cp.async at the
-// start of each step (the pages' ping-pong prefetch).  All waits are bounded.
+// The step's input projection values are fetched with cp.async once the K
+// slice is staged, while the MMAs and the exchange run (the pages' ping-pong
+// prefetch).  All waits are bounded.
 #include <algorithm>
 #include <type_traits>
 
@@ -66,6 +67,14 @@ __device__ unsigned long long g_wtrace[4][1024][32];
                  ? 2 : blockIdx.x == nb_ - 1 ? 3 : -1;                                       \
     if (b_ >= 0 && (threadIdx.x & 31) == 0 && (s) < 1024) g_wtrace[b_][(s)][(k)] = lr::globaltimer_ns();\
   } while (0)
+// per block and step: [0] thread 0's exchange-word store issued, [1] staging
+// done (after the block barrier)
+__device__ unsigned long long g_xtrace[256][512][2];
+#define XTRACE(s, k)                                                                          \
+  do {                                                                                        \
+    if (threadIdx.x == 0 && blockIdx.x < 256 && (s) < 512)                                    \
+      g_xtrace[blockIdx.x][(s)][(k)] = lr::globaltimer_ns();                                  \
+  } while (0)
 // a stamp of warp 0 taken only once v is computed (the shared store waits for v)
 #define PTRACE(s, k, v)                                                                       \
   do {                                                                                        \
@@ -78,6 +87,7 @@ __device__ unsigned long long g_wtrace[4][1024][32];
 #define TTRACE(s, k) ((void)0)
 #define WTRACE(s, k) ((void)0)
 #define PTRACE(s, k, v) ((void)0)
+#define XTRACE(s, k) ((void)0)
 #endif
 
 namespace lr {
@@ -339,17 +349,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     // this step's partial sums: one arrival plus the bytes the peers push (a
     // peer's bytes may land first; the phase cannot complete before this)
     if (!failed && tid == 0) mbar_arrive_expect_tx(rbar, rx_bytes);
-    // this step's input projection values of the own items (consumed after the
-    // contraction, so their latency hides behind it)
-    if (!failed) {
-      for (int it = tid; it < G * items; it += kTThreads) {
-        const int g = it / items, rem = it - g * items;
-        const int uu = rem % Uqc, n = rem / Uqc;
-        cp_async4(gxs + (g * N + n) * Uq + uu,
-                  a.gx + ((int64_t)t * N + n) * GH + (int64_t)g * H + u0 + uq0 + uu);
-      }
-    }
-    cp_async_commit();
     const bool have = !failed && Kc > 0;
     const T* src = s == 0 ? reinterpret_cast<const T*>(a.h0)
                           : y + (int64_t)tp * N * p.ldy + (int64_t)d * H;
@@ -434,18 +433,19 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
     }
     // the staged tiles to the tensor cores' (async) proxy, then one barrier: a
-    // per-atom mbarrier measured slower (each wait costs about 100 ns); the
-    // barrier also publishes every thread's projection prefetch (long landed)
-    cp_async_wait_all();
+    // per-atom mbarrier measured slower (each wait costs about 100 ns)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     TTRACE(s, 1);
+    XTRACE(s, 1);
     if (have) {
       // 2. MMA issue: issuer i is lane 0 of warp kTWarps-1-i and runs pass i
       // into accumulator i (pass 0: W_hi h_hi, 1: W_hi h_lo, 2: W_lo h_hi);
       // descriptors advance by whole atoms and 32-byte K steps inside the
       // start-address field; the padded tail of the last atom multiplies
-      // zeros (B columns >= Kc are staged as zeros, W columns >= Kc are zero)
+      // zeros (B columns >= Kc are staged as zeros, W columns >= Kc are zero;
+      // predicating its K steps off measured slower: the issue loop must stay
+      // minimal)
       const int iss = kTWarps - 1 - warp;
       if (iss >= 0 && iss < NI) {
         if (lane == 0) {
@@ -472,6 +472,19 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
       TTRACE(s, 6);
     }
+    // this step's input projection values, each item's G values fetched by the
+    // thread that consumes them (it waits for its own copies only): issued
+    // after the polls, whose loads would otherwise queue behind these reads
+    // of memory, and consumed after the contraction and the exchange
+    if (!failed) {
+      const int64_t grow = (int64_t)t * N;
+      for (int it = tid; it < items; it += kTThreads) {
+        const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
+        const float* src = a.gx + (grow + n) * GH + u0 + uq0 + uu;
+        for (int g = 0; g < G; ++g) cp_async4(gxs + (g * N + n) * Uq + uu, src + (int64_t)g * H);
+      }
+    }
+    cp_async_commit();
     // wait for the products (every thread, the phase of this step)
     bool mma_ok = true;
     if (have) {
@@ -544,6 +557,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
         const int j = u0 + uq0 + uu;
         const int64_t row = (int64_t)t * N + n;
+        cp_async_wait_all();                    // this thread's projection values
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
         // all partials loaded first (independent shared loads in flight
         // together), then summed in rank order
@@ -565,6 +579,21 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           }
         }
         if (it == tid) PTRACE(s, 26, ov[0] + ov[1] + ov[2] + ov[3] + gv[0]);
+#ifdef LAYER_RNN_TRACE
+        // the same loads once more, now with the code and data warm
+        if (it == tid) {
+          const uint32_t rq = smem_addr(recv + (size_t)uu * Rs + n);
+          float w2 = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int rank = 0; rank < kMaxPushers; ++rank)
+              w2 += (g < G && rank < pushers)
+                        ? ld_shared_f32(rq + 4u * (uint32_t)(g * Uq * Rs + rank * rstride))
+                        : 0.f;
+          PTRACE(s, 31, w2);
+        }
+#endif
         float h, g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, c = 0.f;
         if (p.mode == 1) {
           g0 = sigmoid_fast(gv[0] + ov[0]);
@@ -590,6 +619,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           st_relaxed_u64(a.hx + ((size_t)(s % 3) * N + n) * H + j,
                          ((unsigned long long)(s + 1) << 32) | __float_as_uint(to_f(hs)));
         if (it == tid) PTRACE(s, 28, h);
+        if (it == tid) XTRACE(s, 0);
         y[row * p.ldy + (int64_t)d * H + j] = hs;
         hst[n * Uq + uu] = h;
         if (p.mode == 1) cst[n * Uq + uu] = c;
@@ -803,6 +833,10 @@ extern "C" int rnn_debug_ttrace_copy(void* host, size_t bytes) {
 extern "C" int rnn_debug_fwtrace_copy(void* host, size_t bytes) {
   if (bytes > sizeof(g_wtrace)) bytes = sizeof(g_wtrace);
   return (int)cudaMemcpyFromSymbol(host, g_wtrace, bytes);
+}
+extern "C" int rnn_debug_xtrace_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_xtrace)) bytes = sizeof(g_xtrace);
+  return (int)cudaMemcpyFromSymbol(host, g_xtrace, bytes);
 }
 extern "C" int rnn_debug_ttrace_clear() {
   static unsigned long long zeros[4][1024][8];

@@ -273,33 +273,6 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
     if (!failed && s > 0 && tid == 0) mbar_arrive_expect_tx(rbar, rx_bytes);
     BTRACE(s, 0);
-    // pointwise inputs of time t (fp32 sources by cp.async; bf16 ones are read
-    // in the pointwise loop)
-    if (!failed && s < nT) {
-      const int sc = rv ? t : t + 1, sp = rv ? t + 1 : t;
-      for (int it = tid; it < items; it += kBThreads) {
-        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
-        const int64_t row = (int64_t)t * N + n;
-        if (!a.dy_bf16)
-          cp_async4(pin + 0 * icap + it,
-                    reinterpret_cast<const float*>(a.dy) + row * p.lddy + (int64_t)d * H + j);
-        if (p.mode == 0) {
-          cp_async4(pin + 1 * icap + it, a.gates + row * H + j);
-        } else {
-          const float* gp = a.gates + row * 4 * H + j;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) cp_async4(pin + (1 + g) * icap + it, gp + (int64_t)g * H);
-          if (p.mode == 1) {
-            cp_async4(pin + 5 * icap + it, a.cseq + ((int64_t)sc * N + n) * H + j);
-            cp_async4(pin + 6 * icap + it, a.cseq + ((int64_t)sp * N + n) * H + j);
-          } else if (!BF) {
-            cp_async4(pin + 6 * icap + it,
-                      reinterpret_cast<const float*>(hseq) + ((int64_t)sp * N + n) * H + j);
-          }
-        }
-      }
-    }
-    cp_async_commit();
     const bool have = !failed && s > 0 && Kc > 0;
     // 1. staging of the previous step's dG_h slice: task (atom, row part) ->
     // warp; the warp polls the exchange words of its atom (value and step in
@@ -370,10 +343,10 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         }
       }
     }
-    cp_async_wait_all();  // this thread's pointwise inputs (it reads only its own)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     BTRACE(s, 1);
+
     // 2. MMA issue: issuer i is lane 0 of warp kBWarps-1-i and runs pass i
     // into accumulator i (pass 0: W_hi g_hi, 1: W_hi g_lo, 2: W_lo g_hi); the
     // padded tail of the last atom multiplies zeros
@@ -403,6 +376,36 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
       }
     }
     BTRACE(s, 6);
+    // pointwise inputs of time t, issued after the polls (whose loads would
+    // otherwise queue behind these reads of memory) and consumed after the
+    // contraction and the exchange, each by the thread that fetched it (fp32
+    // sources by cp.async; bf16 ones are read
+    // in the pointwise loop)
+    if (!failed && s < nT) {
+      const int sc = rv ? t : t + 1, sp = rv ? t + 1 : t;
+      for (int it = tid; it < items; it += kBThreads) {
+        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+        const int64_t row = (int64_t)t * N + n;
+        if (!a.dy_bf16)
+          cp_async4(pin + 0 * icap + it,
+                    reinterpret_cast<const float*>(a.dy) + row * p.lddy + (int64_t)d * H + j);
+        if (p.mode == 0) {
+          cp_async4(pin + 1 * icap + it, a.gates + row * H + j);
+        } else {
+          const float* gp = a.gates + row * 4 * H + j;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) cp_async4(pin + (1 + g) * icap + it, gp + (int64_t)g * H);
+          if (p.mode == 1) {
+            cp_async4(pin + 5 * icap + it, a.cseq + ((int64_t)sc * N + n) * H + j);
+            cp_async4(pin + 6 * icap + it, a.cseq + ((int64_t)sp * N + n) * H + j);
+          } else if (!BF) {
+            cp_async4(pin + 6 * icap + it,
+                      reinterpret_cast<const float*>(hseq) + ((int64_t)sp * N + n) * H + j);
+          }
+        }
+      }
+    }
+    cp_async_commit();
     bool mma_ok = true;
     if (have) {
       mma_ok = mbar_wait_bounded(mbar, mma_phase, p.status, p.timeout_ns);
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     }
     BTRACE(s, 3);
     if (live) {
+      cp_async_wait_all();  // this thread's pointwise inputs (it reads only its own)
       for (int it = tid; it < items; it += kBThreads) {
         const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
         float dhf;
