@@ -109,6 +109,7 @@ struct TcLayout {
   uint32_t recv;            // [2][Pk][G*Uq][Nm] f32 partial sums pushed by the cluster
   uint32_t hst, cst;        // [N][Uq] f32 state of the own units
   uint32_t gxs;             // [G][N][Uq] f32 this step's projection values
+  uint32_t outs;            // [6][N][Uq] f32 the previous step's h, gates, c (stored late)
   uint32_t total;
 };
 
@@ -129,6 +130,8 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
   off += (uint32_t)pl.Uq * N * 4u;
   L.gxs = off;
   off += (uint32_t)G * pl.Uq * N * 4u;
+  L.outs = off;
+  off += 6u * pl.Uq * N * 4u;
   L.total = (off + 1023u) & ~1023u;
   return L;
 }
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   float* hst = reinterpret_cast<float*>(base + Lo.hst);
   float* cst = reinterpret_cast<float*>(base + Lo.cst);
   float* gxs = reinterpret_cast<float*>(base + Lo.gxs);
+  float* outs = reinterpret_cast<float*>(base + Lo.outs);
   const uint32_t atom_bytes = (uint32_t)Nm * 128u;
   const uint32_t mbar = smem_addr(&mma_bar);
   const uint32_t rbar0 = smem_addr(&recv_bar[0]);
@@ -339,6 +343,37 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     e_uo = u - e_owner * Uq;
   }
   const int i_uu = Uqc > 0 ? tid % Uqc : 0, i_n = Uqc > 0 ? tid / Uqc : 0;
+  const int icap = Uq * N;  // stride of one array of the output stash
+  // the outputs of step sp (y, the saved gates, c_t, the h sequence) from the
+  // stash, each item by the thread that computed it: written one step late,
+  // after the next step's polls, so that these stores do not queue ahead of
+  // the poll loads
+  auto flush = [&](int sp) {
+    const int tq = d ? nT - 1 - sp : sp;
+    const int slot = d ? tq : tq + 1;
+    for (int it = tid; it < items; it += kTThreads) {
+      const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
+      const int j = u0 + uq0 + uu;
+      const int64_t row = (int64_t)tq * N + n;
+      const float h = outs[it];
+      const T hs = from_f<T>(h);
+      y[row * p.ldy + (int64_t)d * H + j] = hs;
+      if (a.gates) {
+        if (p.mode == 0) {
+          a.gates[row * H + j] = h;
+        } else {
+          float* gp = a.gates + row * 4 * H + j;
+          gp[0] = outs[icap + it];
+          gp[H] = outs[2 * icap + it];
+          gp[2 * H] = outs[3 * icap + it];
+          gp[3 * H] = outs[4 * icap + it];
+        }
+      }
+      if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = outs[5 * icap + it];
+      if (hseq) hseq[((int64_t)slot * N + n) * H + j] = hs;
+    }
+  };
+  int pend = -1;  // the step whose outputs wait in the stash
 
   for (int s = 0; s < nT; ++s) {
     const int t = d ? nT - 1 - s : s;
@@ -472,6 +507,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
       TTRACE(s, 6);
     }
+    if (pend >= 0) flush(pend);
+    pend = -1;
     // this step's input projection values, each item's G values fetched by the
     // thread that consumes them (it waits for its own copies only): issued
     // after the polls, whose loads would otherwise queue behind these reads
@@ -550,13 +587,12 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     if (live) {
       // the partial sums of each gate (rank order, fixed; ranks with an empty K
       // slice push nothing) feed the gate math;
-      // the exchange word of h_t goes out first, the workspace stores after it
+      // the exchange word of h_t goes out first; the workspace outputs wait in
+      // the stash until the next step
       const size_t rstride = (size_t)G * Uq * Rs;
-      const int slot = d ? t : t + 1;
       for (int it = tid; it < items; it += kTThreads) {
         const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
         const int j = u0 + uq0 + uu;
-        const int64_t row = (int64_t)t * N + n;
         cp_async_wait_all();                    // this thread's projection values
         const float* gv = gxs + n * Uq + uu;    // gate g at gv[g * N * Uq]
         // all partials loaded first (independent shared loads in flight
@@ -620,21 +656,17 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                          ((unsigned long long)(s + 1) << 32) | __float_as_uint(to_f(hs)));
         if (it == tid) PTRACE(s, 28, h);
         if (it == tid) XTRACE(s, 0);
-        y[row * p.ldy + (int64_t)d * H + j] = hs;
         hst[n * Uq + uu] = h;
         if (p.mode == 1) cst[n * Uq + uu] = c;
-        if (a.gates) {
-          if (p.mode == 0) {
-            a.gates[row * H + j] = h;
-          } else {
-            float* gp = a.gates + row * 4 * H + j;
-            gp[0] = g0; gp[H] = g1; gp[2 * H] = g2; gp[3 * H] = g3;
-          }
-        }
-        if (a.cseq) a.cseq[((int64_t)slot * N + n) * H + j] = c;
-        if (hseq) hseq[((int64_t)slot * N + n) * H + j] = hs;
+        outs[it] = h;
+        outs[icap + it] = g0;
+        outs[2 * icap + it] = g1;
+        outs[3 * icap + it] = g2;
+        outs[4 * icap + it] = g3;
+        outs[5 * icap + it] = c;
         if (it == tid) PTRACE(s, 29, h);
       }
+      pend = s;
     }
     PTRACE(s, 30, 0.f);
     TTRACE(s, 4);
@@ -642,6 +674,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
     __syncthreads();
   }
+  if (pend >= 0) flush(pend);
   fence_before();
   cl_sync();  // no block leaves while a peer may still store into it
   if (s_fail == 0) {
