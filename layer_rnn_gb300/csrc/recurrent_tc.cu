@@ -100,7 +100,8 @@ constexpr int kTThreads = 256;
 constexpr int kTWarps = kTThreads / 32;
 constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
 constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
-constexpr int kPollRows = 16;   // exchange rows a lane polls at once
+constexpr int kPollRows = 16;   // exchange rows a lane polls at once (protocol probe)
+constexpr int kPollRows4 = 8;   // rows of 4 words a lane of the forward polls at once
 constexpr int kMaxPushers = 8;  // largest cluster of the plan
 
 // shared memory layout (offsets in bytes from a 1024-aligned base)
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Mb > kTM || N > Nm ||
                        Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
                        pl.KC > kMaxAtoms || pl.Kk > Kp || Pk > kMaxPushers || a.hx == nullptr ||
-                       (H & 1) != 0;
+                       (H & 3) != 0 || (pl.Kk & 3) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     s_mma_bad = 0;
@@ -431,34 +432,43 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
             }
           }
         } else {
-          // lane l holds units 2l, 2l+1 of the atom (the 4-byte word l & 3 of
-          // 16-byte chunk l >> 2 in the swizzled row), up to kPollRows rows in
-          // flight at once
-          const bool lane_in = 2 * lane < kn;
-          const uint32_t woff = (uint32_t)(lane & 3) * 4u;
-          for (int r0 = 0; r0 < nr; r0 += kPollRows) {
-            const int nb = min(kPollRows, nr - r0);
-            unsigned long long w0[kPollRows], w1[kPollRows];
-            if (!poll_tagged<kPollRows>(hxp + ka + 2 * lane, part + r0 * parts, parts, H, nb,
-                                        lane_in, (unsigned)s, w0, w1, p.status, p.timeout_ns) &&
+          // lane l takes the rows of half l >> 4 of the task's rows (rows
+          // part + (2 i + (l >> 4)) * parts) and units 4 (l & 15) .. +3 of the
+          // atom (bytes 8 (l & 1) .. +7 of 16-byte chunk (l & 15) >> 1 of the
+          // swizzled row): one 32-byte load per row, two rows per warp load,
+          // up to kPollRows4 rows of a lane in flight at once
+          const int hsub = lane >> 4, q4 = lane & 15;
+          const bool lane_in = 4 * q4 < kn;  // slices and atoms hold multiples of 4 units
+          const uint32_t woff = (uint32_t)(q4 & 1) * 8u;
+          const int nl = (nr - hsub + 1) / 2;  // this lane's rows
+          for (int r0 = 0; r0 < (nr + 1) / 2; r0 += kPollRows4) {  // warp-uniform trip count
+            const int nb = max(0, min(kPollRows4, nl - r0));
+            unsigned long long w[kPollRows4][4];
+            if (!poll_tagged4<kPollRows4>(hxp + ka + 4 * q4, part + (2 * r0 + hsub) * parts,
+                                          2 * parts, H, nb, lane_in, (unsigned)s, w, p.status,
+                                          p.timeout_ns) &&
                 lane == 0)
               s_fail = 1;  // the data is not used: the status word holds the failure
             if (lane_in) {
 #pragma unroll
-              for (int j = 0; j < kPollRows; ++j) {
+              for (int j = 0; j < kPollRows4; ++j) {
                 if (j >= nb) break;
-                const int n = part + (r0 + j) * parts;
-                const uint32_t off = sw_off(n, lane >> 2) + woff;
-                const float f0 = __uint_as_float((uint32_t)w0[j]);
-                const float f1 = __uint_as_float((uint32_t)w1[j]);
+                const int n = part + (2 * (r0 + j) + hsub) * parts;
+                const uint32_t off = sw_off(n, q4 >> 1) + woff;
+                const float f0 = __uint_as_float((uint32_t)w[j][0]);
+                const float f1 = __uint_as_float((uint32_t)w[j][1]);
+                const float f2 = __uint_as_float((uint32_t)w[j][2]);
+                const float f3 = __uint_as_float((uint32_t)w[j][3]);
                 if (BF) {
-                  *reinterpret_cast<uint32_t*>(bh + off) =
-                      (__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16);
+                  *reinterpret_cast<uint2*>(bh + off) =
+                      make_uint2((__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16),
+                                 (__float_as_uint(f2) >> 16) | ((__float_as_uint(f3) >> 16) << 16));
                 } else {
-                  uint32_t hw, lw;
-                  split_f16x2(f0 * h_scale, f1 * h_scale, hw, lw);
-                  *reinterpret_cast<uint32_t*>(bh + off) = hw;
-                  *reinterpret_cast<uint32_t*>(bl + off) = lw;
+                  uint32_t h0, l0, h1, l1;
+                  split_f16x2(f0 * h_scale, f1 * h_scale, h0, l0);
+                  split_f16x2(f2 * h_scale, f3 * h_scale, h1, l1);
+                  *reinterpret_cast<uint2*>(bh + off) = make_uint2(h0, h1);
+                  *reinterpret_cast<uint2*>(bl + off) = make_uint2(l0, l1);
                 }
               }
             }

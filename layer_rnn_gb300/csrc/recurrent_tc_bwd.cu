@@ -26,8 +26,9 @@
 // asynchronous stores that complete the owner's receive barrier) to the block
 // that owns each unit's pointwise step; the owners wait for their barrier,
 // sum the partials in a fixed order, run the gate-gradient chain, and write
-// dG_h with its exchange words (GRU: then dG_x, which no block of this launch
-// reads).  The step's pointwise inputs (dy, the saved gates, c_t
+// the exchange words of dG_h; the canonical dG_h (GRU: and dG_x), which no
+// block of this launch reads, waits in shared memory and is stored after the
+// next step's polls.  The step's pointwise inputs (dy, the saved gates, c_t
 // and c_{t-1}) are fetched with cp.async at the start of the step.
 #include <algorithm>
 #include <type_traits>
@@ -63,17 +64,12 @@ constexpr int kBMaxAtoms = 16;
 constexpr int kBPollRows = 16;  // exchange rows a lane polls at once
 constexpr int kBMaxPushers = 16;  // largest cluster of the plan
 
-__device__ __forceinline__ int owner_flag_b(int u, int Ur, int Uq, int Pk) {
-  const int r = u / Ur;
-  return r * Pk + (u - r * Ur) / Uq;
-}
-
 struct BLayout {
   uint32_t b_hi, b_lo;   // staged B tiles: KC atoms x (Nm rows x 128 bytes)
   uint32_t raw;          // fp32: the staged dG_h slice before its split, [N][Kp + 4]
   uint32_t recv;         // [2][Pk][Uq][Nm + 4] f32
   uint32_t st_dc, st_carry;  // [Uq*N] f32: LSTM dc, GRU dh*z
-  uint32_t stash;        // [3][Uq*N] f32: GRU dG_x, stored after the release
+  uint32_t stash;        // [7][Uq*N] f32: GRU dG_x, then dG_h (stored one step late)
   uint32_t pin;          // [kNIn][Uq*N] f32
   uint32_t total;
 };
@@ -96,7 +92,7 @@ __host__ __device__ inline BLayout b_layout(const RecPlan& pl, int N, bool bf) {
   L.st_carry = off;
   off += (uint32_t)pl.Uq * N * 4u;
   L.stash = off;
-  off += 3u * pl.Uq * N * 4u;
+  off += 7u * pl.Uq * N * 4u;
   L.pin = off;
   off += (uint32_t)kNIn * pl.Uq * N * 4u;
   L.total = (off + 1023u) & ~1023u;
@@ -263,10 +259,29 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   cl_sync();
   fence_after();
   uint32_t mma_phase = 0;
+  // the gate gradients of step sp (dG_h; GRU: also dG_x) from the stash, each
+  // item by the thread that computed it: written one step late, after the
+  // next step's polls, so that these stores do not queue ahead of the polls
+  const int ngo = p.mode == 1 ? 4 : p.mode == 2 ? 3 : 1;
+  auto flush = [&](int sp) {
+    const int tq = rv ? sp : nT - 1 - sp;
+    for (int it = tid; it < items; it += kBThreads) {
+      const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
+      const int64_t row = (int64_t)tq * N + n;
+      T* gho = dgh + row * GH + j;  // dG_x itself, except for the GRU
+      for (int g = 0; g < ngo; ++g) gho[(int64_t)g * H] = from_f<T>(stash[(3 + g) * icap + it]);
+      if (p.mode == 2) {
+        T* gxo = dgx + row * GH + j;
+        gxo[0] = from_f<T>(stash[it]);
+        gxo[H] = from_f<T>(stash[icap + it]);
+        gxo[2 * H] = from_f<T>(stash[2 * icap + it]);
+      }
+    }
+  };
+  int pend = -1;  // the step whose gradients wait in the stash
 
   for (int s = 0; s <= nT; ++s) {
     const int t = rv ? s : nT - 1 - s;   // time processed at this step (s < nT)
-    const int tp = rv ? s - 1 : nT - s;  // time processed at the previous step (s > 0)
     const bool failed = s_fail != 0;     // read after the previous step's barrier
     // the partials of step s >= 1 land in buffer and barrier s & 1 (use
     // (s - 1) >> 1 of that barrier): one arrival plus the peers' bytes
@@ -376,6 +391,8 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
       }
     }
     BTRACE(s, 6);
+    if (pend >= 0) flush(pend);
+    pend = -1;
     // pointwise inputs of time t, issued after the polls (whose loads would
     // otherwise queue behind these reads of memory) and consumed after the
     // contraction and the exchange, each by the thread that fetched it (fp32
@@ -491,7 +508,6 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
                               : pin[it];
         const float dh = dyv + dhf;
         const float g0 = pin[1 * icap + it];
-        T* gxo = dgx + row * GH + j;
         // the exchange words of this step's dG_h (value as stored, and the
         // step that reads it: every step below nT, the last one included,
         // has a successor that multiplies it)
@@ -529,32 +545,22 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         } else {  // tanh RNN: g0 = h_t
           gh[0] = dh * (1.f - g0 * g0);
         }
-        T* gho = dgh + row * GH + j;  // dG_x itself, except for the GRU
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           if (g >= ng) break;
           const T v = from_f<T>(gh[g]);
           if (xw) st_relaxed_u64(xo + (int64_t)g * H, tag | __float_as_uint(to_f(v)));
-          gho[(int64_t)g * H] = v;
+          stash[(3 + g) * icap + it] = gh[g];
         }
       }
+      if (s < nT) pend = s;
     }
     BTRACE(s, 4);
     BTRACE(s, 5);
-    // GRU: dG_x (read by the dense phases only) after the exchange words, by
-    // the thread that computed it
-    if (live && p.mode == 2 && s < nT) {
-      for (int it = tid; it < items; it += kBThreads) {
-        const int uu = it % Uqc, n = it / Uqc, j = u0 + uq0 + uu;
-        T* gxo = dgx + ((int64_t)t * N + n) * GH + j;
-        gxo[0] = from_f<T>(stash[it]);
-        gxo[H] = from_f<T>(stash[icap + it]);
-        gxo[2 * H] = from_f<T>(stash[2 * icap + it]);
-      }
-    }
     if ((!live || s_mma_bad) && tid == 0) s_fail = 1;
     __syncthreads();
   }
+  if (pend >= 0) flush(pend);
   fence_before();
   cl_sync();  // no block leaves while a peer may still store into it
   fence_before();

@@ -246,6 +246,48 @@ __device__ __forceinline__ bool poll_tagged(const unsigned long long* p, int row
   return __all_sync(0xffffffffu, ok);
 }
 
+// As poll_tagged, four consecutive words per row (one 32-byte load, 32-byte
+// aligned): word i of row j of this lane lands in w[j][i].
+template <int R>
+__device__ __forceinline__ bool poll_tagged4(const unsigned long long* p, int row0, int rstep,
+                                             int64_t ld, int nb, bool active, unsigned tag,
+                                             unsigned long long (&w)[R][4], int* status,
+                                             long long timeout_ns) {
+  unsigned pending = active ? ((1u << nb) - 1u) : 0u;
+  unsigned long long t0 = 0;
+  unsigned it = 0;
+  bool ok = true;
+  while (pending) {
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if ((pending >> j) & 1u) {
+        const unsigned long long* q = p + (int64_t)(row0 + j * rstep) * ld;
+        asm volatile("ld.relaxed.gpu.global.v4.b64 {%0, %1, %2, %3}, [%4];"
+                     : "=l"(w[j][0]), "=l"(w[j][1]), "=l"(w[j][2]), "=l"(w[j][3])
+                     : "l"(q)
+                     : "memory");
+      }
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (((pending >> j) & 1u) && (unsigned)(w[j][0] >> 32) == tag &&
+          (unsigned)(w[j][1] >> 32) == tag && (unsigned)(w[j][2] >> 32) == tag &&
+          (unsigned)(w[j][3] >> 32) == tag)
+        pending &= ~(1u << j);
+    if (!pending) break;
+    if (it == 0) t0 = globaltimer_ns();
+    if ((++it & 31u) == 0) {
+      if (ld_volatile_int(status) != kDevOk) {
+        ok = false;
+      } else if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+        atomicCAS(status, kDevOk, kDevTimeout);
+        ok = false;
+      }
+      if (!ok) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
