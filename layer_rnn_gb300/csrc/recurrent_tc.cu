@@ -100,7 +100,6 @@ constexpr int kTThreads = 256;
 constexpr int kTWarps = kTThreads / 32;
 constexpr int kTM = 128;        // MMA M (rows of W per block, padded)
 constexpr int kMaxAtoms = 16;   // K atoms (128 bytes of K per row) of a block's slice
-constexpr int kPollRows = 16;   // exchange rows a lane polls at once (protocol probe)
 constexpr int kPollRows4 = 8;   // rows of 4 words a lane of the forward polls at once
 constexpr int kMaxPushers = 8;  // largest cluster of the plan
 
@@ -730,7 +729,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_cons
   const int pushers = min(Pk, (H + Kk - 1) / Kk);
   const uint32_t rbar0 = smem_addr(&recv_bar[0]);
   const bool cfg_bad = cl_size() != (unsigned)Pk || cl_rank() != (unsigned)q || a.hx == nullptr ||
-                       Pk > 32;
+                       Pk > 32 || (H & 3) != 0 || (Kk & 3) != 0;
   if (tid == 0) {
     s_fail = cfg_bad;
     if (cfg_bad) atomicCAS(p.status, kDevOk, kDevCheck);
@@ -750,11 +749,13 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_step_probe(const __grid_cons
         const int at = task % KCu, part = task / KCu;
         const int ka = at * EPA, kn = min(EPA, Kc - ka);
         const int nr = (N - part + parts - 1) / parts;
-        for (int r0 = 0; r0 < nr; r0 += kPollRows) {
-          unsigned long long w0[kPollRows], w1[kPollRows];
-          if (!poll_tagged<kPollRows>(hxp + ka + 2 * lane, part + r0 * parts, parts, H,
-                                      min(kPollRows, nr - r0), 2 * lane < kn, (unsigned)s, w0,
-                                      w1, p.status, p.timeout_ns) &&
+        const int hsub = lane >> 4, q4 = lane & 15;
+        const int nl = (nr - hsub + 1) / 2;
+        for (int r0 = 0; r0 < (nr + 1) / 2; r0 += kPollRows4) {
+          unsigned long long w[kPollRows4][4];
+          if (!poll_tagged4<kPollRows4>(hxp + ka + 4 * q4, part + (2 * r0 + hsub) * parts,
+                                        2 * parts, H, max(0, min(kPollRows4, nl - r0)),
+                                        4 * q4 < kn, (unsigned)s, w, p.status, p.timeout_ns) &&
               lane == 0)
             s_fail = 1;
         }

@@ -61,7 +61,7 @@ constexpr int kBWarps = kBThreads / 32;
 constexpr int kBM = 128;    // MMA M: output units per row group (padded)
 constexpr int kNIn = 7;     // pointwise inputs per item: dy, 4 gates, c_t, c_{t-1} / h_{t-1}
 constexpr int kBMaxAtoms = 16;
-constexpr int kBPollRows = 16;  // exchange rows a lane polls at once
+constexpr int kBPollRows4 = 8;  // rows of 4 words a lane polls at once
 constexpr int kBMaxPushers = 16;  // largest cluster of the plan
 
 struct BLayout {
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
                        (ncols & (ncols - 1u)) != 0 || ncols < 32u || Ur > kBM || N > Nm ||
                        Nm % 16 != 0 || Nm > 256 || Kp % EPA != 0 || pl.KC * EPA != Kp ||
                        pl.KC > kBMaxAtoms || pl.Kk > Kp || Uq * Pk < Ur || Pk > kBMaxPushers ||
-                       a.hx == nullptr || (GH & 1) != 0;
+                       a.hx == nullptr || (GH & 3) != 0 || (pl.Kk & 3) != 0;
   if (tid == 0) {
     s_fail = ld_volatile_int(p.status) != kDevOk || cfg_bad;
     s_mma_bad = 0;
@@ -301,28 +301,37 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         const int at = task % KCu, part = task / KCu;
         const int ka = at * EPA, kn = min(EPA, Kc - ka);
         const int nr = (N - part + parts - 1) / parts;  // rows part, part + parts, ...
-        const bool lane_in = 2 * lane < kn;  // lane l: gate rows ka + 2l, ka + 2l + 1
-        for (int r0 = 0; r0 < nr; r0 += kBPollRows) {
-          const int nb = min(kBPollRows, nr - r0);
-          unsigned long long w0[kBPollRows], w1[kBPollRows];
-          if (!poll_tagged<kBPollRows>(gxp + ka + 2 * lane, part + r0 * parts, parts, GH, nb,
-                                       lane_in, (unsigned)s, w0, w1, p.status, p.timeout_ns) &&
+        // lane l takes the rows of half l >> 4 of the task's rows (rows
+        // part + (2 i + (l >> 4)) * parts) and gate rows ka + 4 (l & 15) .. +3:
+        // one 32-byte load per row, two rows per warp load
+        const int hsub = lane >> 4, q4 = lane & 15;
+        const bool lane_in = 4 * q4 < kn;  // slices and atoms hold multiples of 4 gate rows
+        const int nl = (nr - hsub + 1) / 2;  // this lane's rows
+        for (int r0 = 0; r0 < (nr + 1) / 2; r0 += kBPollRows4) {  // warp-uniform trip count
+          const int nb = max(0, min(kBPollRows4, nl - r0));
+          unsigned long long w[kBPollRows4][4];
+          if (!poll_tagged4<kBPollRows4>(gxp + ka + 4 * q4, part + (2 * r0 + hsub) * parts,
+                                         2 * parts, GH, nb, lane_in, (unsigned)s, w, p.status,
+                                         p.timeout_ns) &&
               lane == 0)
             s_fail = 1;  // the data is not used: the status word holds the failure
           if (!lane_in) continue;
 #pragma unroll
-          for (int j = 0; j < kBPollRows; ++j) {
+          for (int j = 0; j < kBPollRows4; ++j) {
             if (j >= nb) break;
-            const int n = part + (r0 + j) * parts;
-            const float f0 = __uint_as_float((uint32_t)w0[j]);
-            const float f1 = __uint_as_float((uint32_t)w1[j]);
+            const int n = part + (2 * (r0 + j) + hsub) * parts;
+            const float f0 = __uint_as_float((uint32_t)w[j][0]);
+            const float f1 = __uint_as_float((uint32_t)w[j][1]);
+            const float f2 = __uint_as_float((uint32_t)w[j][2]);
+            const float f3 = __uint_as_float((uint32_t)w[j][3]);
             if (BF) {
-              *reinterpret_cast<uint32_t*>(base + Lo.b_hi + (uint32_t)at * atom_bytes +
-                                           sw_off(n, lane >> 2) + (uint32_t)(lane & 3) * 4u) =
-                  (__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16);
+              *reinterpret_cast<uint2*>(base + Lo.b_hi + (uint32_t)at * atom_bytes +
+                                        sw_off(n, q4 >> 1) + (uint32_t)(q4 & 1) * 8u) =
+                  make_uint2((__float_as_uint(f0) >> 16) | ((__float_as_uint(f1) >> 16) << 16),
+                             (__float_as_uint(f2) >> 16) | ((__float_as_uint(f3) >> 16) << 16));
             } else {
-              *reinterpret_cast<float2*>(raw + n * Ks + ka + 2 * lane) = make_float2(f0, f1);
-              lmax = fmaxf(lmax, fmaxf(fabsf(f0), fabsf(f1)));
+              *reinterpret_cast<float4*>(raw + n * Ks + ka + 4 * q4) = make_float4(f0, f1, f2, f3);
+              lmax = fmaxf(lmax, fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
             }
           }
         }
