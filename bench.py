@@ -35,12 +35,12 @@ from layer_rnn_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "LSTM/GRU fwd+bwd sequences/s and effective TFLOP/s at DS2 shape, 1×GB300"
 PHASE_NAMES = ("input_gemm", "rec_fwd", "rec_bwd", "dx_gemm", "dw_gemm")
-PHASE_KERNELS = {"input_gemm": "gemm_tc_kernel (+ split_kernel): input projection",
+PHASE_KERNELS = {"input_gemm": "gemm_tc_kernel (+ absmax, split_f16): input projection",
                  "rec_fwd": "rec_fwd_* persistent recurrent forward",
                  "rec_bwd": "rec_bwd_* persistent recurrent backward",
-                 "dx_gemm": "gemm_tc_kernel (+ split_kernel): dX",
-                 "dw_gemm": "gemm_tc_kernel (+ split/transpose, splitk_reduce, colsum): dW, db"}
-# nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25 -> tf32 = bf16 x 1.1/2.25
+                 "dx_gemm": "gemm_tc_kernel (+ absmax, split_f16): dX",
+                 "dw_gemm": "gemm_tc_kernel (+ absmax, split_f16 / transpose, splitk_reduce, "
+                            "colsum): dW, db"}
 
 
 def gates(mode):
@@ -435,14 +435,12 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
         if on_tensor:
             if dt == "bf16":
                 return "tensor", bf16_sus, "%s bf16 dense, sustained (cuBLAS loop)" % peak_src
-            if ph == "rec_fwd" and paths[0] == "tensor":
-                return ("tensor", bf16_sus / 3.0,
-                        "%s bf16 sustained / 3 passes: fp32 as three fp16 passes on "
-                        "scaled hi / lo splits (fp16 and bf16 share the kind::f16 rate)"
-                        % peak_src)
-            return ("tensor", bf16_sus * 1.1 / 2.25 / 3.0,
-                    "%s bf16 sustained x 1.1/2.25 (nominal tf32/bf16) / 3 passes: fp32 as "
-                    "3xTF32" % peak_src)
+            # every fp32 tensor-core phase (dense GEMMs and both recurrent
+            # kernels) runs three kind::f16 passes on scaled fp16 hi / lo pairs
+            return ("tensor", bf16_sus / 3.0,
+                    "%s bf16 sustained / 3 passes: fp32 as three fp16 passes on "
+                    "scaled hi / lo splits (fp16 and bf16 share the kind::f16 rate)"
+                    % peak_src)
         return ("alu", fp32_simt_peak_tflops(num_sms, sm_clk),
                 "fp32 FMA issue peak: %d SMs x 128 lanes x 2 flop x %.0f MHz (derived)"
                 % (num_sms, sm_clk))

@@ -337,11 +337,15 @@ rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t
  * the library's packing kernel asynchronously on `stream` into caller
  * buffers, so a test can check that the packing loses and invents nothing.
  *
- * rnn_debug_split_tf32: the tf32 hi / lo split of the dense phases' fp32
- * operands.  src [rows][cols] (row stride lds floats) -> hi, lo (lo may be
- * NULL) [rows][cols] (transpose = 0) or [cols][rows] (transpose = 1), row
- * stride ldd floats.  hi keeps the top 10 mantissa bits of each value, lo =
- * value - hi (both fp32, so hi + lo reproduces the value exactly).
+ * rnn_debug_split_f16: the scaled fp16 pairs of the dense phases' fp32
+ * operands.  src [rows][cols] (row stride lds floats) -> hi, lo (fp16)
+ * [rows][cols] (transpose = 0) or [cols][rows] (transpose = 1), row stride
+ * ldd elements; *maxbits (a 4-byte device word) receives the largest |value|
+ * as its float bit pattern.  With s = 2^(13 - E), E the binary exponent of
+ * that largest magnitude (s = 1 when it is 0 or not finite; 13 - E clamped
+ * to [-126, 126]): hi = fp16(value * s) and lo = fp16(value * s - hi), both
+ * rounded to nearest even, so hi + lo equals value * s within 2^-22 of it
+ * (down to the fp16 subnormal range).
  *
  * rnn_debug_transpose_bf16: the K-major bf16 operand copy of the dense
  * phases.  src [rows][cols] (row stride lds elements) -> dst [cols][rows]
@@ -360,9 +364,9 @@ rnn_status_t rnn_measure_step_protocol(rnn_t h, void* stream, int64_t N, int64_t
  * = b_ih + b_hh of that row (GRU: b_in on n_x, b_hn on n_h).  Rows of units
  * j >= H are zero.  wp_bytes / bias_bytes are the buffers' sizes:
  * RNN_ERR_WORKSPACE_TOO_SMALL when they are short. */
-rnn_status_t rnn_debug_split_tf32(const float* src, int64_t rows, int64_t cols, int64_t lds,
-                                  float* hi, float* lo, int64_t ldd, int transpose,
-                                  void* stream);
+rnn_status_t rnn_debug_split_f16(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                                 void* hi, void* lo, int64_t ldd, int transpose, unsigned* maxbits,
+                                 void* stream);
 rnn_status_t rnn_debug_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds,
                                       void* dst, int64_t ldd, void* stream);
 rnn_status_t rnn_debug_wf_pack(rnn_t h, void* stream, int64_t N, int layer, const void* W,

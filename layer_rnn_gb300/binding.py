@@ -63,7 +63,7 @@ SIGNATURES = {
     "rnn_get_paths": (_i32, [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_int)]),
     "rnn_measure_step_protocol": (_i32, [_vp, _vp, _i64, _i64, ctypes.POINTER(ctypes.c_double)]),
-    "rnn_debug_split_tf32": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp]),
+    "rnn_debug_split_f16": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _vp]),
     "rnn_debug_transpose_bf16": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp]),
     "rnn_debug_wf_pack": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _pi64]),
     "rnn_status_string": (ctypes.c_char_p, [_i32]),
@@ -198,8 +198,9 @@ def rnn_measure_step_protocol(h, stream, N, steps):
     return us.value
 
 
-def rnn_debug_split_tf32(src, rows, cols, lds, hi, lo, ldd, transpose, stream):
-    _call("rnn_debug_split_tf32", src, rows, cols, lds, hi, lo, ldd, int(transpose), stream)
+def rnn_debug_split_f16(src, rows, cols, lds, hi, lo, ldd, transpose, maxbits, stream):
+    _call("rnn_debug_split_f16", src, rows, cols, lds, hi, lo, ldd, int(transpose), maxbits,
+          stream)
 
 
 def rnn_debug_transpose_bf16(src, rows, cols, lds, dst, ldd, stream):

@@ -94,16 +94,17 @@ struct WsLayout {
 int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 
 // ----------------------------------------------------------------------------
-// tensor-core GEMM operands: every operand is presented K-major; fp32 operands
-// are split into hi / lo parts; copies live in a scratch region
+// tensor-core GEMM operands: every operand is presented K-major with 16-bit
+// elements; fp32 operands as scaled fp16 (hi, lo) pairs; copies live in a
+// scratch region
 // ----------------------------------------------------------------------------
 constexpr int kMaxKsplit = 8;
 
-int64_t kpad(int64_t K, bool tf32) { return tf32 ? (K + 3) / 4 * 4 : (K + 7) / 8 * 8; }
+int64_t kpad(int64_t K) { return (K + 7) / 8 * 8; }  // 16-byte rows
 
 // bytes of one operand copy: rows x K (hi and lo for fp32)
-int64_t opnd_bytes(int64_t rows, int64_t K, bool tf32) {
-  return align256(rows * kpad(K, tf32) * (tf32 ? 4 : 2)) * (tf32 ? 2 : 1);
+int64_t opnd_bytes(int64_t rows, int64_t K, bool f32) {
+  return align256(rows * kpad(K) * 2) * (f32 ? 2 : 1);
 }
 
 // whether a call may take the layer-wavefront path (host-side conditions; the
@@ -164,18 +165,32 @@ struct Scratch {
   }
 };
 
-// One GEMM operand given by strides (element (r, k) at p[r * sr + k * sk]) as a
-// K-major TcGemm operand; copies into `sc` when needed.  false: cannot.
+// Largest magnitude of an fp32 GEMM operand given by strides (element (r, k)
+// at p[r * sr + k * sk], K-major or stored transposed) into *mx (atomicMax: a
+// word zeroed before, possibly shared with another operand).
+bool operand_absmax(const void* p, int64_t rows, int64_t K, int64_t sr, int64_t sk, unsigned* mx,
+                    int num_sms, cudaStream_t st) {
+  const float* f = static_cast<const float*>(p);
+  const cudaError_t e = sk == 1 ? absmax_operand(f, rows, K, sr, mx, num_sms, st)
+                                : absmax_operand(f, K, rows, sk, mx, num_sms, st);
+  return e == cudaSuccess;
+}
+
+// One GEMM operand given by strides as a K-major TcGemm operand; copies into
+// `sc` when needed (fp32: scaled fp16 pairs with the scale of *mx).  false:
+// cannot.
 bool prep_operand(const void* p, int64_t rows, int64_t K, int64_t sr, int64_t sk, bool tf,
-                  Scratch* sc, const void** hi, const void** lo, int64_t* ld, cudaStream_t st) {
-  const int64_t kp = kpad(K, tf);
+                  Scratch* sc, const void** hi, const void** lo, int64_t* ld, const unsigned* mx,
+                  cudaStream_t st) {
+  const int64_t kp = kpad(K);
   if (tf) {
-    float* h = static_cast<float*>(sc->take(align256(rows * kp * 4)));
-    float* l = static_cast<float*>(sc->take(align256(rows * kp * 4)));
-    if (!h || !l) return false;
+    void* h = sc->take(align256(rows * kp * 2));
+    void* l = sc->take(align256(rows * kp * 2));
+    if (!h || !l || !mx) return false;
     const bool kmaj = sk == 1;
-    cudaError_t e = kmaj ? split_operand(static_cast<const float*>(p), rows, K, sr, h, l, kp, false, st)
-                         : split_operand(static_cast<const float*>(p), K, rows, sk, h, l, kp, true, st);
+    const float* f = static_cast<const float*>(p);
+    cudaError_t e = kmaj ? split_f16_operand(f, rows, K, sr, h, l, kp, false, mx, st)
+                         : split_f16_operand(f, K, rows, sk, h, l, kp, true, mx, st);
     if (e != cudaSuccess) return false;
     *hi = h;
     *lo = l;
@@ -210,28 +225,65 @@ struct PreparedA {
   const void* hi = nullptr;
   const void* lo = nullptr;
   int64_t ld = 0;
+  const unsigned* mx = nullptr;  // fp32: its largest magnitude
 };
+
+// a zeroed word for an operand's largest magnitude, from the scratch
+unsigned* take_max_word(Scratch* sc, cudaStream_t st) {
+  unsigned* mx = static_cast<unsigned*>(sc->take(256));
+  if (mx && cudaMemsetAsync(mx, 0, 8, st) != cudaSuccess) return nullptr;
+  return mx;
+}
+
+// A prepared for reuse by several GEMMs (fp32: split with its own scale)
+bool prepare_a(const rnn_handle* h, PreparedA* pa, bool tf, Scratch* sc, cudaStream_t st) {
+  if (tf) {
+    unsigned* mx = take_max_word(sc, st);
+    if (!mx || !operand_absmax(pa->src, pa->M, pa->K, pa->sam, pa->sak, mx, h->num_sms, st))
+      return false;
+    pa->mx = mx;
+  }
+  return prep_operand(pa->src, pa->M, pa->K, pa->sam, pa->sak, tf, sc, &pa->hi, &pa->lo, &pa->ld,
+                      pa->mx, st);
+}
 
 rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaStream_t st,
                       const PreparedA* pa = nullptr) {
   if (!(h->flags & RNN_FLAG_SIMT_GEMM)) {
     const bool tf = !g.in_bf16;
     TcGemm t;
-    t.M = g.M; t.N = g.N; t.K = g.K; t.tf32 = tf ? 1 : 0;
+    t.M = g.M; t.N = g.N; t.K = g.K; t.split16 = tf ? 1 : 0;
     const bool reuse = pa && pa->valid && pa->src == g.A && pa->M == g.M && pa->K == g.K &&
-                       pa->sam == g.sam && pa->sak == g.sak;
+                       pa->sam == g.sam && pa->sak == g.sak && g.K2 == 0;
     if (reuse) {
       t.A_hi = pa->hi;
       t.A_lo = pa->lo;
       t.lda = pa->ld;
     }
-    bool ok = (reuse ||
-               prep_operand(g.A, g.M, g.K, g.sam, g.sak, tf, &sc, &t.A_hi, &t.A_lo, &t.lda, st)) &&
-              prep_operand(g.B, g.N, g.K, g.sbn, g.sbk, tf, &sc, &t.B_hi, &t.B_lo, &t.ldb, st);
+    bool ok = true;
+    unsigned* mx = nullptr;  // fp32: [0] largest |A| (and |A2|), [1] largest |B| (and |B2|)
+    if (tf) {
+      mx = take_max_word(&sc, st);
+      ok = mx != nullptr;
+      if (ok && !reuse) ok = operand_absmax(g.A, g.M, g.K, g.sam, g.sak, mx, h->num_sms, st);
+      if (ok) ok = operand_absmax(g.B, g.N, g.K, g.sbn, g.sbk, mx + 1, h->num_sms, st);
+      if (ok && g.K2 > 0)
+        ok = operand_absmax(g.A2, g.M, g.K2, g.sam2, g.sak2, mx, h->num_sms, st) &&
+             operand_absmax(g.B2, g.N, g.K2, g.sbn2, g.sbk2, mx + 1, h->num_sms, st);
+      t.amax = reuse ? pa->mx : mx;
+      t.bmax = mx ? mx + 1 : nullptr;
+    }
+    ok = ok &&
+         (reuse ||
+          prep_operand(g.A, g.M, g.K, g.sam, g.sak, tf, &sc, &t.A_hi, &t.A_lo, &t.lda, mx, st)) &&
+         prep_operand(g.B, g.N, g.K, g.sbn, g.sbk, tf, &sc, &t.B_hi, &t.B_lo, &t.ldb,
+                      mx ? mx + 1 : nullptr, st);
     if (ok && g.K2 > 0) {
       t.K2 = g.K2;
-      ok = prep_operand(g.A2, g.M, g.K2, g.sam2, g.sak2, tf, &sc, &t.A2_hi, &t.A2_lo, &t.lda2, st) &&
-           prep_operand(g.B2, g.N, g.K2, g.sbn2, g.sbk2, tf, &sc, &t.B2_hi, &t.B2_lo, &t.ldb2, st);
+      ok = prep_operand(g.A2, g.M, g.K2, g.sam2, g.sak2, tf, &sc, &t.A2_hi, &t.A2_lo, &t.lda2, mx,
+                        st) &&
+           prep_operand(g.B2, g.N, g.K2, g.sbn2, g.sbk2, tf, &sc, &t.B2_hi, &t.B2_lo, &t.ldb2,
+                        mx ? mx + 1 : nullptr, st);
     }
     if (ok) {
       t.C = g.C; t.ldc = g.ldc; t.out_bf16 = g.out_bf16; t.accumulate = g.accumulate;
@@ -1098,7 +1150,7 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       PreparedA pa;
       if (!(h->flags & RNN_FLAG_SIMT_GEMM) && dgh == dgx) {
         pa.src = dgx; pa.M = GH; pa.K = T * N; pa.sam = 1; pa.sak = GH;
-        pa.valid = prep_operand(dgx, GH, T * N, 1, GH, !bf, &scl, &pa.hi, &pa.lo, &pa.ld, st);
+        pa.valid = prepare_a(h, &pa, !bf, &scl, st);
         if (!pa.valid) scl = sc;
       }
       GemmArgs g;
@@ -1245,14 +1297,23 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
 // ----------------------------------------------------------------------------
 // test hooks: the packed operand forms, produced by the library's own kernels
 // ----------------------------------------------------------------------------
-rnn_status_t rnn_debug_split_tf32(const float* src, int64_t rows, int64_t cols, int64_t lds,
-                                  float* hi, float* lo, int64_t ldd, int transpose,
-                                  void* stream) {
-  if (!src || !hi || rows < 1 || cols < 1 || lds < cols || ldd < (transpose ? rows : cols))
+rnn_status_t rnn_debug_split_f16(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                                 void* hi, void* lo, int64_t ldd, int transpose, unsigned* maxbits,
+                                 void* stream) {
+  if (!src || !hi || !lo || !maxbits || rows < 1 || cols < 1 || lds < cols ||
+      ldd < (transpose ? rows : cols))
     return RNN_ERR_INVALID_ARG;
-  if (!aligned(src, 16) || !aligned(hi, 16) || !aligned(lo, 16)) return RNN_ERR_MISALIGNED;
-  return cuda_status(split_operand(src, rows, cols, lds, hi, lo, ldd, transpose != 0,
-                                   static_cast<cudaStream_t>(stream)));
+  if (!aligned(src, 16) || !aligned(hi, 16) || !aligned(lo, 16) || !aligned(maxbits, 4))
+    return RNN_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaMemsetAsync(maxbits, 0, 4, st);
+  if (e == cudaSuccess) e = absmax_operand(src, rows, cols, lds, maxbits, sms, st);
+  if (e == cudaSuccess)
+    e = split_f16_operand(src, rows, cols, lds, hi, lo, ldd, transpose != 0, maxbits, st);
+  return cuda_status(e);
 }
 
 rnn_status_t rnn_debug_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds,

@@ -29,11 +29,14 @@ struct GemmArgs {
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
 
 // tensor-core GEMM: C[M][N] (+)= sum_k A[m][k] B[n][k] (+ second product),
-// A / B K-major (row stride lda / ldb elements); tf32 = 1: fp32 operands given
-// as hi / lo splits (three passes), tf32 = 0: bf16 operands (one pass)
+// A / B K-major (row stride lda / ldb elements, 16-bit); split16 = 1: fp32
+// operands given as scaled fp16 (hi, lo) pairs (three passes; amax / bmax: the
+// largest |A| over both products, the largest |B|, as float bit patterns),
+// split16 = 0: bf16 operands (one pass)
 struct TcGemm {
   int64_t M = 0, N = 0, K = 0, K2 = 0;
-  int tf32 = 1;
+  int split16 = 1;
+  const unsigned* amax = nullptr; const unsigned* bmax = nullptr;
   const void* A_hi = nullptr; const void* A_lo = nullptr; int64_t lda = 0;
   const void* B_hi = nullptr; const void* B_lo = nullptr; int64_t ldb = 0;
   const void* A2_hi = nullptr; const void* A2_lo = nullptr; int64_t lda2 = 0;
@@ -47,11 +50,17 @@ struct TcGemm {
 bool gemm_tc_supported(const TcGemm& g);
 cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st);
 // K splits worth using for an M x N output with K_total contraction length
-int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms);
-// fp32 [rows][cols] (row stride lds) -> hi / lo (lo may be null), [rows][cols]
-// or transposed [cols][rows], row stride ldd
-cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t lds, float* hi,
-                          float* lo, int64_t ldd, bool transpose, cudaStream_t st);
+int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms);
+// largest |x| of fp32 [rows][cols] (row stride lds) into *mx (atomicMax of the
+// float bit pattern: the caller zeroes *mx first; several operands may share it)
+cudaError_t absmax_operand(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                           unsigned* mx, int num_sms, cudaStream_t st);
+// fp32 [rows][cols] (row stride lds) -> scaled fp16 pairs hi / lo, [rows][cols]
+// or transposed [cols][rows], row stride ldd, with the scale of the largest
+// magnitude *mx (written by absmax_operand before)
+cudaError_t split_f16_operand(const float* src, int64_t rows, int64_t cols, int64_t lds, void* hi,
+                              void* lo, int64_t ldd, bool transpose, const unsigned* mx,
+                              cudaStream_t st);
 cudaError_t transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
                            int64_t ldd, cudaStream_t st);
 

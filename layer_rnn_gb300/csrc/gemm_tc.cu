@@ -5,11 +5,13 @@
 //   C[m][n] (+)= sum_k A[m][k] * B[n][k]   (+ a second product over K2)
 //
 // A and B are K-major (row-major with K contiguous).  bf16 operands run one
-// kind::f16 pass.  fp32 operands run three kind::tf32 passes on pre-split
-// operands, A_hi*B_hi + A_hi*B_lo + A_lo*B_hi, where x_hi is x with its low 13
-// mantissa bits cleared (exactly representable in tf32) and x_lo = x - x_hi
-// (the split of the error-compensated tf32 GEMM of Ootomo & Yokota, 2022),
-// which keeps the product error near fp32 level.
+// kind::f16 pass.  fp32 operands run as scaled fp16 pairs, x s = hi + lo
+// (hi = fp16(x s), lo = fp16(x s - hi), s a power of two per operand that maps
+// its largest magnitude below 2^14): three kind::f16 passes, A_hi*B_hi +
+// A_hi*B_lo + A_lo*B_hi, into one fp32 accumulator, multiplied by 1/(s_A s_B)
+// in the epilogue.  About 22 significant bits per operand, as the
+// error-compensated split of Ootomo & Yokota (2022) on tf32, at the f16
+// tensor rate and with 16-bit operands (half the bytes per K of tf32 pairs).
 //
 // One CTA computes one 128 x BN output tile (or one K range of it when the
 // problem is split along K; the partial tiles are then summed in a fixed order
@@ -17,6 +19,7 @@
 // and all four warps read the accumulator out of tensor memory for the
 // epilogue.  Every mbarrier wait is bounded by %globaltimer.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <mutex>
@@ -46,6 +49,8 @@ struct TcKParams {
   int64_t bias2_limit;
   int bias_bf16;
   float* part;          // split-K partials [ksplit][M][N] (fp32), or null
+  const unsigned* amax;  // scaled fp16 pairs: largest |A|, |B| (float bit patterns)
+  const unsigned* bmax;
   int* status;
   long long timeout_ns;
 };
@@ -118,16 +123,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t acc) {
   asm volatile(
@@ -162,7 +157,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN, bool TF32>
+// operand scale exponent from the largest magnitude (the split kernels use
+// the same function); defined with the split kernels below
+__device__ __forceinline__ int f16_scale_exp(unsigned mb);
+__device__ __forceinline__ float pow2f(int e);
+
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcKParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -171,8 +171,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int abort_flag;
   constexpr int kA = BM * 128;                     // bytes of one A tile
   constexpr int kB = BN * 128;                     // bytes of one B tile
-  constexpr int kStage = (kA + kB) * (TF32 ? 2 : 1);
-  constexpr uint32_t kIdesc = (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) |
+  constexpr int kStage = (kA + kB) * (SPLIT ? 2 : 1);
+  // kind::f16, fp32 accumulate; A and B fp16 (0, scaled pairs) or bf16 (1)
+  constexpr uint32_t kIdesc = (1u << 4) | ((SPLIT ? 0u : 1u) << 7) | ((SPLIT ? 0u : 1u) << 10) |
                               ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.stages;
@@ -215,12 +216,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t fb = full0 + 8 * s;
       mbar_expect_tx(fb, (uint32_t)kStage);
       const bool second = kb >= p.nk1;
-      const int kx = (second ? kb - p.nk1 : kb) * (TF32 ? 32 : 64);
+      const int kx = (second ? kb - p.nk1 : kb) * 64;
       const CUtensorMap* ah = second ? &maps.a2h : &maps.a1h;
       const CUtensorMap* bh = second ? &maps.b2h : &maps.b1h;
       tma_load_2d(st, ah, kx, m0, fb);
       tma_load_2d(st + kA, bh, kx, n0, fb);
-      if (TF32) {
+      if (SPLIT) {
         const CUtensorMap* al = second ? &maps.a2l : &maps.a1l;
         const CUtensorMap* bl = second ? &maps.b2l : &maps.b1l;
         tma_load_2d(st + kA + kB, al, kx, m0, fb);
@@ -240,11 +241,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
         const uint64_t adv = (uint64_t)(kk * 2);
         const uint32_t acc0 = (it > 0 || kk > 0) ? 1u : 0u;
-        if (TF32) {
+        if (SPLIT) {
+          // hi hi + hi lo + lo hi into one accumulator (lo is not rescaled)
           const uint64_t al = sw128_desc(st + kA + kB), bl = sw128_desc(st + 2 * kA + kB);
-          mma_tf32(tmem, ah + adv, bh + adv, kIdesc, acc0);
-          mma_tf32(tmem, ah + adv, bl + adv, kIdesc, 1u);
-          mma_tf32(tmem, al + adv, bh + adv, kIdesc, 1u);
+          mma_f16(tmem, ah + adv, bh + adv, kIdesc, acc0);
+          mma_f16(tmem, ah + adv, bl + adv, kIdesc, 1u);
+          mma_f16(tmem, al + adv, bh + adv, kIdesc, 1u);
         } else {
           mma_f16(tmem, ah + adv, bh + adv, kIdesc, acc0);
         }
@@ -280,6 +282,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
     const int rbase = m0 + warp * 32;
+    // scaled fp16 pairs: the product carries s_A s_B (powers of two)
+    float ia = 1.f, ib = 1.f;
+    if (SPLIT) {
+      ia = pow2f(-f16_scale_exp(*p.amax));
+      ib = pow2f(-f16_scale_exp(*p.bmax));
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       const int n = n0 + c0 + lane;
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = rbase + r;
         if (row >= p.M) break;
         float x = tile[r * (BN + 1) + c0 + lane];
+        if (SPLIT) x = x * ia * ib;
         if (p.part) {
           p.part[((int64_t)z * p.M + row) * p.N + n] = x;
           continue;
@@ -343,14 +352,138 @@ __global__ void splitk_reduce_kernel(const float* part, int ks, int64_t M, int64
 }
 
 // ---------------------------------------------------------------------------
-// operand preparation: fp32 -> (hi, lo) split, optionally transposed; bf16
-// transpose.  32 x 32 tiles through shared memory.
+// operand preparation: fp32 -> scaled fp16 (hi, lo) pairs, optionally
+// transposed; bf16 transpose
 // ---------------------------------------------------------------------------
-__global__ void split_kernel(const float* src, int64_t rows, int64_t cols, int64_t lds,
-                             float* hi, float* lo, int64_t ldd, int transpose) {
+// ---------------------------------------------------------------------------
+// fp32 operands as scaled fp16 pairs: x * s = hi + lo + e with hi = fp16(x s),
+// lo = fp16(x s - hi) (unscaled: the three products hi hi, hi lo, lo hi go to
+// one accumulator), |e| <= 2^-22 |x s| for |x s| >= 2^-14; s is a power of
+// two per operand that maps the operand's largest magnitude into
+// [2^13, 2^14) (fp16 holds up to 65504), and the product is multiplied by
+// 1 / (s_A s_B) in the epilogue (exact: powers of two).  Elements more than
+// 2^27 below the largest lose relative precision; they weigh less than
+// 2^-27 of it in any sum.
+// ---------------------------------------------------------------------------
+
+// largest |x| of an operand, as the bit pattern of a non-negative float
+// (ordered like the values): atomicMax into *out, which starts at 0
+__global__ void __launch_bounds__(256) absmax_kernel(const float* __restrict__ src, int64_t rows,
+                                                     int64_t cols, int64_t lds, unsigned* out) {
+  unsigned m = 0;
+  const int64_t total = rows * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cols, c = i - r * cols;
+    m = max(m, __float_as_uint(src[r * lds + c]) & 0x7FFFFFFFu);
+  }
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(out, m);
+}
+
+// the same for 16-byte aligned rows whose length is a multiple of 4
+__global__ void __launch_bounds__(256) absmax_v_kernel(const float* __restrict__ src, int64_t rows,
+                                                       int64_t cols, int64_t lds, unsigned* out) {
+  unsigned m = 0;
+  const int64_t cv = cols / 4, total = rows * cv;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cv, c = (i - r * cv) * 4;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    m = max(max(m, __float_as_uint(v.x) & 0x7FFFFFFFu),
+            max(max(__float_as_uint(v.y) & 0x7FFFFFFFu, __float_as_uint(v.z) & 0x7FFFFFFFu),
+                __float_as_uint(v.w) & 0x7FFFFFFFu));
+  }
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(out, m);
+}
+
+// exponent sh of the scale s = 2^sh for an operand whose largest magnitude
+// has the bit pattern `mb`: the largest lands in [2^13, 2^14); an all-zero or
+// non-finite operand gets s = 1
+__device__ __forceinline__ int f16_scale_exp(unsigned mb) {
+  if (mb == 0u || mb >= 0x7F800000u) return 0;
+  const int E = (int)(mb >> 23) - 127;  // largest in [2^E, 2^(E+1)) (E = -127: subnormal)
+  return min(max(13 - E, -126), 126);
+}
+__device__ __forceinline__ float pow2f(int e) {  // 2^e, -126 <= e <= 127
+  return __uint_as_float((unsigned)(e + 127) << 23);
+}
+
+__device__ __forceinline__ void f16_pair(float v, float s, __half& h, __half& l) {
+  const float x = v * s;  // exact: s is a power of two (no overflow: |x| < 2^14)
+  h = __float2half_rn(x);
+  l = __float2half_rn(x - __half2float(h));  // x - h is exact in fp32
+}
+
+// plain split, 4 columns per thread and step (16-byte aligned source rows,
+// 8-byte aligned destination rows, cols % 4 == 0)
+__global__ void __launch_bounds__(256) split_f16_v_kernel(const float* __restrict__ src,
+                                                          int64_t rows, int64_t cols, int64_t lds,
+                                                          __half* __restrict__ hi,
+                                                          __half* __restrict__ lo, int64_t ldd,
+                                                          const unsigned* maxbits) {
+  const float s = pow2f(f16_scale_exp(*maxbits));
+  const int64_t cv = cols / 4, total = rows * cv;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cv, c = (i - r * cv) * 4;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    __align__(8) __half h[4], l[4];
+    f16_pair(v.x, s, h[0], l[0]);
+    f16_pair(v.y, s, h[1], l[1]);
+    f16_pair(v.z, s, h[2], l[2]);
+    f16_pair(v.w, s, h[3], l[3]);
+    *reinterpret_cast<uint2*>(hi + r * ldd + c) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(lo + r * ldd + c) = *reinterpret_cast<const uint2*>(l);
+  }
+}
+
+// transposing split: a 64 x 64 tile through shared memory (row pitch 65
+// floats), 16-byte reads; each thread writes 4 output columns (8 bytes) of a
+// row (rows % 4 == 0, 16-byte aligned source rows, 8-byte aligned destination)
+__global__ void __launch_bounds__(256) split_f16_tt_kernel(const float* __restrict__ src,
+                                                           int64_t rows, int64_t cols,
+                                                           int64_t lds, __half* __restrict__ hi,
+                                                           __half* __restrict__ lo, int64_t ldd,
+                                                           const unsigned* maxbits) {
+  __shared__ float tile[64][65];
+  const float s = pow2f(f16_scale_exp(*maxbits));
+  const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+  const int tid = threadIdx.x, q = tid & 15, sub = tid >> 4;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int row = p * 16 + sub;
+    const int64_t r = r0 + row, c = c0 + 4 * q;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows && c < cols) v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    tile[row][4 * q + 0] = v.x;
+    tile[row][4 * q + 1] = v.y;
+    tile[row][4 * q + 2] = v.z;
+    tile[row][4 * q + 3] = v.w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int oc = p * 16 + sub;
+    const int64_t orow = c0 + oc, ocol = r0 + 4 * q;
+    if (orow >= cols || ocol >= rows) continue;
+    __align__(8) __half h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f16_pair(tile[4 * q + i][oc], s, h[i], l[i]);
+    *reinterpret_cast<uint2*>(hi + orow * ldd + ocol) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(lo + orow * ldd + ocol) = *reinterpret_cast<const uint2*>(l);
+  }
+}
+
+// generic split (any shape and alignment), optionally transposed
+__global__ void split_f16_kernel(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                                 __half* hi, __half* lo, int64_t ldd, int transpose,
+                                 const unsigned* maxbits) {
   __shared__ float tile[32][33];
+  const float s = pow2f(f16_scale_exp(*maxbits));
   const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int k = ty; k < 32; k += 8) {
     const int64_t r = r0 + k, c = c0 + tx;
     tile[k][tx] = (r < rows && c < cols) ? src[r * lds + c] : 0.f;
@@ -370,75 +503,10 @@ __global__ void split_kernel(const float* src, int64_t rows, int64_t cols, int64
       ocol = c0 + tx;
       if (orow >= rows || ocol >= cols) continue;
     }
-    const float h = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+    __half h, l;
+    f16_pair(v, s, h, l);
     hi[orow * ldd + ocol] = h;
-    if (lo) lo[orow * ldd + ocol] = v - h;
-  }
-}
-
-// tf32 hi/lo split for aligned shapes (16-byte aligned buffers, row strides
-// and column counts multiples of 4; rows a multiple of 4 when transposing).
-// Plain (split_v_kernel): one 16-byte vector of 4 columns per thread and loop
-// step.  Transposing (split_tt_kernel): a 64 x 64 tile through shared memory
-// (row pitch 65 floats), read and written with 16-byte accesses, a warp
-// covering two 256-byte row pieces per access on both sides.  (A
-// register-blocked transposing version, 8 x 4 per thread with 16-byte stores
-// to 32 rows at once, measured slower than the 32 x 32 tile of split_kernel.)
-__device__ __forceinline__ float4 tf32_hi4(float4 v) {
-  return make_float4(__uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u),
-                     __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u),
-                     __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u),
-                     __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u));
-}
-
-__global__ void __launch_bounds__(256) split_v_kernel(const float* __restrict__ src, int64_t rows,
-                                                      int64_t cols, int64_t lds,
-                                                      float* __restrict__ hi,
-                                                      float* __restrict__ lo, int64_t ldd) {
-  const int64_t cv = cols / 4, total = rows * cv;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / cv, c = (i - r * cv) * 4;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
-    const float4 h = tf32_hi4(v);
-    *reinterpret_cast<float4*>(hi + r * ldd + c) = h;
-    if (lo)
-      *reinterpret_cast<float4*>(lo + r * ldd + c) =
-          make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
-  }
-}
-
-__global__ void __launch_bounds__(256) split_tt_kernel(const float* __restrict__ src, int64_t rows,
-                                                       int64_t cols, int64_t lds,
-                                                       float* __restrict__ hi,
-                                                       float* __restrict__ lo, int64_t ldd) {
-  __shared__ float tile[64][65];
-  const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-  const int tid = threadIdx.x, q = tid & 15, sub = tid >> 4;  // 16 vectors x 16 rows a pass
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const int row = p * 16 + sub;
-    const int64_t r = r0 + row, c = c0 + 4 * q;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < rows && c < cols) v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
-    tile[row][4 * q + 0] = v.x;
-    tile[row][4 * q + 1] = v.y;
-    tile[row][4 * q + 2] = v.z;
-    tile[row][4 * q + 3] = v.w;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const int oc = p * 16 + sub;  // source column = output row within the tile
-    const int64_t orow = c0 + oc, ocol = r0 + 4 * q;
-    if (orow >= cols || ocol >= rows) continue;
-    const float4 v = make_float4(tile[4 * q + 0][oc], tile[4 * q + 1][oc], tile[4 * q + 2][oc],
-                                 tile[4 * q + 3][oc]);
-    const float4 h = tf32_hi4(v);
-    *reinterpret_cast<float4*>(hi + orow * ldd + ocol) = h;
-    if (lo)
-      *reinterpret_cast<float4*>(lo + orow * ldd + ocol) =
-          make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+    lo[orow * ldd + ocol] = l;
   }
 }
 
@@ -541,11 +609,11 @@ bool operand_ok(const void* p, int64_t ld, int e) {
   return p && (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * e) % 16 == 0);
 }
 
-template <int BN, bool TF32>
+template <int BN, bool SPLIT>
 cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaStream_t st) {
-  constexpr int kStage = (BM * 128 + BN * 128) * (TF32 ? 2 : 1);
+  constexpr int kStage = (BM * 128 + BN * 128) * (SPLIT ? 2 : 1);
   const size_t smem = (size_t)kp.stages * kStage + 1024;
-  auto fn = gemm_tc_kernel<BN, TF32>;
+  auto fn = gemm_tc_kernel<BN, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   fn<<<grid, kTcThreads, smem, st>>>(maps, kp);
@@ -577,23 +645,20 @@ bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* d
 // tile reads each A tile once for twice the MMA work of a 128 x 128 tile,
 // which matters because the operand stream from L2 (about 64 bytes per clock
 // per SM) otherwise limits the tensor pipe (bf16 128 x 128 tiles need ~117).
-int gemm_tc_bn(int64_t N, bool tf32) {
-  (void)tf32;
-  return N >= 192 ? 256 : N > 64 ? 128 : 64;
-}
+int gemm_tc_bn(int64_t N) { return N >= 192 ? 256 : N > 64 ? 128 : 64; }
 
 // Split of K that minimises a wave model: the grid runs in ceil(units / SMs)
 // waves of ceil(nkt / ks) 128-byte K blocks each, plus the fp32 partial sums
 // (written and read once per split) at HBM speed, in K-block time units.
-int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms) {
-  const int BN = gemm_tc_bn(N, tf32);
+int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms) {
+  const int BN = gemm_tc_bn(N);
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int64_t nkt = (K_total * (tf32 ? 4 : 2) + 127) / 128;
+  const int64_t nkt = (K_total * 2 + 127) / 128;
   if (nkt < 8 || num_sms < 1) return 1;
-  // one K block of one tile: 2*128*BN*(128/e) flop (x3 passes for fp32) on
-  // one SM at about 1/152 of the dense rate (bf16 2.25, tf32 1.1 PFLOP/s)
-  const double kb_flop = 2.0 * BM * BN * (tf32 ? 32.0 * 3.0 : 64.0);
-  const double sm_rate = (tf32 ? 1.1e15 : 2.25e15) / 152.0;
+  // one K block of one tile: 2*128*BN*64 flop (x3 passes for scaled fp16
+  // pairs) on one SM at about 1/152 of the dense f16 rate (2.25 PFLOP/s)
+  const double kb_flop = 2.0 * BM * BN * 64.0 * (split16 ? 3.0 : 1.0);
+  const double sm_rate = 2.25e15 / 152.0;
   const double t_kb = kb_flop / sm_rate;
   const double red_per_split = 8.0 * (double)M * N / 6.0e12 / t_kb;
   int best_ks = 1;
@@ -612,37 +677,41 @@ int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool tf32, int num_sms
 }
 
 bool gemm_tc_supported(const TcGemm& g) {
-  const int e = g.tf32 ? 4 : 2;
+  const int e = 2;
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
   if (!operand_ok(g.A_hi, g.lda, e) || !operand_ok(g.B_hi, g.ldb, e)) return false;
-  if (g.tf32 && (!operand_ok(g.A_lo, g.lda, e) || !operand_ok(g.B_lo, g.ldb, e))) return false;
+  if (g.split16 && (!operand_ok(g.A_lo, g.lda, e) || !operand_ok(g.B_lo, g.ldb, e) || !g.amax ||
+                    !g.bmax))
+    return false;
   if (g.K2 > 0) {
     if (!operand_ok(g.A2_hi, g.lda2, e) || !operand_ok(g.B2_hi, g.ldb2, e)) return false;
-    if (g.tf32 && (!operand_ok(g.A2_lo, g.lda2, e) || !operand_ok(g.B2_lo, g.ldb2, e)))
+    if (g.split16 && (!operand_ok(g.A2_lo, g.lda2, e) || !operand_ok(g.B2_lo, g.ldb2, e)))
       return false;
   }
   return encode_fn() != nullptr;
 }
 
 cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
-  const bool tf32 = g.tf32 != 0;
-  const int BN = gemm_tc_bn(g.N, tf32);
+  const bool sp = g.split16 != 0;
+  const int BN = gemm_tc_bn(g.N);
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
-  bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, !tf32, BM) &&
-            make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, !tf32, BN);
-  if (tf32)
-    ok = ok && make_map(&maps.a1l, g.A_lo, g.M, g.K, g.lda, false, BM) &&
-         make_map(&maps.b1l, g.B_lo, g.N, g.K, g.ldb, false, BN);
+  // every operand is 16-bit (fp16 pairs or bf16): TMA copies bytes, so one
+  // 16-bit map type serves both
+  bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, true, BM) &&
+            make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, true, BN);
+  if (sp)
+    ok = ok && make_map(&maps.a1l, g.A_lo, g.M, g.K, g.lda, true, BM) &&
+         make_map(&maps.b1l, g.B_lo, g.N, g.K, g.ldb, true, BN);
   if (g.K2 > 0) {
-    ok = ok && make_map(&maps.a2h, g.A2_hi, g.M, g.K2, g.lda2, !tf32, BM) &&
-         make_map(&maps.b2h, g.B2_hi, g.N, g.K2, g.ldb2, !tf32, BN);
-    if (tf32)
-      ok = ok && make_map(&maps.a2l, g.A2_lo, g.M, g.K2, g.lda2, false, BM) &&
-           make_map(&maps.b2l, g.B2_lo, g.N, g.K2, g.ldb2, false, BN);
+    ok = ok && make_map(&maps.a2h, g.A2_hi, g.M, g.K2, g.lda2, true, BM) &&
+         make_map(&maps.b2h, g.B2_hi, g.N, g.K2, g.ldb2, true, BN);
+    if (sp)
+      ok = ok && make_map(&maps.a2l, g.A2_lo, g.M, g.K2, g.lda2, true, BM) &&
+           make_map(&maps.b2l, g.B2_lo, g.N, g.K2, g.ldb2, true, BN);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const int kpe = tf32 ? 32 : 64;
+  const int kpe = 64;
   TcKParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.M = (int)g.M;
@@ -650,8 +719,10 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   kp.nk1 = (int)((g.K + kpe - 1) / kpe);
   kp.nk2 = g.K2 > 0 ? (int)((g.K2 + kpe - 1) / kpe) : 0;
   kp.ksplit = std::max(1, g.ksplit);
-  const int stage = (BM * 128 + BN * 128) * (tf32 ? 2 : 1);
+  const int stage = (BM * 128 + BN * 128) * (sp ? 2 : 1);
   kp.stages = std::max(2, std::min(8, kSmemBudget / stage));
+  kp.amax = g.amax;
+  kp.bmax = g.bmax;
   kp.status = g.status;
   kp.timeout_ns = g.timeout_ns;
   if (kp.ksplit > 1) {
@@ -669,7 +740,7 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   }
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)kp.ksplit);
   cudaError_t e;
-  if (tf32)
+  if (sp)
     e = BN == 256   ? launch_tc<256, true>(maps, kp, grid, st)
         : BN == 128 ? launch_tc<128, true>(maps, kp, grid, st)
                     : launch_tc<64, true>(maps, kp, grid, st);
@@ -687,27 +758,45 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t split_operand(const float* src, int64_t rows, int64_t cols, int64_t lds, float* hi,
-                          float* lo, int64_t ldd, bool transpose, cudaStream_t st) {
+cudaError_t absmax_operand(const float* src, int64_t rows, int64_t cols, int64_t lds,
+                           unsigned* mx, int num_sms, cudaStream_t st) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const bool al = cols % 4 == 0 && lds % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0;
+  const int64_t work = al ? rows * (cols / 4) : rows * cols;
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256,
+                                                                  (int64_t)std::max(1, num_sms) * 8));
+  if (al)
+    absmax_v_kernel<<<blocks, 256, 0, st>>>(src, rows, cols, lds, mx);
+  else
+    absmax_kernel<<<blocks, 256, 0, st>>>(src, rows, cols, lds, mx);
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t split_f16_operand(const float* src, int64_t rows, int64_t cols, int64_t lds, void* hi,
+                              void* lo, int64_t ldd, bool transpose, const unsigned* mx,
+                              cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  __half* h = static_cast<__half*>(hi);
+  __half* l = static_cast<__half*>(lo);
   const bool al = cols % 4 == 0 && lds % 4 == 0 && ldd % 4 == 0 &&
                   reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
-                  reinterpret_cast<uintptr_t>(hi) % 16 == 0 &&
-                  reinterpret_cast<uintptr_t>(lo) % 16 == 0;
+                  reinterpret_cast<uintptr_t>(hi) % 8 == 0 &&
+                  reinterpret_cast<uintptr_t>(lo) % 8 == 0;
   if (al && transpose && rows % 4 == 0 && (rows + 63) / 64 <= 65535) {
     dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
-    split_tt_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd);
+    split_f16_tt_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, h, l, ldd, mx);
     g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError();
   }
   if (al && !transpose) {
     const int64_t blocks = std::min<int64_t>((rows * (cols / 4) + 255) / 256, 152 * 16);
-    split_v_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd);
+    split_f16_v_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, rows, cols, lds, h, l, ldd, mx);
     g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError();
   }
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
-  split_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, hi, lo, ldd, transpose ? 1 : 0);
+  split_f16_kernel<<<grid, 256, 0, st>>>(src, rows, cols, lds, h, l, ldd, transpose ? 1 : 0, mx);
   g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -2,10 +2,12 @@
 hooks: every packed form the kernels read must hold exactly the canonical
 values, nothing lost, nothing invented.
 
-* tf32 hi / lo split of the dense phases' fp32 operands: hi + lo == value in
-  fp32 arithmetic, bit for bit; hi keeps the top 10 mantissa bits; the
-  transposing variants put element (i, j) at (j, i).  The shapes cover the
-  vectorised, tiled-transpose and generic kernels (aligned and ragged sizes).
+* scaled fp16 pairs of the dense phases' fp32 operands: the largest
+  magnitude, the power-of-two scale it fixes, hi = fp16(value * s) and
+  lo = fp16(value * s - hi) bit for bit as documented, hi + lo within 2^-22
+  of value * s; the transposing variants put element (i, j) at (j, i).  The
+  shapes cover the vectorised, tiled-transpose and generic kernels (aligned
+  and ragged sizes).
 * bf16 K-major copies: dst == src^T bit for bit, aligned and ragged.
 * the layer wavefront's packed rows: unpacked here from the documented
   layout (independently of the library), every row equals the canonical
@@ -40,28 +42,36 @@ def _stream():
     (256, 800, 0), (6000 // 8, 800, 1), (3200, 64, 1),   # vectorised / tiled transpose
     (37, 19, 0), (37, 19, 1), (130, 75, 1), (1, 1, 0),    # ragged: the generic kernel
 ])
-def test_tf32_split_is_exact(rows, cols, transpose):
+def test_f16_split_pairs(rows, cols, transpose):
     import torch
     from layer_rnn_gb300 import binding as B
     rng = np.random.Generator(np.random.PCG64(rows * 1000 + cols))
     # magnitudes over many binades, negative zero, subnormals
-    v = (rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-30, 30, (rows, cols))))
+    v = (rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-12, 12, (rows, cols))))
     v = v.astype(np.float32)
     v.ravel()[:3] = np.array([-0.0, 1e-40, -3e-39], dtype=np.float32)[: min(3, v.size)]
     src = torch.from_numpy(v).cuda()
     shape = (cols, rows) if transpose else (rows, cols)
-    hi = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
-    lo = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
-    B.rnn_debug_split_tf32(src.data_ptr(), rows, cols, cols, hi.data_ptr(), lo.data_ptr(),
-                           shape[1], transpose, _stream())
+    hi = torch.full(shape, float("nan"), dtype=torch.float16, device="cuda")
+    lo = torch.full(shape, float("nan"), dtype=torch.float16, device="cuda")
+    mx = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    B.rnn_debug_split_f16(src.data_ptr(), rows, cols, cols, hi.data_ptr(), lo.data_ptr(),
+                          shape[1], transpose, mx.data_ptr(), _stream())
     torch.cuda.synchronize()
-    h, l = hi.cpu().numpy(), lo.cpu().numpy()
     ref = v.T if transpose else v
-    assert np.array_equal((h + l).view(np.uint32), ref.view(np.uint32)) or \
-        np.array_equal(h + l, ref)
-    assert np.all((h.view(np.uint32) & 0x1FFF) == 0)  # tf32: 10 explicit mantissa bits
-    # hi is the value truncated to tf32, so lo carries what hi dropped
-    assert np.array_equal(h.view(np.uint32), ref.view(np.uint32) & 0xFFFFE000)
+    mb = int(mx[0].item()) & 0xFFFFFFFF
+    assert mb == int(np.abs(v).max().view(np.uint32))
+    # the documented scale: the largest magnitude lands in [2^13, 2^14)
+    E = (mb >> 23) - 127
+    s = 1.0 if mb == 0 or mb >= 0x7F800000 else 2.0 ** min(max(13 - E, -126), 126)
+    x = (ref.astype(np.float64) * s).astype(np.float32)  # exact: s is a power of two
+    eh = x.astype(np.float16)                             # round to nearest even
+    el = (x - eh.astype(np.float32)).astype(np.float16)   # x - hi is exact in fp32
+    h, l = hi.cpu().numpy(), lo.cpu().numpy()
+    assert np.array_equal(h.view(np.uint16), eh.view(np.uint16))
+    assert np.array_equal(l.view(np.uint16), el.view(np.uint16))
+    err = np.abs(x.astype(np.float64) - h.astype(np.float64) - l.astype(np.float64))
+    assert np.all(err <= 2.0 ** -22 * np.abs(x) + 2.0 ** -25)
 
 
 @pytest.mark.parametrize("rows,cols", [(512, 1024), (128, 4096), (33, 17), (200, 72)])
