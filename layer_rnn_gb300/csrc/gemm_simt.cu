@@ -222,14 +222,35 @@ __global__ void __launch_bounds__(256) colsum_part_kernel(const T* src, int64_t 
     if (cv + e < cols) out[e] = acc[e];
 }
 
-__global__ void colsum_final_kernel(const float* part, int64_t chunks, int64_t cols, void* dst,
-                                    int dst_bf16) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+// pass 2: a block per 32 columns; warp w adds the chunks w, w + 8, ... of
+// its lane's column (four loads in flight), then the eight warp sums are added
+// in warp order: a fixed order, so the result is deterministic
+__global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ part,
+                                                           int64_t chunks, int64_t cols, void* dst,
+                                                           int dst_bf16) {
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + lane;
   float t = 0.f;
-  for (int64_t k = 0; k < chunks; ++k) t += part[k * cols + c];
-  if (dst_bf16) reinterpret_cast<bf16*>(dst)[c] = __float2bfloat16_rn(t);
-  else reinterpret_cast<float*>(dst)[c] = t;
+  if (c < cols) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    int64_t k = w;
+    for (; k + 24 < chunks; k += 32) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) a[q] += __ldg(part + (k + 8 * q) * cols + c);
+    }
+    for (; k < chunks; k += 8) a[0] += __ldg(part + k * cols + c);
+    t = (a[0] + a[1]) + (a[2] + a[3]);
+  }
+  red[w][lane] = t;
+  __syncthreads();
+  if (w == 0 && c < cols) {
+    float u = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) u += red[q][lane];
+    if (dst_bf16) reinterpret_cast<bf16*>(dst)[c] = __float2bfloat16_rn(u);
+    else reinterpret_cast<float*>(dst)[c] = u;
+  }
 }
 
 }  // namespace
@@ -282,8 +303,8 @@ cudaError_t colsum(void* dst, int dst_bf16, const void* src, int src_bf16, int64
     else
       colsum_part_kernel<float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(src), rows,
                                                       cols, ld, rpc, scratch);
-    colsum_final_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(scratch, chunks, cols, dst,
-                                                                        dst_bf16);
+    colsum_final_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(scratch, chunks, cols, dst,
+                                                                      dst_bf16);
     g_kernel_launches.fetch_add(2, std::memory_order_relaxed);
     return cudaGetLastError();
   }

@@ -327,6 +327,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : "memory");
 }
 
+// C = sum_z part[z] (+ bias) (+ C); fixed order over z; four columns per
+// thread and step (N % 4 == 0, ldc % 4 == 0, fp32 output, 16-byte aligned)
+__global__ void __launch_bounds__(256) splitk_reduce_v_kernel(
+    const float* __restrict__ part, int ks, int64_t M, int64_t N, float* C, int64_t ldc,
+    int accumulate, const void* bias1, const void* bias2, int64_t bias2_limit, int bias_bf16) {
+  const int64_t nv = N / 4, total = M * nv, plane = M * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / nv, n = (i - m * nv) * 4;
+    float4 x = __ldg(reinterpret_cast<const float4*>(part + m * N + n));
+    for (int zz = 1; zz < ks; ++zz) {
+      const float4 y = __ldg(reinterpret_cast<const float4*>(part + (int64_t)zz * plane + m * N + n));
+      x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+    }
+    float b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (bias1) b[u] += load_any(bias1, n + u, bias_bf16);
+      if (bias2 && n + u < bias2_limit) b[u] += load_any(bias2, n + u, bias_bf16);
+    }
+    x.x += b[0]; x.y += b[1]; x.z += b[2]; x.w += b[3];
+    float4* c = reinterpret_cast<float4*>(C + m * ldc + n);
+    if (accumulate) {
+      const float4 o = *c;
+      x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
+    }
+    *c = x;
+  }
+}
+
 // C = sum_z part[z] (+ bias) (+ C); fixed order over z
 __global__ void splitk_reduce_kernel(const float* part, int ks, int64_t M, int64_t N, void* C,
                                      int64_t ldc, int out_bf16, int accumulate, const void* bias1,
@@ -381,21 +411,40 @@ __global__ void __launch_bounds__(256) absmax_kernel(const float* __restrict__ s
   if ((threadIdx.x & 31) == 0 && m) atomicMax(out, m);
 }
 
-// the same for 16-byte aligned rows whose length is a multiple of 4
+// the same for 16-byte aligned rows whose length is a multiple of 4: four
+// 16-byte loads in flight per thread, one atomic per block
 __global__ void __launch_bounds__(256) absmax_v_kernel(const float* __restrict__ src, int64_t rows,
                                                        int64_t cols, int64_t lds, unsigned* out) {
+  __shared__ unsigned red[8];
   unsigned m = 0;
   const int64_t cv = cols / 4, total = rows * cv;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  auto amax4 = [](float4 v) {
+    return max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+               max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
+  };
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < total; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = i + u * stride, r = j / cv, c = (j - r * cv) * 4;
+      v[u] = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = max(m, amax4(v[u]));
+  }
+  for (; i < total; i += stride) {
     const int64_t r = i / cv, c = (i - r * cv) * 4;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
-    m = max(max(m, __float_as_uint(v.x) & 0x7FFFFFFFu),
-            max(max(__float_as_uint(v.y) & 0x7FFFFFFFu, __float_as_uint(v.z) & 0x7FFFFFFFu),
-                __float_as_uint(v.w) & 0x7FFFFFFFu));
+    m = max(m, amax4(__ldg(reinterpret_cast<const float4*>(src + r * lds + c))));
   }
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0 && m) atomicMax(out, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, red[w]);
+    if (m) atomicMax(out, m);
+  }
 }
 
 // exponent sh of the scale s = 2^sh for an operand whose largest magnitude
@@ -750,10 +799,20 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
                     : launch_tc<64, false>(maps, kp, grid, st);
   if (e != cudaSuccess || kp.ksplit == 1) return e;
   const int64_t total = g.M * g.N;
-  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
-  splitk_reduce_kernel<<<blocks, 256, 0, st>>>(g.part, kp.ksplit, g.M, g.N, g.C, g.ldc, g.out_bf16,
-                                               g.accumulate, g.bias1, g.bias2, g.bias2_limit,
-                                               g.bias_bf16);
+  const bool vec = !g.out_bf16 && g.N % 4 == 0 && g.ldc % 4 == 0 &&
+                   reinterpret_cast<uintptr_t>(g.C) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(g.part) % 16 == 0;
+  if (vec) {
+    const int blocks = (int)std::min<int64_t>((total / 4 + 255) / 256, 152 * 8);
+    splitk_reduce_v_kernel<<<blocks, 256, 0, st>>>(g.part, kp.ksplit, g.M, g.N,
+                                                   static_cast<float*>(g.C), g.ldc, g.accumulate,
+                                                   g.bias1, g.bias2, g.bias2_limit, g.bias_bf16);
+  } else {
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(g.part, kp.ksplit, g.M, g.N, g.C, g.ldc,
+                                                 g.out_bf16, g.accumulate, g.bias1, g.bias2,
+                                                 g.bias2_limit, g.bias_bf16);
+  }
   g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }
@@ -763,8 +822,8 @@ cudaError_t absmax_operand(const float* src, int64_t rows, int64_t cols, int64_t
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const bool al = cols % 4 == 0 && lds % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0;
   const int64_t work = al ? rows * (cols / 4) : rows * cols;
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256,
-                                                                  (int64_t)std::max(1, num_sms) * 8));
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((work + 1023) / 1024,
+                                                                  (int64_t)std::max(1, num_sms) * 4));
   if (al)
     absmax_v_kernel<<<blocks, 256, 0, st>>>(src, rows, cols, lds, mx);
   else
