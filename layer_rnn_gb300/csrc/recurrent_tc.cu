@@ -141,7 +141,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   typedef typename std::conditional<BF, bf16, float>::type T;
   constexpr int NI = BF ? 1 : 3;   // issuing threads = accumulators (one per pass)
   constexpr int EPA = 64;            // K elements (16-bit) per 128-byte atom
-  constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
   __shared__ __align__(8) uint64_t recv_bar[2];  // partial sums of steps s (s & 1) landed
@@ -346,8 +345,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   const int icap = Uq * N;  // stride of one array of the output stash
   // the outputs of step sp (y, the saved gates, c_t, the h sequence) from the
   // stash, each item by the thread that computed it: written one step late,
-  // after the next step's polls, so that these stores do not queue ahead of
-  // the poll loads
+  // after the next step's polls and MMA issue, so that these stores do not
+  // queue ahead of the poll loads
   auto flush = [&](int sp) {
     const int tq = d ? nT - 1 - sp : sp;
     const int slot = d ? tq : tq + 1;
@@ -498,11 +497,13 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
           const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
           fence_after();
+          // a loop over the atoms: the fully unrolled issue (mma_pass_n)
+          // measured slower in this kernel (more code in the step loop)
           for (int at = 0; at < KCu; ++at) {
             const uint64_t bd = bd0 + (uint64_t)at * bstep;
             const uint32_t acol = acol0 + (uint32_t)(at * 32);
-  #pragma unroll
-            for (int kk = 0; kk < EPA / KSTEP; ++kk)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
               mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
                          (at | kk) ? 1u : 0u);
           }
@@ -516,8 +517,6 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
       TTRACE(s, 6);
     }
-    if (pend >= 0) flush(pend);
-    pend = -1;
     // this step's input projection values, each item's G values fetched by the
     // thread that consumes them (it waits for its own copies only): issued
     // after the polls, whose loads would otherwise queue behind these reads
@@ -583,6 +582,11 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       }
       if (warp == 0) WTRACE(s, 25);
     }
+    // the previous step's outputs, while the partners' partials are in flight
+    // (issued here, not beside the MMA issue, whose issuing lanes share their
+    // schedulers with these warps)
+    if (pend >= 0) flush(pend);
+    pend = -1;
     // 4. the threads with pointwise items wait for this step's partials: the
     // pushes complete the owner's barrier themselves, so no cluster barrier
     // and no release of this block's earlier global stores is waited for

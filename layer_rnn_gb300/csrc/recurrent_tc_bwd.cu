@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   typedef typename std::conditional<BF, bf16, float>::type T;
   constexpr int NI = BF ? 1 : 3;     // issuing threads = accumulators (one per pass)
   constexpr int EPA = 64;            // K elements (16-bit) per 128-byte atom
-  constexpr int KSTEP = 16;          // K per MMA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
   __shared__ __align__(8) uint64_t recv_bar[2];  // partials of steps s (s & 1) landed
@@ -383,14 +382,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           const uint64_t bstep = (uint64_t)(atom_bytes >> 4);
           const uint32_t acol0 = tmem + ((!BF && iss == 2) ? a_lo_col : a_col);
           fence_after();
-          for (int at = 0; at < KCu; ++at) {
-            const uint64_t bd = bd0 + (uint64_t)at * bstep;
-            const uint32_t acol = acol0 + (uint32_t)(at * 32);
-#pragma unroll
-            for (int kk = 0; kk < EPA / KSTEP; ++kk)
-              mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
-                         (at | kk) ? 1u : 0u);
-          }
+          mma_pass_n(KCu, dcol, acol0, bd0, bstep, idesc);
           asm volatile(
               "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                   mbar)

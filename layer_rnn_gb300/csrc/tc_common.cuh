@@ -114,6 +114,45 @@ __device__ __forceinline__ void mma_a_tmem(bool bf, uint32_t d, uint32_t a, uint
         : "memory");
 }
 
+// The MMAs of one pass over NA K atoms of 64 16-bit elements (four K steps of
+// 16 each): A from tensor memory (32 columns per atom), B from the swizzled
+// shared tile (atoms bstep descriptor units apart), accumulate into dcol from
+// the second MMA on.  Fully unrolled: the issuing thread runs a straight line
+// of MMA instructions (a loop with a runtime trip count issues them about half
+// as fast).
+template <int NA>
+__device__ __forceinline__ void mma_pass(uint32_t dcol, uint32_t acol0, uint64_t bd0,
+                                         uint64_t bstep, uint32_t idesc) {
+#pragma unroll
+  for (int at = 0; at < NA; ++at)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_a_tmem(true, dcol, acol0 + (uint32_t)(at * 32 + kk * 8),
+                 bd0 + (uint64_t)at * bstep + (uint64_t)(kk * 2), idesc, (at | kk) ? 1u : 0u);
+}
+
+// mma_pass for a runtime atom count: straight lines up to 8 atoms, a loop
+// beyond
+__device__ __forceinline__ void mma_pass_n(int na, uint32_t dcol, uint32_t acol0, uint64_t bd0,
+                                           uint64_t bstep, uint32_t idesc) {
+  switch (na) {
+    case 1: mma_pass<1>(dcol, acol0, bd0, bstep, idesc); return;
+    case 2: mma_pass<2>(dcol, acol0, bd0, bstep, idesc); return;
+    case 3: mma_pass<3>(dcol, acol0, bd0, bstep, idesc); return;
+    case 4: mma_pass<4>(dcol, acol0, bd0, bstep, idesc); return;
+    case 5: mma_pass<5>(dcol, acol0, bd0, bstep, idesc); return;
+    case 6: mma_pass<6>(dcol, acol0, bd0, bstep, idesc); return;
+    case 7: mma_pass<7>(dcol, acol0, bd0, bstep, idesc); return;
+    case 8: mma_pass<8>(dcol, acol0, bd0, bstep, idesc); return;
+    default:
+      for (int at = 0; at < na; ++at)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_a_tmem(true, dcol, acol0 + (uint32_t)(at * 32 + kk * 8),
+                     bd0 + (uint64_t)at * bstep + (uint64_t)(kk * 2), idesc, (at | kk) ? 1u : 0u);
+  }
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
