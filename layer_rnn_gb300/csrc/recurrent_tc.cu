@@ -499,11 +499,21 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
           fence_after();
           // a loop over the atoms: the fully unrolled issue (mma_pass_n)
           // measured slower in this kernel (more code in the step loop)
-          for (int at = 0; at < KCu; ++at) {
+          for (int at = 0; at + 1 < KCu; ++at) {
             const uint64_t bd = bd0 + (uint64_t)at * bstep;
             const uint32_t acol = acol0 + (uint32_t)(at * 32);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
+              mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
+                         (at | kk) ? 1u : 0u);
+          }
+          {
+            // the last atom: only its K steps that hold some of the slice
+            const int at = KCu - 1;
+            const int ksl = (Kc - at * EPA + 15) / 16;
+            const uint64_t bd = bd0 + (uint64_t)at * bstep;
+            const uint32_t acol = acol0 + (uint32_t)(at * 32);
+            for (int kk = 0; kk < ksl; ++kk)
               mma_a_tmem(true, dcol, acol + (uint32_t)(kk * 8), bd + (uint64_t)(kk * 2), idesc,
                          (at | kk) ? 1u : 0u);
           }
