@@ -12,9 +12,12 @@
 //
 // fp32 operands are split into fp16 pairs, x = (hi + lo * 2^-11) / scale
 // (hi = fp16(x * scale), lo = fp16((x * scale - hi) * 2^11)), with power-of-
-// two scales per block: W_hh^T's from its slice once, dG_h's from the staged
-// slice of every step (gradients have no fixed range), so the slice's largest
-// magnitude maps just below 2^14.  The product keeps hi*hi + hi*lo + lo*hi:
+// two scales per block: W_hh^T's from its slice once (its largest magnitude
+// just below 2^14), dG_h's per step (gradients have no fixed range): the
+// slice is split as it is polled with a scale predicted from the previous
+// step's slice (three binades of room for growth), and split again from its
+// fp32 copy only when this step's largest magnitude would overflow that scale
+// or sit more than nine binades under it.  The product keeps hi*hi + hi*lo + lo*hi:
 // three passes of 16 K, each issued by its own thread into its own
 // accumulator, about 22 significant bits per operand as three tf32 passes,
 // in half the MMA instructions.  bf16 runs one pass.
@@ -278,6 +281,10 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     }
   };
   int pend = -1;  // the step whose gradients wait in the stash
+  // fp32: the dG_h scale exponent predicted from the previous step's slice
+  int pred_eh = 0;
+  float pred_scale = 1.f;
+  bool pred_ok = false;
 
   for (int s = 0; s <= nT; ++s) {
     const int t = rv ? s : nT - 1 - s;   // time processed at this step (s < nT)
@@ -331,43 +338,72 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
             } else {
               *reinterpret_cast<float4*>(raw + n * Ks + ka + 4 * q4) = make_float4(f0, f1, f2, f3);
               lmax = fmaxf(lmax, fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+              if (pred_ok) {
+                // split now with the predicted scale (kept if the step's max
+                // turns out to fit it)
+                uint32_t h0, l0, h1, l1;
+                split_f16x2(f0 * pred_scale, f1 * pred_scale, h0, l0);
+                split_f16x2(f2 * pred_scale, f3 * pred_scale, h1, l1);
+                const uint32_t off = (uint32_t)at * atom_bytes + sw_off(n, q4 >> 1) +
+                                     (uint32_t)(q4 & 1) * 8u;
+                *reinterpret_cast<uint2*>(base + Lo.b_hi + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2*>(base + Lo.b_lo + off) = make_uint2(l0, l1);
+              }
             }
           }
         }
       }
     }
     float out_scale = 1.f;
+    // the staged tiles (bf16, or fp32 split with the predicted scale) to the
+    // tensor cores' proxy before the barrier that ends the staging
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (!BF) {
-      // the step's dG_h scale, then the split into the B tiles
+      // the step's dG_h scale (its largest magnitude just below 2^14); the
+      // tiles split with the predicted scale stand when that maps the largest
+      // magnitude into [2^4, 2^15) (no fp16 overflow, at most 9 binades of
+      // precision headroom given up), else the slice is split again
       for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
       if (lane == 0) s_red[warp] = lmax;
       __syncthreads();
+      bool keep = true;
       if (have) {
         float hm = 0.f;
         for (int w = 0; w < kBWarps; ++w) hm = fmaxf(hm, s_red[w]);
         int eh = 0;
         if (hm > 0.f) (void)frexpf(hm, &eh);
         eh = min(max(14 - eh, -100), 100);
-        const float h_scale = ldexpf(1.f, eh);
-        out_scale = ldexpf(1.f, -(ew + eh));
-        for (int idx = tid; idx < N * KCu * 8; idx += kBThreads) {
-          const int c = idx & 7, at = (idx >> 3) % KCu, n = (idx >> 3) / KCu;
-          const float* rp = raw + n * Ks + at * EPA + c * 8;
-          const float4 v0 = *reinterpret_cast<const float4*>(rp);
-          const float4 v1 = *reinterpret_cast<const float4*>(rp + 4);
-          uint4 h4, l4;
-          split_f16x2(v0.x * h_scale, v0.y * h_scale, h4.x, l4.x);
-          split_f16x2(v0.z * h_scale, v0.w * h_scale, h4.y, l4.y);
-          split_f16x2(v1.x * h_scale, v1.y * h_scale, h4.z, l4.z);
-          split_f16x2(v1.z * h_scale, v1.w * h_scale, h4.w, l4.w);
-          const uint32_t off = (uint32_t)at * atom_bytes + sw_off(n, c);
-          *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = h4;
-          *reinterpret_cast<uint4*>(base + Lo.b_lo + off) = l4;
+        keep = pred_ok && pred_eh >= eh - 9 && pred_eh <= eh + 1;
+        out_scale = ldexpf(1.f, -(ew + (keep ? pred_eh : eh)));
+        // the next step's prediction: three binades of room for growth
+        pred_eh = eh - 3;
+        pred_scale = ldexpf(1.f, pred_eh);
+        pred_ok = true;
+        if (!keep) {
+          const float h_scale = ldexpf(1.f, eh);
+          for (int idx = tid; idx < N * KCu * 8; idx += kBThreads) {
+            const int c = idx & 7, at = (idx >> 3) % KCu, n = (idx >> 3) / KCu;
+            const float* rp = raw + n * Ks + at * EPA + c * 8;
+            const float4 v0 = *reinterpret_cast<const float4*>(rp);
+            const float4 v1 = *reinterpret_cast<const float4*>(rp + 4);
+            uint4 h4, l4;
+            split_f16x2(v0.x * h_scale, v0.y * h_scale, h4.x, l4.x);
+            split_f16x2(v0.z * h_scale, v0.w * h_scale, h4.y, l4.y);
+            split_f16x2(v1.x * h_scale, v1.y * h_scale, h4.z, l4.z);
+            split_f16x2(v1.z * h_scale, v1.w * h_scale, h4.w, l4.w);
+            const uint32_t off = (uint32_t)at * atom_bytes + sw_off(n, c);
+            *reinterpret_cast<uint4*>(base + Lo.b_hi + off) = h4;
+            *reinterpret_cast<uint4*>(base + Lo.b_lo + off) = l4;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
       }
+      // a block-uniform decision: the second barrier only when the slice was
+      // split again
+      if (have && !keep) __syncthreads();
+    } else {
+      __syncthreads();
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
     BTRACE(s, 1);
 
     // 2. MMA issue: issuer i is lane 0 of warp kBWarps-1-i and runs pass i
