@@ -42,6 +42,7 @@
 // slice is staged, while the MMAs and the exchange run (the pages' ping-pong
 // prefetch).  All waits are bounded.
 #include <algorithm>
+#include <cstdio>
 #include <type_traits>
 
 #include "common.cuh"
@@ -168,6 +169,11 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t GH = (int64_t)G * H;
 
+#ifdef LAYER_RNN_TRACE
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    printf("%s plan: P %d cluster %d Ur %d Uq %d Kk %d K %d KC %d Nm %d cols %d\n", "fwd", pl.P,
+           pl.cluster, pl.Ur, pl.Uq, pl.Kk, pl.K, pl.KC, pl.nbp, pl.lda);
+#endif
   const uint32_t base_s = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
   const TcLayout Lo = tc_layout(pl, G, N, BF);

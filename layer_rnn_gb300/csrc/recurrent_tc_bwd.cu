@@ -34,6 +34,7 @@
 // next step's polls.  The step's pointwise inputs (dy, the saved gates, c_t
 // and c_{t-1}) are fetched with cp.async at the start of the step.
 #include <algorithm>
+#include <cstdio>
 #include <type_traits>
 
 #include "common.cuh"
@@ -130,6 +131,11 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
   const int KCu = (Kc + EPA - 1) / EPA;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+#ifdef LAYER_RNN_TRACE
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    printf("%s plan: P %d cluster %d Ur %d Uq %d Kk %d K %d KC %d Nm %d cols %d\n", "bwd", pl.P,
+           pl.cluster, pl.Ur, pl.Uq, pl.Kk, pl.K, pl.KC, pl.nbp, pl.lda);
+#endif
   const uint32_t base_s = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* base = smem_raw + (base_s - smem_addr(smem_raw));
   const BLayout Lo = b_layout(pl, N, BF);
@@ -681,10 +687,13 @@ bool rec_tc_bwd_plan(int mode, int bf16, int D, int H, int N, int num_sms, size_
     pl.smem = std::max<size_t>(L.total + 1024, 120 * 1024);
     if (pl.smem > smem_limit) continue;
     if (D * pl.P > num_sms) continue;
-    // MMA issue (K slice, passes), the push of Ur rows, the owners' reduction
-    // over Pk partials and their pointwise items
-    const double cost = (double)Kp * (Nm / 32.0) * 2.0 + (double)Ur * N / 16.0 +
-                        (double)Uq * N * (Pk / 4.0 + 8.0);
+    // MMA issue (K slice, passes), the staging of the K slice (its polls:
+    // rows of the slice per lane), the push of Ur rows, the owners' reduction
+    // over Pk partials and their pointwise items.  Without the staging term
+    // the GRU took clusters of 8 (slices of 5 atoms) and staged 60 % slower
+    // than with clusters of 16.
+    const double cost = (double)Kp * (Nm / 32.0) * 2.0 + (double)Kp * N / 4.0 +
+                        (double)Ur * N / 16.0 + (double)Uq * N * (Pk / 4.0 + 8.0);
     if (!found || cost < best) {
       found = true;
       best = cost;
