@@ -502,6 +502,16 @@ bool bwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPl
   return plan_rec(h, true, N, one, 1) == RNN_OK && one->tc;
 }
 
+// Forward of a bidirectional layer: when both directions together only fit a
+// CUDA-core kernel, the two directions run one after the other, each on the
+// tensor-core plan for one direction (5-layer bidirectional LSTM at H = 800:
+// 2 x 3.6 us per step against 13.2 us for the pair on the cluster kernel).
+bool fwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPlan* one) {
+  if (h->D != 2 || both.tc || h->mode == RNN_GRU_TF || (h->flags & RNN_FLAG_SIMT_RECURRENT))
+    return false;
+  return plan_rec(h, false, N, one, 1) == RNN_OK && one->tc;
+}
+
 void fill_rec_common(rnn_handle* h, int64_t T, int64_t N, RecParams* rp) {
   rp->mode = h->mode;
   rp->T = (int)T;
@@ -658,11 +668,12 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc, &wf_used);
     if (wf_used || s != RNN_OK) return s;
   }
-  RecPlan plan;
+  RecPlan plan, plan_one;
   s = plan_rec(h, false, N, &plan, h->D, lengths != nullptr);
   if (s != RNN_OK) return s;
+  const bool in_turn = !lengths && fwd_directions_in_turn(h, N, plan, &plan_one);
   unsigned long long* hx[2] = {nullptr, nullptr};
-  if (plan.tc) {
+  if (plan.tc || in_turn) {
     for (int d = 0; d < h->D; ++d) {
       hx[d] = static_cast<unsigned long long*>(sc.take(rec_tc_xchg_bytes((int)N, (int)H)));
       if (!hx[d]) return RNN_ERR_WORKSPACE_TOO_SMALL;
@@ -714,9 +725,23 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
     }
     {
       PhaseScope ps(h, st, RNN_PHASE_REC_FWD);
-      s = cuda_status(rp.plan.tc        ? rec_tc_launch(rp, st)
-                      : rp.plan.cluster ? rec_cluster_launch(false, rp, st)
-                                        : rec_forward(rp, st));
+      if (in_turn) {
+        // one launch per direction; the second runs its time order reversed
+        // and writes its half of y
+        for (int d = 0; d < 2 && s == RNN_OK; ++d) {
+          RecParams r1 = rp;
+          r1.plan = plan_one;
+          r1.D = 1;
+          r1.dir[0] = rp.dir[d];
+          r1.dir[0].rev = d;
+          r1.dir[0].y = static_cast<char*>(out) + (int64_t)d * H * e;
+          s = cuda_status(rec_tc_launch(r1, st));
+        }
+      } else {
+        s = cuda_status(rp.plan.tc        ? rec_tc_launch(rp, st)
+                        : rp.plan.cluster ? rec_cluster_launch(false, rp, st)
+                                          : rec_forward(rp, st));
+      }
       if (s != RNN_OK) return s;
     }
     if (drop_masks && l < h->L - 1) {
@@ -1285,7 +1310,8 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
   } else {
     s = plan_rec(h, false, N, &pl);
     if (s != RNN_OK) return s;
-    *fwd = kind(pl);
+    RecPlan one;
+    *fwd = fwd_directions_in_turn(h, N, pl, &one) ? kind(one) : kind(pl);
   }
   s = plan_rec(h, true, N, &pl);
   if (s != RNN_OK) return s;

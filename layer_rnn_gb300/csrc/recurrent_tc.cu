@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   const int b = blockIdx.x - d * P;
   const int r = b / Pk, q = b - r * Pk;
   const RecDirArgs& a = p.dir[d];
+  const int rv = a.rev >= 0 ? a.rev : d;       // reversed time order
   const int H = p.H, N = p.N, nT = p.T, G = p.G, Ur = pl.Ur, Uq = pl.Uq;
   const int Nm = pl.nbp;                       // MMA N (columns of D)
   const int Kp = pl.K;                         // padded K slice (elements)
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     const float cv = a.c0 ? a.c0[o] : 0.f;
     hst[n * Uq + uu] = hv;
     cst[n * Uq + uu] = cv;
-    const int slot0 = d ? nT : 0;
+    const int slot0 = rv ? nT : 0;
     if (a.hseq) reinterpret_cast<T*>(a.hseq)[(int64_t)slot0 * N * H + o] = from_f<T>(hv);
     if (a.cseq) a.cseq[(int64_t)slot0 * N * H + o] = cv;
   }
@@ -354,8 +355,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   // after the next step's polls and MMA issue, so that these stores do not
   // queue ahead of the poll loads
   auto flush = [&](int sp) {
-    const int tq = d ? nT - 1 - sp : sp;
-    const int slot = d ? tq : tq + 1;
+    const int tq = rv ? nT - 1 - sp : sp;
+    const int slot = rv ? tq : tq + 1;
     for (int it = tid; it < items; it += kTThreads) {
       const int uu = it == tid ? i_uu : it % Uqc, n = it == tid ? i_n : it / Uqc;
       const int j = u0 + uq0 + uu;
@@ -381,8 +382,8 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
   int pend = -1;  // the step whose outputs wait in the stash
 
   for (int s = 0; s < nT; ++s) {
-    const int t = d ? nT - 1 - s : s;
-    const int tp = d ? t + 1 : t - 1;
+    const int t = rv ? nT - 1 - s : s;
+    const int tp = rv ? t + 1 : t - 1;
     const bool failed = s_fail != 0;  // read after the previous step's barrier
     const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
     TTRACE(s, 0);
