@@ -324,15 +324,22 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream.synchronize()
 
-    def step():
-        r.forward_training(x, h0, c0, W, y, hy, cy, ws, stream)
-        r.backward_data(W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
-        r.backward_weights(x, h0, y, ws, dW, stream)
+    set0 = dict(x=x, h0=h0, c0=c0, W=W, dy=dy, dhy=dhy, dcy=dcy, y=y, hy=hy, cy=cy, dx=dx,
+                dh0=dh0, dc0=dc0, dW=dW)
+
+    def step_with(t):
+        r.forward_training(t["x"], t["h0"], t["c0"], t["W"], t["y"], t["hy"], t["cy"], ws, stream)
+        r.backward_data(t["W"], t["dy"], t["dhy"], t["dcy"], t["dx"], t["dh0"], t["dc0"], ws,
+                        stream)
+        r.backward_weights(t["x"], t["h0"], t["y"], ws, t["dW"], stream)
         if dist is not None:
             # data parallel over the batch: the one exchange, the sum of the
             # ranks' weight gradients (NCCL, on the launching stream)
             with torch.cuda.stream(stream):
-                dp.allreduce_grads(dW, dist)
+                dp.allreduce_grads(t["dW"], dist)
+
+    def step():
+        step_with(set0)
 
     def timed(n, fn):
         evs = []
@@ -380,31 +387,65 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
     B.rnn_enable_phase_timing(r.h, 0)
     launches_per_step = sum(n for _, n in phases.values()) / args.steps
 
-    # end to end: pinned host inputs in, results out, every step
+    # end to end: every step copies its inputs in from pinned host memory and
+    # its results out to pinned host memory, as a training loop does: the
+    # copies of step k+1's inputs and of step k-1's results run on two copy
+    # streams under step k's compute (inputs and results double-buffered on
+    # the device), and the K steps are timed as one region.  No L2 flush inside
+    # it: a step's data (about 0.4 GB at DS2 sizes) is larger than L2.
+    in_keys = ("x", "h0", "c0", "W", "dy", "dhy", "dcy")
+    out_keys = ("y", "hy", "cy", "dx", "dh0", "dc0", "dW")
     pin = {}
-    for k, t in dict(x=x, h0=h0, c0=c0, W=W, dy=dy, dhy=dhy, dcy=dcy).items():
-        if t is not None:
-            pin[k] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            pin[k].copy_(t)
-    outs = dict(y=y, hy=hy, cy=cy, dx=dx, dh0=dh0, dc0=dc0, dW=dW)
-    pout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            for k, t in outs.items() if t is not None}
+    for k in in_keys:
+        if set0[k] is not None:
+            pin[k] = torch.empty(set0[k].shape, dtype=set0[k].dtype, pin_memory=True)
+            pin[k].copy_(set0[k])
+    pout = {k: torch.empty(set0[k].shape, dtype=set0[k].dtype, pin_memory=True)
+            for k in out_keys if set0[k] is not None}
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = sum(t.numel() * t.element_size() for t in pout.values())
-    dev_in = dict(x=x, h0=h0, c0=c0, W=W, dy=dy, dhy=dhy, dcy=dcy)
+    with torch.cuda.stream(stream):
+        set1 = {k: (torch.empty_like(v) if v is not None else None) for k, v in set0.items()}
+    sets = (set0, set1)
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for k, t in pin.items():
-                dev_in[k].copy_(t, non_blocking=True)
-        step()
-        with torch.cuda.stream(stream):
-            for k, t in pout.items():
-                t.copy_(outs[k], non_blocking=True)
+    def e2e_run(K):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        s_in.wait_event(start)
+        done, copied = [None] * K, [None] * K
+        for k in range(K):
+            t = sets[k % 2]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(done[k - 2])      # step k-2 has read these inputs
+                for key, h in pin.items():
+                    t[key].copy_(h, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            stream.wait_event(ready)
+            if k >= 2:
+                stream.wait_event(copied[k - 2])      # step k-2's results are out
+            step_with(t)
+            done[k] = torch.cuda.Event()
+            done[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[k])
+                for key, h in pout.items():
+                    h.copy_(t[key], non_blocking=True)
+                copied[k] = torch.cuda.Event()
+                copied[k].record(s_out)
+        stream.wait_event(copied[K - 1])
+        end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end) / K
 
+    e2e_run(2)  # warm-up: the second buffer set and the copy streams
     barrier(dist)
-    ms_e2e = timed(args.steps, e2e_step)
-    ms_e2e_max = max_over_ranks(statistics.mean(ms_e2e), dist, dev)
+    ms_e2e = e2e_run(args.steps)
+    ms_e2e_max = max_over_ranks(ms_e2e, dist, dev)
     # the step protocol of the tensor-core recurrent forward alone (exchange
     # words written and polled, cluster barrier; no work): the term of the
     # recurrence's latency bound that no arithmetic removes
@@ -516,7 +557,10 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
                      "avg_phase_ms": round(avg_ms, 4)},
         "e2e": {"value": round(aggregate_sequences_per_s(N, ws_n, ms_e2e_max), 2), "unit": "sequences/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(ms_e2e_max, 4)},
+                "ms_per_step": round(ms_e2e_max, 4),
+                "copies": "every step's inputs in from and results out to pinned host memory, "
+                          "on two copy streams under the neighbouring steps' compute "
+                          "(double-buffered on the device); the K steps timed as one region"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "wall_s_timed_region": round(wall, 3),
         "clocks": clocks,
