@@ -694,7 +694,16 @@ bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* d
 // tile reads each A tile once for twice the MMA work of a 128 x 128 tile,
 // which matters because the operand stream from L2 (about 64 bytes per clock
 // per SM) otherwise limits the tensor pipe (bf16 128 x 128 tiles need ~117).
-int gemm_tc_bn(int64_t N) { return N >= 192 ? 256 : N > 64 ? 128 : 64; }
+int gemm_tc_bn(int64_t N) {
+  if (N <= 64) return 64;
+  if (N < 192) return 128;
+  // 256 wide reads each A tile once for twice the MMA work; 128 wide when
+  // the last 256-wide tile would waste more than a tenth of the columns more
+  // (N = 800: 1024 columns against 896; measured faster for the dX and GRU
+  // weight-gradient GEMMs of the DS2 layer)
+  const double w256 = (double)((N + 255) / 256 * 256) / N, w128 = (double)((N + 127) / 128 * 128) / N;
+  return w256 > w128 + 0.1 ? 128 : 256;
+}
 
 // Split of K that minimises a wave model: the grid runs in ceil(units / SMs)
 // waves of ceil(nkt / ks) 128-byte K blocks each, plus the fp32 partial sums
