@@ -112,14 +112,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// shared-memory matrix descriptor: K-major tile of rows x 128 bytes, 128-byte
-// swizzle, 8-row groups 1024 bytes apart (tile base 1024-byte aligned)
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// shared-memory matrix descriptor: K-major tile of rows x ROWB bytes (128 or
+// 64), swizzled over the row (128- or 64-byte swizzle), 8-row groups
+// 8 * ROWB bytes apart (tile base 1024-byte aligned)
+template <int ROWB>
+__device__ __forceinline__ uint64_t sw_desc(uint32_t saddr) {
+  static_assert(ROWB == 128 || ROWB == 64, "128- or 64-byte rows");
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;            // leading byte offset (unused for this layout)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
-  d |= (uint64_t)1 << 46;            // descriptor version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for this layout)
+  d |= (uint64_t)((8 * ROWB) >> 4) << 32;    // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)(ROWB == 128 ? 2 : 4) << 61;  // 128- or 64-byte swizzle
   return d;
 }
 
@@ -169,8 +172,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t bars[2 * 8 + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  constexpr int kA = BM * 128;                     // bytes of one A tile
-  constexpr int kB = BN * 128;                     // bytes of one B tile
+  // K bytes per tile row and stage: 64 for the fp16 pairs at BN = 256 (four
+  // operand tiles a stage: 48 KB, so four stages fit instead of two), else
+  // 128 (at BN = 128 the 64-byte rows measured slower: twice the stages for
+  // the same data)
+  constexpr int ROWB = (SPLIT && BN == 256) ? 64 : 128;
+  constexpr int kA = BM * ROWB;                    // bytes of one A tile
+  constexpr int kB = BN * ROWB;                    // bytes of one B tile
   constexpr int kStage = (kA + kB) * (SPLIT ? 2 : 1);
   // kind::f16, fp32 accumulate; A and B fp16 (0, scaled pairs) or bf16 (1)
   constexpr uint32_t kIdesc = (1u << 4) | ((SPLIT ? 0u : 1u) << 7) | ((SPLIT ? 0u : 1u) << 10) |
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t fb = full0 + 8 * s;
       mbar_expect_tx(fb, (uint32_t)kStage);
       const bool second = kb >= p.nk1;
-      const int kx = (second ? kb - p.nk1 : kb) * 64;
+      const int kx = (second ? kb - p.nk1 : kb) * (ROWB / 2);
       const CUtensorMap* ah = second ? &maps.a2h : &maps.a1h;
       const CUtensorMap* bh = second ? &maps.b2h : &maps.b1h;
       tma_load_2d(st, ah, kx, m0, fb);
@@ -236,14 +244,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mbar_wait(full0 + 8 * s, ph, p.status, p.timeout_ns, &abort_flag)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t st = base + (uint32_t)(s * kStage);
-      const uint64_t ah = sw128_desc(st), bh = sw128_desc(st + kA);
+      const uint64_t ah = sw_desc<ROWB>(st), bh = sw_desc<ROWB>(st + kA);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
+      for (int kk = 0; kk < ROWB / 32; ++kk) {  // 32 bytes of K per instruction
         const uint64_t adv = (uint64_t)(kk * 2);
         const uint32_t acc0 = (it > 0 || kk > 0) ? 1u : 0u;
         if (SPLIT) {
           // hi hi + hi lo + lo hi into one accumulator (lo is not rescaled)
-          const uint64_t al = sw128_desc(st + kA + kB), bl = sw128_desc(st + 2 * kA + kB);
+          const uint64_t al = sw_desc<ROWB>(st + kA + kB), bl = sw_desc<ROWB>(st + 2 * kA + kB);
           mma_f16(tmem, ah + adv, bh + adv, kIdesc, acc0);
           mma_f16(tmem, ah + adv, bl + adv, kIdesc, 1u);
           mma_f16(tmem, al + adv, bh + adv, kIdesc, 1u);
@@ -638,20 +646,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// K-major operand [rows][K] with row stride ld (elements); box = kpe x box_rows
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld, bool bf,
-              int box_rows) {
+// K-major 16-bit operand [rows][K] with row stride ld (elements); box =
+// row_bytes / 2 x box_rows, swizzled over row_bytes (128 or 64)
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld,
+              int row_bytes, int box_rows) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc || !ptr) return false;
-  const int e = bf ? 2 : 4;
+  if (!enc || !ptr || (row_bytes != 128 && row_bytes != 64)) return false;
+  const int e = 2;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * e)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)(row_bytes / e), (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-             const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool operand_ok(const void* p, int64_t ld, int e) {
@@ -660,7 +669,7 @@ bool operand_ok(const void* p, int64_t ld, int e) {
 
 template <int BN, bool SPLIT>
 cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaStream_t st) {
-  constexpr int kStage = (BM * 128 + BN * 128) * (SPLIT ? 2 : 1);
+  constexpr int kStage = (BM + BN) * ((SPLIT && BN == 256) ? 64 : 128) * (SPLIT ? 2 : 1);
   const size_t smem = (size_t)kp.stages * kStage + 1024;
   auto fn = gemm_tc_kernel<BN, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -756,20 +765,21 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   memset(&maps, 0, sizeof(maps));
   // every operand is 16-bit (fp16 pairs or bf16): TMA copies bytes, so one
   // 16-bit map type serves both
-  bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, true, BM) &&
-            make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, true, BN);
+  const int rowb = (sp && BN == 256) ? 64 : 128;  // K bytes per tile row and stage
+  bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, rowb, BM) &&
+            make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, rowb, BN);
   if (sp)
-    ok = ok && make_map(&maps.a1l, g.A_lo, g.M, g.K, g.lda, true, BM) &&
-         make_map(&maps.b1l, g.B_lo, g.N, g.K, g.ldb, true, BN);
+    ok = ok && make_map(&maps.a1l, g.A_lo, g.M, g.K, g.lda, rowb, BM) &&
+         make_map(&maps.b1l, g.B_lo, g.N, g.K, g.ldb, rowb, BN);
   if (g.K2 > 0) {
-    ok = ok && make_map(&maps.a2h, g.A2_hi, g.M, g.K2, g.lda2, true, BM) &&
-         make_map(&maps.b2h, g.B2_hi, g.N, g.K2, g.ldb2, true, BN);
+    ok = ok && make_map(&maps.a2h, g.A2_hi, g.M, g.K2, g.lda2, rowb, BM) &&
+         make_map(&maps.b2h, g.B2_hi, g.N, g.K2, g.ldb2, rowb, BN);
     if (sp)
-      ok = ok && make_map(&maps.a2l, g.A2_lo, g.M, g.K2, g.lda2, true, BM) &&
-           make_map(&maps.b2l, g.B2_lo, g.N, g.K2, g.ldb2, true, BN);
+      ok = ok && make_map(&maps.a2l, g.A2_lo, g.M, g.K2, g.lda2, rowb, BM) &&
+           make_map(&maps.b2l, g.B2_lo, g.N, g.K2, g.ldb2, rowb, BN);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const int kpe = 64;
+  const int kpe = rowb / 2;
   TcKParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.M = (int)g.M;
@@ -777,7 +787,7 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   kp.nk1 = (int)((g.K + kpe - 1) / kpe);
   kp.nk2 = g.K2 > 0 ? (int)((g.K2 + kpe - 1) / kpe) : 0;
   kp.ksplit = std::max(1, g.ksplit);
-  const int stage = (BM * 128 + BN * 128) * (sp ? 2 : 1);
+  const int stage = (BM + BN) * rowb * (sp ? 2 : 1);
   kp.stages = std::max(2, std::min(8, kSmemBudget / stage));
   kp.amax = g.amax;
   kp.bmax = g.bmax;
