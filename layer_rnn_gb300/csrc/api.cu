@@ -247,9 +247,16 @@ bool prepare_a(const rnn_handle* h, PreparedA* pa, bool tf, Scratch* sc, cudaStr
                       pa->mx, st);
 }
 
+// Below this many multiply-adds a dense phase runs on the CUDA cores: the
+// tensor-core path's operand preparation (max and split kernels, fp32) costs
+// more launches than the product is worth (a 5-step, batch-2 LSTM ran about
+// 20 % slower end to end with it)
+constexpr int64_t kTinyGemmMacs = int64_t(1) << 20;
+
 rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaStream_t st,
                       const PreparedA* pa = nullptr) {
-  if (!(h->flags & RNN_FLAG_SIMT_GEMM)) {
+  const bool tiny = g.M * g.N * (g.K + g.K2) < kTinyGemmMacs;
+  if (!(h->flags & RNN_FLAG_SIMT_GEMM) && !tiny) {
     const bool tf = !g.in_bf16;
     TcGemm t;
     t.M = g.M; t.N = g.N; t.K = g.K; t.split16 = tf ? 1 : 0;
@@ -1173,7 +1180,8 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N, c
       // dG_x^T, presented once for both weight GEMMs when dG_h is dG_x
       Scratch scl = sc;
       PreparedA pa;
-      if (!(h->flags & RNN_FLAG_SIMT_GEMM) && dgh == dgx) {
+      if (!(h->flags & RNN_FLAG_SIMT_GEMM) && dgh == dgx &&
+          GH * std::min<int64_t>(I_l, H) * T * N >= kTinyGemmMacs) {
         pa.src = dgx; pa.M = GH; pa.K = T * N; pa.sam = 1; pa.sak = GH;
         pa.valid = prepare_a(h, &pa, !bf, &scl, st);
         if (!pa.valid) scl = sc;
