@@ -277,7 +277,7 @@ def run_ours(args, cfg):
         g = measure(args, wl.WORKLOADS["ds2_gru"], dist, dev, rank, ws_n, local)
         line["gru"] = {k: g[k] for k in ("value", "unit", "ms_per_step", "effective_tflops",
                                          "phases", "recurrent_paths", "roofline", "e2e",
-                                         "gpu_launches", "clocks")}
+                                         "varlen", "gpu_launches", "clocks")}
         line["gru"]["config"] = g["config"]
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, spent = time_oracle(cfg, budget_s=args.cpu_budget)
@@ -446,6 +446,29 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
     barrier(dist)
     ms_e2e = e2e_run(args.steps)
     ms_e2e_max = max_over_ranks(ms_e2e, dist, dev)
+
+    # the same batch padded to T with per-sequence lengths (the *_varlen
+    # calls), device-resident like the main line
+    lens_np = wl.make_lengths(cfg, seed=cfg["seed"] + rank)
+    lens = torch.tensor(lens_np, dtype=torch.int32, device=dev)
+    vpaths = B.rnn_get_paths_varlen(r.h, N)
+
+    def step_varlen():
+        r.forward_training_varlen(lens, x, h0, c0, W, y, hy, cy, ws, stream)
+        r.backward_data_varlen(lens, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+        r.backward_weights(x, h0, y, ws, dW, stream)
+        if dist is not None:
+            with torch.cuda.stream(stream):
+                dp.allreduce_grads(dW, dist)
+
+    for _ in range(args.warmup):
+        step_varlen()
+    barrier(dist)
+    ms_var = statistics.mean(timed(args.steps, step_varlen))
+    ms_var_max = max_over_ranks(ms_var, dist, dev)
+    st = r.check_status(stream)
+    if st != 0:
+        raise RuntimeError("device status %d in the varlen steps" % st)
     # the step protocol of the tensor-core recurrent forward alone (exchange
     # words written and polled, cluster barrier; no work): the term of the
     # recurrence's latency bound that no arithmetic removes
@@ -561,6 +584,14 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
                 "copies": "every step's inputs in from and results out to pinned host memory, "
                           "on two copy streams under the neighbouring steps' compute "
                           "(double-buffered on the device); the K steps timed as one region"},
+        "varlen": {"value": round(aggregate_sequences_per_s(N, ws_n, ms_var_max), 2),
+                   "unit": "sequences/s", "ms_per_step": round(ms_var_max, 4),
+                   "recurrent_paths": {"fwd": vpaths[0], "bwd": vpaths[1]},
+                   "lengths": "padded to T=%d; one sequence of length T, the others uniform "
+                              "in [%d, %d] (mean %.1f); rnn_forward_training_varlen + "
+                              "rnn_backward_data_varlen + rnn_backward_weights, L2 flushed "
+                              "before every step"
+                              % (T, (T + 1) // 2, T, float(lens_np.mean()))},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "wall_s_timed_region": round(wall, 3),
         "clocks": clocks,

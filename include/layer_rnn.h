@@ -235,9 +235,11 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N,
  * needs no lengths (the zero gate gradients drop the padded steps); the padded
  * entries of x must be finite, because dW_ih multiplies them by zero.
  * Values outside 0..T act as 0 or T.  The lengths buffer is read by the
- * enqueued kernels: keep it unchanged until they have run.  These calls run
- * on the CUDA-core recurrent kernels (no wavefront, no tensor-core recurrence;
- * the dense phases still use the tensor cores).
+ * enqueued kernels: keep it unchanged until they have run.  These calls take
+ * no layer wavefront; their recurrent phases run on the tensor-core kernels
+ * that give each block its own slice where those fit (rnn_get_paths_varlen
+ * names the choice), else on the staged CUDA-core kernels; the dense phases
+ * use the tensor cores as without lengths.
  * Errors: as the calls without lengths, and RNN_ERR_INVALID_ARG for a NULL
  * lengths, RNN_ERR_MISALIGNED for one not 4-byte aligned. */
 rnn_status_t rnn_forward_training_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
@@ -312,6 +314,11 @@ typedef enum {
   RNN_PATH_WAVEFRONT = 4   /* tcgen05 layer wavefront, all layers in one launch */
 } rnn_path_t;
 rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
+/* The same for the *_varlen calls (per-sequence lengths): they never take the
+ * layer wavefront, and their recurrent phases run on the tensor-core kernels
+ * that give each block its own slice (RNN_PATH_TENSOR) where those fit, else
+ * on the staged CUDA-core kernels. */
+rnn_status_t rnn_get_paths_varlen(rnn_t h, int64_t N, int* fwd, int* bwd);
 
 /* The step protocol of the tensor-core recurrent forward, timed alone.  The
  * pages have no counterpart of this call: it measures the part of a

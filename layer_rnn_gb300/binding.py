@@ -62,6 +62,8 @@ SIGNATURES = {
     "rnn_get_phase_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _pi64]),
     "rnn_get_paths": (_i32, [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_int)]),
+    "rnn_get_paths_varlen": (_i32, [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int)]),
     "rnn_measure_step_protocol": (_i32, [_vp, _vp, _i64, _i64, ctypes.POINTER(ctypes.c_double)]),
     "rnn_debug_split_f16": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _vp]),
     "rnn_debug_transpose_bf16": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp]),
@@ -240,6 +242,13 @@ def rnn_get_paths(h, N):
     """(forward, backward) recurrent kernel paths of a call with batch N."""
     f, b = ctypes.c_int(), ctypes.c_int()
     _call("rnn_get_paths", h, N, ctypes.byref(f), ctypes.byref(b))
+    return PATHS[f.value], PATHS[b.value]
+
+
+def rnn_get_paths_varlen(h, N):
+    """(forward, backward) recurrent kernel paths of the *_varlen calls."""
+    f, b = ctypes.c_int(), ctypes.c_int()
+    _call("rnn_get_paths_varlen", h, N, ctypes.byref(f), ctypes.byref(b))
     return PATHS[f.value], PATHS[b.value]
 
 

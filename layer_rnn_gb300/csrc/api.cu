@@ -458,10 +458,21 @@ struct PhaseScope {
 rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl, int D,
                       bool varlen = false) {
   const bool bf = h->dtype == RNN_BF16;
+  // per-sequence lengths: the one-block-per-slice tensor-core kernels (forward
+  // and backward) and the staged CUDA-core kernels read them
+  if (varlen && h->mode != RNN_GRU_TF && !(h->flags & RNN_FLAG_SIMT_RECURRENT)) {
+    if (!backward && rec_tc_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
+                                 h->max_clusters, pl))
+      return RNN_OK;
+    if (backward &&
+        rec_tc_bwd_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
+                        h->bwd_caps, pl) &&
+        (size_t)pl->P * D * 128 <= kSyncBytes - 64)
+      return RNN_OK;
+  }
   if (varlen || h->mode == RNN_GRU_TF) {
-    // per-sequence lengths, and the TensorFlow-flavour GRU's two dependent
-    // contractions per step: the staged CUDA-core kernels are the ones that
-    // run them
+    // the TensorFlow-flavour GRU's two dependent contractions per step, and
+    // lengths where no tensor-core plan fits: the staged CUDA-core kernels
     // (the TensorFlow-flavour GRU has the GRU's sizes: three gate blocks)
     if (!rec_make_plan(backward, h->mode == RNN_GRU_TF ? RNN_GRU : h->mode, bf, D, (int)h->H,
                        (int)N, h->num_sms, h->smem_optin, pl, false))
@@ -503,20 +514,22 @@ rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl) {
 // the tensor-core plan for one direction (5-layer bidirectional LSTM: 24 us
 // per step for the pair against 2 x 7 us).  GRU and tanh-RNN layers measured
 // no better this way.
-bool bwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPlan* one) {
+bool bwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPlan* one,
+                            bool varlen) {
   if (h->D != 2 || both.tc || h->mode != RNN_LSTM || (h->flags & RNN_FLAG_SIMT_RECURRENT))
     return false;
-  return plan_rec(h, true, N, one, 1) == RNN_OK && one->tc;
+  return plan_rec(h, true, N, one, 1, varlen) == RNN_OK && one->tc;
 }
 
 // Forward of a bidirectional layer: when both directions together only fit a
 // CUDA-core kernel, the two directions run one after the other, each on the
 // tensor-core plan for one direction (5-layer bidirectional LSTM at H = 800:
 // 2 x 3.6 us per step against 13.2 us for the pair on the cluster kernel).
-bool fwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPlan* one) {
+bool fwd_directions_in_turn(rnn_handle* h, int64_t N, const RecPlan& both, RecPlan* one,
+                            bool varlen) {
   if (h->D != 2 || both.tc || h->mode == RNN_GRU_TF || (h->flags & RNN_FLAG_SIMT_RECURRENT))
     return false;
-  return plan_rec(h, false, N, one, 1) == RNN_OK && one->tc;
+  return plan_rec(h, false, N, one, 1, varlen) == RNN_OK && one->tc;
 }
 
 void fill_rec_common(rnn_handle* h, int64_t T, int64_t N, RecParams* rp) {
@@ -678,7 +691,7 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
   RecPlan plan, plan_one;
   s = plan_rec(h, false, N, &plan, h->D, lengths != nullptr);
   if (s != RNN_OK) return s;
-  const bool in_turn = !lengths && fwd_directions_in_turn(h, N, plan, &plan_one);
+  const bool in_turn = fwd_directions_in_turn(h, N, plan, &plan_one, lengths != nullptr);
   unsigned long long* hx[2] = {nullptr, nullptr};
   if (plan.tc || in_turn) {
     for (int d = 0; d < h->D; ++d) {
@@ -726,7 +739,8 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
         a.hseq = mp<char>(ws, lay.at(RNN_WS_HSEQ, l, d).off);
         a.gates = mp<float>(ws, lay.at(RNN_WS_GATES, l, d).off);
         a.cseq = h->mode == RNN_LSTM ? mp<float>(ws, lay.at(RNN_WS_CSEQ, l, d).off) : nullptr;
-      } else if (lengths) {
+      } else if (lengths && !plan.tc && !in_turn) {
+        // the staged kernels read the carried states back from here
         a.hseq = hseq_scratch + (int64_t)d * (T + 1) * NH * e;
       }
     }
@@ -988,7 +1002,7 @@ static rnn_status_t backward_data_impl(rnn_t h, void* stream, int64_t T, int64_t
   RecPlan plan, plan_one;
   s = plan_rec(h, true, N, &plan, h->D, lengths != nullptr);
   const bool in_turn =
-      s == RNN_OK && !lengths && bwd_directions_in_turn(h, N, plan, &plan_one);
+      s == RNN_OK && bwd_directions_in_turn(h, N, plan, &plan_one, lengths != nullptr);
   if (s != RNN_OK) return finish(h, st, s);
   Scratch sc;
   sc.base = ws + lay.at(RNN_WS_GEMM, 0, 0).off;
@@ -1300,7 +1314,7 @@ rnn_status_t rnn_get_phase_times(rnn_t h, double* ms, int64_t* launches) {
   return RNN_OK;
 }
 
-rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
+static rnn_status_t get_paths(rnn_t h, int64_t N, int* fwd, int* bwd, bool varlen) {
   if (!h || !fwd || !bwd || N < 1) return RNN_ERR_INVALID_ARG;
   rnn_status_t s = device_setup(h);
   if (s != RNN_OK) return s;
@@ -1311,21 +1325,29 @@ rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
   };
   WfPlan wp;
   RecPlan pl;
-  if (wf_candidate(h, N) &&
+  if (!varlen && wf_candidate(h, N) &&
       wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &wp) &&
       (size_t)h->L * wp.Pr * 128 <= kSyncBytes - 64) {
     *fwd = RNN_PATH_WAVEFRONT;
   } else {
-    s = plan_rec(h, false, N, &pl);
+    s = plan_rec(h, false, N, &pl, h->D, varlen);
     if (s != RNN_OK) return s;
     RecPlan one;
-    *fwd = fwd_directions_in_turn(h, N, pl, &one) ? kind(one) : kind(pl);
+    *fwd = fwd_directions_in_turn(h, N, pl, &one, varlen) ? kind(one) : kind(pl);
   }
-  s = plan_rec(h, true, N, &pl);
+  s = plan_rec(h, true, N, &pl, h->D, varlen);
   if (s != RNN_OK) return s;
   RecPlan one;
-  *bwd = bwd_directions_in_turn(h, N, pl, &one) ? kind(one) : kind(pl);
+  *bwd = bwd_directions_in_turn(h, N, pl, &one, varlen) ? kind(one) : kind(pl);
   return RNN_OK;
+}
+
+rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd) {
+  return get_paths(h, N, fwd, bwd, false);
+}
+
+rnn_status_t rnn_get_paths_varlen(rnn_t h, int64_t N, int* fwd, int* bwd) {
+  return get_paths(h, N, fwd, bwd, true);
 }
 
 // ----------------------------------------------------------------------------

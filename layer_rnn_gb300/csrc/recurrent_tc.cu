@@ -137,7 +137,7 @@ __host__ __device__ inline TcLayout tc_layout(const RecPlan& pl, int G, int N, b
   return L;
 }
 
-template <bool BF>
+template <bool BF, bool VL>  // VL: per-sequence lengths (p.lengths) are read
 __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant__ RecParams p) {
   typedef typename std::conditional<BF, bf16, float>::type T;
   constexpr int NI = BF ? 1 : 3;   // issuing threads = accumulators (one per pass)
@@ -349,6 +349,13 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
     e_uo = u - e_owner * Uq;
   }
   const int i_uu = Uqc > 0 ? tid % Uqc : 0, i_n = Uqc > 0 ? tid / Uqc : 0;
+  // the valid length of this thread's first item's sequence (read once, off
+  // the steps' critical path); other items read theirs when they run
+  const int i_len = (VL && tid < items) ? __ldg(p.lengths + i_n) : 0x7fffffff;
+  auto seq_len = [&](int it, int n) {
+    if constexpr (!VL) return 0x7fffffff;
+    else return it == tid ? i_len : __ldg(p.lengths + n);
+  };
   const int icap = Uq * N;  // stride of one array of the output stash
   // the outputs of step sp (y, the saved gates, c_t, the h sequence) from the
   // stash, each item by the thread that computed it: written one step late,
@@ -363,7 +370,9 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
       const int64_t row = (int64_t)tq * N + n;
       const float h = outs[it];
       const T hs = from_f<T>(h);
-      y[row * p.ldy + (int64_t)d * H + j] = hs;
+      // past the sequence's length the output is zero (the state is kept)
+      const bool act = !VL || tq < seq_len(it, n);
+      y[row * p.ldy + (int64_t)d * H + j] = act ? hs : from_f<T>(0.f);
       if (a.gates) {
         if (p.mode == 0) {
           a.gates[row * H + j] = h;
@@ -677,6 +686,12 @@ __global__ void __launch_bounds__(kTThreads, 1) rec_fwd_tc(const __grid_constant
         } else {
           h = tanh_fast(gv[0] + ov[0]);
         }
+        if (VL && t >= seq_len(it, n)) {
+          // past the sequence's length: the state is kept (its gates are
+          // still stored; the backward does not read them there)
+          h = hst[n * Uq + uu];
+          if (p.mode == 1) c = cst[n * Uq + uu];
+        }
         const T hs = from_f<T>(h);
         if (it == tid) PTRACE(s, 27, h);
         // the exchange word of h_t: its value as stored (what y holds) and the
@@ -911,7 +926,8 @@ extern "C" int rnn_debug_ttrace_clear() {
 
 cudaError_t rec_tc_launch(const RecParams& p, cudaStream_t st) {
   const RecPlan& pl = p.plan;
-  void* fn = p.bf16 ? (void*)rec_fwd_tc<true> : (void*)rec_fwd_tc<false>;
+  void* fn = p.lengths ? (p.bf16 ? (void*)rec_fwd_tc<true, true> : (void*)rec_fwd_tc<false, true>)
+                       : (p.bf16 ? (void*)rec_fwd_tc<true, false> : (void*)rec_fwd_tc<false, false>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;

@@ -103,7 +103,7 @@ __host__ __device__ inline BLayout b_layout(const RecPlan& pl, int N, bool bf) {
   return L;
 }
 
-template <bool BF>
+template <bool BF, bool VL>  // VL: per-sequence lengths (p.lengths) are read
 __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant__ RecParams p) {
   typedef typename std::conditional<BF, bf16, float>::type T;
   constexpr int NI = BF ? 1 : 3;     // issuing threads = accumulators (one per pass)
@@ -287,6 +287,10 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
     }
   };
   int pend = -1;  // the step whose gradients wait in the stash
+  // the valid length of this thread's first item's sequence (read once, off
+  // the steps' critical path); other items read theirs when they run
+  const int i_len =
+      (VL && tid < items) ? __ldg(p.lengths + tid / max(1, Uqc)) : 0x7fffffff;
   // fp32: the dG_h scale exponent predicted from the previous step's slice
   int pred_eh = 0;
   float pred_scale = 1.f;
@@ -559,7 +563,15 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
         const unsigned long long tag = (unsigned long long)(s + 1) << 32;
         float gh[4];
         int ng = 1;
-        if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
+        if (VL && t >= (it == tid ? i_len : __ldg(p.lengths + n))) {
+          // a step the forward skipped (past the sequence's length): no gate
+          // gradients, dy unused, dh and (LSTM) dc pass straight through
+          ng = ngo;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) gh[g] = 0.f;
+          if (p.mode == 2) stash[it] = stash[icap + it] = stash[2 * icap + it] = 0.f;
+          st_carry[it] = dhf;
+        } else if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
           const float cc = pin[5 * icap + it], cpv = pin[6 * icap + it];
           const float tc = tanh_fast(cc);
@@ -570,6 +582,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           gh[3] = dh * tc * g3 * (1.f - g3);
           ng = 4;
           st_dc[it] = dc * g1;
+          if (VL) st_carry[it] = 0.f;  // a pass-through ends here
         } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
           const float g1 = pin[2 * icap + it], g2 = pin[3 * icap + it], g3 = pin[4 * icap + it];
           const int sp = rv ? t + 1 : t;
@@ -587,6 +600,7 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
           st_carry[it] = dh * g1;
         } else {  // tanh RNN: g0 = h_t
           gh[0] = dh * (1.f - g0 * g0);
+          if (VL) st_carry[it] = 0.f;
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -613,14 +627,15 @@ __global__ void __launch_bounds__(kBThreads, 1) rec_bwd_tc(const __grid_constant
                  : "memory");
 }
 
-void* bwd_kernel(bool bf) {
-  return bf ? (void*)rec_bwd_tc<true> : (void*)rec_bwd_tc<false>;
+void* bwd_kernel(bool bf, bool varlen) {
+  return varlen ? (bf ? (void*)rec_bwd_tc<true, true> : (void*)rec_bwd_tc<false, true>)
+                : (bf ? (void*)rec_bwd_tc<true, false> : (void*)rec_bwd_tc<false, false>);
 }
 
 }  // namespace
 
 int rec_tc_bwd_capacity(int cluster, size_t smem) {
-  void* fn = bwd_kernel(false);
+  void* fn = bwd_kernel(false, false);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -717,7 +732,7 @@ extern "C" int rnn_debug_btrace_clear() {
 
 cudaError_t rec_tc_bwd_launch(const RecParams& p, cudaStream_t st) {
   const RecPlan& pl = p.plan;
-  void* fn = bwd_kernel(p.bf16 != 0);
+  void* fn = bwd_kernel(p.bf16 != 0, p.lengths != nullptr);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;

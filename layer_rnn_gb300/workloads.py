@@ -136,3 +136,15 @@ def make_inputs(cfg, seed=None):
         out["c0"] = None
         out["dcy"] = None
     return out
+
+
+def make_lengths(cfg, seed=None):
+    """Per-sequence valid lengths for a padded batch of the workload: one
+    sequence of the full T (the padding length is the longest sequence's),
+    the others uniform integers in [ceil(T/2), T] -- a mix of utterance
+    lengths within a factor of two, as a length-bucketed batch holds."""
+    rng = np.random.Generator(np.random.PCG64((cfg["seed"] if seed is None else seed) + 7919))
+    T, N = cfg["T"], cfg["N"]
+    lens = rng.integers((T + 1) // 2, T + 1, size=N)
+    lens[0] = T
+    return lens.astype(np.int32)

@@ -7,7 +7,10 @@ Lengths cover the degenerate cases: 0 (nothing runs: y is zero, hy = h0,
 dh0 = dhy), 1, T - 1 and T; both directions and stacked layers (the reverse
 direction starts at each sequence's last valid step; the layer above reads
 zeros past the length), fp32 and bf16, batches that are not multiples of a
-tile.
+tile.  The tensor-core recurrent kernels run the shapes they fit (their
+choice is asserted for the DS2 hidden size, both modes, and for a
+bidirectional layer whose directions run in turn); the staged CUDA-core
+kernels run the same lengths when the tensor cores are switched off.
 """
 
 import zlib
@@ -52,14 +55,36 @@ def _lengths(T, N, seed):
     return np.array((base + list(extra))[:N], dtype=np.int32)
 
 
-@pytest.mark.parametrize("case", CASES, ids=[_cid(c) for c in CASES])
-def test_varlen_parity(case):
+# shapes whose recurrent phases take the tensor-core kernels with lengths:
+# mode, L, bidir, T, N, I, H, dtype
+TC_CASES = [
+    ("lstm", 1, False, 9, 20, 48, 800, "f32"),   # the DS2 layer's batch and hidden size
+    ("gru", 1, False, 8, 48, 40, 800, "f32"),
+    ("lstm", 1, True, 5, 24, 32, 800, "f32"),    # the directions in turn
+    ("rnn_tanh", 1, False, 7, 40, 24, 256, "f32"),
+    ("lstm", 2, False, 6, 72, 16, 256, "bf16"),
+    ("gru", 1, True, 6, 36, 16, 200, "bf16"),
+]
+
+
+def _paths(cfg, flags=0):
+    from layer_rnn_gb300 import binding as B
+    r = B.Rnn(cfg["mode"], cfg["L"], cfg["bidir"], cfg["I"], cfg["H"], cfg["dtype"], flags)
+    try:
+        return B.rnn_get_paths_varlen(r.h, cfg["N"])
+    finally:
+        r.close()
+
+
+def _check_case(case, flags=0, expect=None):
     mode, L, bidir, T, N, I, H, dt = case
     seed = zlib.crc32(_cid(case).encode()) % 10000
     cfg = wl.make_config(mode, L, bidir, T, N, I, H, dt, 0.3, seed=seed)
+    if expect is not None:
+        assert _paths(cfg, flags) == expect
     inp = wl.make_inputs(cfg)
     lengths = _lengths(T, N, seed)
-    gpu = harness.run_gpu(cfg, inp, lengths=lengths)
+    gpu = harness.run_gpu(cfg, inp, lengths=lengths, flags=flags)
     ref = harness.run_oracle(cfg, inp, lengths=lengths)
     harness.assert_parity(cfg, gpu, ref)
     for n, ln in enumerate(lengths):
@@ -73,13 +98,42 @@ def test_varlen_parity(case):
         assert np.array_equal(gpu["cy_inf"], gpu["cy"])
 
 
-def test_full_lengths_match_the_fixed_length_calls():
-    # every length equal to T: the CUDA-core varlen path and the default path
-    # (tensor cores where they fit) agree with each other within the bars
-    cfg = wl.make_config("gru", 1, True, 6, 8, 16, 32, "f32", 0.3, seed=3)
+@pytest.mark.parametrize("case", CASES, ids=[_cid(c) for c in CASES])
+def test_varlen_parity(case):
+    _check_case(case)
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[_cid(c) for c in TC_CASES])
+def test_varlen_tensor_core_kernels(case):
+    _check_case(case, expect=("tensor", "tensor"))
+
+
+@pytest.mark.parametrize("case", [CASES[3], CASES[6], TC_CASES[0]],
+                         ids=[_cid(c) for c in (CASES[3], CASES[6], TC_CASES[0])])
+def test_varlen_staged_kernels(case):
+    from layer_rnn_gb300 import binding as B
+    _check_case(case, flags=B.RNN_FLAG_SIMT_RECURRENT, expect=("staged", "staged"))
+
+
+@pytest.mark.parametrize("shape", [(6, 8, 16, 32), (5, 20, 32, 800)])
+def test_full_lengths_match_the_fixed_length_calls(shape):
+    # every length equal to T: the varlen calls and the fixed-length calls
+    # agree with each other within the bars, and bit for bit where both run
+    # the same recurrent kernels
+    from layer_rnn_gb300 import binding as B
+    T, N, I, H = shape
+    cfg = wl.make_config("gru", 1, True, T, N, I, H, "f32", 0.3, seed=3)
     inp = wl.make_inputs(cfg)
-    a = harness.run_gpu(cfg, inp, lengths=np.full(8, 6, dtype=np.int32))
+    a = harness.run_gpu(cfg, inp, lengths=np.full(N, T, dtype=np.int32))
     b = harness.run_gpu(cfg, inp)
     ref = harness.run_oracle(cfg, inp)
     harness.assert_parity(cfg, a, ref)
     harness.assert_parity(cfg, b, ref)
+    r = B.Rnn(cfg["mode"], cfg["L"], cfg["bidir"], I, H, cfg["dtype"], 0)
+    try:
+        same = B.rnn_get_paths_varlen(r.h, N) == B.rnn_get_paths(r.h, N)
+    finally:
+        r.close()
+    if same:
+        for k in ("y", "hy", "dx", "dh0", "dW"):
+            assert np.array_equal(a[k], b[k]), k
