@@ -469,6 +469,34 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
     st = r.check_status(stream)
     if st != 0:
         raise RuntimeError("device status %d in the varlen steps" % st)
+
+    # stacks: the same batch with inter-layer dropout (the *_dropout calls)
+    drop = None
+    if L > 1:
+        p_drop = 0.3
+        masks = torch.tensor(wl.make_dropout_masks(cfg, p_drop, seed=cfg["seed"] + rank),
+                             device=dev)
+
+        def step_dropout():
+            r.forward_training_dropout(p_drop, masks, x, h0, c0, W, y, hy, cy, ws, stream)
+            r.backward_data_dropout(p_drop, masks, W, dy, dhy, dcy, dx, dh0, dc0, ws, stream)
+            r.backward_weights(x, h0, y, ws, dW, stream)
+            if dist is not None:
+                with torch.cuda.stream(stream):
+                    dp.allreduce_grads(dW, dist)
+
+        for _ in range(args.warmup):
+            step_dropout()
+        barrier(dist)
+        ms_drop = max_over_ranks(statistics.mean(timed(args.steps, step_dropout)), dist, dev)
+        st = r.check_status(stream)
+        if st != 0:
+            raise RuntimeError("device status %d in the dropout steps" % st)
+        drop = {"value": round(aggregate_sequences_per_s(N, ws_n, ms_drop), 2),
+                "unit": "sequences/s", "ms_per_step": round(ms_drop, 4), "p": p_drop,
+                "calls": "rnn_forward_training_dropout + rnn_backward_data_dropout + "
+                         "rnn_backward_weights, seeded Bernoulli masks, L2 flushed before "
+                         "every step"}
     # the step protocol of the tensor-core recurrent forward alone (exchange
     # words written and polled, cluster barrier; no work): the term of the
     # recurrence's latency bound that no arithmetic removes
@@ -592,6 +620,7 @@ def measure(args, cfg, dist, dev, rank, ws_n, local):
                               "rnn_backward_data_varlen + rnn_backward_weights, L2 flushed "
                               "before every step"
                               % (T, (T + 1) // 2, T, float(lens_np.mean()))},
+        "dropout": drop,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "wall_s_timed_region": round(wall, 3),
         "clocks": clocks,

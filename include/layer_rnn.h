@@ -235,11 +235,10 @@ rnn_status_t rnn_backward_weights(rnn_t h, void* stream, int64_t T, int64_t N,
  * needs no lengths (the zero gate gradients drop the padded steps); the padded
  * entries of x must be finite, because dW_ih multiplies them by zero.
  * Values outside 0..T act as 0 or T.  The lengths buffer is read by the
- * enqueued kernels: keep it unchanged until they have run.  These calls take
- * no layer wavefront; their recurrent phases run on the tensor-core kernels
- * that give each block its own slice where those fit (rnn_get_paths_varlen
- * names the choice), else on the staged CUDA-core kernels; the dense phases
- * use the tensor cores as without lengths.
+ * enqueued kernels: keep it unchanged until they have run.  The recurrent
+ * phases run on the layer wavefront and the tensor-core kernels where those
+ * fit (rnn_get_paths_varlen names the choice), else on the staged CUDA-core
+ * kernels; the dense phases use the tensor cores as without lengths.
  * Errors: as the calls without lengths, and RNN_ERR_INVALID_ARG for a NULL
  * lengths, RNN_ERR_MISALIGNED for one not 4-byte aligned. */
 rnn_status_t rnn_forward_training_varlen(rnn_t h, void* stream, int64_t T, int64_t N,
@@ -264,9 +263,11 @@ rnn_status_t rnn_backward_data_varlen(rnn_t h, void* stream, int64_t T, int64_t 
  * multiplied by mask_l / (1 - p); y, hy and cy are not dropped.
  * rnn_backward_data_dropout must get the same p and masks.
  * rnn_backward_weights needs neither, because the workspace keeps the dropped
- * inputs.  Inference does not drop.  For L = 1, masks may be NULL.  These
- * calls take the layer-by-layer path: no wavefront.  The masks buffer is read
- * by the enqueued kernels: keep it unchanged until they have run.
+ * inputs.  Inference does not drop.  For L = 1, masks may be NULL.  The
+ * forward takes the same recurrent kernels as rnn_forward_training (the layer
+ * wavefront applies the masks as each layer writes its output).  The masks
+ * buffer is read by the enqueued kernels: keep it unchanged until they have
+ * run.
  * Errors: as the calls without dropout, and RNN_ERR_INVALID_ARG for p outside
  * [0, 1) or NULL masks with L > 1. */
 rnn_status_t rnn_forward_training_dropout(rnn_t h, void* stream, int64_t T, int64_t N,
@@ -314,10 +315,9 @@ typedef enum {
   RNN_PATH_WAVEFRONT = 4   /* tcgen05 layer wavefront, all layers in one launch */
 } rnn_path_t;
 rnn_status_t rnn_get_paths(rnn_t h, int64_t N, int* fwd, int* bwd);
-/* The same for the *_varlen calls (per-sequence lengths): they never take the
- * layer wavefront, and their recurrent phases run on the tensor-core kernels
- * that give each block its own slice (RNN_PATH_TENSOR) where those fit, else
- * on the staged CUDA-core kernels. */
+/* The same for the *_varlen calls (per-sequence lengths): the layer
+ * wavefront and the tensor-core kernels read the lengths where they fit,
+ * else the staged CUDA-core kernels run the recurrent phases. */
 rnn_status_t rnn_get_paths_varlen(rnn_t h, int64_t N, int* fwd, int* bwd);
 
 /* The step protocol of the tensor-core recurrent forward, timed alone.  The

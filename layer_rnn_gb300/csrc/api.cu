@@ -458,11 +458,16 @@ struct PhaseScope {
 rnn_status_t plan_rec(rnn_handle* h, bool backward, int64_t N, RecPlan* pl, int D,
                       bool varlen = false) {
   const bool bf = h->dtype == RNN_BF16;
-  // per-sequence lengths: the one-block-per-slice tensor-core kernels (forward
-  // and backward) and the staged CUDA-core kernels read them
+  // per-sequence lengths: the tensor-core kernels (the forward, both backward
+  // kernels) and the staged CUDA-core kernels read them
   if (varlen && h->mode != RNN_GRU_TF && !(h->flags & RNN_FLAG_SIMT_RECURRENT)) {
     if (!backward && rec_tc_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
                                  h->max_clusters, pl))
+      return RNN_OK;
+    if (backward &&
+        rec_tcm_bwd_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->cluster_smem,
+                         h->max_clusters, pl) &&
+        (size_t)pl->P * D * 128 <= kSyncBytes - 64)
       return RNN_OK;
     if (backward &&
         rec_tc_bwd_plan(h->mode, bf, D, (int)h->H, (int)N, h->num_sms, h->smem_optin,
@@ -593,9 +598,11 @@ rnn_status_t input_projection(rnn_handle* h, cudaStream_t st, int l, int64_t T, 
 rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N,
                                const void* x, const void* h0, const void* c0, const void* W,
                                void* y, void* hy, void* cy, char* ws, bool training, Scratch sc,
-                               bool* used) {
+                               bool* used, const int* lengths = nullptr,
+                               const uint8_t* drop_masks = nullptr, float drop_p = 0.f) {
   *used = false;
   if (!wf_candidate(h, N)) return RNN_OK;
+  if (drop_masks && !training) return RNN_OK;
   WfPlan pl;
   if (!wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &pl))
     return RNN_OK;
@@ -616,6 +623,7 @@ rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_
   p.timeout_ns = h->timeout_ns;
   p.fault_block = h->fault_block;
   p.fault_step = h->fault_step;
+  p.lengths = lengths;
   WsLayout lay;
   if (training) lay = ws_layout(h, T, N);
   const int64_t rows = (int64_t)pl.Pr * pl.R * pl.Ur;
@@ -642,6 +650,11 @@ rnn_status_t forward_wavefront(rnn_handle* h, cudaStream_t st, int64_t T, int64_
     a.c0 = (c0 && h->mode == RNN_LSTM) ? cp<float>(c0, l * NH * 4) : nullptr;
     a.hy = hy ? mp<char>(hy, l * NH * e) : nullptr;
     a.cy = (cy && h->mode == RNN_LSTM) ? mp<float>(cy, l * NH * 4) : nullptr;
+    if (drop_masks && l < h->L - 1) {
+      // this layer's output reaches the next layer dropped
+      a.drop_mask = drop_masks + (int64_t)l * T * NH;
+      a.drop_scale = 1.f / (1.f - drop_p);
+    }
   }
   *used = true;
   {
@@ -684,8 +697,9 @@ rnn_status_t forward_impl(rnn_handle* h, cudaStream_t st, int64_t T, int64_t N, 
   }
   bool wf_used = false;
   rnn_status_t s = RNN_OK;
-  if (!lengths && !drop_masks) {  // the wavefront chains the layers inside one launch
-    s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc, &wf_used);
+  {  // the wavefront chains the layers inside one launch
+    s = forward_wavefront(h, st, T, N, x, h0, c0, W, y, hy, cy, ws, training, sc, &wf_used,
+                          lengths, drop_masks, drop_p);
     if (wf_used || s != RNN_OK) return s;
   }
   RecPlan plan, plan_one;
@@ -1325,7 +1339,7 @@ static rnn_status_t get_paths(rnn_t h, int64_t N, int* fwd, int* bwd, bool varle
   };
   WfPlan wp;
   RecPlan pl;
-  if (!varlen && wf_candidate(h, N) &&
+  if (wf_candidate(h, N) &&
       wf_plan(h->mode, 1, h->L, h->D, h->I, h->H, N, h->num_sms, h->smem_optin, &wp) &&
       (size_t)h->L * wp.Pr * 128 <= kSyncBytes - 64) {
     *fwd = RNN_PATH_WAVEFRONT;

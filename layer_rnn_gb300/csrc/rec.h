@@ -87,8 +87,10 @@ struct RecParams {
   int fault_block = -1, fault_step = -1;
   // valid length of each sequence ([N] int32, device), or null: every sequence
   // runs all T steps.  A step t >= lengths[n] keeps sequence n's state and
-  // outputs zero (values outside 0..T act as 0 or T).  Only the staged
-  // CUDA-core kernels (rec_make_plan with allow_direct = false) read it.
+  // outputs zero (values outside 0..T act as 0 or T).  The tensor-core
+  // kernels (forward, backward, batch-as-M backward) and the staged CUDA-core
+  // kernels (rec_make_plan with allow_direct = false) read it; the direct and
+  // cluster kernels do not.
   const int* lengths = nullptr;
   RecDirArgs dir[2];
 };

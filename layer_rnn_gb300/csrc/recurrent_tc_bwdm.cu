@@ -127,6 +127,7 @@ __host__ __device__ inline MLayout m_layout(const RecPlan& pl, int N) {
   return L;
 }
 
+template <bool VL>  // VL: per-sequence lengths (p.lengths) are read
 __global__ void __launch_bounds__(kMThreads, 1)
     rec_bwd_tcm(const __grid_constant__ MMaps maps, const __grid_constant__ RecParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -434,9 +435,21 @@ __global__ void __launch_bounds__(kMThreads, 1)
         return;
       }
       const int64_t row = (int64_t)t * N + n;
+      bf16* gxo = dgx + row * GH + j;
+      if (VL && t >= __ldg(p.lengths + n)) {
+        // a step the forward skipped (past the sequence's length): no gate
+        // gradients, dy unused, dh and (LSTM) dc pass straight through
+        const int G = p.mode == 1 ? 4 : p.mode == 2 ? 3 : 1;
+        for (int g = 0; g < G; ++g) gxo[(int64_t)g * H] = __float2bfloat16_rn(0.f);
+        if (p.mode == 2) {
+          bf16* gho = dgh + row * GH + j;
+          for (int g = 0; g < 3; ++g) gho[(int64_t)g * H] = __float2bfloat16_rn(0.f);
+        }
+        st_carry[it] = dhf;
+        return;
+      }
       const float dh = v[0] + dhf;
       const float g0 = v[1];
-      bf16* gxo = dgx + row * GH + j;
       if (p.mode == 1) {  // LSTM: g0..g3 = i, f, g, o
         const float g1 = v[2], g2 = v[3], g3 = v[4], cc = v[5], cpv = v[6];
         const float tc = tanhf(cc);
@@ -446,6 +459,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         gxo[2 * H] = __float2bfloat16_rn(dc * g0 * (1.f - g2 * g2));
         gxo[3 * H] = __float2bfloat16_rn(dh * tc * g3 * (1.f - g3));
         st_dc[it] = dc * g1;
+        if (VL) st_carry[it] = 0.f;  // a pass-through ends here
       } else if (p.mode == 2) {  // GRU: g0..g3 = r, z, n, W_hn h + b_hn
         const float g1 = v[2], g2 = v[3], g3 = v[4];
         const float hp = __bfloat162float(hseq[((int64_t)sp * N + n) * H + j]);
@@ -462,6 +476,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         st_carry[it] = dh * g1;
       } else {  // tanh RNN: g0 = h_t
         gxo[0] = __float2bfloat16_rn(dh * (1.f - g0 * g0));
+        if (VL) st_carry[it] = 0.f;
       }
     };
     if (!failed) {
@@ -624,7 +639,7 @@ cudaError_t rec_tcm_bwd_launch(const RecParams& p, cudaStream_t st) {
     if (!tma_encode(&maps.a[d], 3, true, p.dir[d].dgh, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  void* fn = (void*)rec_bwd_tcm;
+  void* fn = p.lengths ? (void*)rec_bwd_tcm<true> : (void*)rec_bwd_tcm<false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;

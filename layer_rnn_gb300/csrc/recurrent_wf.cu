@@ -185,6 +185,9 @@ __device__ __forceinline__ float tanh_hw(float x) {
 }
 __device__ __forceinline__ float sigm_hw(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
 
+// EXT: per-sequence lengths and / or inter-layer dropout are in use (a
+// separate instance, so the plain path carries none of their code)
+template <bool EXT>
 __global__ void __launch_bounds__(kWThreads, 1)
     rec_wf_kernel(const __grid_constant__ WfMaps maps, const __grid_constant__ WfParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -299,6 +302,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const unsigned* prev_flags = flags + (size_t)(l > 0 ? l - 1 : 0) * pl.Pr * fstride;
   const int arow = r * R * Ur;   // first packed row of this block
   const int64_t GsH = (int64_t)p.Gs * H;
+  // the x part's time coordinate: row t of x, or of the layer below's
+  // dropped output; else slot t + 1 of the layer below's hidden states
+  const bool x_row0 = l == 0 || (EXT && p.layer[l - 1].drop_mask != nullptr);
+  const float dscale = a.drop_scale;
+  // sequence n's step t: inside its length?
+  auto active = [&](int t, int n) {
+    if constexpr (!EXT) return true;
+    else return p.lengths == nullptr || t < __ldg(p.lengths + n);
+  };
+  // the value of y for output h at element e: zero past the length, the
+  // dropped value where dropout applies
+  auto y_value = [&](float h, bool act, int64_t e) {
+    if constexpr (!EXT) return h;
+    else {
+      if (!act) return 0.f;
+      if (a.drop_mask == nullptr) return h;
+      return __ldg(a.drop_mask + e) != 0 ? __bfloat162float(__float2bfloat16_rn(h)) * dscale : 0.f;
+    }
+  };
 
   for (int t = 0; t < nT && !failed; ++t) {
     WTRACE(t, 0);
@@ -332,7 +354,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                        : "memory");
           tma_2d(dst, &maps.a[l], c * kChunk, arow, fb);
           if (c < nchx)
-            tma_3d(dst + bytesA, &maps.bx[l], c * kChunk, 0, l == 0 ? t : t + 1, fb);
+            tma_3d(dst + bytesA, &maps.bx[l], c * kChunk, 0, x_row0 ? t : t + 1, fb);
           else
             tma_3d(dst + bytesA, &maps.bh[l], (c - nchx) * kChunk, 0, t, fb);
         }
@@ -416,24 +438,34 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const float a3 = pick4(got[0], got[1], got[2], got[3], (3 - g) & 3) + bias[3];
           const int n = cg * 4 + g;
           float& stv = st_s[(cg >> 1) * kWThreads + tid];
-          float o0, o1, o2, o3, h;
+          float o0, o1, o2, o3, h, sn;
           if (p.mode == 1) {  // LSTM: i, f, g, o
             o0 = sigm_hw(a0);
             o1 = sigm_hw(a1);
             o2 = tanh_hw(a2);
             o3 = sigm_hw(a3);
-            const float c = fmaf(o1, stv, o0 * o2);
-            h = o3 * tanh_hw(c);
-            stv = c;
+            sn = fmaf(o1, stv, o0 * o2);
+            h = o3 * tanh_hw(sn);
           } else {  // GRU: r, z, W_in x + b_in, W_hn h + b_hn
             o0 = sigm_hw(a0);
             o1 = sigm_hw(a1);
             o2 = tanh_hw(fmaf(o0, a3, a2));
             o3 = a3;
             h = fmaf(o1, stv - o2, o2);  // (1 - z) n + z h
-            stv = h;
+            sn = h;
           }
-          if (!unit_ok || n >= N) continue;
+          const bool in = unit_ok && n < N;
+          const bool act = !in || active(t, n);
+          if (act) {
+            stv = sn;
+          } else {
+            // past the sequence's length: the state is kept (the LSTM's
+            // h_{t-1} as stored in slot t by this thread, the GRU's state)
+            h = p.mode == 1 ? __bfloat162float(reinterpret_cast<const bf16*>(a.hseq)
+                                                   [(int64_t)t * N * H + (int64_t)n * H + j])
+                            : stv;
+          }
+          if (!in) continue;
           const int64_t row = row0 + n;
           const int64_t o = (int64_t)n * H + j;
           if (a.gates) {
@@ -441,7 +473,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             gp[0] = o0; gp[H] = o1; gp[2 * H] = o2; gp[3 * H] = o3;
           }
           hs[o] = __float2bfloat16_rn(h);
-          if (a.y) store_bf16(a.y, row * H + j, h);
+          if (a.y) store_bf16(a.y, row * H + j, y_value(h, act, row * H + j));
           if (p.mode == 1 && a.cseq) a.cseq[(int64_t)(t + 1) * N * H + o] = stv;
           if (last) {
             if (a.hy) store_bf16(a.hy, o, h);
@@ -458,11 +490,16 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const int n = cg * 4 + i;
             if (!unit_ok || n >= N) continue;
             const int64_t row = row0 + n;
-            const float h = tanh_hw(v[i] + bias[0]);
+            const float hn = tanh_hw(v[i] + bias[0]);
             const int64_t o = (int64_t)n * H + j;
+            const bool act = active(t, n);
+            // past the sequence's length: h_{t-1} as stored in slot t
+            const float h = act ? hn
+                                : __bfloat162float(reinterpret_cast<const bf16*>(a.hseq)
+                                                       [(int64_t)t * N * H + o]);
             hs[o] = __float2bfloat16_rn(h);
-            if (a.y) store_bf16(a.y, row * H + j, h);
-            if (a.gates) a.gates[row * GsH + j] = h;
+            if (a.y) store_bf16(a.y, row * H + j, y_value(h, act, row * H + j));
+            if (a.gates) a.gates[row * GsH + j] = hn;
             if (last && a.hy) store_bf16(a.hy, o, h);
           }
         }
@@ -622,12 +659,20 @@ cudaError_t wf_launch(const WfParams& p, cudaStream_t st) {
       const uint64_t I = (uint64_t)p.I;
       const uint64_t dx[3] = {I, N, T}, sx[2] = {I * 2, N * I * 2};
       if (!tma_encode(&maps.bx[0], 3, true, p.x, dx, sx, bb)) return cudaErrorInvalidValue;
+    } else if (p.layer[l - 1].drop_mask) {
+      // the layer below's dropped output, [T][N][H]
+      if (!p.layer[l - 1].y) return cudaErrorInvalidValue;
+      const uint64_t dy[3] = {H, N, T};
+      if (!tma_encode(&maps.bx[l], 3, true, p.layer[l - 1].y, dy, sh, bb))
+        return cudaErrorInvalidValue;
     } else {
       if (!tma_encode(&maps.bx[l], 3, true, p.layer[l - 1].hseq, dh, sh, bb))
         return cudaErrorInvalidValue;
     }
   }
-  void* fn = (void*)rec_wf_kernel;
+  bool ext = p.lengths != nullptr;
+  for (int l = 0; l < p.L; ++l) ext = ext || p.layer[l].drop_mask != nullptr;
+  void* fn = ext ? (void*)rec_wf_kernel<true> : (void*)rec_wf_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;

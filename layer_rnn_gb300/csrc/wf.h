@@ -36,6 +36,11 @@ struct WfLayer {
   float* cseq = nullptr;        // [T+1][N][H] or null
   void* hy = nullptr;           // [N][H] or null
   float* cy = nullptr;          // [N][H] or null
+  // inter-layer dropout (training, every layer but the last): y holds this
+  // layer's output dropped, bf16(bf16(h) * drop_scale) where the mask byte
+  // [T][N][H] is nonzero, else 0, and the layer above reads its input from y
+  const uint8_t* drop_mask = nullptr;
+  float drop_scale = 1.f;
 };
 
 struct WfParams {
@@ -47,6 +52,9 @@ struct WfParams {
   int* status = nullptr;
   long long timeout_ns = 0;
   int fault_block = -1, fault_step = -1;
+  // valid length of each sequence ([N] int32, device) or null: a step
+  // t >= lengths[n] keeps sequence n's state and writes zero to y
+  const int* lengths = nullptr;
   WfLayer layer[kWfMaxLayers];
 };
 

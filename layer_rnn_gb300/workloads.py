@@ -148,3 +148,12 @@ def make_lengths(cfg, seed=None):
     lens = rng.integers((T + 1) // 2, T + 1, size=N)
     lens[0] = T
     return lens.astype(np.int32)
+
+
+def make_dropout_masks(cfg, p, seed=None):
+    """0/1 inter-layer dropout masks, [L-1, T, N, D*H] uint8, each element 1
+    with probability 1 - p (Bernoulli draws from the seeded generator)."""
+    rng = np.random.Generator(np.random.PCG64((cfg["seed"] if seed is None else seed) + 104729))
+    L, T, N, H = cfg["L"], cfg["T"], cfg["N"], cfg["H"]
+    D = num_directions(cfg)
+    return (rng.random((max(0, L - 1), T, N, D * H)) >= p).astype(np.uint8)

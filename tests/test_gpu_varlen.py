@@ -55,15 +55,20 @@ def _lengths(T, N, seed):
     return np.array((base + list(extra))[:N], dtype=np.int32)
 
 
-# shapes whose recurrent phases take the tensor-core kernels with lengths:
-# mode, L, bidir, T, N, I, H, dtype
+# shapes whose recurrent phases take the tensor-core kernels or the layer
+# wavefront with lengths: mode, L, bidir, T, N, I, H, dtype, (fwd, bwd) paths
 TC_CASES = [
-    ("lstm", 1, False, 9, 20, 48, 800, "f32"),   # the DS2 layer's batch and hidden size
-    ("gru", 1, False, 8, 48, 40, 800, "f32"),
-    ("lstm", 1, True, 5, 24, 32, 800, "f32"),    # the directions in turn
-    ("rnn_tanh", 1, False, 7, 40, 24, 256, "f32"),
-    ("lstm", 2, False, 6, 72, 16, 256, "bf16"),
-    ("gru", 1, True, 6, 36, 16, 200, "bf16"),
+    ("lstm", 1, False, 9, 20, 48, 800, "f32", ("tensor", "tensor")),  # the DS2 layer
+    ("gru", 1, False, 8, 48, 40, 800, "f32", ("tensor", "tensor")),
+    ("lstm", 1, True, 5, 24, 32, 800, "f32", ("tensor", "tensor")),   # directions in turn
+    ("rnn_tanh", 1, False, 7, 40, 24, 256, "f32", ("tensor", "tensor")),
+    ("gru", 1, True, 6, 36, 16, 200, "bf16", ("tensor", "tensor")),
+    # unidirectional bf16 stacks: the wavefront; batches of 64..128 take the
+    # batch-as-M backward
+    ("lstm", 2, False, 6, 72, 16, 256, "bf16", ("wavefront", "tensor")),
+    ("lstm", 4, False, 7, 128, 32, 128, "bf16", ("wavefront", "tensor")),
+    ("gru", 3, False, 8, 40, 16, 48, "bf16", ("wavefront", "tensor")),
+    ("rnn_tanh", 2, False, 9, 96, 24, 40, "bf16", ("wavefront", "tensor")),
 ]
 
 
@@ -103,13 +108,15 @@ def test_varlen_parity(case):
     _check_case(case)
 
 
-@pytest.mark.parametrize("case", TC_CASES, ids=[_cid(c) for c in TC_CASES])
+@pytest.mark.parametrize("case", TC_CASES, ids=[_cid(c[:8]) for c in TC_CASES])
 def test_varlen_tensor_core_kernels(case):
-    _check_case(case, expect=("tensor", "tensor"))
+    _check_case(case[:8], expect=case[8])
 
 
-@pytest.mark.parametrize("case", [CASES[3], CASES[6], TC_CASES[0]],
-                         ids=[_cid(c) for c in (CASES[3], CASES[6], TC_CASES[0])])
+STAGED = [CASES[3], CASES[6], TC_CASES[0][:8], TC_CASES[6][:8]]
+
+
+@pytest.mark.parametrize("case", STAGED, ids=[_cid(c) for c in STAGED])
 def test_varlen_staged_kernels(case):
     from layer_rnn_gb300 import binding as B
     _check_case(case, flags=B.RNN_FLAG_SIMT_RECURRENT, expect=("staged", "staged"))
@@ -136,4 +143,28 @@ def test_full_lengths_match_the_fixed_length_calls(shape):
         r.close()
     if same:
         for k in ("y", "hy", "dx", "dh0", "dW"):
+            assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("shape", [("lstm", 3, 8, 24, 16, 32), ("gru", 2, 6, 80, 16, 48),
+                                   ("rnn_tanh", 2, 5, 16, 8, 24)])
+def test_full_lengths_on_the_wavefront(shape):
+    # every length equal to T on a unidirectional bf16 stack: the varlen calls
+    # run the wavefront and the tensor-core backward as the fixed-length calls
+    # do, and give the same results bit for bit
+    from layer_rnn_gb300 import binding as B
+    mode, L, T, N, I, H = shape
+    cfg = wl.make_config(mode, L, False, T, N, I, H, "bf16", 0.3, seed=5)
+    r = B.Rnn(mode, L, False, I, H, "bf16", 0)
+    try:
+        paths = B.rnn_get_paths_varlen(r.h, N)
+        assert paths == B.rnn_get_paths(r.h, N)
+        assert paths[0] == "wavefront"
+    finally:
+        r.close()
+    inp = wl.make_inputs(cfg)
+    a = harness.run_gpu(cfg, inp, lengths=np.full(N, T, dtype=np.int32))
+    b = harness.run_gpu(cfg, inp)
+    for k in ("y", "hy", "cy", "dx", "dh0", "dc0", "dW", "y_inf", "hy_inf"):
+        if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k
