@@ -51,12 +51,17 @@ struct TcKParams {
   float* part;          // split-K partials [ksplit][M][N] (fp32), or null
   const unsigned* amax;  // scaled fp16 pairs: largest |A|, |B| (float bit patterns)
   const unsigned* bmax;
+  // the epilogue's stores: 0 plain stores, 1 TMA stores of C (fp32, no
+  // accumulate) through maps.cout [M][N], 2 TMA stores of the split-K
+  // partials through maps.cout [ksplit][M][N]
+  int tma_out;
   int* status;
   long long timeout_ns;
 };
 
 struct TcMaps {
   CUtensorMap a1h, a1l, b1h, b1l, a2h, a2l, b2h, b2l;
+  CUtensorMap cout;  // fp32 output (tma_out != 0), box 32 x 32 (x 1), 128-byte swizzle
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -142,6 +147,29 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// tile store from shared memory (the box the map names at {x, y} or
+// {x, y, z}); completion tracked by the issuing thread's bulk groups
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -172,6 +200,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t bars[2 * 8 + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float s_bias[BN];  // the tile's column bias (TMA-store epilogue)
   // K bytes per tile row and stage: 64 for the fp16 pairs at BN = 256 (four
   // operand tiles a stage: 48 KB, so four stages fit instead of two), else
   // 128 (at BN = 128 the 64-byte rows measured slower: twice the stages for
@@ -201,6 +230,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (p.tma_out) {
+    for (int c = threadIdx.x; c < BN; c += kTcThreads) {
+      const int n = n0 + c;
+      float b = 0.f;
+      if (p.tma_out == 1 && n < p.N) {
+        if (p.bias1) b += load_any(p.bias1, n, p.bias_bf16);
+        if (p.bias2 && n < p.bias2_limit) b += load_any(p.bias2, n, p.bias_bf16);
+      }
+      s_bias[c] = b;
+    }
   }
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -270,7 +310,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   bool ok = true;
   if (have_k) ok = mbar_wait(done, 0, p.status, p.timeout_ns, &abort_flag);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (ok && !abort_flag) {
+  if (ok && !abort_flag && p.tma_out) {
+    // the pipeline stages are free now: warp w stages its 32 rows, 32 columns
+    // at a time, in the 128-byte-swizzled layout of a 32 x 32 fp32 box (16-byte
+    // piece j of row r at piece j ^ (r & 7): conflict-free vector stores), and
+    // one lane stores each box with TMA (full lines; rows and columns past
+    // the output are clipped by the map)
+    // the scales one at a time, as the plain epilogue applies them (their
+    // product alone may leave the fp32 range where the result does not)
+    float ia = 1.f, ib = 1.f;
+    if (SPLIT) {
+      ia = pow2f(-f16_scale_exp(*p.amax));
+      ib = pow2f(-f16_scale_exp(*p.bmax));
+    }
+    const int row0 = m0 + warp * 32;
+    const uint32_t wbuf = base + (uint32_t)(warp * 32 * BN * 4);
+    if (row0 < p.M) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        if (n0 + c0 >= p.N) break;
+        float v[32];
+        if (have_k) {
+          tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        const uint32_t rb = wbuf + (uint32_t)c0 * 128u + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4),
+                       fmaf(v[4 * j] * ia, ib, s_bias[c0 + 4 * j]),
+                       fmaf(v[4 * j + 1] * ia, ib, s_bias[c0 + 4 * j + 1]),
+                       fmaf(v[4 * j + 2] * ia, ib, s_bias[c0 + 4 * j + 2]),
+                       fmaf(v[4 * j + 3] * ia, ib, s_bias[c0 + 4 * j + 3]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (p.tma_out == 2)
+            tma_store_3d(&maps.cout, wbuf + (uint32_t)c0 * 128u, n0 + c0, row0, z);
+          else
+            tma_store_2d(&maps.cout, wbuf + (uint32_t)c0 * 128u, n0 + c0, row0);
+        }
+      }
+      if (lane == 0) {
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      }
+      __syncwarp();
+    }
+  } else if (ok && !abort_flag) {
     // the pipeline stages are free now: each warp stages its 32 rows x BN
     // accumulators in shared memory (row pitch BN + 1 floats, conflict-free),
     // then writes them row by row, 32 consecutive columns per instruction
@@ -796,6 +885,14 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   if (kp.ksplit > 1) {
     kp.part = g.part;
     if (!kp.part) return cudaErrorInvalidValue;
+    // partials [ksplit][M][N] fp32 through a 3-D map (rows past M clipped
+    // within each split)
+    if (reinterpret_cast<uintptr_t>(g.part) % 16 == 0 && g.N % 4 == 0) {
+      const uint64_t dims[3] = {(uint64_t)g.N, (uint64_t)g.M, (uint64_t)kp.ksplit};
+      const uint64_t strides[2] = {(uint64_t)g.N * 4, (uint64_t)g.N * g.M * 4};
+      const uint32_t box[3] = {32u, 32u, 1u};
+      if (tma_encode(&maps.cout, 3, false, g.part, dims, strides, box)) kp.tma_out = 2;
+    }
   } else {
     kp.C = g.C;
     kp.ldc = g.ldc;
@@ -805,7 +902,17 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
     kp.bias2 = g.bias2;
     kp.bias2_limit = g.bias2_limit;
     kp.bias_bf16 = g.bias_bf16;
+    // fp32 C written whole (no accumulate): TMA stores
+    if (!g.out_bf16 && !g.accumulate && reinterpret_cast<uintptr_t>(g.C) % 16 == 0 &&
+        g.ldc % 4 == 0) {
+      const uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)g.M};
+      const uint64_t strides[1] = {(uint64_t)g.ldc * 4};
+      const uint32_t box[2] = {32u, 32u};
+      if (tma_encode(&maps.cout, 2, false, g.C, dims, strides, box)) kp.tma_out = 1;
+    }
   }
+  // the TMA-store epilogue stages 32 rows x BN fp32 per warp in the stages
+  if (kp.tma_out && (size_t)kp.stages * stage < (size_t)4 * 32 * BN * 4) kp.tma_out = 0;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)kp.ksplit);
   cudaError_t e;
   if (sp)
