@@ -16,11 +16,13 @@
 //     read as zeros) while one thread issues the MMAs;
 //   * the accumulator D[n][u] (tensor memory, lane = batch row) is pushed, 4
 //     units per 16-byte DSMEM store, to the block that owns the units'
-//     pointwise step; the owners sum the Pk partials in a fixed order, run the
+//     pointwise step (with two partial-sum buffers as st.async stores that
+//     complete the owner's barrier for the step, else plain stores and a
+//     cluster barrier); the owners sum the partials in a fixed order, run the
 //     gate-gradient chain and store dG (bf16), then release their step flag.
 // The loads read what other blocks stored, so the writer fences its stores to
 // the async proxy before its release and the reader after its acquire.  All
-// waits are bounded; cluster barriers run on every step, work or not.
+// waits are bounded.
 #include <cuda.h>
 
 #include <algorithm>
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     rec_bwd_tcm(const __grid_constant__ MMaps maps, const __grid_constant__ RecParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kMStages + 1];
+  __shared__ __align__(8) uint64_t rbars[2];  // partial sums landed (two buffers)
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail, s_stop, s_issued;
   const RecPlan& pl = p.plan;
@@ -182,6 +185,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
+    for (int i = 0; i < 2; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rbars[i])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 2 && !cfg_bad) {
@@ -223,6 +228,20 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(Urp >> 3) << 17) |
                          ((uint32_t)(kMRows >> 4) << 24);
   bool failed = s_fail != 0;
+  // with two partial-sum buffers the partials of step s land in buffer s & 1
+  // with barrier-completing st.async stores that complete rbars[s & 1]: the
+  // owner waits for the bytes, not for a cluster barrier.  Only blocks with a
+  // K slice push (one with an empty slice waits on no flag and would run
+  // ahead); a pusher's step-s pushes follow its own step s-1 sums and the
+  // flags of step s - 1, so buffer s & 1 is free again by then.
+  const bool async_rx = pl.rbufs == 2;
+  const int pushers = (int)min((int64_t)Pk, (GH + max(1, pl.Kk) - 1) / max(1, pl.Kk));
+  const uint32_t rx_bytes = (uint32_t)(pushers * N * ((Uqc + 3) / 4) * 16);
+  const uint32_t rbar0 = smem_addr(&rbars[0]);
+  // every block's barriers are initialised before any peer pushes into them
+  fence_before();
+  cl_sync();
+  fence_after();
   uint32_t chunk_it = 0;  // ring position (chunks issued over all steps)
   uint32_t done_ph = 0;
   const int q4 = warp & 3, half = warp >> 2;
@@ -394,7 +413,9 @@ __global__ void __launch_bounds__(kMThreads, 1)
     // push the accumulator rows (batch n) to the owners of the units, 4 units
     // per 16-byte store (Uq is a multiple of 4)
     float* recv = recv0 + (size_t)(pl.rbufs == 2 ? (s & 1) : 0) * Pk * N * Uq;
-    if (!failed && s > 0) {
+    const uint32_t rbar = rbar0 + 8u * (uint32_t)(s & 1);
+    if (async_rx && !failed && s > 0 && tid == 0) mbar_arrive_expect_tx(rbar, rx_bytes);
+    if (!failed && s > 0 && (!async_rx || Kc > 0)) {
       for (int cg = half; cg < Urp / 4; cg += 2) {
         float v[4];
         tmem_ld4m(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(cg * 4), v);
@@ -402,16 +423,30 @@ __global__ void __launch_bounds__(kMThreads, 1)
         if (nrow >= N || u >= Urc) continue;
         const int owner = u / Uq, uo = u - owner * Uq;
         if (owner >= Pk) continue;
-        st_peer4(recv + ((size_t)q * N + nrow) * Uq + uo, (unsigned)owner, have ? v[0] : 0.f,
-                 have ? v[1] : 0.f, have ? v[2] : 0.f, have ? v[3] : 0.f);
+        float* dst = recv + ((size_t)q * N + nrow) * Uq + uo;
+        if (async_rx)
+          st_async4(dst, rbar, (unsigned)owner, have ? v[0] : 0.f, have ? v[1] : 0.f,
+                    have ? v[2] : 0.f, have ? v[3] : 0.f);
+        else
+          st_peer4(dst, (unsigned)owner, have ? v[0] : 0.f, have ? v[1] : 0.f, have ? v[2] : 0.f,
+                   have ? v[3] : 0.f);
       }
     }
     fence_before();
-    cl_sync();
+    if (async_rx) {
+      // this step's partials: the owners' threads wait for the pushed bytes
+      if (!failed && s > 0 && tid < items &&
+          !mbar_wait_cluster_bounded(rbar, (uint32_t)((s - 1) >> 1) & 1u, p.status,
+                                     p.timeout_ns))
+        s_fail = 1;
+    } else {
+      cl_sync();
+    }
     if (!failed && s > 0) {
+      const int nsum = async_rx ? pushers : Pk;
       for (int it = tid; it < items; it += kMThreads) {
         const int uu = it % Uqc, n = it / Uqc;
-        outs[n * Uq + uu] = sum_strided<8>(recv + (size_t)n * Uq + uu, (size_t)N * Uq, Pk);
+        outs[n * Uq + uu] = sum_strided<8>(recv + (size_t)n * Uq + uu, (size_t)N * Uq, nsum);
       }
     }
     // one partial-sum buffer: nobody pushes the next step's partials before
@@ -419,6 +454,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     if (pl.rbufs == 1) cl_sync();
     cp_async_wait_all();
     __syncthreads();
+    failed = s_fail != 0;  // a wait for the partials may have given up
     MTRACE(s, 2);
     // one item's gate-gradient chain; v = its inputs (unused at s == nT)
     auto point = [&](int it, const float (&v)[kMNIn]) {
