@@ -298,7 +298,8 @@ rnn_status_t run_gemm(const rnn_handle* h, const GemmArgs& g, Scratch sc, cudaSt
       t.bias_bf16 = g.bias_bf16;
       t.status = h->d_status;
       t.timeout_ns = h->timeout_ns;
-      const int ks = g.no_split ? 1 : gemm_tc_splitk(g.M, g.N, g.K + g.K2, tf, h->num_sms);
+      int ks = 1;
+      gemm_tc_shape(g.M, g.N, g.K + g.K2, tf, h->num_sms, !g.no_split, &t.bn, &ks);
       if (ks > 1) {
         t.part = static_cast<float*>(sc.take(ks * g.M * g.N * 4));
         if (t.part) t.ksplit = ks;

@@ -44,13 +44,16 @@ struct TcGemm {
   void* C = nullptr; int64_t ldc = 0; int out_bf16 = 0; int accumulate = 0;
   const void* bias1 = nullptr; const void* bias2 = nullptr; int64_t bias2_limit = 0;
   int bias_bf16 = 0;
+  int bn = 0;  // output tile width (64, 128, 160, 256; 0: chosen by the wave model)
   int ksplit = 1; float* part = nullptr;  // split-K partials [ksplit][M][N]
   int* status = nullptr; long long timeout_ns = 2000000000LL;
 };
 bool gemm_tc_supported(const TcGemm& g);
 cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st);
-// K splits worth using for an M x N output with K_total contraction length
-int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms);
+// tile width and K split for an M x N output with K_total contraction length
+// (allow_split = false: one split)
+void gemm_tc_shape(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms,
+                   bool allow_split, int* bn, int* ksplit);
 // largest |x| of fp32 [rows][cols] (row stride lds) into *mx (atomicMax of the
 // float bit pattern: the caller zeroes *mx first; several operands may share it)
 cudaError_t absmax_operand(const float* src, int64_t rows, int64_t cols, int64_t lds,

@@ -201,11 +201,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float s_bias[BN];  // the tile's column bias (TMA-store epilogue)
-  // K bytes per tile row and stage: 64 for the fp16 pairs at BN = 256 (four
-  // operand tiles a stage: 48 KB, so four stages fit instead of two), else
-  // 128 (at BN = 128 the 64-byte rows measured slower: twice the stages for
-  // the same data)
-  constexpr int ROWB = (SPLIT && BN == 256) ? 64 : 128;
+  // K bytes per tile row and stage: 64 for the fp16 pairs at BN > 128 (four
+  // operand tiles a stage: 48 KB at BN = 256, so four stages fit instead of
+  // two), else 128 (at BN = 128 the 64-byte rows measured slower: twice the
+  // stages for the same data)
+  constexpr int ROWB = (SPLIT && BN > 128) ? 64 : 128;
+  // tensor-memory columns: a power of two of at least 32
+  constexpr uint32_t kCols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
   constexpr int kA = BM * ROWB;                    // bytes of one A tile
   constexpr int kB = BN * ROWB;                    // bytes of one B tile
   constexpr int kStage = (kA + kB) * (SPLIT ? 2 : 1);
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tmem_slot)),
-                 "r"(BN)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 2)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
                  : "memory");
 }
 
@@ -758,7 +760,7 @@ bool operand_ok(const void* p, int64_t ld, int e) {
 
 template <int BN, bool SPLIT>
 cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaStream_t st) {
-  constexpr int kStage = (BM + BN) * ((SPLIT && BN == 256) ? 64 : 128) * (SPLIT ? 2 : 1);
+  constexpr int kStage = (BM + BN) * ((SPLIT && BN > 128) ? 64 : 128) * (SPLIT ? 2 : 1);
   const size_t smem = (size_t)kp.stages * kStage + 1024;
   auto fn = gemm_tc_kernel<BN, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -788,48 +790,54 @@ bool tma_encode(void* map, int rank, bool bf, const void* ptr, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output tile width: 256 columns when the output is wide enough.  A 128 x 256
-// tile reads each A tile once for twice the MMA work of a 128 x 128 tile,
-// which matters because the operand stream from L2 (about 64 bytes per clock
-// per SM) otherwise limits the tensor pipe (bf16 128 x 128 tiles need ~117).
-int gemm_tc_bn(int64_t N) {
-  if (N <= 64) return 64;
-  if (N < 192) return 128;
-  // 256 wide reads each A tile once for twice the MMA work; 128 wide when
-  // the last 256-wide tile would waste more than a tenth of the columns more
-  // (N = 800: 1024 columns against 896; measured faster for the dX and GRU
-  // weight-gradient GEMMs of the DS2 layer)
-  const double w256 = (double)((N + 255) / 256 * 256) / N, w128 = (double)((N + 127) / 128 * 128) / N;
-  return w256 > w128 + 0.1 ? 128 : 256;
+// Tile width and K split from a wave model.  One 64-element K block of a
+// 128 x BN tile costs the larger of its MMA time (three passes for scaled fp16
+// pairs, at about 1/152 of the dense f16 rate per SM) and its operand feed
+// (128 + BN rows of 128 bytes, twice for hi and lo, at about 64 bytes per
+// clock per SM: wide tiles read each A tile once for more MMA work).  The grid
+// runs in ceil(units / SMs) waves of ceil(nkt / ks) K blocks plus a fixed
+// cost per tile (launch, pipeline fill, epilogue: about 10 us, fitted to the
+// DS2 GEMMs); a split adds its fp32 partial sums (written and read once) at
+// HBM speed.  A 160-wide tile pays where it empties the last wave: the DS2
+// dX (N = 800) runs 2 waves of 47 x 5 tiles instead of 3 of 47 x 7 at 128,
+// and the weight gradients one wave of 25 x 5 tiles with no split.  (224
+// wide measured no faster than 256 at the same number of waves.)
+namespace {
+double kb_clocks(int BN, bool split16) {
+  const double mma = 2.0 * BM * BN * 64.0 * (split16 ? 3.0 : 1.0) / (2.25e15 / 152.0 / 2.07e9);
+  const double feed = (double)(BM + BN) * 128.0 * (split16 ? 2.0 : 1.0) / 64.0;
+  return std::max(mma, feed);
 }
+}  // namespace
 
-// Split of K that minimises a wave model: the grid runs in ceil(units / SMs)
-// waves of ceil(nkt / ks) 128-byte K blocks each, plus the fp32 partial sums
-// (written and read once per split) at HBM speed, in K-block time units.
-int gemm_tc_splitk(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms) {
-  const int BN = gemm_tc_bn(N);
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+void gemm_tc_shape(int64_t M, int64_t N, int64_t K_total, bool split16, int num_sms,
+                   bool allow_split, int* bn_out, int* ks_out) {
   const int64_t nkt = (K_total * 2 + 127) / 128;
-  if (nkt < 8 || num_sms < 1) return 1;
-  // one K block of one tile: 2*128*BN*64 flop (x3 passes for scaled fp16
-  // pairs) on one SM at about 1/152 of the dense f16 rate (2.25 PFLOP/s)
-  const double kb_flop = 2.0 * BM * BN * 64.0 * (split16 ? 3.0 : 1.0);
-  const double sm_rate = 2.25e15 / 152.0;
-  const double t_kb = kb_flop / sm_rate;
-  const double red_per_split = 8.0 * (double)M * N / 6.0e12 / t_kb;
-  int best_ks = 1;
-  double best = 0;
-  for (int ks = 1; ks <= 8; ++ks) {
-    if (ks > 1 && nkt / ks < 4) break;
-    const int64_t units = tiles * ks;
-    const double waves = (double)((units + num_sms - 1) / num_sms);
-    const double cost = waves * (double)((nkt + ks - 1) / ks) + (ks > 1 ? red_per_split * ks : 0.0);
-    if (ks == 1 || cost < best) {
-      best = cost;
-      best_ks = ks;
+  const int sms = std::max(1, num_sms);
+  const double red_clk = 8.0 * (double)M * N / 6.0e12 * 2.07e9;  // per split
+  int best_bn = N <= 64 ? 64 : 128, best_ks = 1;
+  double best = -1;
+  const double fixed_clk = 20000.0;  // per tile and wave
+  for (int BN : {64, 128, 160, 256}) {
+    if ((BN == 64) != (N <= 64)) continue;
+    if (BN > 128 && BN > (N + 31) / 32 * 32) continue;  // no tile wider than the output
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const double t_kb = kb_clocks(BN, split16);
+    for (int ks = 1; ks <= 8; ++ks) {
+      if (ks > 1 && (!allow_split || nkt < 8 || nkt / ks < 4)) break;
+      const int64_t units = tiles * ks;
+      const double waves = (double)((units + sms - 1) / sms);
+      const double cost = waves * ((double)((nkt + ks - 1) / ks) * t_kb + fixed_clk) +
+                          (ks > 1 ? red_clk * ks : 0.0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        best_bn = BN;
+        best_ks = ks;
+      }
     }
   }
-  return best_ks;
+  *bn_out = best_bn;
+  *ks_out = best_ks;
 }
 
 bool gemm_tc_supported(const TcGemm& g) {
@@ -849,12 +857,14 @@ bool gemm_tc_supported(const TcGemm& g) {
 
 cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   const bool sp = g.split16 != 0;
-  const int BN = gemm_tc_bn(g.N);
+  int BN = g.bn, ks_unused = 1;
+  if (BN == 0) gemm_tc_shape(g.M, g.N, g.K + g.K2, sp, 148, false, &BN, &ks_unused);
+  if (BN != 64 && BN != 128 && BN != 160 && BN != 256) return cudaErrorInvalidValue;
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
   // every operand is 16-bit (fp16 pairs or bf16): TMA copies bytes, so one
   // 16-bit map type serves both
-  const int rowb = (sp && BN == 256) ? 64 : 128;  // K bytes per tile row and stage
+  const int rowb = (sp && BN > 128) ? 64 : 128;  // K bytes per tile row and stage
   bool ok = make_map(&maps.a1h, g.A_hi, g.M, g.K, g.lda, rowb, BM) &&
             make_map(&maps.b1h, g.B_hi, g.N, g.K, g.ldb, rowb, BN);
   if (sp)
@@ -917,10 +927,12 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   cudaError_t e;
   if (sp)
     e = BN == 256   ? launch_tc<256, true>(maps, kp, grid, st)
+        : BN == 160 ? launch_tc<160, true>(maps, kp, grid, st)
         : BN == 128 ? launch_tc<128, true>(maps, kp, grid, st)
                     : launch_tc<64, true>(maps, kp, grid, st);
   else
     e = BN == 256   ? launch_tc<256, false>(maps, kp, grid, st)
+        : BN == 160 ? launch_tc<160, false>(maps, kp, grid, st)
         : BN == 128 ? launch_tc<128, false>(maps, kp, grid, st)
                     : launch_tc<64, false>(maps, kp, grid, st);
   if (e != cudaSuccess || kp.ksplit == 1) return e;
