@@ -317,7 +317,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // at a time, in the 128-byte-swizzled layout of a 32 x 32 fp32 box (16-byte
     // piece j of row r at piece j ^ (r & 7): conflict-free vector stores), and
     // one lane stores each box with TMA (full lines; rows and columns past
-    // the output are clipped by the map)
+    // the output are clipped by the map).  Box bases are 4 KB apart from the
+    // 1024-byte-aligned ring base, as the swizzle wants.
     // the scales one at a time, as the plain epilogue applies them (their
     // product alone may leave the fp32 range where the result does not)
     float ia = 1.f, ib = 1.f;
@@ -326,7 +327,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ib = pow2f(-f16_scale_exp(*p.bmax));
     }
     const int row0 = m0 + warp * 32;
-    const uint32_t wbuf = base + (uint32_t)(warp * 32 * BN * 4);
+    // two 4 KB boxes per warp, alternating: a box is rewritten once the
+    // store that read it has finished reading (at most one store pending)
+    const uint32_t wbuf = base + (uint32_t)(warp * 2 * 4096);
     if (row0 < p.M) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -338,7 +341,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        const uint32_t rb = wbuf + (uint32_t)c0 * 128u + (uint32_t)lane * 128u;
+        const uint32_t box = wbuf + (uint32_t)((c0 >> 5) & 1) * 4096u;
+        if (c0 >= 64) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+        }
+        const uint32_t rb = box + (uint32_t)lane * 128u;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4),
@@ -350,15 +358,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (p.tma_out == 2)
-            tma_store_3d(&maps.cout, wbuf + (uint32_t)c0 * 128u, n0 + c0, row0, z);
+            tma_store_3d(&maps.cout, box, n0 + c0, row0, z);
           else
-            tma_store_2d(&maps.cout, wbuf + (uint32_t)c0 * 128u, n0 + c0, row0);
+            tma_store_2d(&maps.cout, box, n0 + c0, row0);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
       }
-      if (lane == 0) {
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-      }
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       __syncwarp();
     }
   } else if (ok && !abort_flag) {
@@ -761,7 +767,9 @@ bool operand_ok(const void* p, int64_t ld, int e) {
 template <int BN, bool SPLIT>
 cudaError_t launch_tc(const TcMaps& maps, const TcKParams& kp, dim3 grid, cudaStream_t st) {
   constexpr int kStage = (BM + BN) * ((SPLIT && BN > 128) ? 64 : 128) * (SPLIT ? 2 : 1);
-  const size_t smem = (size_t)kp.stages * kStage + 1024;
+  // at least 80 KB: never three CTAs on an SM (their accumulators would not
+  // all fit in its tensor memory)
+  const size_t smem = std::max<size_t>((size_t)kp.stages * kStage + 1024, 80 * 1024);
   auto fn = gemm_tc_kernel<BN, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -921,8 +929,15 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
       if (tma_encode(&maps.cout, 2, false, g.C, dims, strides, box)) kp.tma_out = 1;
     }
   }
-  // the TMA-store epilogue stages 32 rows x BN fp32 per warp in the stages
-  if (kp.tma_out && (size_t)kp.stages * stage < (size_t)4 * 32 * BN * 4) kp.tma_out = 0;
+  // two CTAs per SM (a ring of at most 100 KB each: one CTA's accumulator
+  // drain and stores run under the other's main loop) with the TMA-store
+  // epilogue, whose staging is small
+  if (kp.tma_out && g.ctas_per_sm == 2) kp.stages = std::max(2, std::min(8, (100 * 1024) / stage));
+  // the TMA-store epilogue stages two 32 x 32 fp32 boxes per warp in the
+  // ring, the plain one a 32 x (BN + 1) fp32 tile per warp
+  if (kp.tma_out && (size_t)kp.stages * stage < (size_t)4 * 2 * 4096) kp.tma_out = 0;
+  if (!kp.tma_out && (size_t)kp.stages * stage < (size_t)4 * 32 * (BN + 1) * 4)
+    return cudaErrorInvalidValue;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)kp.ksplit);
   cudaError_t e;
   if (sp)
