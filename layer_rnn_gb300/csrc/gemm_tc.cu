@@ -17,7 +17,10 @@
 // problem is split along K; the partial tiles are then summed in a fixed order
 // by splitk_reduce_kernel).  Thread 0 issues the TMA loads, thread 32 the MMAs,
 // and all four warps read the accumulator out of tensor memory for the
-// epilogue.  Every mbarrier wait is bounded by %globaltimer.
+// epilogue, which stores fp32 results written whole with TMA (32 x 32 boxes)
+// and the others through a padded shared-memory tile.  The tile width and
+// the K split come from a wave model (gemm_tc_shape); multi-wave fp32 GEMMs
+// run two CTAs per SM.  Every mbarrier wait is bounded by %globaltimer.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
