@@ -95,3 +95,19 @@ def test_all_ones_masks_without_dropout_match_the_plain_calls(shape):
     for k in ("y", "hy", "cy", "dx", "dh0", "dc0", "dW"):
         if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("name", ["bi5_gru", "lstm4_bf16"])
+def test_dropout_workload_parity(name):
+    # the bench's stacks with the bench's masks (p = 0.3): bi5_gru at full
+    # size, layer by layer; lstm4_bf16 on the wavefront at T = 128 (the
+    # oracle's float64 masks stay below 0.5 GB; every step does the same work)
+    cfg = wl.WORKLOADS[name]
+    if name == "lstm4_bf16":
+        cfg = wl.with_sizes(cfg, T=128)
+    inp = wl.make_inputs(cfg)
+    p = 0.3
+    masks = wl.make_dropout_masks(cfg, p)
+    gpu = harness.run_gpu(cfg, inp, inference=False, dropout=(p, masks))
+    ref = harness.run_oracle(cfg, inp, dropout=(p, list(masks.astype(np.float64))))
+    harness.assert_parity(cfg, gpu, ref)

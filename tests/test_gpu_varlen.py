@@ -168,3 +168,19 @@ def test_full_lengths_on_the_wavefront(shape):
     for k in ("y", "hy", "cy", "dx", "dh0", "dc0", "dW", "y_inf", "hy_inf"):
         if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("name", ["ds2_lstm", "ds2_gru", "lstm4_bf16"])
+def test_varlen_workload_parity(name):
+    # the bench's batches with the bench's lengths (one sequence of length T,
+    # the others uniform in [T/2, T]), at full size, in the bench's launch
+    # configuration
+    cfg = wl.WORKLOADS[name]
+    inp = wl.make_inputs(cfg)
+    lengths = wl.make_lengths(cfg)
+    gpu = harness.run_gpu(cfg, inp, lengths=lengths)
+    ref = harness.run_oracle(cfg, inp, lengths=lengths)
+    harness.assert_parity(cfg, gpu, ref)
+    for n, ln in enumerate(lengths):
+        assert not gpu["y"][ln:, n].any(), n
+    assert np.array_equal(gpu["y_inf"], gpu["y"])
