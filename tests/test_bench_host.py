@@ -6,6 +6,7 @@ capture."""
 import json
 import os
 
+import numpy as np
 import pytest
 
 
@@ -87,3 +88,28 @@ def test_committed_traffic_entries_name_existing_profiles():
             assert os.path.exists(os.path.join(bench.ROOT, ent["source"])), (wl, ph)
             assert os.path.exists(os.path.join(bench.ROOT, ent["profile"])), (wl, ph)
             assert ent["dram_bytes_per_launch"] > 0
+
+
+def test_bench_lengths_follow_the_stated_recipe():
+    # one sequence of the full T, the others in [ceil(T/2), T], seeded
+    from layer_rnn_gb300 import workloads as wl
+    for name in ("ds2_lstm", "lstm4_bf16", "tiny_lstm"):
+        cfg = wl.WORKLOADS[name]
+        T, N = cfg["T"], cfg["N"]
+        a = wl.make_lengths(cfg)
+        assert a.dtype == np.int32 and a.shape == (N,)
+        assert a[0] == T and a.max() == T and a.min() >= (T + 1) // 2
+        assert np.array_equal(a, wl.make_lengths(cfg))
+        assert not np.array_equal(a, wl.make_lengths(cfg, seed=cfg["seed"] + 1)) or N < 3
+
+
+def test_bench_dropout_masks_follow_the_stated_recipe():
+    # 0/1 bytes over [L-1, T, N, D*H], ones with probability 1 - p, seeded
+    from layer_rnn_gb300 import workloads as wl
+    cfg = wl.WORKLOADS["bi5_gru"]
+    m = wl.make_dropout_masks(cfg, 0.3)
+    assert m.dtype == np.uint8 and m.shape == (cfg["L"] - 1, cfg["T"], cfg["N"], 2 * cfg["H"])
+    assert set(np.unique(m)) <= {0, 1}
+    assert abs(m.mean() - 0.7) < 0.01
+    assert np.array_equal(m, wl.make_dropout_masks(cfg, 0.3))
+    assert wl.make_dropout_masks(wl.WORKLOADS["ds2_lstm"], 0.3).shape[0] == 0
