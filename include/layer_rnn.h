@@ -380,6 +380,22 @@ rnn_status_t rnn_debug_wf_pack(rnn_t h, void* stream, int64_t N, int layer, cons
                                void* wp, int64_t wp_bytes, float* bias, int64_t bias_bytes,
                                int64_t* layout);
 
+/* Test hook for the dense phases' launch shape (host only; no device is
+ * touched).  For C[M][N] over a contraction of K_total on num_sms SMs, with
+ * scaled fp16 pairs (split16 = 1, fp32 operands) or bf16 (0), K splits
+ * allowed or not (allow_split), *bn receives the output tile width (64, 128,
+ * 160 or 256 columns; tiles are 128 rows) and *ksplit the number of K splits
+ * that the library's wave model picks: per tile and 64-element K block the
+ * larger of the MMA time and the operand feed, times ceil(tiles * ksplit /
+ * num_sms) waves, plus a fixed cost per tile and wave and the split's partial
+ * sums.  A GEMM of more than one wave whose fp32 result is written whole is
+ * then re-planned for 2 * num_sms (two CTAs per SM); this hook gives the
+ * plan for the num_sms it is asked about.
+ * Errors: RNN_ERR_INVALID_ARG for M, N or K_total < 1, num_sms < 1 or a
+ * NULL output. */
+rnn_status_t rnn_debug_gemm_shape(int64_t M, int64_t N, int64_t K_total, int split16, int num_sms,
+                                  int allow_split, int* bn, int* ksplit);
+
 /* Static description of the status code. */
 const char* rnn_status_string(rnn_status_t s);
 

@@ -66,6 +66,8 @@ SIGNATURES = {
                                     ctypes.POINTER(ctypes.c_int)]),
     "rnn_measure_step_protocol": (_i32, [_vp, _vp, _i64, _i64, ctypes.POINTER(ctypes.c_double)]),
     "rnn_debug_split_f16": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _vp]),
+    "rnn_debug_gemm_shape": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32,
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "rnn_debug_transpose_bf16": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp]),
     "rnn_debug_wf_pack": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _pi64]),
     "rnn_status_string": (ctypes.c_char_p, [_i32]),
@@ -243,6 +245,14 @@ def rnn_get_paths(h, N):
     f, b = ctypes.c_int(), ctypes.c_int()
     _call("rnn_get_paths", h, N, ctypes.byref(f), ctypes.byref(b))
     return PATHS[f.value], PATHS[b.value]
+
+
+def rnn_debug_gemm_shape(M, N, K_total, split16, num_sms, allow_split=True):
+    """(tile width, K splits) the dense phases' wave model picks (host only)."""
+    bn, ks = ctypes.c_int(), ctypes.c_int()
+    _call("rnn_debug_gemm_shape", M, N, K_total, int(split16), num_sms, int(allow_split),
+          ctypes.byref(bn), ctypes.byref(ks))
+    return bn.value, ks.value
 
 
 def rnn_get_paths_varlen(h, N):

@@ -1376,6 +1376,13 @@ rnn_status_t rnn_get_paths_varlen(rnn_t h, int64_t N, int* fwd, int* bwd) {
 // ----------------------------------------------------------------------------
 // test hooks: the packed operand forms, produced by the library's own kernels
 // ----------------------------------------------------------------------------
+rnn_status_t rnn_debug_gemm_shape(int64_t M, int64_t N, int64_t K_total, int split16, int num_sms,
+                                  int allow_split, int* bn, int* ksplit) {
+  if (M < 1 || N < 1 || K_total < 1 || num_sms < 1 || !bn || !ksplit) return RNN_ERR_INVALID_ARG;
+  gemm_tc_shape(M, N, K_total, split16 != 0, num_sms, allow_split != 0, bn, ksplit);
+  return RNN_OK;
+}
+
 rnn_status_t rnn_debug_split_f16(const float* src, int64_t rows, int64_t cols, int64_t lds,
                                  void* hi, void* lo, int64_t ldd, int transpose, unsigned* maxbits,
                                  void* stream) {

@@ -198,3 +198,34 @@ def test_dropout_calls_reject_bad_arguments_before_any_launch(B):
                                                 256, None, None, 256, ws - 1) == 3
     finally:
         B.rnn_destroy(h)
+
+
+@pytest.mark.parametrize("shape,expect", [
+    # the DS2 layer's dense GEMMs on 148 SMs (fp32, scaled fp16 pairs)
+    ((6000, 3200, 800, 1), (256, 1)),   # input projection: 5 waves of 47 x 13
+    ((6000, 800, 3200, 1), (160, 1)),   # dX: 2 waves of 47 x 5 (3 of 47 x 7 at 128)
+    ((3200, 800, 6000, 1), (160, 1)),   # dW: one wave of 25 x 5, no split
+    # bf16 stacks: the widest tile
+    ((65536, 4096, 1024, 0), (256, 1)),
+    # narrow outputs take 64-wide tiles
+    ((1000, 48, 256, 1), (64, 1)),
+])
+def test_gemm_shape_model_picks_the_documented_shapes(B, shape, expect):
+    M, N, K, sp = shape
+    assert B.rnn_debug_gemm_shape(M, N, K, sp, 148) == expect
+
+
+def test_gemm_shape_model_properties(B):
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        M, N, K = (int(v) for v in rng.integers(1, 20000, size=3))
+        sp = int(rng.integers(0, 2))
+        bn, ks = B.rnn_debug_gemm_shape(M, N, K, sp, 148)
+        assert bn in (64, 128, 160, 256) and 1 <= ks <= 8
+        assert (bn == 64) == (N <= 64)
+        assert bn <= max(128, (N + 31) // 32 * 32)
+        nkt = (K * 2 + 127) // 128
+        assert ks == 1 or nkt // ks >= 4
+        assert B.rnn_debug_gemm_shape(M, N, K, sp, 148, allow_split=False)[1] == 1
+    with pytest.raises(B.RnnError):
+        B.rnn_debug_gemm_shape(0, 10, 10, 1, 148)
