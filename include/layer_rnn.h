@@ -384,7 +384,7 @@ rnn_status_t rnn_debug_wf_pack(rnn_t h, void* stream, int64_t N, int layer, cons
  * touched).  For C[M][N] over a contraction of K_total on num_sms SMs, with
  * scaled fp16 pairs (split16 = 1, fp32 operands) or bf16 (0), K splits
  * allowed or not (allow_split), *bn receives the output tile width (64, 128,
- * 160 or 256 columns; tiles are 128 rows) and *ksplit the number of K splits
+ * 160, 192 or 256 columns; tiles are 128 rows) and *ksplit the number of K splits
  * that the library's wave model picks: per tile and 64-element K block the
  * larger of the MMA time and the operand feed, times ceil(tiles * ksplit /
  * num_sms) waves, plus a fixed cost per tile and wave and the split's partial

@@ -44,7 +44,7 @@ struct TcGemm {
   void* C = nullptr; int64_t ldc = 0; int out_bf16 = 0; int accumulate = 0;
   const void* bias1 = nullptr; const void* bias2 = nullptr; int64_t bias2_limit = 0;
   int bias_bf16 = 0;
-  int bn = 0;  // output tile width (64, 128, 160, 256; 0: chosen by the wave model)
+  int bn = 0;  // output tile width (64, 128, 160, 192, 256; 0: chosen by the wave model)
   int ctas_per_sm = 1;  // 2: a smaller ring, two CTAs per SM (fp32 C or partials only)
   int ksplit = 1; float* part = nullptr;  // split-K partials [ksplit][M][N]
   int* status = nullptr; long long timeout_ns = 2000000000LL;

@@ -829,7 +829,7 @@ void gemm_tc_shape(int64_t M, int64_t N, int64_t K_total, bool split16, int num_
   int best_bn = N <= 64 ? 64 : 128, best_ks = 1;
   double best = -1;
   const double fixed_clk = 20000.0;  // per tile and wave
-  for (int BN : {64, 128, 160, 256}) {
+  for (int BN : {64, 128, 160, 192, 256}) {
     if ((BN == 64) != (N <= 64)) continue;
     if (BN > 128 && BN > (N + 31) / 32 * 32) continue;  // no tile wider than the output
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -870,7 +870,7 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   const bool sp = g.split16 != 0;
   int BN = g.bn, ks_unused = 1;
   if (BN == 0) gemm_tc_shape(g.M, g.N, g.K + g.K2, sp, 148, false, &BN, &ks_unused);
-  if (BN != 64 && BN != 128 && BN != 160 && BN != 256) return cudaErrorInvalidValue;
+  if (BN != 64 && BN != 128 && BN != 160 && BN != 192 && BN != 256) return cudaErrorInvalidValue;
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
   // every operand is 16-bit (fp16 pairs or bf16): TMA copies bytes, so one
@@ -945,11 +945,13 @@ cudaError_t gemm_tc(const TcGemm& g, cudaStream_t st) {
   cudaError_t e;
   if (sp)
     e = BN == 256   ? launch_tc<256, true>(maps, kp, grid, st)
+        : BN == 192 ? launch_tc<192, true>(maps, kp, grid, st)
         : BN == 160 ? launch_tc<160, true>(maps, kp, grid, st)
         : BN == 128 ? launch_tc<128, true>(maps, kp, grid, st)
                     : launch_tc<64, true>(maps, kp, grid, st);
   else
     e = BN == 256   ? launch_tc<256, false>(maps, kp, grid, st)
+        : BN == 192 ? launch_tc<192, false>(maps, kp, grid, st)
         : BN == 160 ? launch_tc<160, false>(maps, kp, grid, st)
         : BN == 128 ? launch_tc<128, false>(maps, kp, grid, st)
                     : launch_tc<64, false>(maps, kp, grid, st);

@@ -221,7 +221,7 @@ def test_gemm_shape_model_properties(B):
         M, N, K = (int(v) for v in rng.integers(1, 20000, size=3))
         sp = int(rng.integers(0, 2))
         bn, ks = B.rnn_debug_gemm_shape(M, N, K, sp, 148)
-        assert bn in (64, 128, 160, 256) and 1 <= ks <= 8
+        assert bn in (64, 128, 160, 192, 256) and 1 <= ks <= 8
         assert (bn == 64) == (N <= 64)
         assert bn <= max(128, (N + 31) // 32 * 32)
         nkt = (K * 2 + 127) // 128
